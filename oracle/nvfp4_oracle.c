@@ -97,14 +97,18 @@ float orc_amax(const float* x, int64_t n) {
 float orc_global_scale(float amax) { return amax / 2688.0f; }
 
 /* Encode one block of 16 values that share the E4M3 scale s (already chosen).
- * t = e4m3(s) * g; q = e2m1(x / t).  If t is zero every code is a signed zero. */
+ * t = e4m3(s) * g is the block's decode step; the FP32 order is fixed as one
+ * reciprocal per block and one product per element:
+ *   r = 1 / t;  q = e2m1(x * r).
+ * If t is zero every code is a signed zero. */
 static void encode_block(const float* x, int64_t stride, float t, uint32_t* codes16) {
+  float r = (t == 0.0f) ? 0.0f : 1.0f / t;
   for (int i = 0; i < 16; ++i) {
     float v = x[(int64_t)i * stride];
     if (t == 0.0f)
       codes16[i] = signbit(v) ? 8u : 0u;
     else
-      codes16[i] = orc_e2m1_encode(v / t);
+      codes16[i] = orc_e2m1_encode(v * r);
   }
 }
 

@@ -150,7 +150,7 @@ def test_global_max_block_encodes_448():
 
 def test_quant_is_nearest_representable():
     """Each scale is the E4M3 value nearest amax_blk/(6g) and each code the E2M1
-    value nearest x/t (brute force over all candidates)."""
+    value nearest x * (1/t) (brute force over all candidates)."""
     rng = np.random.default_rng(4)
     x = (rng.standard_normal((16, 128)) * np.exp(rng.uniform(-3, 3, (16, 1)))).astype(np.float32)
     x[3, 5:21] = 0.0  # a zero block
@@ -168,8 +168,9 @@ def test_quant_is_nearest_representable():
             s = q.scales[r, b]
             assert s in s_best
             t = np.float32(orc.e4m3_decode(s)) * g
+            rcp = np.float32(1.0) / t if t != 0 else np.float32(0)
             for i in range(16):
-                want = (8 if np.signbit(blk[i]) else 0) if t == 0 else _e2m1_brute(blk[i] / t)
+                want = (8 if np.signbit(blk[i]) else 0) if t == 0 else _e2m1_brute(blk[i] * rcp)
                 assert codes[r, b * 16 + i] == want
 
 
