@@ -100,13 +100,14 @@ float orc_global_scale(float amax) { return amax / 2688.0f; }
  * t = e4m3(s) * g is the block's decode step; the FP32 order is fixed as one
  * reciprocal per block and one product per element:
  *   r = 1 / t;  q = e2m1(x * r).
- * If t is zero every code is a signed zero. */
+ * If t is zero every code is a signed zero, and a zero element always gets the
+ * signed-zero code. */
 static void encode_block(const float* x, int64_t stride, float t, uint32_t* codes16) {
   float r = (t == 0.0f) ? 0.0f : 1.0f / t;
   for (int i = 0; i < 16; ++i) {
     float v = x[(int64_t)i * stride];
-    if (t == 0.0f)
-      codes16[i] = signbit(v) ? 8u : 0u;
+    if (t == 0.0f || v == 0.0f)
+      codes16[i] = signbit(v) ? 8u : 0u; /* also when 1/t overflowed: 0 * inf */
     else
       codes16[i] = orc_e2m1_encode(v * r);
   }
