@@ -1,0 +1,236 @@
+/*
+ * libpact — NVFP4 LoRA linear layer for GB300 (sm_103a): C ABI.
+ *
+ * The method: "PACT: NVFP4 Data-Flow LoRA Fine-Tuning on Consumer GPUs".
+ *   Table 6  NVFP4 format: E2M1 elements, one E4M3 scale per block of 16 elements.
+ *   Table 7  Precision allocation: frozen projections are NVFP4 GEMMs with FP32
+ *            accumulation and BF16 output, backed by cached forward and backward
+ *            NVFP4 weight layouts; RMSNorm keeps its NVFP4 output and an FP32
+ *            per-token statistic; SiLU-multiply keeps separate NVFP4 gate/up
+ *            copies; the LoRA branch runs BF16 GEMMs on the reconstructed shared
+ *            input; residual gradients accumulate in BF16.
+ *   Figure 3 The LoRA linear layer's forward and backward paths.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory.  Scratch ("ws") is passed in by the caller; its
+ *     size comes from the matching *_workspace_size() query and it must be 256-byte
+ *     aligned.  The contents of ws need not be initialised.
+ *   - All calls are asynchronous on the given CUDA stream (0 = legacy default
+ *     stream) and never synchronise the host.  Per-tensor scales stay on the
+ *     device.
+ *   - BF16 tensors are passed as uint16_t bit patterns, row-major.
+ *   - A call validates its arguments on the host and returns a pact_status without
+ *     launching anything when they are invalid; pact_last_error() then describes
+ *     the problem (thread-local).  A launch failure returns PACT_ERR_CUDA.
+ *   - Errors raised inside a kernel (a bounded wait that ran out) are recorded in
+ *     a device status word that pact_check_status() reads.
+ *   - Outputs must not alias inputs unless a call says so.
+ */
+#ifndef PACT_H
+#define PACT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pact_stream_t; /* a cudaStream_t */
+
+typedef enum pact_status {
+  PACT_OK = 0,
+  PACT_ERR_INVALID_ARG = 1,  /* null pointer, bad rank, workspace too small, ... */
+  PACT_ERR_SHAPE = 2,        /* a dimension breaks the call's divisibility rule */
+  PACT_ERR_ALIGN = 3,        /* a pointer breaks the call's alignment rule */
+  PACT_ERR_ARCH = 4,         /* the current device is not sm_103 */
+  PACT_ERR_CUDA = 5,         /* a CUDA runtime or driver call failed */
+  PACT_ERR_TIMEOUT = 6,      /* a kernel's bounded wait ran out (pact_check_status) */
+  PACT_ERR_DEVICE_STATUS = 7 /* another kernel-side check failed (pact_check_status) */
+} pact_status;
+
+/*
+ * An NVFP4 tensor X [rows, cols] (Table 6), cols % 16 == 0:
+ *   codes  u8 [rows, cols/2], row stride cols/2 bytes; two E2M1 codes per byte,
+ *          the even column in the low nibble.  Code = sign*8 + index of the
+ *          magnitude in {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ *   sf     u8 E4M3 block scales in the layout the block-scaled tensor-core MMA
+ *          reads: atoms of 128 rows x 4 blocks (512 bytes) ordered row-block
+ *          major, with C16p = pad4(cols/16):
+ *            offset(r, c) = ((r/128)*(C16p/4) + c/4)*512 + (r%32)*16
+ *                           + ((r%128)/32)*4 + c%4,
+ *          pad128(rows) * C16p bytes in total; pad entries are zero.
+ *   g      device pointer to the FP32 per-tensor scale.
+ * Value of element (r, c):  e2m1(code) * e4m3(sf) * g.
+ * codes and sf must be 16-byte aligned (128-byte aligned for GEMM operands).
+ */
+typedef struct pact_nvfp4 {
+  void* codes;
+  void* sf;
+  float* g;
+  int64_t rows;
+  int64_t cols;
+} pact_nvfp4;
+
+/* Bytes of the code array and of the scale array of an NVFP4 [rows, cols] tensor. */
+size_t pact_nvfp4_codes_bytes(int64_t rows, int64_t cols);
+size_t pact_nvfp4_sf_bytes(int64_t rows, int64_t cols);
+
+/*
+ * Activation quantisation to NVFP4 (Table 6 format; Table 7: both GEMM operands
+ * are NVFP4, so X and dY are quantised before the frozen-projection GEMMs).
+ *   amax_t = max |x|;  g = amax_t / (6*448);  per block of 16 along a row:
+ *   s = e4m3_rne_satfinite(amax_blk / (6*g));  t = e4m3(s)*g;
+ *   q = e2m1_rne_satfinite(x * (1/t))  (one reciprocal per block; signed zero
+ *   codes when t == 0).
+ * x: BF16 [M, K], row stride ldx elements (ldx >= K, ldx % 8 == 0), 16-byte aligned.
+ * amax_opt: optional device pointer to a precomputed amax_t (skips the first pass).
+ * out: codes/sf/g preallocated for [M, K]; out->rows == M, out->cols == K.
+ * Rules: M >= 1, K % 64 == 0.  ws: pact_quant_nvfp4_workspace_size() bytes.
+ */
+size_t pact_quant_nvfp4_workspace_size(int64_t M, int64_t K);
+int pact_quant_nvfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                     const float* amax_opt, pact_nvfp4* out, void* ws, size_t ws_bytes,
+                     pact_stream_t stream);
+
+/*
+ * Offline pack of the frozen weight W [N, K] (FP32, row-major; Y = X W^T) into the
+ * cached NVFP4 layouts (abstract: "cached forward and backward weight layouts";
+ * Table 7 "State retained for backward").  One E4M3 scale per 16x16 tile of W
+ * (RTN, g = amax(W)/2688), so both layouts hold the same effective weights:
+ *   forward layout  [N, K], blocks of 16 along K  (B operand of Y = X W^T)
+ *   backward layout [K, N], blocks of 16 along N  (B operand of dX = dY W)
+ * and dequant(backward) == dequant(forward)^T exactly.
+ * Rules: N % 64 == 0, K % 64 == 0, W 16-byte aligned.
+ * ws: pact_pack_weight_workspace_size() bytes.
+ */
+size_t pact_pack_weight_workspace_size(int64_t N, int64_t K);
+int pact_pack_weight_fwd(const float* W, int64_t N, int64_t K, pact_nvfp4* out_fwd,
+                         void* ws, size_t ws_bytes, pact_stream_t stream);
+int pact_pack_weight_bwd(const float* W, int64_t N, int64_t K, pact_nvfp4* out_bwd,
+                         void* ws, size_t ws_bytes, pact_stream_t stream);
+
+/*
+ * LoRA linear forward (Table 7 rows "Frozen projections" and "LoRA branch";
+ * Figure 3):
+ *   Y = g_x g_w (Xq Wq^T) + scale * (Xhat A) B   [+ residual]
+ * with FP32 accumulation and BF16 output; Xhat = dequant(Xq) is the shared NVFP4
+ * input of both branches.  The NVFP4 GEMM runs on tcgen05 block-scaled tensor
+ * cores; the LoRA product is fused into the same accumulator.
+ *   xq     NVFP4 [M, K];  w_fwd NVFP4 [N, K] (forward layout)
+ *   A      BF16 [K, r];   B BF16 [r, N];  1 <= r <= 64;  scale = alpha / r
+ *   residual_opt  BF16 [M, N] added in FP32 before the BF16 cast (may alias y)
+ *   y      BF16 [M, N] output
+ *   out_amax_opt  if non-null, receives max |y| over the BF16 output
+ * Rules: M >= 1, K % 64 == 0, N % 64 == 0; all pointers 16-byte aligned, NVFP4
+ * codes/sf 128-byte aligned.  ws: pact_lora_linear_fwd_workspace_size() bytes.
+ */
+size_t pact_lora_linear_fwd_workspace_size(int64_t M, int64_t N, int64_t K, int r);
+int pact_lora_linear_fwd(const pact_nvfp4* xq, const pact_nvfp4* w_fwd, const uint16_t* A,
+                         const uint16_t* B, int r, float scale, const uint16_t* residual_opt,
+                         uint16_t* y, float* out_amax_opt, void* ws, size_t ws_bytes,
+                         pact_stream_t stream);
+
+/*
+ * LoRA linear input gradient (Table 7: "NVFP4 input-gradient GEMMs" on the cached
+ * backward layout; LoRA branch "BF16 ... input gradients"):
+ *   dX = g_dy g_w (dYq Wbwd^T) + scale * (dY B^T) A^T   [+ dX_prev if accumulate]
+ *   dyq    NVFP4 [M, N];  dy BF16 [M, N] (the same gradient before quantisation,
+ *          used by the BF16 LoRA branch);  w_bwd NVFP4 [K, N] (backward layout)
+ *   A BF16 [K, r];  B BF16 [r, N];  1 <= r <= 64;  scale = alpha / r
+ *   accumulate  0: dx = result;  1: dx += result (BF16 gradient accumulation,
+ *               e.g. the q/k/v input gradients summed into one dX)
+ *   dx     BF16 [M, K] output
+ * Rules as for the forward.  ws: pact_lora_linear_dgrad_workspace_size() bytes.
+ */
+size_t pact_lora_linear_dgrad_workspace_size(int64_t M, int64_t N, int64_t K, int r);
+int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact_nvfp4* w_bwd,
+                           const uint16_t* A, const uint16_t* B, int r, float scale,
+                           int accumulate, uint16_t* dx, void* ws, size_t ws_bytes,
+                           pact_stream_t stream);
+
+/*
+ * Fused RMSNorm -> NVFP4 (abstract: "reuses quantized RMSNorm outputs"; Table 7
+ * "RMSNorm": BF16 input, FP32 normalisation, retains the NVFP4 output and the FP32
+ * per-token statistic).  Per row:
+ *   ss by a fixed order (row split in blocks of 16; lane l = 0..31 sums blocks
+ *   l, l+32, ... element by element; butterfly over offsets 16, 8, 4, 2, 1);
+ *   rstd = 1 / sqrt(ss/H + eps);  y_j = (x_j * rstd) * gamma_j   (FP32);
+ * then y (FP32, never rounded to BF16) is quantised like pact_quant_nvfp4.
+ *   x BF16 [M, H];  gamma BF16 [H];  yq NVFP4 [M, H] out;  rstd FP32 [M] out.
+ * Rules: M >= 1, H % 64 == 0, H <= 16384.  ws: pact_rmsnorm_quant_workspace_size().
+ */
+size_t pact_rmsnorm_quant_workspace_size(int64_t M, int64_t H);
+int pact_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M, int64_t H,
+                       float eps, pact_nvfp4* yq, float* rstd, void* ws, size_t ws_bytes,
+                       pact_stream_t stream);
+
+/*
+ * Fused SiLU-multiply -> NVFP4 (abstract: "saves gate/up activations in NVFP4";
+ * Table 7 "SiLU-multiply": BF16 gate/up inputs, FP32 arithmetic, separate NVFP4
+ * gate/up copies retained for backward).
+ *   gateup BF16 [M, 2I]: gate = columns [0, I), up = columns [I, 2I).
+ *   h = (gate / (1 + exp(-gate))) * up in FP32, with exp evaluated by the fixed
+ *   recipe of pact_test_pexp; hq = NVFP4(h); gate_q = NVFP4(gate); up_q = NVFP4(up),
+ *   each with its own per-tensor scale.
+ *   amax3_opt: optional device FP32[3] = {amax(h), amax(gate), amax(up)}.
+ * Rules: M >= 1, I % 64 == 0.  ws: pact_silu_mul_quant_workspace_size() bytes.
+ */
+size_t pact_silu_mul_quant_workspace_size(int64_t M, int64_t I);
+int pact_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I, const float* amax3_opt,
+                        pact_nvfp4* hq, pact_nvfp4* gate_q, pact_nvfp4* up_q, void* ws,
+                        size_t ws_bytes, pact_stream_t stream);
+
+/*
+ * SiLU-multiply backward (Table 7: FP32 reconstruction from the NVFP4 gate/up
+ * copies and derivatives, BF16 gradients).  With g, u the dequantised copies and
+ * s = 1/(1+exp(-g)):  dgate = dh*u*s*(1 + g*(1-s)),  dup = dh*g*s.
+ *   gate_q, up_q NVFP4 [M, I];  dh BF16 [M, I];  dgateup BF16 [M, 2I] out
+ *   (dgate in columns [0, I), dup in [I, 2I)).
+ *   out_amax_opt: if non-null receives max |dgateup| (BF16 values), for a
+ *   following single-pass pact_quant_nvfp4.
+ * Rules: M >= 1, I % 64 == 0.
+ */
+int pact_silu_mul_bwd(const pact_nvfp4* gate_q, const pact_nvfp4* up_q, const uint16_t* dh,
+                      uint16_t* dgateup, float* out_amax_opt, pact_stream_t stream);
+
+/*
+ * RMSNorm backward (Table 7: FP32 reconstruction and reduction, BF16 gradient):
+ * n = dequant(yq)/gamma, dn = dy*gamma, c = sum_j(dn_j n_j)/H,
+ * dx = rstd*(dn - n*c)  [+ dres]  (dres: residual-stream gradient, BF16 addition).
+ *   yq NVFP4 [M, H] (the forward output);  gamma BF16 [H];  rstd FP32 [M];
+ *   dy BF16 [M, H];  dres_opt BF16 [M, H] or NULL (may alias dx);  dx BF16 [M, H].
+ * Rules: M >= 1, H % 64 == 0, H <= 16384.
+ */
+int pact_rmsnorm_bwd(const pact_nvfp4* yq, const uint16_t* gamma, const float* rstd,
+                     const uint16_t* dy, const uint16_t* dres_opt, uint16_t* dx,
+                     pact_stream_t stream);
+
+/*
+ * The FP32 exp recipe used by pact_silu_mul_quant, exposed so that it can be
+ * compared bit for bit with another implementation: Cody-Waite reduction
+ * x = n ln2 + f (ln2 split in a 16-bit head and a tail), degree-7 Taylor
+ * polynomial of e^f by Horner's rule with fused multiply-adds, exact scaling by
+ * 2^n; +inf above 0x1.62e42ep+6, 0 below -0x1.9fe368p+6.  x, y FP32 [n] (device).
+ */
+int pact_test_pexp(const float* x, float* y, int64_t n, pact_stream_t stream);
+
+/* Synchronises the stream, then returns and clears the device status word:
+ * PACT_OK, PACT_ERR_TIMEOUT or PACT_ERR_DEVICE_STATUS.  For tests and debugging. */
+int pact_check_status(pact_stream_t stream);
+
+/* PACT_OK when the current CUDA device is sm_103 (GB300), else PACT_ERR_ARCH. */
+int pact_device_supported(void);
+
+/* Description of the last error returned on this host thread ("" if none). */
+const char* pact_last_error(void);
+
+/* Library version string. */
+const char* pact_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PACT_H */

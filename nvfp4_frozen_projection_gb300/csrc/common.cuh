@@ -1,0 +1,182 @@
+// Device helpers shared by the libpact kernels (sm_103a only).
+//
+// NVFP4 (Table 6 of "PACT: NVFP4 Data-Flow LoRA Fine-Tuning on Consumer GPUs"):
+// E2M1 elements, one E4M3 scale per block of 16, plus an FP32 per-tensor scale.
+// Conversions use the hardware cvt instructions (RN, satfinite); every FP32 step
+// of the encode is an explicit __f*_rn intrinsic so the compiler cannot contract
+// or reorder it.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#if defined(__CUDA_ARCH__) && !defined(__CUDA_ARCH_FEAT_SM103_ALL)
+#error "libpact kernels are written for sm_103a only"
+#endif
+
+namespace pact {
+
+// ------------------------------------------------------------------ layout
+__host__ __device__ __forceinline__ int64_t pad_to(int64_t x, int64_t m) {
+  return (x + m - 1) / m * m;
+}
+
+// Byte offset of the E4M3 scale of (row r, block c) in the 128x4-atom layout read
+// by the block-scaled tensor-core MMA (c16p = pad4(cols/16)).
+__host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t c16p) {
+  return ((r >> 7) * (c16p >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 +
+         (c & 3);
+}
+
+// ------------------------------------------------------------------ codecs
+// E4M3 (satfinite, RN) of a non-negative FP32 value -> byte.
+__device__ __forceinline__ uint32_t e4m3_from_f32(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return (uint32_t)(r & 0xFFu);
+}
+
+// E4M3 byte -> FP32 (exact, through FP16).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)(b & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu)));
+}
+
+// Two non-negative magnitudes -> E2M1 magnitude codes (RN, satfinite at 6):
+// lo in bits 0..3, hi in bits 4..7.
+__device__ __forceinline__ uint32_t e2m1x2_mag(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t sign_bit(float x) { return __float_as_uint(x) >> 31; }
+
+// Encode 8 FP32 values that share the block decode step t (with rcp = 1/t) into
+// 8 E2M1 codes packed in a uint32 (element 0 in bits 0..3).  Signed-zero codes
+// when t == 0 or the element is zero.
+__device__ __forceinline__ uint32_t encode8(const float* x, float t, float rcp) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    float a0 = fabsf(x[i]), a1 = fabsf(x[i + 1]);
+    uint32_t mag = (t == 0.0f) ? 0u : e2m1x2_mag(__fmul_rn(a0, rcp), __fmul_rn(a1, rcp));
+    if (a0 == 0.0f) mag &= 0xF0u;
+    if (a1 == 0.0f) mag &= 0x0Fu;
+    uint32_t b = mag | (sign_bit(x[i]) << 3) | (sign_bit(x[i + 1]) << 7);
+    w |= b << (4 * i);
+  }
+  return w;
+}
+
+// Per-tensor scale and its block-scale divisor.
+struct TensorScale {
+  float g;  // amax / 2688
+  float d;  // 6 * g
+};
+__device__ __forceinline__ TensorScale tensor_scale(float amax) {
+  TensorScale s;
+  s.g = __fdiv_rn(amax, 2688.0f);
+  s.d = __fmul_rn(6.0f, s.g);
+  return s;
+}
+
+// Block scale byte and decode step for a block whose absolute maximum is amax_blk.
+__device__ __forceinline__ uint32_t block_scale(float amax_blk, TensorScale ts, float* t,
+                                                float* rcp) {
+  uint32_t s = (ts.g == 0.0f) ? 0u : e4m3_from_f32(__fdiv_rn(amax_blk, ts.d));
+  float tt = __fmul_rn(e4m3_to_f32(s), ts.g);
+  *t = tt;
+  *rcp = (tt == 0.0f) ? 0.0f : __fdiv_rn(1.0f, tt);
+  return s;
+}
+
+// ------------------------------------------------------------------ bf16
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// max |bf16| over 8 packed values, as FP32 bits (non-negative, so unsigned order).
+__device__ __forceinline__ uint32_t absmax_bf16x8_bits(const uint4& v) {
+  uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                        __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+  return (hi > lo ? hi : lo) << 16;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Block-wide max of non-negative float bits, folded into *dst with one atomic per CTA.
+__device__ __forceinline__ void block_max_atomic(uint32_t v, unsigned* dst) {
+  __shared__ uint32_t red[32];
+  v = __reduce_max_sync(0xFFFFFFFFu, v);
+  int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int nw = (blockDim.x + 31) >> 5;
+    uint32_t x = lane < nw ? red[lane] : 0u;
+    x = __reduce_max_sync(0xFFFFFFFFu, x);
+    if (lane == 0 && x != 0u) atomicMax(dst, x);
+  }
+}
+
+// ------------------------------------------------------------------ exp recipe
+// exp(x) by a fixed FP32 recipe (Cody-Waite reduction with a 16-bit head of ln 2,
+// degree-7 Taylor polynomial in Horner form with fused multiply-adds, exact
+// scaling by 2^n), so that independent implementations agree bit for bit.
+__device__ __forceinline__ float scale_pow2(float p, int n) {
+  if (n > 127) return __fmul_rn(__fmul_rn(p, 0x1p+64f), __int_as_float((n - 64 + 127) << 23));
+  if (n < -126) return __fmul_rn(__fmul_rn(p, __int_as_float((n + 64 + 127) << 23)), 0x1p-64f);
+  return __fmul_rn(p, __int_as_float((n + 127) << 23));
+}
+
+__device__ __forceinline__ float pexp(float x) {
+  if (x != x) return x;
+  if (x > 0x1.62e42ep+6f) return __int_as_float(0x7F800000);
+  if (x < -0x1.9fe368p+6f) return 0.0f;
+  float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
+  float f = __fmaf_rn(-n, 0x1.62e400p-1f, x);
+  f = __fmaf_rn(-n, 0x1.7f7d1cp-20f, f);
+  float p = 0x1.a01a02p-13f;
+  p = __fmaf_rn(p, f, 0x1.6c16c2p-10f);
+  p = __fmaf_rn(p, f, 0x1.111112p-7f);
+  p = __fmaf_rn(p, f, 0x1.555556p-5f);
+  p = __fmaf_rn(p, f, 0x1.555556p-3f);
+  p = __fmaf_rn(p, f, 0x1.000000p-1f);
+  p = __fmaf_rn(p, f, 1.0f);
+  p = __fmaf_rn(p, f, 1.0f);
+  return scale_pow2(p, (int)n);
+}
+
+// h = (g / (1 + exp(-g))) * u, FP32, fixed order.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  float e = pexp(-g);
+  float den = __fadd_rn(1.0f, e);
+  float s = __fdiv_rn(g, den);
+  return __fmul_rn(s, u);
+}
+
+}  // namespace pact

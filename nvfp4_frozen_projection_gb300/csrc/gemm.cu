@@ -1,0 +1,375 @@
+// NVFP4 frozen-projection GEMM with the fused LoRA branch, for sm_103a.
+//
+// "PACT: NVFP4 Data-Flow LoRA Fine-Tuning on Consumer GPUs", Table 7:
+//   frozen projections = NVFP4 GEMMs with FP32 accumulation and BF16 output
+//   (forward Y = X W^T on the cached forward layout, input gradient dX = dY W on
+//   the cached backward layout); LoRA branch = BF16 GEMMs on the reconstructed
+//   shared input; Figure 3: both branches sum into the layer output.
+//
+//   OUT[m, n] = s * ( sum_k A[m,k] B[n,k]  +  sum_j LA[m,j] LB[n,j] )  [+ ADD[m, n]]
+//
+// A [M, K] and B [N, K] are NVFP4 (E2M1 codes + UE4M3 scales per 16 along K); the
+// first sum runs on the block-scaled tensor cores (tcgen05.mma kind::mxf4nvf4,
+// block16).  LA [M, RP] and LB [N, RP] are BF16: the LoRA down-projection output,
+// pre-scaled so that s * LA LB^T equals the LoRA term, and the LoRA
+// up-projection; their product runs as tcgen05.mma kind::f16 into the same TMEM
+// accumulator.  s = g_a * g_b (or 1 when either per-tensor scale is zero, in which
+// case the NVFP4 operand is all zero).
+//
+// Structure: one persistent CTA per SM, 6 warps.
+//   warp 0     TMA producer: A/B tiles (128B/64B swizzled) and the scale-factor
+//              atoms (plain bulk copies) into a STAGES-deep shared-memory ring;
+//              the LoRA operands once per tile.
+//   warp 1     TMEM allocator and MMA issuer (one thread): scale factors
+//              shared -> TMEM with tcgen05.cp, then the MMAs; tcgen05.commit
+//              frees ring slots and publishes the finished accumulator.
+//   warps 2-5  epilogue: TMEM -> registers (tcgen05.ld), scale, optional addend,
+//              BF16 cast, global store, optional amax.
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace pact {
+
+__device__ unsigned g_pact_status;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+
+template <int BN, int BK, int STAGES, int RP>
+struct GemmCfg {
+  static constexpr int BM = 128;
+  static constexpr int ROWB = BK / 2;   // bytes of one tile row per stage
+  static constexpr int KSUB = BK / 64;  // K=64 MMAs per stage
+  static constexpr int NRB = BN / 128;  // 128-row scale atoms of the B tile
+  static constexpr int A_BYTES = BM * ROWB;
+  static constexpr int B_BYTES = BN * ROWB;
+  static constexpr int SFA_BYTES = KSUB * 512;
+  static constexpr int SFB_BYTES = NRB * KSUB * 512;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int LA_OFF = STAGES * STAGE_BYTES;
+  static constexpr int LA_BYTES = BM * RP * 2;
+  static constexpr int LB_OFF = LA_OFF + LA_BYTES;
+  static constexpr int LB_BYTES = BN * RP * 2;
+  static constexpr int BAR_OFF = LB_OFF + LB_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  static constexpr uint32_t AB_SWZ = ROWB == 128 ? 2u : 4u;  // 128B or 64B swizzle
+  static constexpr uint32_t AB_SBO = 8 * ROWB;                // 8-row swizzle atom
+  static constexpr uint32_t L_SWZ = RP == 16 ? 6u : (RP == 32 ? 4u : 2u);
+  static constexpr uint32_t L_SBO = 8 * RP * 2;
+  static constexpr int SF_BASE = 256;                          // TMEM column
+  static constexpr int SF_COLS = 4 * KSUB * (1 + NRB);         // per stage
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(BN == 128 || BN == 256, "BN");
+  static_assert(BK == 128 || BK == 256, "BK");
+  static_assert(RP == 16 || RP == 32 || RP == 64, "RP");
+  static_assert(SF_BASE + STAGES * SF_COLS <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0 && LA_OFF % 1024 == 0 && LB_OFF % 1024 == 0, "align");
+};
+
+// Instruction descriptors (M = 128, K-major A and B, dense).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int n) {
+  // atype = btype = E2M1 (1), scale type UE4M3 (bit 23 = 0)
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  // D = F32 (bits 4-5 = 1), A = B = BF16 (1)
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void raise_error(volatile uint32_t* abort_flag, unsigned* status,
+                                            unsigned code) {
+  *abort_flag = 1u;
+  atomicOr(status, code);
+}
+
+template <int BN, int BK, int STAGES, int RP>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmLA,
+                 const __grid_constant__ CUtensorMap tmLB, const GemmParams p) {
+  using C = GemmCfg<BN, BK, STAGES, RP>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t bar0 = base + C::BAR_OFF;
+  const uint32_t lora_full = bar0 + 8 * (2 * STAGES);
+  const uint32_t lora_empty = lora_full + 8;
+  const uint32_t acc_full = lora_full + 16;
+  const uint32_t acc_empty = lora_full + 24;
+  const uint32_t final_bar = lora_full + 32;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 200);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 204);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = p.num_m * p.num_n;
+  const int nks = (p.K + BK - 1) / BK;
+  const int rb_total = (p.N + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar0 + 8 * s, 1);
+      mbar_init(bar0 + 8 * (STAGES + s), 1);
+    }
+    mbar_init(lora_full, 1);
+    mbar_init(lora_empty, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
+    mbar_init(final_bar, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if (p.lora_steps) {
+      prefetch_tensormap(&tmLA);
+      prefetch_tensormap(&tmLB);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, lphase = 0;
+      uint32_t pend = 0, pend_par = 0, lpend = 0, lpend_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % p.num_m) * C::BM;
+        const int n0 = (tile / p.num_m) * BN;
+        if (p.lora_steps) {
+          if (!mbar_wait(lora_empty, lphase ^ 1u, kWaitLimitNs, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(lora_full, C::LA_BYTES + C::LB_BYTES);
+          tma_load_2d(base + C::LA_OFF, &tmLA, 0, m0, lora_full);
+          tma_load_2d(base + C::LB_OFF, &tmLB, 0, n0, lora_full);
+          lpend = 1u;
+          lpend_par = lphase;
+          lphase ^= 1u;
+        }
+        const int nrb = min(C::NRB, rb_total - n0 / 128);
+        for (int ks = 0; ks < nks; ++ks) {
+          const uint32_t fb = bar0 + 8 * stage;
+          if (!mbar_wait(bar0 + 8 * (STAGES + stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int ksub = min(C::KSUB, (p.K - ks * BK) / 64);
+          const uint32_t sb = base + stage * C::STAGE_BYTES;
+          mbar_expect_tx(fb, C::A_BYTES + C::B_BYTES + (uint32_t)(ksub * 512 * (1 + nrb)));
+          tma_load_2d(sb, &tmA, ks * C::ROWB, m0, fb);
+          tma_load_2d(sb + C::A_BYTES, &tmB, ks * C::ROWB, n0, fb);
+          const size_t katom = (size_t)ks * C::KSUB;
+          bulk_load(sb + C::A_BYTES + C::B_BYTES,
+                    p.sfa + ((size_t)(m0 / 128) * (p.k16p / 4) + katom) * 512,
+                    (uint32_t)(ksub * 512), fb);
+          for (int rb = 0; rb < nrb; ++rb)
+            bulk_load(sb + C::A_BYTES + C::B_BYTES + C::SFA_BYTES + rb * C::KSUB * 512,
+                      p.sfb + ((size_t)(n0 / 128 + rb) * (p.k16p / 4) + katom) * 512,
+                      (uint32_t)(ksub * 512), fb);
+          pend |= 1u << stage;
+          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_TMA);
+        // let copies already in flight land before the CTA can exit
+        for (int s = 0; s < STAGES; ++s)
+          if (pend & (1u << s)) mbar_wait(bar0 + 8 * s, (pend_par >> s) & 1u, 10000000ull, nullptr);
+        if (lpend) mbar_wait(lora_full, lpend_par, 10000000ull, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, lphase = 0, aphase = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_nvf4(BN);
+      const uint32_t idesc_l = idesc_bf16(BN);
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(acc_empty, aphase ^ 1u, kWaitLimitNs, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t accum = 0;
+        if (p.lora_steps) {
+          if (!mbar_wait(lora_full, lphase, kWaitLimitNs, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int j = 0; j < p.lora_steps; ++j) {
+            const uint64_t da = smem_desc(base + C::LA_OFF + 32 * j, 16, C::L_SBO, C::L_SWZ);
+            const uint64_t db = smem_desc(base + C::LB_OFF + 32 * j, 16, C::L_SBO, C::L_SWZ);
+            mma_bf16(tmem, da, db, idesc_l, accum);
+            accum = 1;
+          }
+          mma_commit(lora_empty);
+          lphase ^= 1u;
+        }
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!mbar_wait(bar0 + 8 * stage, phase, kWaitLimitNs, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sb = base + stage * C::STAGE_BYTES;
+          const uint32_t sfa_s = sb + C::A_BYTES + C::B_BYTES;
+          const uint32_t sfb_s = sfa_s + C::SFA_BYTES;
+          const uint32_t tsf = tmem + C::SF_BASE + stage * C::SF_COLS;
+#pragma unroll
+          for (int j = 0; j < C::KSUB; ++j) {
+            tmem_cp_sf_atom(tsf + 4 * j, smem_desc(sfa_s + 512 * j, 16, 128, 0));
+#pragma unroll
+            for (int rb = 0; rb < C::NRB; ++rb)
+              tmem_cp_sf_atom(tsf + 4 * C::KSUB + (j * C::NRB + rb) * 4,
+                              smem_desc(sfb_s + rb * C::KSUB * 512 + 512 * j, 16, 128, 0));
+          }
+          const int ksub = min(C::KSUB, (p.K - ks * BK) / 64);
+          for (int j = 0; j < ksub; ++j) {
+            const uint64_t da = smem_desc(sb + 32 * j, 16, C::AB_SBO, C::AB_SWZ);
+            const uint64_t db = smem_desc(sb + C::A_BYTES + 32 * j, 16, C::AB_SBO, C::AB_SWZ);
+            mma_nvf4(tmem, da, db, idesc, tsf + 4 * j, tsf + 4 * C::KSUB + j * C::NRB * 4, accum);
+            accum = 1;
+          }
+          mma_commit(bar0 + 8 * (STAGES + stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(acc_full);
+        aphase ^= 1u;
+      }
+      if (!ok) raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_MMA);
+      // every MMA issued by this thread has completed once final_bar flips
+      mma_commit(final_bar);
+      mbar_wait(final_bar, 0, kWaitLimitNs, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const float ga = *p.ga, gb = *p.gb;
+    const float s_main = (ga > 0.0f && gb > 0.0f) ? __fmul_rn(ga, gb) : 1.0f;
+    uint32_t amax = 0;
+    uint32_t aphase = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const int m0 = (tile % p.num_m) * C::BM;
+      const int n0 = (tile / p.num_m) * BN;
+      if (!mbar_wait(acc_full, aphase, kWaitLimitNs, abort_flag)) {
+        raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_EPI);
+        break;
+      }
+      tc_fence_after();
+      const int m = m0 + q * 32 + lane;
+      const bool row_ok = m < p.M;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
+        tmem_ld_wait();
+        const int n = n0 + c;
+        if (row_ok && n < p.N) {
+          float f[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[i]), s_main);
+          const size_t off = (size_t)m * p.N + n;
+          if (p.addend) {
+            const uint4* ad = reinterpret_cast<const uint4*>(p.addend + off);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float r8[8];
+              bf16x8_to_f32(ad[k], r8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) f[8 * k + i] = __fadd_rn(f[8 * k + i], r8[i]);
+            }
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+            amax = max(amax, max((w[i] & 0x7FFFu) << 16, (w[i] >> 16 & 0x7FFFu) << 16));
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.out + off);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      aphase ^= 1u;
+    }
+    if (p.out_amax) {
+      amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+      if (lane == 0 && amax) atomicMax(p.out_amax, amax);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+template <int BN, int BK, int STAGES, int RP>
+static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
+  using C = GemmCfg<BN, BK, STAGES, RP>;
+  auto kern = k_gemm_nvfp4<BN, BK, STAGES, RP>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int ntiles = L.p.num_m * L.p.num_n;
+  const int grid = ntiles < L.num_sms ? ntiles : L.num_sms;
+  kern<<<grid, 192, C::SMEM_BYTES, stream>>>(L.tmA, L.tmB, L.tmLA, L.tmLB, L.p);
+  return cudaGetLastError();
+}
+
+int gemm_block_n(int64_t N) { return (N % 256 == 0) ? 256 : 128; }
+
+cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rp, cudaStream_t stream) {
+  if (bn == 256) {
+    if (rp == 16) return launch_cfg<256, 256, 3, 16>(L, stream);
+    if (rp == 32) return launch_cfg<256, 256, 3, 32>(L, stream);
+    return launch_cfg<256, 256, 3, 64>(L, stream);
+  }
+  if (rp == 16) return launch_cfg<128, 256, 4, 16>(L, stream);
+  if (rp == 32) return launch_cfg<128, 256, 4, 32>(L, stream);
+  return launch_cfg<128, 256, 4, 64>(L, stream);
+}
+
+cudaError_t status_word_ptr(unsigned** ptr) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_pact_status);
+}
+
+}  // namespace pact

@@ -1,0 +1,81 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pact {
+
+// Device status word bits (read and cleared by pact_check_status).
+enum : unsigned {
+  PACT_DEV_TIMEOUT = 1u,
+  PACT_DEV_ROLE_TMA = 1u << 8,
+  PACT_DEV_ROLE_MMA = 1u << 9,
+  PACT_DEV_ROLE_EPI = 1u << 10,
+};
+
+struct GemmParams {
+  const uint8_t* sfa;      // A scale atoms (128x4 layout, pad4(K/16) blocks per row)
+  const uint8_t* sfb;      // B scale atoms
+  const float* ga;         // per-tensor scale of A (device)
+  const float* gb;         // per-tensor scale of B (device)
+  const uint16_t* addend;  // BF16 [M, N] added before the cast, or null (may alias out)
+  uint16_t* out;           // BF16 [M, N]
+  unsigned* out_amax;      // max |out| as FP32 bits, or null
+  unsigned* status;        // device status word
+  int M, N, K;             // out [M, N], reduction over K
+  int k16p;                // pad4(K/16)
+  int num_m, num_n;        // tile grid
+  int lora_steps;          // K=16 BF16 MMAs of the LoRA product per tile (0 = none)
+};
+
+struct GemmLaunch {
+  CUtensorMap tmA, tmB, tmLA, tmLB;
+  GemmParams p;
+  int num_sms;
+};
+
+int gemm_block_n(int64_t N);
+cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rp, cudaStream_t stream);
+cudaError_t status_word_ptr(unsigned** ptr);
+
+cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                              const float* amax_opt, uint8_t* codes, uint8_t* sf, float* g,
+                              unsigned* ws_amax, int num_sms, cudaStream_t stream);
+cudaError_t launch_pack_weight(const float* W, int64_t N, int64_t K, int backward,
+                               uint8_t* codes, uint8_t* sf, float* g, unsigned* ws_amax,
+                               int num_sms, cudaStream_t stream);
+
+// LoRA down-projections (BF16 tensor cores, FP32 accumulate), written pre-scaled
+// as the left LoRA operand [M, RP] of the fused GEMM, plus the padded right
+// operand [rows, RP].
+cudaError_t launch_lora_down_fwd(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
+                                 const float* gw, int64_t M, int64_t K, const uint16_t* A,
+                                 const uint16_t* B, int r, int rp, float scale, int64_t N,
+                                 uint16_t* t_out, uint16_t* bt_out, int num_sms,
+                                 cudaStream_t stream);
+cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const float* gw,
+                                   int64_t M, int64_t N, const uint16_t* A, const uint16_t* B,
+                                   int r, int rp, float scale, int64_t K, uint16_t* u_out,
+                                   uint16_t* ap_out, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M,
+                                 int64_t H, float eps, uint8_t* codes, uint8_t* sf, float* g,
+                                 float* rstd, unsigned* ws_amax, int num_sms,
+                                 cudaStream_t stream);
+cudaError_t launch_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I,
+                                  const float* amax3_opt, uint8_t* const codes[3],
+                                  uint8_t* const sf[3], float* const g[3], unsigned* ws_amax3,
+                                  int num_sms, cudaStream_t stream);
+cudaError_t launch_silu_mul_bwd(const uint8_t* gc, const uint8_t* gsf, const float* gg,
+                                const uint8_t* uc, const uint8_t* usf, const float* ug,
+                                const uint16_t* dh, int64_t M, int64_t I, uint16_t* dgu,
+                                unsigned* out_amax, int num_sms, cudaStream_t stream);
+cudaError_t launch_rmsnorm_bwd(const uint8_t* yc, const uint8_t* ysf, const float* yg,
+                               const uint16_t* gamma, const float* rstd, const uint16_t* dy,
+                               const uint16_t* dres, int64_t M, int64_t H, uint16_t* dx,
+                               int num_sms, cudaStream_t stream);
+cudaError_t launch_pexp(const float* x, float* y, int64_t n, cudaStream_t stream);
+
+}  // namespace pact

@@ -1,0 +1,468 @@
+// Fused nonlinear kernels around the NVFP4 projections.
+//
+// "PACT: NVFP4 Data-Flow LoRA Fine-Tuning on Consumer GPUs", Table 7:
+//   RMSNorm        forward: BF16 input, FP32 normalisation; retained: NVFP4 output
+//                  and the FP32 per-token statistic; backward: FP32 reconstruction
+//                  and reduction, BF16 gradient.
+//   SiLU-multiply  forward: BF16 gate/up inputs, FP32 arithmetic; retained:
+//                  separate NVFP4 gate/up copies; backward: FP32 reconstruction and
+//                  derivatives, BF16 gradients.
+// The abstract adds that forward nonlinear ops read BF16 (never dequantised
+// NVFP4) inputs, and that the RMSNorm output is quantised once and reused by the
+// following projections.
+//
+// Quantising a tensor needs its global amax first, so each fused quantiser runs
+// two passes: pass 1 computes the statistic/activation and its amax, pass 2
+// recomputes the FP32 values (re-reading the input, mostly from L2) and encodes.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pact {
+
+// ============================================================== RMSNorm forward
+// One warp per row.  Lane l owns blocks l, l+32, ... (BPL of them); the sum of
+// squares runs block by block, element by element, then a butterfly over the
+// lanes (offsets 16, 8, 4, 2, 1).  The same order is the oracle's.
+template <int BPL>
+__device__ __forceinline__ float row_rstd(const uint4 (*xv)[2], int nb, int lane, float H,
+                                          float eps) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int j = 0; j < BPL; ++j) {
+    if (lane + 32 * j < nb) {
+      float f[16];
+      bf16x8_to_f32(xv[j][0], f);
+      bf16x8_to_f32(xv[j][1], f + 8);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc = __fadd_rn(acc, __fmul_rn(f[i], f[i]));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1)
+    acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, off));
+  const float ms = __fdiv_rn(acc, H);
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+template <int BPL>
+__global__ void __launch_bounds__(256) k_rmsnorm_stat(const uint16_t* __restrict__ x,
+                                                      const uint16_t* __restrict__ gamma,
+                                                      int64_t M, int64_t H, float eps,
+                                                      float* __restrict__ rstd,
+                                                      unsigned* __restrict__ amax_bits) {
+  const int lane = threadIdx.x & 31;
+  const int nb = (int)(H >> 4);
+  uint32_t amax = 0;
+  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < M;
+       row += (int64_t)gridDim.x * 8) {
+    uint4 xv[BPL][2];
+    const uint16_t* xr = x + row * H;
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+      const int b = lane + 32 * j;
+      if (b < nb) {
+        const uint4* p = reinterpret_cast<const uint4*>(xr + b * 16);
+        xv[j][0] = __ldg(p);
+        xv[j][1] = __ldg(p + 1);
+      }
+    }
+    const float rs = row_rstd<BPL>(xv, nb, lane, (float)H, eps);
+    if (lane == 0) rstd[row] = rs;
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+      const int b = lane + 32 * j;
+      if (b < nb) {
+        float f[16], gm[16];
+        bf16x8_to_f32(xv[j][0], f);
+        bf16x8_to_f32(xv[j][1], f + 8);
+        const uint4* gp = reinterpret_cast<const uint4*>(gamma + b * 16);
+        bf16x8_to_f32(__ldg(gp), gm);
+        bf16x8_to_f32(__ldg(gp + 1), gm + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float y = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
+          amax = max(amax, __float_as_uint(y) & 0x7FFFFFFFu);
+        }
+      }
+    }
+  }
+  block_max_atomic(amax, amax_bits);
+}
+
+// Pass 2: y recomputed from x and the stored rstd, then encoded.  Rows are walked
+// in reverse so the tail of the tensor, last touched by pass 1, is read from L2
+// first.  Rows past M up to pad128(M) get zero scale bytes.
+template <int BPL>
+__global__ void __launch_bounds__(256) k_rmsnorm_encode(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
+    const float* __restrict__ rstd, int64_t M, int64_t Mpad, int64_t H,
+    const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ sf, float* __restrict__ g_out) {
+  const int lane = threadIdx.x & 31;
+  const int nb = (int)(H >> 4);
+  const TensorScale ts = tensor_scale(__uint_as_float(*amax_bits));
+  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
+  for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < Mpad;
+       w += (int64_t)gridDim.x * 8) {
+    const int64_t row = Mpad - 1 - w;
+    if (row >= M) {
+#pragma unroll
+      for (int j = 0; j < BPL; ++j) {
+        const int b = lane + 32 * j;
+        if (b < nb) sf[sf_offset(row, b, nb)] = 0;
+      }
+      continue;
+    }
+    const float rs = rstd[row];
+    const uint16_t* xr = x + row * H;
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+      const int b = lane + 32 * j;
+      if (b < nb) {
+        const uint4* p = reinterpret_cast<const uint4*>(xr + b * 16);
+        const uint4* gp = reinterpret_cast<const uint4*>(gamma + b * 16);
+        float f[16], gm[16];
+        bf16x8_to_f32(__ldg(p), f);
+        bf16x8_to_f32(__ldg(p + 1), f + 8);
+        bf16x8_to_f32(__ldg(gp), gm);
+        bf16x8_to_f32(__ldg(gp + 1), gm + 8);
+        uint32_t am = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          f[i] = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
+          am = max(am, __float_as_uint(f[i]) & 0x7FFFFFFFu);
+        }
+        float t, rcp;
+        const uint32_t s = block_scale(__uint_as_float(am), ts, &t, &rcp);
+        uint2 cw;
+        cw.x = encode8(f, t, rcp);
+        cw.y = encode8(f + 8, t, rcp);
+        *reinterpret_cast<uint2*>(codes + row * (H >> 1) + b * 8) = cw;
+        sf[sf_offset(row, b, nb)] = (uint8_t)s;
+      }
+    }
+  }
+}
+
+// ============================================================== SiLU-multiply
+// Pass 1: amax of h, gate and up.  One thread per block of 16 columns.
+__global__ void __launch_bounds__(256) k_silu_amax(const uint16_t* __restrict__ gu, int64_t M,
+                                                   int64_t I, unsigned* __restrict__ amax3) {
+  const int64_t bpr = I >> 4;
+  const int64_t total = M * bpr;
+  uint32_t ah = 0, ag = 0, au = 0;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = it / bpr, b = it - row * bpr;
+    const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2 * I + b * 16);
+    const uint4* up = reinterpret_cast<const uint4*>(gu + row * 2 * I + I + b * 16);
+    const uint4 g0 = ldg_stream(gp), g1 = ldg_stream(gp + 1);
+    const uint4 u0 = ldg_stream(up), u1 = ldg_stream(up + 1);
+    ag = max(ag, max(absmax_bf16x8_bits(g0), absmax_bf16x8_bits(g1)));
+    au = max(au, max(absmax_bf16x8_bits(u0), absmax_bf16x8_bits(u1)));
+    float gf[16], uf[16];
+    bf16x8_to_f32(g0, gf);
+    bf16x8_to_f32(g1, gf + 8);
+    bf16x8_to_f32(u0, uf);
+    bf16x8_to_f32(u1, uf + 8);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ah = max(ah, __float_as_uint(silu_mul(gf[i], uf[i])) & 0x7FFFFFFFu);
+  }
+  block_max_atomic(ah, amax3 + 0);
+  block_max_atomic(ag, amax3 + 1);
+  block_max_atomic(au, amax3 + 2);
+}
+
+// Pass 2: one thread per block of 16 columns of one row; encodes h, gate and up.
+struct SiluOut {
+  uint8_t* codes[3];
+  uint8_t* sf[3];
+  float* g[3];
+};
+
+__global__ void __launch_bounds__(256) k_silu_encode(const uint16_t* __restrict__ gu, int64_t M,
+                                                     int64_t Mpad, int64_t I,
+                                                     const float* __restrict__ amax3_opt,
+                                                     const unsigned* __restrict__ amax3,
+                                                     SiluOut out) {
+  TensorScale ts[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    ts[k] = tensor_scale(amax3_opt ? amax3_opt[k] : __uint_as_float(amax3[k]));
+    if (blockIdx.x == 0 && threadIdx.x == 0) *out.g[k] = ts[k].g;
+  }
+  const int64_t bpr = I >> 4;
+  const int64_t total = Mpad * bpr;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = it / bpr, b = it - row * bpr;
+    const int64_t so = sf_offset(row, b, bpr);
+    if (row >= M) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k) out.sf[k][so] = 0;
+      continue;
+    }
+    const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2 * I + b * 16);
+    const uint4* up = reinterpret_cast<const uint4*>(gu + row * 2 * I + I + b * 16);
+    float v[3][16];
+    bf16x8_to_f32(ldg_stream(gp), v[1]);
+    bf16x8_to_f32(ldg_stream(gp + 1), v[1] + 8);
+    bf16x8_to_f32(ldg_stream(up), v[2]);
+    bf16x8_to_f32(ldg_stream(up + 1), v[2] + 8);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[0][i] = silu_mul(v[1][i], v[2][i]);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      uint32_t am = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) am = max(am, __float_as_uint(v[k][i]) & 0x7FFFFFFFu);
+      float t, rcp;
+      const uint32_t s = block_scale(__uint_as_float(am), ts[k], &t, &rcp);
+      uint2 cw;
+      cw.x = encode8(v[k], t, rcp);
+      cw.y = encode8(v[k] + 8, t, rcp);
+      *reinterpret_cast<uint2*>(out.codes[k] + row * (I >> 1) + b * 8) = cw;
+      out.sf[k][so] = (uint8_t)s;
+    }
+  }
+}
+
+// ============================================================== backward kernels
+// Dequantise one block of 16 (codes: 8 bytes) in FP32.
+__device__ __forceinline__ void dequant16(uint2 cw, uint32_t sfb, float g, float* out) {
+  const float s = __fmul_rn(e4m3_to_f32(sfb), g);
+  const uint32_t w[2] = {cw.x, cw.y};
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t q = (w[h] >> (4 * i)) & 0xFu;
+      // magnitudes {0, .5, 1, 1.5} = i/2 for i < 4; {2, 3, 4, 6} = 2^(i/2-1) * (1 or 1.5)
+      const uint32_t i7 = q & 7u;
+      const float mag = i7 < 4u ? 0.5f * (float)i7
+                                : (float)(1u << ((i7 >> 1) - 1u)) * ((i7 & 1u) ? 1.5f : 1.0f);
+      out[8 * h + i] = __fmul_rn((q & 8u) ? -mag : mag, s);
+    }
+}
+
+// SiLU-multiply backward; one thread per block of 16 columns.
+__global__ void __launch_bounds__(256) k_silu_bwd(
+    const uint8_t* __restrict__ gc, const uint8_t* __restrict__ gsf, const float* __restrict__ gg,
+    const uint8_t* __restrict__ uc, const uint8_t* __restrict__ usf, const float* __restrict__ ug,
+    const uint16_t* __restrict__ dh, int64_t M, int64_t I, uint16_t* __restrict__ dgu,
+    unsigned* __restrict__ out_amax) {
+  const int64_t bpr = I >> 4;
+  const int64_t total = M * bpr;
+  const float g_gate = *gg, g_up = *ug;
+  uint32_t amax = 0;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = it / bpr, b = it - row * bpr;
+    const int64_t so = sf_offset(row, b, bpr);
+    float gv[16], uv[16], d[16];
+    dequant16(*reinterpret_cast<const uint2*>(gc + row * (I >> 1) + b * 8), gsf[so], g_gate, gv);
+    dequant16(*reinterpret_cast<const uint2*>(uc + row * (I >> 1) + b * 8), usf[so], g_up, uv);
+    const uint4* dp = reinterpret_cast<const uint4*>(dh + row * I + b * 16);
+    bf16x8_to_f32(ldg_stream(dp), d);
+    bf16x8_to_f32(ldg_stream(dp + 1), d + 8);
+    uint32_t og[8], ou[8];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      float rg[2], ru[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float gk = gv[i + k], uk = uv[i + k], dk = d[i + k];
+        const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, pexp(-gk)));
+        const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gk, __fsub_rn(1.0f, sg))));
+        rg[k] = __fmul_rn(__fmul_rn(dk, uk), dsilu);
+        ru[k] = __fmul_rn(dk, __fmul_rn(gk, sg));
+      }
+      og[i / 2] = pack_bf16x2(rg[0], rg[1]);
+      ou[i / 2] = pack_bf16x2(ru[0], ru[1]);
+      amax = max(amax, max(max((og[i / 2] & 0x7FFFu) << 16, (og[i / 2] >> 16 & 0x7FFFu) << 16),
+                           max((ou[i / 2] & 0x7FFFu) << 16, (ou[i / 2] >> 16 & 0x7FFFu) << 16)));
+    }
+    uint4* pg = reinterpret_cast<uint4*>(dgu + row * 2 * I + b * 16);
+    uint4* pu = reinterpret_cast<uint4*>(dgu + row * 2 * I + I + b * 16);
+    pg[0] = make_uint4(og[0], og[1], og[2], og[3]);
+    pg[1] = make_uint4(og[4], og[5], og[6], og[7]);
+    pu[0] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+    pu[1] = make_uint4(ou[4], ou[5], ou[6], ou[7]);
+  }
+  if (out_amax) block_max_atomic(amax, out_amax);
+}
+
+// RMSNorm backward; one warp per row, lane l owns blocks l, l+32, ...
+// n = yhat / gamma, dn = dy * gamma, c = sum(dn * n) / H, dx = rstd (dn - n c) [+ dres].
+template <int BPL>
+__global__ void __launch_bounds__(256) k_rmsnorm_bwd(
+    const uint8_t* __restrict__ yc, const uint8_t* __restrict__ ysf, const float* __restrict__ yg,
+    const uint16_t* __restrict__ gamma, const float* __restrict__ rstd,
+    const uint16_t* __restrict__ dy, const uint16_t* dres, int64_t M, int64_t H,
+    uint16_t* dx) {
+  const int lane = threadIdx.x & 31;
+  const int nb = (int)(H >> 4);
+  const float g = *yg;
+  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < M;
+       row += (int64_t)gridDim.x * 8) {
+    float dot = 0.0f;
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+      const int b = lane + 32 * j;
+      if (b < nb) {
+        float yv[16], gm[16], d[16];
+        dequant16(*reinterpret_cast<const uint2*>(yc + row * (H >> 1) + b * 8),
+                  ysf[sf_offset(row, b, nb)], g, yv);
+        const uint4* gp = reinterpret_cast<const uint4*>(gamma + b * 16);
+        bf16x8_to_f32(__ldg(gp), gm);
+        bf16x8_to_f32(__ldg(gp + 1), gm + 8);
+        const uint4* dp = reinterpret_cast<const uint4*>(dy + row * H + b * 16);
+        bf16x8_to_f32(__ldg(dp), d);
+        bf16x8_to_f32(__ldg(dp + 1), d + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dot += (d[i] * gm[i]) * (yv[i] / gm[i]);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
+    const float c = dot / (float)H;
+    const float rs = rstd[row];
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+      const int b = lane + 32 * j;
+      if (b < nb) {
+        float yv[16], gm[16], d[16], r[16];
+        dequant16(*reinterpret_cast<const uint2*>(yc + row * (H >> 1) + b * 8),
+                  ysf[sf_offset(row, b, nb)], g, yv);
+        const uint4* gp = reinterpret_cast<const uint4*>(gamma + b * 16);
+        bf16x8_to_f32(__ldg(gp), gm);
+        bf16x8_to_f32(__ldg(gp + 1), gm + 8);
+        const uint4* dp = reinterpret_cast<const uint4*>(dy + row * H + b * 16);
+        bf16x8_to_f32(__ldg(dp), d);
+        bf16x8_to_f32(__ldg(dp + 1), d + 8);
+        if (dres) {
+          const uint4* rp = reinterpret_cast<const uint4*>(dres + row * H + b * 16);
+          bf16x8_to_f32(rp[0], r);
+          bf16x8_to_f32(rp[1], r + 8);
+        }
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          float v[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const float n = yv[i + k] / gm[i + k];
+            const float dn = d[i + k] * gm[i + k];
+            v[k] = rs * (dn - n * c);
+            if (dres) v[k] += r[i + k];
+          }
+          o[i / 2] = pack_bf16x2(v[0], v[1]);
+        }
+        uint4* op = reinterpret_cast<uint4*>(dx + row * H + b * 16);
+        op[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        op[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  }
+}
+
+__global__ void k_pexp(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    y[i] = pexp(x[i]);
+}
+
+// ============================================================== launchers
+static int blocks_for(int64_t work, int threads, int cap) {
+  int64_t b = (work + threads - 1) / threads;
+  return (int)(b < 1 ? 1 : (b > cap ? cap : b));
+}
+
+template <typename F>
+static cudaError_t dispatch_bpl(int64_t H, F&& f) {
+  const int bpl = (int)(((H >> 4) + 31) / 32);
+  switch (bpl) {
+    case 1: return f(std::integral_constant<int, 1>());
+    case 2: return f(std::integral_constant<int, 2>());
+    case 3: return f(std::integral_constant<int, 3>());
+    case 4: return f(std::integral_constant<int, 4>());
+    case 5: case 6: return f(std::integral_constant<int, 6>());
+    case 7: case 8: return f(std::integral_constant<int, 8>());
+    case 9: case 10: case 11: case 12: return f(std::integral_constant<int, 12>());
+    case 13: case 14: case 15: case 16: return f(std::integral_constant<int, 16>());
+    case 17: case 18: case 19: case 20: case 21: case 22: case 23: case 24:
+      return f(std::integral_constant<int, 24>());
+    default: return f(std::integral_constant<int, 32>());
+  }
+}
+
+cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M,
+                                 int64_t H, float eps, uint8_t* codes, uint8_t* sf, float* g,
+                                 float* rstd, unsigned* ws_amax, int num_sms,
+                                 cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(ws_amax, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  const int64_t Mpad = pad_to(M, 128);
+  return dispatch_bpl(H, [&](auto bpl) {
+    constexpr int BPL = decltype(bpl)::value;
+    k_rmsnorm_stat<BPL><<<blocks_for(M, 8, num_sms * 8), 256, 0, stream>>>(x, gamma, M, H, eps,
+                                                                            rstd, ws_amax);
+    k_rmsnorm_encode<BPL><<<blocks_for(Mpad, 8, num_sms * 8), 256, 0, stream>>>(
+        x, gamma, rstd, M, Mpad, H, ws_amax, codes, sf, g);
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I,
+                                  const float* amax3_opt, uint8_t* const codes[3],
+                                  uint8_t* const sf[3], float* const g[3], unsigned* ws_amax3,
+                                  int num_sms, cudaStream_t stream) {
+  if (!amax3_opt) {
+    cudaError_t e = cudaMemsetAsync(ws_amax3, 0, 3 * sizeof(unsigned), stream);
+    if (e != cudaSuccess) return e;
+    k_silu_amax<<<blocks_for(M * (I / 16), 256, num_sms * 8), 256, 0, stream>>>(gateup, M, I,
+                                                                                 ws_amax3);
+  }
+  SiluOut o;
+  for (int k = 0; k < 3; ++k) {
+    o.codes[k] = codes[k];
+    o.sf[k] = sf[k];
+    o.g[k] = g[k];
+  }
+  const int64_t Mpad = pad_to(M, 128);
+  k_silu_encode<<<blocks_for(Mpad * (I / 16), 256, num_sms * 16), 256, 0, stream>>>(
+      gateup, M, Mpad, I, amax3_opt, ws_amax3, o);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul_bwd(const uint8_t* gc, const uint8_t* gsf, const float* gg,
+                                const uint8_t* uc, const uint8_t* usf, const float* ug,
+                                const uint16_t* dh, int64_t M, int64_t I, uint16_t* dgu,
+                                unsigned* out_amax, int num_sms, cudaStream_t stream) {
+  if (out_amax) {
+    cudaError_t e = cudaMemsetAsync(out_amax, 0, sizeof(unsigned), stream);
+    if (e != cudaSuccess) return e;
+  }
+  k_silu_bwd<<<blocks_for(M * (I / 16), 256, num_sms * 16), 256, 0, stream>>>(
+      gc, gsf, gg, uc, usf, ug, dh, M, I, dgu, out_amax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_bwd(const uint8_t* yc, const uint8_t* ysf, const float* yg,
+                               const uint16_t* gamma, const float* rstd, const uint16_t* dy,
+                               const uint16_t* dres, int64_t M, int64_t H, uint16_t* dx,
+                               int num_sms, cudaStream_t stream) {
+  return dispatch_bpl(H, [&](auto bpl) {
+    constexpr int BPL = decltype(bpl)::value;
+    k_rmsnorm_bwd<BPL><<<blocks_for(M, 8, num_sms * 8), 256, 0, stream>>>(
+        yc, ysf, yg, gamma, rstd, dy, dres, M, H, dx);
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_pexp(const float* x, float* y, int64_t n, cudaStream_t stream) {
+  k_pexp<<<blocks_for(n, 256, 4096), 256, 0, stream>>>(x, y, n);
+  return cudaGetLastError();
+}
+
+}  // namespace pact

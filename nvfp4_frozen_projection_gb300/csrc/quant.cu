@@ -1,0 +1,194 @@
+// Activation quantisation and frozen-weight packing to NVFP4.
+//
+// "PACT: NVFP4 Data-Flow LoRA Fine-Tuning on Consumer GPUs", Table 6 (format) and
+// Table 7 (NVFP4 GEMM operands; cached forward and backward weight layouts).
+//
+// Both operations are HBM-bound and two-pass: the per-tensor scale g = amax/2688
+// must be known before the first code is written, so pass 1 reduces amax into a
+// device word and pass 2 re-reads the tensor (mostly from L2) and encodes it.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pact {
+
+// ---------------------------------------------------------------- pass 1: amax
+// max |x| over BF16 [M, K] (row stride ldx elements), folded into *amax_bits.
+__global__ void __launch_bounds__(256) k_amax_bf16(const uint16_t* __restrict__ x, int64_t M,
+                                                   int64_t K, int64_t ldx,
+                                                   unsigned* __restrict__ amax_bits) {
+  const int64_t vpr = K >> 3;  // 16-byte vectors per row
+  const int64_t total = M * vpr;
+  uint32_t m = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (ldx == K) {
+    const uint4* p = reinterpret_cast<const uint4*>(x);
+    for (; v + 3 * stride < total; v += 4 * stride) {
+      uint4 a = ldg_stream(p + v), b = ldg_stream(p + v + stride);
+      uint4 c = ldg_stream(p + v + 2 * stride), d = ldg_stream(p + v + 3 * stride);
+      m = max(m, max(max(absmax_bf16x8_bits(a), absmax_bf16x8_bits(b)),
+                     max(absmax_bf16x8_bits(c), absmax_bf16x8_bits(d))));
+    }
+    for (; v < total; v += stride) m = max(m, absmax_bf16x8_bits(ldg_stream(p + v)));
+  } else {
+    for (; v < total; v += stride) {
+      int64_t r = v / vpr, c = v - r * vpr;
+      m = max(m, absmax_bf16x8_bits(ldg_stream(x + r * ldx + c * 8)));
+    }
+  }
+  block_max_atomic(m, amax_bits);
+}
+
+// max |W| over FP32 [n] (contiguous), folded into *amax_bits.
+__global__ void __launch_bounds__(256) k_amax_f32(const float* __restrict__ w, int64_t n,
+                                                  unsigned* __restrict__ amax_bits) {
+  const int64_t nv = n >> 2;
+  uint32_t m = 0;
+  const uint4* p = reinterpret_cast<const uint4*>(w);
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nv;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    uint4 a = ldg_stream(p + v);
+    m = max(m, max(max(a.x & 0x7FFFFFFFu, a.y & 0x7FFFFFFFu),
+                   max(a.z & 0x7FFFFFFFu, a.w & 0x7FFFFFFFu)));
+  }
+  block_max_atomic(m, amax_bits);
+}
+
+// ---------------------------------------------------------------- pass 2: encode
+// One thread encodes 64 consecutive elements (4 blocks) of one row: 128 bytes in,
+// 32 code bytes and one 4-byte scale word out.  Threads past row M (up to
+// pad128(M)) write zero scale words so the padded scale array is fully defined.
+__global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__ x, int64_t M,
+                                                    int64_t K, int64_t ldx, int64_t Mpad,
+                                                    const float* __restrict__ amax_opt,
+                                                    const unsigned* __restrict__ amax_bits,
+                                                    uint8_t* __restrict__ codes,
+                                                    uint8_t* __restrict__ sf,
+                                                    float* __restrict__ g_out) {
+  const float amax = amax_opt ? *amax_opt : __uint_as_float(*amax_bits);
+  const TensorScale ts = tensor_scale(amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
+  const int64_t chunks = K >> 6;
+  const int64_t total = Mpad * chunks;
+  const int64_t c16p = K >> 4;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = it / chunks, ch = it - r * chunks;
+    uint32_t sfw = 0;
+    if (r < M) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + r * ldx + ch * 64);
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = ldg_stream(src + i);
+      uint32_t w[8];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        float f[16];
+        bf16x8_to_f32(v[2 * b], f);
+        bf16x8_to_f32(v[2 * b + 1], f + 8);
+        float amax_blk = __uint_as_float(
+            max(absmax_bf16x8_bits(v[2 * b]), absmax_bf16x8_bits(v[2 * b + 1])));
+        float t, rcp;
+        uint32_t s = block_scale(amax_blk, ts, &t, &rcp);
+        w[2 * b] = encode8(f, t, rcp);
+        w[2 * b + 1] = encode8(f + 8, t, rcp);
+        sfw |= s << (8 * b);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(codes + r * (K >> 1) + ch * 32);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    *reinterpret_cast<uint32_t*>(sf + sf_offset(r, ch * 4, c16p)) = sfw;
+  }
+}
+
+// ---------------------------------------------------------------- weight pack
+// One warp per 16x16 tile of W [N, K]: the tile's amax gives one E4M3 scale shared
+// by the forward layout ([N, K], blocks along K) and the backward layout ([K, N],
+// blocks along N), so both hold the same effective weights.
+// Lane l handles tile row l/2, columns 8*(l%2) .. +8.
+__global__ void __launch_bounds__(256) k_pack_weight(const float* __restrict__ W, int64_t N,
+                                                     int64_t K,
+                                                     const unsigned* __restrict__ amax_bits,
+                                                     int backward, uint8_t* __restrict__ codes,
+                                                     uint8_t* __restrict__ sf,
+                                                     float* __restrict__ g_out) {
+  __shared__ uint8_t nib[8][16][17];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const TensorScale ts = tensor_scale(__uint_as_float(*amax_bits));
+  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
+  const int64_t tiles_k = K >> 4;
+  const int64_t ntiles = (N >> 4) * tiles_k;
+  const int i = lane >> 1, h = lane & 1;
+  for (int64_t tile = (int64_t)blockIdx.x * 8 + warp; tile < ntiles;
+       tile += (int64_t)gridDim.x * 8) {
+    const int64_t tn = tile / tiles_k, tk = tile - tn * tiles_k;
+    const float4* src = reinterpret_cast<const float4*>(W + (tn * 16 + i) * K + tk * 16 + 8 * h);
+    float4 a = __ldg(src), b = __ldg(src + 1);
+    float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = max(m, __float_as_uint(f[j]) & 0x7FFFFFFFu);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    float t, rcp;
+    const uint32_t s = block_scale(__uint_as_float(m), ts, &t, &rcp);
+    const uint32_t w = encode8(f, t, rcp);
+    if (!backward) {
+      const int64_t n = tn * 16 + i;
+      *reinterpret_cast<uint32_t*>(codes + n * (K >> 1) + tk * 8 + 4 * h) = w;
+      if (h == 0) sf[sf_offset(n, tk, K >> 4)] = (uint8_t)s;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) nib[warp][i][8 * h + j] = (uint8_t)((w >> (4 * j)) & 0xFu);
+      __syncwarp();
+      // lane now handles backward row k = tk*16 + i, columns n = tn*16 + 8h .. +8
+      uint32_t o = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o |= (uint32_t)nib[warp][8 * h + j][i] << (4 * j);
+      const int64_t k = tk * 16 + i;
+      *reinterpret_cast<uint32_t*>(codes + k * (N >> 1) + tn * 8 + 4 * h) = o;
+      if (h == 0) sf[sf_offset(k, tn, N >> 4)] = (uint8_t)s;
+      __syncwarp();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+static int grid_for(int64_t work, int threads, int max_blocks) {
+  int64_t b = (work + threads - 1) / threads;
+  if (b > max_blocks) b = max_blocks;
+  if (b < 1) b = 1;
+  return (int)b;
+}
+
+cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                              const float* amax_opt, uint8_t* codes, uint8_t* sf, float* g,
+                              unsigned* ws_amax, int num_sms, cudaStream_t stream) {
+  if (!amax_opt) {
+    cudaError_t e = cudaMemsetAsync(ws_amax, 0, sizeof(unsigned), stream);
+    if (e != cudaSuccess) return e;
+    k_amax_bf16<<<grid_for(M * K / 8, 256, num_sms * 8), 256, 0, stream>>>(x, M, K, ldx,
+                                                                            ws_amax);
+  }
+  const int64_t Mpad = pad_to(M, 128);
+  k_quant_bf16<<<grid_for(Mpad * (K / 64), 256, num_sms * 16), 256, 0, stream>>>(
+      x, M, K, ldx, Mpad, amax_opt, ws_amax, codes, sf, g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weight(const float* W, int64_t N, int64_t K, int backward,
+                               uint8_t* codes, uint8_t* sf, float* g, unsigned* ws_amax,
+                               int num_sms, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(ws_amax, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  const int64_t rows = backward ? K : N, cols = backward ? N : K;
+  e = cudaMemsetAsync(sf, 0, (size_t)(pad_to(rows, 128) * pad_to(cols / 16, 4)), stream);
+  if (e != cudaSuccess) return e;
+  k_amax_f32<<<grid_for(N * K / 4, 256, num_sms * 8), 256, 0, stream>>>(W, N * K, ws_amax);
+  const int64_t ntiles = (N / 16) * (K / 16);
+  k_pack_weight<<<grid_for(ntiles * 32, 256, num_sms * 16), 256, 0, stream>>>(
+      W, N, K, ws_amax, backward, codes, sf, g);
+  return cudaGetLastError();
+}
+
+}  // namespace pact
