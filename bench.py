@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 LoRA-linear hot path on one GB300 (or N replicas).
+
+One step = one forward + input-gradient pass of the Llama-3B-shaped decoder-layer
+projection stack (workload "layer-3b": M = 8 x 1024 tokens, hidden 3072,
+q/k/v/o 3072 -> 3072/1024/1024/3072, gate|up 3072 -> 2 x 8192, down 8192 -> 3072,
+r = 16 LoRA on every projection): both fused RMSNorm -> NVFP4 quantisers, every
+activation/gradient quantisation, the fused SiLU-multiply -> NVFP4, the 14 NVFP4
+GEMMs with fused LoRA branches, and the RMSNorm and SiLU-multiply backward
+kernels.  The attention core and its backward are replaced by seeded tensors.
+
+metric = NVFP4 frozen-projection GEMM FLOPs (2*M*N*K over the 14 GEMMs) divided by
+the wall time of the whole step (all kernels), in TFLOP/s.  Also reported:
+layer tokens/s, the quantiser's GB/s, and each GEMM kernel's own TFLOP/s.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch one process per GPU with torch.distributed.run; the path has no
+exchange step, so the ranks are independent replicas (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+# the oracle's BLAS may use every host core for the CPU baseline
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_frozen_projection_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "NVFP4 LoRA-linear fwd+dgrad TFLOPS (% FP4 peak); quant GB/s; layer tokens/s"
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [s.strip() for s in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.remove(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------------- oracle leg
+def oracle_stack_sample(d, packs, rows: int):
+    """The oracle run over the first `rows` tokens of the layer-3b step (same call
+    sequence as the GPU step; activations rounded to BF16 where the GPU stores
+    BF16).  Returns the GEMM FLOPs of the sample."""
+    import oracle as orc
+    b = wl.bf16_round
+    sl = slice(0, rows)
+    x, attn, dy = d["x"][sl], d["attn"][sl], d["dy"][sl]
+    dq, dk, dv = d["dq"][sl], d["dk"][sl], d["dv"][sl]
+    P = {k: d[k] for k in ("q", "k", "v", "o", "gate_up", "down")}
+
+    def fwd(name, xq, residual=None):
+        p = P[name]
+        return orc.lora_linear_fwd(xq, packs[name][0], p.A, p.B, p.alpha, residual=residual)
+
+    def dgrad(name, gq, g, prev=None):
+        p = P[name]
+        return orc.lora_linear_dgrad(gq, g, packs[name][1], p.A, p.B, p.alpha, dx_prev=prev)
+
+    xq1, rstd1 = orc.rmsnorm_quant(x, d["gamma1"], d["eps"])
+    for n in ("q", "k", "v"):
+        fwd(n, xq1)
+    h1 = b(fwd("o", orc.quantize(attn), residual=x))
+    xq2, rstd2 = orc.rmsnorm_quant(h1, d["gamma2"], d["eps"])
+    gu = b(fwd("gate_up", xq2))
+    hq, gq, uq = orc.silu_mul_quant(gu)
+    fwd("down", hq, residual=h1)
+    dh = b(dgrad("down", orc.quantize(dy), dy))
+    dgu = b(orc.silu_mul_bwd(gq, uq, dh))
+    dxn2 = b(dgrad("gate_up", orc.quantize(dgu), dgu))
+    dh1 = b(orc.rmsnorm_bwd(xq2, d["gamma2"], rstd2, dxn2, dres=dy))
+    dgrad("o", orc.quantize(dh1), dh1)
+    dxn1 = b(dgrad("q", orc.quantize(dq), dq))
+    dxn1 = b(dgrad("k", orc.quantize(dk), dk, dxn1))
+    dxn1 = b(dgrad("v", orc.quantize(dv), dv, dxn1))
+    orc.rmsnorm_bwd(xq1, d["gamma1"], rstd1, dxn1, dres=dh1)
+    return wl.gemm_flops_per_step(5, m=rows)
+
+
+def oracle_packs(d):
+    import oracle as orc
+    return {k: orc.pack_weight(d[k].W) for k in ("q", "k", "v", "o", "gate_up", "down")}
+
+
+def cpu_baseline(d, rows=128, target_s=10.0):
+    """Time the oracle (as it stands) on a bounded sample of the step."""
+    packs = oracle_packs(d)
+    oracle_stack_sample(d, packs, 16)  # warm caches / lazy loads
+    n, t = 0, 0.0
+    flops = 0.0
+    t0 = time.perf_counter()
+    while t < target_s or n == 0:
+        flops += oracle_stack_sample(d, packs, rows)
+        n += 1
+        t = time.perf_counter() - t0
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"first {rows} tokens of the layer-3b step (fwd+dgrad chain, 14 FP64 "
+                      f"GEMMs on exactly dequantised operands), {n} pass(es) in {t:.1f} s; "
+                      "weight packs excluded (offline, as on the GPU)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    d = wl.layer3b()
+    packs = oracle_packs(d)
+    rows = 64
+    for _ in range(args.warmup):
+        oracle_stack_sample(d, packs, rows)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += oracle_stack_sample(d, packs, rows)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "layer-3b", "tokens_per_step": rows, "hidden": 3072,
+                   "intermediate": 8192, "r": 16},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"each step: first {rows} tokens of the layer-3b step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------- GPU leg
+def build_stack(d, dev):
+    import nvfp4_frozen_projection_gb300 as pk
+    from nvfp4_frozen_projection_gb300.stack import DecoderProjectionStack, LoraLinear
+
+    def t32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+
+    proj = {}
+    for k in ("q", "k", "v", "o", "gate_up", "down"):
+        p = d[k]
+        proj[k] = LoraLinear(t32(p.W), t32(p.A).bfloat16(), t32(p.B).bfloat16(), p.scale)
+    stack = DecoderProjectionStack(d["x"].shape[0], proj, t32(d["gamma1"]).bfloat16(),
+                                   t32(d["gamma2"]).bfloat16(), float(d["eps"]))
+    torch.cuda.synchronize()
+    pk.pact_check_status()
+    return stack
+
+
+def time_gemm_kernels(stack, inputs, reps):
+    """Per-GEMM kernel time (CUDA events around the GEMM kernel alone, on the launch
+    stream), averaged over reps eager calls."""
+    import nvfp4_frozen_projection_gb300 as pk
+    x, attn, dy, dq, dk, dv = inputs
+    stack.forward(x, attn)
+    stack.backward(dy, dq, dk, dv)
+    calls = {
+        "q.fwd": lambda: stack.p["q"].forward(stack.xq1, stack.q),
+        "k.fwd": lambda: stack.p["k"].forward(stack.xq1, stack.k),
+        "o.fwd": lambda: stack.p["o"].forward(stack.attnq, stack.h1, residual=x),
+        "gate_up.fwd": lambda: stack.p["gate_up"].forward(stack.xq2, stack.gu),
+        "down.fwd": lambda: stack.p["down"].forward(stack.hq, stack.out, residual=stack.h1),
+        "down.dgrad": lambda: stack.p["down"].dgrad(stack.dyq, dy, stack.dh),
+        "gate_up.dgrad": lambda: stack.p["gate_up"].dgrad(stack.dguq, stack.dgu, stack.dxn2),
+        "q.dgrad": lambda: stack.p["q"].dgrad(stack.dqq, dq, stack.dxn1),
+        "k.dgrad": lambda: stack.p["k"].dgrad(stack.dkq, dk, stack.dxn1, accumulate=True),
+    }
+    m = stack.m
+    flops = {"q.fwd": (3072, 3072), "k.fwd": (1024, 3072), "o.fwd": (3072, 3072),
+             "gate_up.fwd": (16384, 3072), "down.fwd": (3072, 8192), "down.dgrad": (8192, 3072),
+             "gate_up.dgrad": (3072, 16384), "q.dgrad": (3072, 3072), "k.dgrad": (3072, 1024)}
+    out = {}
+    for name, fn in calls.items():
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        fn()
+        for b, e in evs:
+            pk.pact_profile_next_gemm(b, e)
+            fn()
+        torch.cuda.synchronize()
+        ms = statistics.mean(b.elapsed_time(e) for b, e in evs)
+        n_, k_ = flops[name]
+        f = 2.0 * m * n_ * k_
+        out[name] = {"ms": ms, "tflops": f / (ms * 1e-3) / 1e12, "flops": f}
+    return out
+
+
+def time_call(fn, reps):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    fn()
+    for b, e in evs:
+        b.record()
+        fn()
+        e.record()
+    torch.cuda.synchronize()
+    return statistics.mean(b.elapsed_time(e) for b, e in evs)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-graph", action="store_true", help="replay the step eagerly")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from nvfp4_frozen_projection_gb300 import build as pkbuild
+    pkbuild.build()
+    import nvfp4_frozen_projection_gb300 as pk
+    if not pk.pact_device_supported():
+        raise RuntimeError(pk.load_library().pact_last_error().decode())
+
+    d = wl.layer3b()
+    stack = build_stack(d, dev)
+    names = ("x", "attn", "dy", "dq", "dk", "dv")
+    host_in = [torch.from_numpy(np.ascontiguousarray(d[n], np.float32)).bfloat16().pin_memory()
+               for n in names]
+    inputs = [h.to(dev) for h in host_in]
+    x, attn, dy, dq, dk, dv = inputs
+
+    def step():
+        stack.forward(x, attn)
+        stack.backward(dy, dq, dk, dv)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    pk.pact_check_status()
+
+    graph = None
+    n0 = pk.pact_launch_count()
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        launches_per_step = pk.pact_launch_count() - n0
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        run = graph.replay
+    else:
+        step()
+        launches_per_step = pk.pact_launch_count() - n0
+        run = step
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---------------- timed region: K steps, inputs resident in HBM
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_begin.record()
+        for _ in range(args.steps):
+            run()
+        t_end.record()
+        torch.cuda.synchronize()
+    barrier()
+    ms = t_begin.elapsed_time(t_end) / args.steps
+    clocks = clk.summary()
+    pk.pact_check_status()
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    flops = stack.gemm_flops()
+    value = flops * world / (ms * 1e-3) / 1e12
+    tokens_per_s = stack.m * world / (ms * 1e-3)
+
+    # ---------------- end to end: pinned host inputs in, result (dx) out, per step
+    host_out = torch.empty_like(stack.dx, device="cpu").pin_memory()
+    barrier()
+    torch.cuda.synchronize()
+    e_begin, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_begin.record()
+    for _ in range(args.steps):
+        for h, dvc in zip(host_in, inputs):
+            dvc.copy_(h, non_blocking=True)
+        run()
+        host_out.copy_(stack.dx, non_blocking=True)
+    e_end.record()
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e_begin.elapsed_time(e_end) / args.steps
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    # ---------------- per-kernel live timing (GEMM kernels alone; quantiser)
+    kern = time_gemm_kernels(stack, inputs, reps=max(5, args.steps // 2))
+    P, src = peaks()
+    fp4_peak = P["bf16_tflops"] * FP4_OVER_BF16
+    step_share = {k: v["ms"] for k, v in kern.items()}
+    dominant = max(step_share, key=step_share.get)
+    dk_ = kern[dominant]
+    m, hid = stack.m, stack.hidden
+    q_ms = time_call(lambda: pk.pact_quant_nvfp4(dy, out=stack.dyq), reps=10)
+    q_bytes = m * hid * (2 + 0.5 + 1 / 16)
+    r_ms = time_call(lambda: pk.pact_rmsnorm_quant(x, stack.gamma1, stack.eps, out=stack.xq1,
+                                                   rstd=stack.rstd1), reps=10)
+    r_bytes = m * hid * (2 + 0.5 + 1 / 16) + 4 * m
+    s_ms = time_call(lambda: pk.pact_silu_mul_quant(stack.gu, outs=(stack.hq, stack.gq, stack.uq)),
+                     reps=10)
+    s_bytes = m * stack.inter * (4 + 3 * (0.5 + 1 / 16))
+    pk.pact_check_status()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4", "data": "synthetic",
+        "config": {"workload": "layer-3b", "tokens_per_step": m, "hidden": hid,
+                   "intermediate": stack.inter, "q_kv_o": [3072, 1024, 1024, 3072], "r": 16,
+                   "gemms_per_step": 14, "gemm_flops_per_step": flops,
+                   "l2": "no flush: one step moves several GB through HBM (L2 is 129 MB)",
+                   "graph": graph is not None, "parallelism": f"replicas x{world}"},
+        "clocks": clocks,
+        "e2e": {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": int(launches_per_step) * args.steps,
+        "layer_tokens_per_s": tokens_per_s,
+        "fp4_peak_frac_step": value / world / fp4_peak,
+        "roofline": {"bound": "tensor", "kernel": f"k_gemm_nvfp4 ({dominant})",
+                     "achieved": dk_["tflops"], "peak": fp4_peak, "unit": "TFLOP/s",
+                     "frac": dk_["tflops"] / fp4_peak, "traffic": None,
+                     "peak_source": f"{src} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
+        "gemm_kernels": {k: {"ms": round(v["ms"], 5), "tflops": round(v["tflops"], 1)}
+                         for k, v in kern.items()},
+        "memory_kernels": {
+            "quant_nvfp4 8192x3072": {"ms": q_ms, "gbs": q_bytes / (q_ms * 1e-3) / 1e9},
+            "rmsnorm_quant 8192x3072": {"ms": r_ms, "gbs": r_bytes / (r_ms * 1e-3) / 1e9},
+            "silu_mul_quant 8192x2x8192": {"ms": s_ms, "gbs": s_bytes / (s_ms * 1e-3) / 1e9},
+            "hbm_peak_gbs": P["hbm_gbs"]},
+        "quant_gbs": q_bytes / (q_ms * 1e-3) / 1e9,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(d)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -216,6 +216,19 @@ int pact_rmsnorm_bwd(const pact_nvfp4* yq, const uint16_t* gamma, const float* r
  */
 int pact_test_pexp(const float* x, float* y, int64_t n, pact_stream_t stream);
 
+/*
+ * Measurement hooks (no counterpart in the method; host-side bookkeeping only).
+ * pact_launch_count: number of libpact kernels launched by this process so far
+ *   (launches replayed from a captured CUDA graph are not counted again).
+ * pact_profile_next_gemm: arm a one-shot recording of two caller-created CUDA
+ *   events (cudaEvent_t, passed as void*) on the launch stream immediately before
+ *   and after the next NVFP4 GEMM kernel launched by this host thread, so that
+ *   the kernel can be timed without the LoRA down-projection launched beside it.
+ *   Pass NULLs to disarm.
+ */
+uint64_t pact_launch_count(void);
+int pact_profile_next_gemm(void* begin_event, void* end_event);
+
 /* Synchronises the stream, then returns and clears the device status word:
  * PACT_OK, PACT_ERR_TIMEOUT or PACT_ERR_DEVICE_STATUS.  For tests and debugging. */
 int pact_check_status(pact_stream_t stream);

@@ -21,7 +21,7 @@ __all__ = [
     "pact_quant_nvfp4", "pact_pack_weight_fwd", "pact_pack_weight_bwd",
     "pact_lora_linear_fwd", "pact_lora_linear_dgrad", "pact_rmsnorm_quant",
     "pact_silu_mul_quant", "pact_silu_mul_bwd", "pact_rmsnorm_bwd", "pact_test_pexp",
-    "pact_check_status", "pact_device_supported",
+    "pact_check_status", "pact_device_supported", "pact_launch_count", "pact_profile_next_gemm",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -67,6 +67,8 @@ _SIGNATURES = {
     "pact_rmsnorm_bwd": (_int, [_SP, _vp, _vp, _vp, _vp, _vp, _vp]),
     "pact_test_pexp": (_int, [_vp, _vp, _i64, _vp]),
     "pact_check_status": (_int, [_vp]),
+    "pact_launch_count": (ctypes.c_uint64, []),
+    "pact_profile_next_gemm": (_int, [_vp, _vp]),
     "pact_device_supported": (_int, []),
     "pact_last_error": (ctypes.c_char_p, []),
     "pact_version": (ctypes.c_char_p, []),
@@ -323,3 +325,14 @@ def pact_check_status() -> None:
 
 def pact_device_supported() -> bool:
     return load_library().pact_device_supported() == 0
+
+
+def pact_launch_count() -> int:
+    """Number of libpact kernels launched by this process so far."""
+    return int(load_library().pact_launch_count())
+
+
+def pact_profile_next_gemm(begin: torch.cuda.Event, end: torch.cuda.Event) -> None:
+    """Record begin/end on the launch stream around the next NVFP4 GEMM kernel."""
+    _check(load_library().pact_profile_next_gemm(ctypes.c_void_p(begin.cuda_event),
+                                                 ctypes.c_void_p(end.cuda_event)))

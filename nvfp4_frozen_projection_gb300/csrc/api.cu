@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -12,6 +13,13 @@
 #include "kernels.h"
 
 using namespace pact;
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+thread_local cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
+}  // namespace
+
+void pact::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 
@@ -115,6 +123,8 @@ int check_nvfp4(const pact_nvfp4* t, const char* name, int64_t rows, int64_t col
   return PACT_OK;
 }
 
+// LoRA rank padded to 16, 32 or 64; the fused GEMM's LoRA operands are twice as
+// wide (a hi/lo BF16 pair of the down-projection output).
 int rp_for(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
 
 }  // namespace
@@ -125,6 +135,14 @@ extern "C" {
 const char* pact_last_error(void) { return g_err; }
 
 const char* pact_version(void) { return "libpact 0.1 (sm_103a)"; }
+
+uint64_t pact_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int pact_profile_next_gemm(void* begin_event, void* end_event) {
+  g_prof_begin = (cudaEvent_t)begin_event;
+  g_prof_end = (cudaEvent_t)end_event;
+  return PACT_OK;
+}
 
 int pact_device_supported(void) {
   DeviceInfo* d;
@@ -214,26 +232,26 @@ int pact_pack_weight_bwd(const float* W, int64_t N, int64_t K, pact_nvfp4* out_b
 // ---------------------------------------------------------------- LoRA linear
 size_t pact_lora_linear_fwd_workspace_size(int64_t M, int64_t N, int64_t, int r) {
   if (M < 1 || N < 1 || r < 1 || r > 64) return 0;
-  const int rp = rp_for(r);
-  return align256((size_t)M * rp * 2) + align256((size_t)N * rp * 2);
+  const int rpe = 2 * rp_for(r);
+  return align256((size_t)M * rpe * 2) + align256((size_t)N * rpe * 2);
 }
 
 size_t pact_lora_linear_dgrad_workspace_size(int64_t M, int64_t, int64_t K, int r) {
   if (M < 1 || K < 1 || r < 1 || r > 64) return 0;
-  const int rp = rp_for(r);
-  return align256((size_t)M * rp * 2) + align256((size_t)K * rp * 2);
+  const int rpe = 2 * rp_for(r);
+  return align256((size_t)M * rpe * 2) + align256((size_t)K * rpe * 2);
 }
 
 // Shared tail of fwd and dgrad: GEMM OUT[M, Nout] over reduction Kr with the
-// NVFP4 operands a [M, Kr], b [Nout, Kr] and the LoRA operands la [M, rp],
-// lb [Nout, rp] (both BF16, in the workspace).
+// NVFP4 operands a [M, Kr], b [Nout, Kr] and the LoRA operands la [M, rpe],
+// lb [Nout, rpe] (both BF16, in the workspace).
 static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int64_t M,
-                    int64_t Nout, int64_t Kr, const uint16_t* la, const uint16_t* lb, int rp,
+                    int64_t Nout, int64_t Kr, const uint16_t* la, const uint16_t* lb, int rpe,
                     const uint16_t* addend, uint16_t* out, float* out_amax,
                     cudaStream_t stream) {
   GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
-  const int bn = gemm_block_n(Nout);
+  const int bn = gemm_block_n(Nout, rpe);
   int rc;
   if ((rc = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->codes, Kr / 2, M, 128, 128,
                      CU_TENSOR_MAP_SWIZZLE_128B)))
@@ -241,12 +259,12 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   if ((rc = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b->codes, Kr / 2, Nout, 128, bn,
                      CU_TENSOR_MAP_SWIZZLE_128B)))
     return rc;
-  const CUtensorMapSwizzle lsw = rp == 16   ? CU_TENSOR_MAP_SWIZZLE_32B
-                                 : rp == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                            : CU_TENSOR_MAP_SWIZZLE_128B;
-  if ((rc = make_map(&L.tmLA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, la, rp, M, rp, 128, lsw)))
+  // LoRA operands: 64-byte rows (rpe 32) or 128-byte chunks of 64 columns.
+  const CUtensorMapSwizzle lsw = rpe == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const uint32_t lbox = rpe == 32 ? 32 : 64;
+  if ((rc = make_map(&L.tmLA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, la, rpe, M, lbox, 128, lsw)))
     return rc;
-  if ((rc = make_map(&L.tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lb, rp, Nout, rp, bn, lsw)))
+  if ((rc = make_map(&L.tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lb, rpe, Nout, lbox, bn, lsw)))
     return rc;
   GemmParams& p = L.p;
   p.sfa = (const uint8_t*)a->sf;
@@ -263,13 +281,18 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   p.k16p = (int)pad_to(Kr / 16, 4);
   p.num_m = (int)((M + 127) / 128);
   p.num_n = (int)((Nout + bn - 1) / bn);
-  p.lora_steps = rp / 16;
+  p.lora_steps = rpe / 16;
   L.num_sms = d->sms;
   if (out_amax) {
     cudaError_t e = cudaMemsetAsync(out_amax, 0, sizeof(float), stream);
     if (e != cudaSuccess) return cuda_fail(e, "amax reset");
   }
-  cudaError_t e = launch_gemm_nvfp4(L, bn, rp, stream);
+  cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
+  g_prof_begin = g_prof_end = nullptr;
+  if (pb && cudaEventRecord(pb, stream) != cudaSuccess) return cuda_fail(cudaGetLastError(), "event");
+  cudaError_t e = launch_gemm_nvfp4(L, bn, rpe, stream);
+  if (e == cudaSuccess && pe && cudaEventRecord(pe, stream) != cudaSuccess)
+    return cuda_fail(cudaGetLastError(), "event");
   return e == cudaSuccess ? PACT_OK : cuda_fail(e, "gemm launch");
 }
 
@@ -301,12 +324,12 @@ int pact_lora_linear_fwd(const pact_nvfp4* xq, const pact_nvfp4* w_fwd, const ui
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
   const int rp = rp_for(r);
   uint16_t* t = (uint16_t*)ws;
-  uint16_t* bt = (uint16_t*)((char*)ws + align256((size_t)M * rp * 2));
+  uint16_t* bt = (uint16_t*)((char*)ws + align256((size_t)M * 2 * rp * 2));
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = launch_lora_down_fwd((const uint8_t*)xq->codes, (const uint8_t*)xq->sf, xq->g,
                                        w_fwd->g, M, K, A, B, r, rp, scale, N, t, bt, d->sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "lora down launch");
-  return run_gemm(d, xq, w_fwd, M, N, K, t, bt, rp, residual_opt, y, out_amax_opt, s);
+  return run_gemm(d, xq, w_fwd, M, N, K, t, bt, 2 * rp, residual_opt, y, out_amax_opt, s);
 }
 
 int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact_nvfp4* w_bwd,
@@ -328,12 +351,13 @@ int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
   const int rp = rp_for(r);
   uint16_t* u = (uint16_t*)ws;
-  uint16_t* ap = (uint16_t*)((char*)ws + align256((size_t)M * rp * 2));
+  uint16_t* ap = (uint16_t*)((char*)ws + align256((size_t)M * 2 * rp * 2));
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = launch_lora_down_dgrad(dy, dyq->g, w_bwd->g, M, N, A, B, r, rp, scale, K, u, ap,
                                          d->sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "lora down launch");
-  return run_gemm(d, dyq, w_bwd, M, K, N, u, ap, rp, accumulate ? dx : nullptr, dx, nullptr, s);
+  return run_gemm(d, dyq, w_bwd, M, K, N, u, ap, 2 * rp, accumulate ? dx : nullptr, dx, nullptr,
+                  s);
 }
 
 // ---------------------------------------------------------------- fused nonlinear ops

@@ -141,6 +141,7 @@ __device__ __forceinline__ void block_max_atomic(uint32_t v, unsigned* dst) {
     x = __reduce_max_sync(0xFFFFFFFFu, x);
     if (lane == 0 && x != 0u) atomicMax(dst, x);
   }
+  __syncthreads();  // red[] may be reused by a following call
 }
 
 // ------------------------------------------------------------------ exp recipe

@@ -10,10 +10,12 @@
 //
 // A [M, K] and B [N, K] are NVFP4 (E2M1 codes + UE4M3 scales per 16 along K); the
 // first sum runs on the block-scaled tensor cores (tcgen05.mma kind::mxf4nvf4,
-// block16).  LA [M, RP] and LB [N, RP] are BF16: the LoRA down-projection output,
-// pre-scaled so that s * LA LB^T equals the LoRA term, and the LoRA
-// up-projection; their product runs as tcgen05.mma kind::f16 into the same TMEM
-// accumulator.  s = g_a * g_b (or 1 when either per-tensor scale is zero, in which
+// block16).  LA [M, RPE] and LB [N, RPE] are BF16: the LoRA down-projection
+// output, pre-scaled so that s * LA LB^T equals the LoRA term and stored as a
+// hi/lo BF16 pair, and the LoRA up-projection stored twice; their product runs as
+// tcgen05.mma kind::f16 (K = 16 per instruction) into the same TMEM accumulator.
+// RPE is 32, 64 or 128 columns, loaded in 128-byte (or one 64-byte) swizzled
+// chunks.  s = g_a * g_b (or 1 when either per-tensor scale is zero, in which
 // case the NVFP4 operand is all zero).
 //
 // Structure: one persistent CTA per SM, 6 warps.
@@ -35,7 +37,7 @@ __device__ unsigned g_pact_status;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 
-template <int BN, int BK, int STAGES, int RP>
+template <int BN, int BK, int STAGES, int RPE>
 struct GemmCfg {
   static constexpr int BM = 128;
   static constexpr int ROWB = BK / 2;   // bytes of one tile row per stage
@@ -46,22 +48,27 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = KSUB * 512;
   static constexpr int SFB_BYTES = NRB * KSUB * 512;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int LCH_BYTES = RPE * 2 > 128 ? 128 : RPE * 2;  // row bytes of a chunk
+  static constexpr int NLCH = RPE * 2 / LCH_BYTES;                    // LoRA operand chunks
+  static constexpr int LA_CHUNK = BM * LCH_BYTES;
+  static constexpr int LB_CHUNK = BN * LCH_BYTES;
   static constexpr int LA_OFF = STAGES * STAGE_BYTES;
-  static constexpr int LA_BYTES = BM * RP * 2;
+  static constexpr int LA_BYTES = NLCH * LA_CHUNK;
   static constexpr int LB_OFF = LA_OFF + LA_BYTES;
-  static constexpr int LB_BYTES = BN * RP * 2;
+  static constexpr int LB_BYTES = NLCH * LB_CHUNK;
   static constexpr int BAR_OFF = LB_OFF + LB_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
   static constexpr uint32_t AB_SWZ = ROWB == 128 ? 2u : 4u;  // 128B or 64B swizzle
   static constexpr uint32_t AB_SBO = 8 * ROWB;                // 8-row swizzle atom
-  static constexpr uint32_t L_SWZ = RP == 16 ? 6u : (RP == 32 ? 4u : 2u);
-  static constexpr uint32_t L_SBO = 8 * RP * 2;
+  static constexpr uint32_t L_SWZ = LCH_BYTES == 64 ? 4u : 2u;    // 64B or 128B swizzle
+  static constexpr uint32_t L_SBO = 8 * LCH_BYTES;
+  static constexpr int L_STEPS_PER_CH = LCH_BYTES / 32;            // K=16 BF16 steps
   static constexpr int SF_BASE = 256;                          // TMEM column
   static constexpr int SF_COLS = 4 * KSUB * (1 + NRB);         // per stage
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(BK == 128 || BK == 256, "BK");
-  static_assert(RP == 16 || RP == 32 || RP == 64, "RP");
+  static_assert(RPE == 32 || RPE == 64 || RPE == 128, "RPE");
   static_assert(SF_BASE + STAGES * SF_COLS <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(STAGE_BYTES % 1024 == 0 && LA_OFF % 1024 == 0 && LB_OFF % 1024 == 0, "align");
@@ -84,12 +91,12 @@ __device__ __forceinline__ void raise_error(volatile uint32_t* abort_flag, unsig
   atomicOr(status, code);
 }
 
-template <int BN, int BK, int STAGES, int RP>
+template <int BN, int BK, int STAGES, int RPE>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmLA,
                  const __grid_constant__ CUtensorMap tmLB, const GemmParams p) {
-  using C = GemmCfg<BN, BK, STAGES, RP>;
+  using C = GemmCfg<BN, BK, STAGES, RPE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -154,8 +161,11 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           mbar_expect_tx(lora_full, C::LA_BYTES + C::LB_BYTES);
-          tma_load_2d(base + C::LA_OFF, &tmLA, 0, m0, lora_full);
-          tma_load_2d(base + C::LB_OFF, &tmLB, 0, n0, lora_full);
+#pragma unroll
+          for (int c = 0; c < C::NLCH; ++c) {
+            tma_load_2d(base + C::LA_OFF + c * C::LA_CHUNK, &tmLA, 64 * c, m0, lora_full);
+            tma_load_2d(base + C::LB_OFF + c * C::LB_CHUNK, &tmLB, 64 * c, n0, lora_full);
+          }
           lpend = 1u;
           lpend_par = lphase;
           lphase ^= 1u;
@@ -218,8 +228,12 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after();
           for (int j = 0; j < p.lora_steps; ++j) {
-            const uint64_t da = smem_desc(base + C::LA_OFF + 32 * j, 16, C::L_SBO, C::L_SWZ);
-            const uint64_t db = smem_desc(base + C::LB_OFF + 32 * j, 16, C::L_SBO, C::L_SWZ);
+            const int ch = j / C::L_STEPS_PER_CH;
+            const uint32_t off = 32u * (uint32_t)(j % C::L_STEPS_PER_CH);
+            const uint64_t da =
+                smem_desc(base + C::LA_OFF + ch * C::LA_CHUNK + off, 16, C::L_SBO, C::L_SWZ);
+            const uint64_t db =
+                smem_desc(base + C::LB_OFF + ch * C::LB_CHUNK + off, 16, C::L_SBO, C::L_SWZ);
             mma_bf16(tmem, da, db, idesc_l, accum);
             accum = 1;
           }
@@ -336,10 +350,10 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ---------------------------------------------------------------- host side
-template <int BN, int BK, int STAGES, int RP>
+template <int BN, int BK, int STAGES, int RPE>
 static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
-  using C = GemmCfg<BN, BK, STAGES, RP>;
-  auto kern = k_gemm_nvfp4<BN, BK, STAGES, RP>;
+  using C = GemmCfg<BN, BK, STAGES, RPE>;
+  auto kern = k_gemm_nvfp4<BN, BK, STAGES, RPE>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -351,21 +365,21 @@ static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
   }
   const int ntiles = L.p.num_m * L.p.num_n;
   const int grid = ntiles < L.num_sms ? ntiles : L.num_sms;
+  note_launch();
   kern<<<grid, 192, C::SMEM_BYTES, stream>>>(L.tmA, L.tmB, L.tmLA, L.tmLB, L.p);
   return cudaGetLastError();
 }
 
-int gemm_block_n(int64_t N) { return (N % 256 == 0) ? 256 : 128; }
+int gemm_block_n(int64_t N, int rpe) { return (N % 256 == 0 && rpe <= 64) ? 256 : 128; }
 
-cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rp, cudaStream_t stream) {
+cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream) {
   if (bn == 256) {
-    if (rp == 16) return launch_cfg<256, 256, 3, 16>(L, stream);
-    if (rp == 32) return launch_cfg<256, 256, 3, 32>(L, stream);
+    if (rpe == 32) return launch_cfg<256, 256, 3, 32>(L, stream);
     return launch_cfg<256, 256, 3, 64>(L, stream);
   }
-  if (rp == 16) return launch_cfg<128, 256, 4, 16>(L, stream);
-  if (rp == 32) return launch_cfg<128, 256, 4, 32>(L, stream);
-  return launch_cfg<128, 256, 4, 64>(L, stream);
+  if (rpe == 32) return launch_cfg<128, 256, 4, 32>(L, stream);
+  if (rpe == 64) return launch_cfg<128, 256, 4, 64>(L, stream);
+  return launch_cfg<128, 256, 4, 128>(L, stream);
 }
 
 cudaError_t status_word_ptr(unsigned** ptr) {

@@ -15,6 +15,9 @@ enum : unsigned {
   PACT_DEV_ROLE_EPI = 1u << 10,
 };
 
+// Counts one kernel launch (pact_launch_count); called before every <<<>>>.
+void note_launch();
+
 struct GemmParams {
   const uint8_t* sfa;      // A scale atoms (128x4 layout, pad4(K/16) blocks per row)
   const uint8_t* sfb;      // B scale atoms
@@ -36,8 +39,10 @@ struct GemmLaunch {
   int num_sms;
 };
 
-int gemm_block_n(int64_t N);
-cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rp, cudaStream_t stream);
+// Tile width (128 or 256) for an output of N columns and a LoRA operand of rpe
+// columns, and the launcher.
+int gemm_block_n(int64_t N, int rpe);
+cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream);
 cudaError_t status_word_ptr(unsigned** ptr);
 
 cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
@@ -48,8 +53,8 @@ cudaError_t launch_pack_weight(const float* W, int64_t N, int64_t K, int backwar
                                int num_sms, cudaStream_t stream);
 
 // LoRA down-projections (BF16 tensor cores, FP32 accumulate), written pre-scaled
-// as the left LoRA operand [M, RP] of the fused GEMM, plus the padded right
-// operand [rows, RP].
+// as the left LoRA operand [M, 2 rp] (hi/lo BF16 pair) of the fused GEMM, plus
+// the padded right operand [rows, 2 rp] (stored twice).
 cudaError_t launch_lora_down_fwd(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
                                  const float* gw, int64_t M, int64_t K, const uint16_t* A,
                                  const uint16_t* B, int r, int rp, float scale, int64_t N,

@@ -8,8 +8,12 @@
 //   forward:  T = Xhat A        Xhat = dequant(Xq) [M, K], A [K, r]   -> [M, r]
 //   dgrad:    U = dY B^T        dY BF16 [M, N],    B [r, N]           -> [M, r]
 //
-// The result is stored as BF16 [M, RP] (RP = r rounded up to 16, 32 or 64, zero
-// padded), multiplied by a factor f chosen so that the GEMM epilogue's single
+// The result v = f * T is stored as BF16 [M, 2 RP] (RP = r rounded up to 16, 32 or
+// 64, zero padded): columns [0, RP) hold hi = bf16(v) and [RP, 2 RP) hold
+// lo = bf16(v - hi), and the right operand is stored twice ([B^T | B^T] or
+// [A | A]), so the fused BF16 LoRA product hi B + lo B carries v to about 16 bits
+// (a single BF16 rounding of v costs up to 2^-9 |v| |B| per term, more than the
+// output tolerance allows).  f is chosen so that the GEMM epilogue's single
 // scale s = g_a g_w turns the fused product into the LoRA term:
 //   forward  f = scale / g_w       (s T' B = g_x g_w X~ A B scale / g_w = scale Xhat A B)
 //   dgrad    f = scale / (g_dy g_w)
@@ -47,6 +51,9 @@ __device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, __half2 
   return pack_bf16x2(f.x, f.y);
 }
 
+// Sums the 8 warps' partial products and stores f * T as a BF16 pair per element:
+// out[m, j] = hi = bf16(v), out[m, RP + j] = lo = bf16(v - hi), so that the fused
+// GEMM's BF16 LoRA product sees v to about 16 significant bits.
 template <int RP>
 __device__ __forceinline__ void reduce_and_store(float (*acc)[4], float* red, int64_t m0,
                                                  int64_t M, float f, uint16_t* out) {
@@ -71,8 +78,11 @@ __device__ __forceinline__ void reduce_and_store(float (*acc)[4], float* red, in
     for (int w = 0; w < 8; ++w) s += red[(w * 16 + row) * RP + col];
     const int64_t m = m0 + row;
     if (m < M) {
-      __nv_bfloat16 b = __float2bfloat16_rn(s * f);
-      out[m * RP + col] = *reinterpret_cast<uint16_t*>(&b);
+      const float v = s * f;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      out[m * (2 * RP) + col] = *reinterpret_cast<const uint16_t*>(&hi);
+      out[m * (2 * RP) + RP + col] = *reinterpret_cast<const uint16_t*>(&lo);
     }
   }
 }
@@ -93,11 +103,11 @@ __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * RP];
   if ((int)blockIdx.x >= row_ctas) {
-    const int64_t total = N * RP;
+    const int64_t total = N * 2 * RP;
     for (int64_t e = (int64_t)(blockIdx.x - row_ctas) * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)(gridDim.x - row_ctas) * blockDim.x) {
-      const int64_t n = e / RP;
-      const int j = (int)(e - n * RP);
+      const int64_t n = e / (2 * RP);
+      const int j = (int)(e - n * 2 * RP) % RP;
       bt_out[e] = j < r ? B[(int64_t)j * N + n] : (uint16_t)0;
     }
     return;
@@ -173,11 +183,11 @@ __global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restr
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * RP];
   if ((int)blockIdx.x >= row_ctas) {
-    const int64_t total = K * RP;
+    const int64_t total = K * 2 * RP;
     for (int64_t e = (int64_t)(blockIdx.x - row_ctas) * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)(gridDim.x - row_ctas) * blockDim.x) {
-      const int64_t k = e / RP;
-      const int j = (int)(e - k * RP);
+      const int64_t k = e / (2 * RP);
+      const int j = (int)(e - k * 2 * RP) % RP;
       ap_out[e] = j < r ? A[k * r + j] : (uint16_t)0;
     }
     return;
@@ -236,6 +246,7 @@ static cudaError_t fwd_rp(const uint8_t* xc, const uint8_t* xsf, const float* gx
                           uint16_t* bt_out, int num_sms, cudaStream_t stream) {
   const int row_ctas = (int)((M + 15) / 16);
   const int extra = (int)((N * RP + 255) / 256) < num_sms ? (int)((N * RP + 255) / 256) : num_sms;
+  note_launch();
   k_lora_down_fwd<RP><<<row_ctas + extra, 256, 0, stream>>>(xc, xsf, gx, gw, M, K, A, B, r,
                                                             scale, N, t_out, bt_out, row_ctas);
   return cudaGetLastError();
@@ -248,6 +259,7 @@ static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* g
                             cudaStream_t stream) {
   const int row_ctas = (int)((M + 15) / 16);
   const int extra = (int)((K * RP + 255) / 256) < num_sms ? (int)((K * RP + 255) / 256) : num_sms;
+  note_launch();
   k_lora_down_dgrad<RP><<<row_ctas + extra, 256, 0, stream>>>(dy, gdy, gw, M, N, A, B, r, scale,
                                                               K, u_out, ap_out, row_ctas);
   return cudaGetLastError();

@@ -405,8 +405,10 @@ cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64
   const int64_t Mpad = pad_to(M, 128);
   return dispatch_bpl(H, [&](auto bpl) {
     constexpr int BPL = decltype(bpl)::value;
+    note_launch();
     k_rmsnorm_stat<BPL><<<blocks_for(M, 8, num_sms * 8), 256, 0, stream>>>(x, gamma, M, H, eps,
                                                                             rstd, ws_amax);
+    note_launch();
     k_rmsnorm_encode<BPL><<<blocks_for(Mpad, 8, num_sms * 8), 256, 0, stream>>>(
         x, gamma, rstd, M, Mpad, H, ws_amax, codes, sf, g);
     return cudaGetLastError();
@@ -420,6 +422,7 @@ cudaError_t launch_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I,
   if (!amax3_opt) {
     cudaError_t e = cudaMemsetAsync(ws_amax3, 0, 3 * sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
+    note_launch();
     k_silu_amax<<<blocks_for(M * (I / 16), 256, num_sms * 8), 256, 0, stream>>>(gateup, M, I,
                                                                                  ws_amax3);
   }
@@ -430,6 +433,7 @@ cudaError_t launch_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I,
     o.g[k] = g[k];
   }
   const int64_t Mpad = pad_to(M, 128);
+  note_launch();
   k_silu_encode<<<blocks_for(Mpad * (I / 16), 256, num_sms * 16), 256, 0, stream>>>(
       gateup, M, Mpad, I, amax3_opt, ws_amax3, o);
   return cudaGetLastError();
@@ -443,6 +447,7 @@ cudaError_t launch_silu_mul_bwd(const uint8_t* gc, const uint8_t* gsf, const flo
     cudaError_t e = cudaMemsetAsync(out_amax, 0, sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
   }
+  note_launch();
   k_silu_bwd<<<blocks_for(M * (I / 16), 256, num_sms * 16), 256, 0, stream>>>(
       gc, gsf, gg, uc, usf, ug, dh, M, I, dgu, out_amax);
   return cudaGetLastError();
@@ -454,6 +459,7 @@ cudaError_t launch_rmsnorm_bwd(const uint8_t* yc, const uint8_t* ysf, const floa
                                int num_sms, cudaStream_t stream) {
   return dispatch_bpl(H, [&](auto bpl) {
     constexpr int BPL = decltype(bpl)::value;
+    note_launch();
     k_rmsnorm_bwd<BPL><<<blocks_for(M, 8, num_sms * 8), 256, 0, stream>>>(
         yc, ysf, yg, gamma, rstd, dy, dres, M, H, dx);
     return cudaGetLastError();
@@ -461,6 +467,7 @@ cudaError_t launch_rmsnorm_bwd(const uint8_t* yc, const uint8_t* ysf, const floa
 }
 
 cudaError_t launch_pexp(const float* x, float* y, int64_t n, cudaStream_t stream) {
+  note_launch();
   k_pexp<<<blocks_for(n, 256, 4096), 256, 0, stream>>>(x, y, n);
   return cudaGetLastError();
 }

@@ -167,10 +167,12 @@ cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
   if (!amax_opt) {
     cudaError_t e = cudaMemsetAsync(ws_amax, 0, sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
+    note_launch();
     k_amax_bf16<<<grid_for(M * K / 8, 256, num_sms * 8), 256, 0, stream>>>(x, M, K, ldx,
                                                                             ws_amax);
   }
   const int64_t Mpad = pad_to(M, 128);
+  note_launch();
   k_quant_bf16<<<grid_for(Mpad * (K / 64), 256, num_sms * 16), 256, 0, stream>>>(
       x, M, K, ldx, Mpad, amax_opt, ws_amax, codes, sf, g);
   return cudaGetLastError();
@@ -184,8 +186,10 @@ cudaError_t launch_pack_weight(const float* W, int64_t N, int64_t K, int backwar
   const int64_t rows = backward ? K : N, cols = backward ? N : K;
   e = cudaMemsetAsync(sf, 0, (size_t)(pad_to(rows, 128) * pad_to(cols / 16, 4)), stream);
   if (e != cudaSuccess) return e;
+  note_launch();
   k_amax_f32<<<grid_for(N * K / 4, 256, num_sms * 8), 256, 0, stream>>>(W, N * K, ws_amax);
   const int64_t ntiles = (N / 16) * (K / 16);
+  note_launch();
   k_pack_weight<<<grid_for(ntiles * 32, 256, num_sms * 16), 256, 0, stream>>>(
       W, N, K, ws_amax, backward, codes, sf, g);
   return cudaGetLastError();

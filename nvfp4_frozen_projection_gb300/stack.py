@@ -1,0 +1,127 @@
+"""LoRA linear layers and the decoder-layer projection stack built on libpact.
+
+"PACT: NVFP4 Data-Flow LoRA Fine-Tuning on Consumer GPUs", Figure 2 (decoder data
+flow) and Table 7 (precision allocation): RMSNorm -> NVFP4 feeds the q/k/v
+projections, the attention output feeds o, a residual add, RMSNorm -> NVFP4 feeds
+the fused gate/up projection, SiLU-multiply -> NVFP4 feeds down, and a second
+residual add.  Attention and its backward are out of scope: the attention output
+and the gradients flowing back into q/k/v are given tensors.
+
+Every operation here is a libpact call; this module only owns buffers and the
+order of calls.  Buffers are allocated once, so one step can be captured in a
+CUDA graph and replayed.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (NVFP4, pact_lora_linear_dgrad, pact_lora_linear_fwd, pact_pack_weight_bwd,
+               pact_pack_weight_fwd, pact_quant_nvfp4, pact_rmsnorm_bwd, pact_rmsnorm_quant,
+               pact_silu_mul_bwd, pact_silu_mul_quant)
+
+
+class LoraLinear:
+    """Frozen weight W [d_out, d_in] packed once into the cached forward and backward
+    NVFP4 layouts, BF16 adapters A [d_in, r] and B [r, d_out], scale = alpha / r."""
+
+    def __init__(self, W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, scale: float):
+        self.d_out, self.d_in = W.shape
+        self.w_fwd = pact_pack_weight_fwd(W)
+        self.w_bwd = pact_pack_weight_bwd(W)
+        self.A, self.B, self.scale = A, B, float(scale)
+
+    def forward(self, xq: NVFP4, y: torch.Tensor, residual=None, out_amax=None):
+        return pact_lora_linear_fwd(xq, self.w_fwd, self.A, self.B, self.scale,
+                                    residual=residual, y=y, out_amax=out_amax)
+
+    def dgrad(self, dyq: NVFP4, dy: torch.Tensor, dx: torch.Tensor, accumulate=False):
+        return pact_lora_linear_dgrad(dyq, dy, self.w_bwd, self.A, self.B, self.scale, dx=dx,
+                                      accumulate=accumulate)
+
+    def gemm_flops(self, m: int) -> float:
+        return 2.0 * m * self.d_in * self.d_out
+
+
+class DecoderProjectionStack:
+    """The seven LoRA projections of a Llama decoder layer with both RMSNorms, the
+    SiLU-multiply and the two residual adds; forward and input-gradient pass."""
+
+    def __init__(self, m: int, proj: dict, gamma1, gamma2, eps: float = 1e-5):
+        self.m = m
+        self.p = proj  # q, k, v, o, gate_up, down -> LoraLinear
+        self.gamma1, self.gamma2, self.eps = gamma1, gamma2, float(eps)
+        hidden = proj["q"].d_in
+        inter = proj["down"].d_in
+        dev = gamma1.device
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.hidden, self.inter = hidden, inter
+        # forward state (the NVFP4 tensors are what backward reuses)
+        self.xq1 = NVFP4.empty(m, hidden, dev)
+        self.rstd1 = torch.empty(m, dtype=torch.float32, device=dev)
+        self.q = torch.empty(m, proj["q"].d_out, **bf)
+        self.k = torch.empty(m, proj["k"].d_out, **bf)
+        self.v = torch.empty(m, proj["v"].d_out, **bf)
+        self.attnq = NVFP4.empty(m, hidden, dev)
+        self.h1 = torch.empty(m, hidden, **bf)
+        self.xq2 = NVFP4.empty(m, hidden, dev)
+        self.rstd2 = torch.empty(m, dtype=torch.float32, device=dev)
+        self.gu = torch.empty(m, 2 * inter, **bf)
+        self.hq = NVFP4.empty(m, inter, dev)
+        self.gq = NVFP4.empty(m, inter, dev)
+        self.uq = NVFP4.empty(m, inter, dev)
+        self.out = torch.empty(m, hidden, **bf)
+        # backward state
+        self.dyq = NVFP4.empty(m, hidden, dev)
+        self.dh = torch.empty(m, inter, **bf)
+        self.dgu = torch.empty(m, 2 * inter, **bf)
+        self.dgu_amax = torch.empty(1, dtype=torch.float32, device=dev)
+        self.dguq = NVFP4.empty(m, 2 * inter, dev)
+        self.dxn2 = torch.empty(m, hidden, **bf)
+        self.dh1 = torch.empty(m, hidden, **bf)
+        self.dh1q = NVFP4.empty(m, hidden, dev)
+        self.dattn = torch.empty(m, hidden, **bf)
+        self.dqq = NVFP4.empty(m, proj["q"].d_out, dev)
+        self.dkq = NVFP4.empty(m, proj["k"].d_out, dev)
+        self.dvq = NVFP4.empty(m, proj["v"].d_out, dev)
+        self.dxn1 = torch.empty(m, hidden, **bf)
+        self.dx = torch.empty(m, hidden, **bf)
+
+    def forward(self, x: torch.Tensor, attn: torch.Tensor) -> torch.Tensor:
+        p = self.p
+        pact_rmsnorm_quant(x, self.gamma1, self.eps, out=self.xq1, rstd=self.rstd1)
+        p["q"].forward(self.xq1, self.q)
+        p["k"].forward(self.xq1, self.k)
+        p["v"].forward(self.xq1, self.v)
+        # attention core (out of scope): its output is the given tensor attn
+        pact_quant_nvfp4(attn, out=self.attnq)
+        p["o"].forward(self.attnq, self.h1, residual=x)
+        pact_rmsnorm_quant(self.h1, self.gamma2, self.eps, out=self.xq2, rstd=self.rstd2)
+        p["gate_up"].forward(self.xq2, self.gu)
+        pact_silu_mul_quant(self.gu, outs=(self.hq, self.gq, self.uq))
+        p["down"].forward(self.hq, self.out, residual=self.h1)
+        return self.out
+
+    def backward(self, dy, dq, dk, dv) -> torch.Tensor:
+        """dy: gradient of the layer output; dq/dk/dv: gradients flowing back from
+        the (out of scope) attention core into the q/k/v outputs."""
+        p = self.p
+        pact_quant_nvfp4(dy, out=self.dyq)
+        p["down"].dgrad(self.dyq, dy, self.dh)
+        pact_silu_mul_bwd(self.gq, self.uq, self.dh, dgateup=self.dgu, out_amax=self.dgu_amax)
+        pact_quant_nvfp4(self.dgu, amax=self.dgu_amax, out=self.dguq)
+        p["gate_up"].dgrad(self.dguq, self.dgu, self.dxn2)
+        pact_rmsnorm_bwd(self.xq2, self.gamma2, self.rstd2, self.dxn2, dres=dy, dx=self.dh1)
+        pact_quant_nvfp4(self.dh1, out=self.dh1q)
+        p["o"].dgrad(self.dh1q, self.dh1, self.dattn)  # into the attention core
+        pact_quant_nvfp4(dq, out=self.dqq)
+        pact_quant_nvfp4(dk, out=self.dkq)
+        pact_quant_nvfp4(dv, out=self.dvq)
+        p["q"].dgrad(self.dqq, dq, self.dxn1)
+        p["k"].dgrad(self.dkq, dk, self.dxn1, accumulate=True)
+        p["v"].dgrad(self.dvq, dv, self.dxn1, accumulate=True)
+        pact_rmsnorm_bwd(self.xq1, self.gamma1, self.rstd1, self.dxn1, dres=self.dh1, dx=self.dx)
+        return self.dx
+
+    def gemm_flops(self) -> float:
+        """2*M*N*K over the 14 frozen-projection GEMMs of one forward + dgrad pass."""
+        return 2.0 * sum(l.gemm_flops(self.m) for l in self.p.values())
