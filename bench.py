@@ -248,7 +248,11 @@ def time_gemm_kernels(stack, inputs, reps):
     for name, fn in calls.items():
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(reps)]
+        for b, e in evs:  # torch creates the CUDA events on first record
+            b.record()
+            e.record()
         fn()
+        torch.cuda.synchronize()
         for b, e in evs:
             pk.pact_profile_next_gemm(b, e)
             fn()
