@@ -133,6 +133,33 @@ int pact_lora_linear_fwd(const pact_nvfp4* xq, const pact_nvfp4* w_fwd, const ui
                          pact_stream_t stream);
 
 /*
+ * LoRA linear forward that allocates nothing and needs no workspace.  The paper
+ * has no counterpart: this is an interface for callers that cannot allocate
+ * device memory or hand in a workspace.  Examples: a plugin whose host framework
+ * passes it only inputs and outputs, code running while a stream is captured into
+ * a CUDA graph (cudaMalloc is not allowed then), or a runtime with a fixed memory
+ * budget where an allocation on the hot path would synchronise the device.
+ *
+ * Same arguments, rules and result as pact_lora_linear_fwd, without ws/ws_bytes.
+ * The scratch lives in a fixed array of PACT_NOALLOC_SCRATCH_BYTES (16 MiB) that
+ * is part of the library image; every GPU that loads libpact holds it until the
+ * process exits.  A call needing more scratch than that
+ * (pact_lora_linear_fwd_workspace_size(M, N, K, r) > 16 MiB) returns
+ * PACT_ERR_SHAPE without launching anything.
+ * - The first call on each device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ * - Every call shares the one array, so calls that overlap on the GPU (different
+ *   streams, or different host threads) race and corrupt each other's results.
+ *   Serialise them, e.g. issue them all on one stream.
+ */
+#define PACT_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+size_t pact_lora_linear_fwd_noalloc_max_scratch(void);
+int pact_lora_linear_fwd_noalloc(const pact_nvfp4* xq, const pact_nvfp4* w_fwd,
+                                 const uint16_t* A, const uint16_t* B, int r, float scale,
+                                 const uint16_t* residual_opt, uint16_t* y, float* out_amax_opt,
+                                 pact_stream_t stream);
+
+/*
  * LoRA linear input gradient (Table 7: "NVFP4 input-gradient GEMMs" on the cached
  * backward layout; LoRA branch "BF16 ... input gradients"):
  *   dX = g_dy g_w (dYq Wbwd^T) + scale * (dY B^T) A^T   [+ dX_prev if accumulate]

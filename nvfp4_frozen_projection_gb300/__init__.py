@@ -19,7 +19,8 @@ import torch
 __all__ = [
     "NVFP4", "PactError", "load_library", "library_path",
     "pact_quant_nvfp4", "pact_pack_weight_fwd", "pact_pack_weight_bwd",
-    "pact_lora_linear_fwd", "pact_lora_linear_dgrad", "pact_rmsnorm_quant",
+    "pact_lora_linear_fwd", "pact_lora_linear_fwd_noalloc", "pact_lora_linear_dgrad",
+    "pact_rmsnorm_quant",
     "pact_silu_mul_quant", "pact_silu_mul_bwd", "pact_rmsnorm_bwd", "pact_test_pexp",
     "pact_check_status", "pact_device_supported", "pact_launch_count", "pact_profile_next_gemm",
 ]
@@ -57,6 +58,8 @@ _SIGNATURES = {
     "pact_pack_weight_bwd": (_int, [_vp, _i64, _i64, _SP, _vp, _sz, _vp]),
     "pact_lora_linear_fwd_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
     "pact_lora_linear_fwd": (_int, [_SP, _SP, _vp, _vp, _int, _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "pact_lora_linear_fwd_noalloc_max_scratch": (_sz, []),
+    "pact_lora_linear_fwd_noalloc": (_int, [_SP, _SP, _vp, _vp, _int, _f32, _vp, _vp, _vp, _vp]),
     "pact_lora_linear_dgrad_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
     "pact_lora_linear_dgrad": (_int, [_SP, _vp, _SP, _vp, _vp, _int, _f32, _int, _vp, _vp, _sz, _vp]),
     "pact_rmsnorm_quant_workspace_size": (_sz, [_i64, _i64]),
@@ -221,6 +224,24 @@ def pact_lora_linear_fwd(xq: NVFP4, w_fwd: NVFP4, A: torch.Tensor, B: torch.Tens
     _check(lib.pact_lora_linear_fwd(ctypes.byref(sx), ctypes.byref(sw), _ptr(A), _ptr(B), r,
                                     float(scale), _ptr(residual), _ptr(y), _ptr(out_amax),
                                     _ptr(ws), ws.numel(), _stream()))
+    return y
+
+
+def pact_lora_linear_fwd_noalloc(xq: NVFP4, w_fwd: NVFP4, A: torch.Tensor, B: torch.Tensor,
+                                 scale: float, y: torch.Tensor,
+                                 residual: torch.Tensor | None = None,
+                                 out_amax: torch.Tensor | None = None) -> torch.Tensor:
+    """pact_lora_linear_fwd for callers that cannot allocate: the output y is
+    preallocated by the caller and the library's fixed scratch array replaces the
+    workspace (calls that overlap on the GPU race on it)."""
+    lib = load_library()
+    _need_cuda(A, torch.bfloat16, "A")
+    _need_cuda(B, torch.bfloat16, "B")
+    _need_cuda(y, torch.bfloat16, "y")
+    sx, sw = xq.struct(), w_fwd.struct()
+    _check(lib.pact_lora_linear_fwd_noalloc(ctypes.byref(sx), ctypes.byref(sw), _ptr(A), _ptr(B),
+                                            A.shape[1], float(scale), _ptr(residual), _ptr(y),
+                                            _ptr(out_amax), _stream()))
     return y
 
 

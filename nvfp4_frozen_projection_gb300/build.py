@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpact.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "lora.cu", "norm_act.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "lora.cu", "norm_act.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr", "-Xptxas", "-v", "-Wno-deprecated-gpu-targets"]

@@ -22,6 +22,12 @@ thread_local cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
 void pact::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
+int fail(int code, const char* fmt, ...);
+}
+
+int pact::report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+namespace {
 
 thread_local char g_err[512] = "";
 

@@ -18,6 +18,9 @@ enum : unsigned {
 // Counts one kernel launch (pact_launch_count); called before every <<<>>>.
 void note_launch();
 
+// Sets the thread's pact_last_error() text and returns code.
+int report_error(int code, const char* msg);
+
 struct GemmParams {
   const uint8_t* sfa;      // A scale atoms (128x4 layout, pad4(K/16) blocks per row)
   const uint8_t* sfb;      // B scale atoms
