@@ -253,6 +253,7 @@ def time_gemm_kernels(stack, inputs, reps):
             e.record()
         fn()
         torch.cuda.synchronize()
+        _gpu_head_start()
         for b, e in evs:
             pk.pact_profile_next_gemm(b, e)
             fn()
@@ -264,10 +265,18 @@ def time_gemm_kernels(stack, inputs, reps):
     return out
 
 
+def _gpu_head_start():
+    """Keep the GPU busy for a few ms so the host enqueues every rep before the GPU
+    reaches it: the events then time GPU execution, not host launch latency."""
+    torch.cuda._sleep(20_000_000)
+
+
 def time_call(fn, reps):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
     fn()
+    torch.cuda.synchronize()
+    _gpu_head_start()
     for b, e in evs:
         b.record()
         fn()

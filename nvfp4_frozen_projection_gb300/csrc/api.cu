@@ -236,16 +236,18 @@ int pact_pack_weight_bwd(const float* W, int64_t N, int64_t K, pact_nvfp4* out_b
 }
 
 // ---------------------------------------------------------------- LoRA linear
+// Workspace: the LoRA left operand [M, 2 rp] (hi|lo BF16 pair) and the padded right
+// operand [rows, rp], both BF16.
 size_t pact_lora_linear_fwd_workspace_size(int64_t M, int64_t N, int64_t, int r) {
   if (M < 1 || N < 1 || r < 1 || r > 64) return 0;
-  const int rpe = 2 * rp_for(r);
-  return align256((size_t)M * rpe * 2) + align256((size_t)N * rpe * 2);
+  const int rp = rp_for(r);
+  return align256((size_t)M * 2 * rp * 2) + align256((size_t)N * rp * 2);
 }
 
 size_t pact_lora_linear_dgrad_workspace_size(int64_t M, int64_t, int64_t K, int r) {
   if (M < 1 || K < 1 || r < 1 || r > 64) return 0;
-  const int rpe = 2 * rp_for(r);
-  return align256((size_t)M * rpe * 2) + align256((size_t)K * rpe * 2);
+  const int rp = rp_for(r);
+  return align256((size_t)M * 2 * rp * 2) + align256((size_t)K * rp * 2);
 }
 
 // Shared tail of fwd and dgrad: GEMM OUT[M, Nout] over reduction Kr with the
@@ -259,18 +261,31 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   std::memset(&L, 0, sizeof(L));
   const int bn = gemm_block_n(Nout, rpe);
   int rc;
-  if ((rc = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->codes, Kr / 2, M, 128, 128,
-                     CU_TENSOR_MAP_SWIZZLE_128B)))
+  const uint32_t rowb = (uint32_t)gemm_stage_row_bytes();
+  const CUtensorMapSwizzle absw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if ((rc = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->codes, Kr / 2, M, rowb, 128,
+                     absw)))
     return rc;
-  if ((rc = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b->codes, Kr / 2, Nout, 128, bn,
-                     CU_TENSOR_MAP_SWIZZLE_128B)))
+  if ((rc = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b->codes, Kr / 2, Nout, rowb, bn,
+                     absw)))
     return rc;
-  // LoRA operands: 64-byte rows (rpe 32) or 128-byte chunks of 64 columns.
-  const CUtensorMapSwizzle lsw = rpe == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-  const uint32_t lbox = rpe == 32 ? 32 : 64;
-  if ((rc = make_map(&L.tmLA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, la, rpe, M, lbox, 128, lsw)))
+  // LoRA operands: la [M, rpe] (hi|lo pair), lb [Nout, rpe/2]; boxes of at most 64
+  // columns (128-byte rows), swizzled by their row width.
+  auto lsw = [](uint32_t cols) {
+    return cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
+                      : (cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+  };
+  const uint32_t rp = (uint32_t)rpe / 2;
+  const uint32_t abox = rpe < 64 ? (uint32_t)rpe : 64, bbox = rp < 64 ? rp : 64;
+  if ((rc = make_map(&L.tmLA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, la, rpe, M, abox, 128,
+                     lsw(abox))))
     return rc;
-  if ((rc = make_map(&L.tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lb, rpe, Nout, lbox, bn, lsw)))
+  if ((rc = make_map(&L.tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lb, rp, Nout, bbox, bn,
+                     lsw(bbox))))
+    return rc;
+  // output: 32 x 32 BF16 blocks written by TMA stores from the epilogue
+  if ((rc = make_map(&L.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, Nout, M, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_NONE)))
     return rc;
   GemmParams& p = L.p;
   p.sfa = (const uint8_t*)a->sf;

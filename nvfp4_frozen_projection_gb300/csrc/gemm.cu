@@ -18,15 +18,19 @@
 // chunks.  s = g_a * g_b (or 1 when either per-tensor scale is zero, in which
 // case the NVFP4 operand is all zero).
 //
-// Structure: one persistent CTA per SM, 6 warps.
-//   warp 0     TMA producer: A/B tiles (128B/64B swizzled) and the scale-factor
-//              atoms (plain bulk copies) into a STAGES-deep shared-memory ring;
-//              the LoRA operands once per tile.
-//   warp 1     TMEM allocator and MMA issuer (one thread): scale factors
-//              shared -> TMEM with tcgen05.cp, then the MMAs; tcgen05.commit
-//              frees ring slots and publishes the finished accumulator.
-//   warps 2-5  epilogue: TMEM -> registers (tcgen05.ld), scale, optional addend,
-//              BF16 cast, global store, optional amax.
+// Structure: one persistent CTA per SM, 14 warps.
+//   warp 0      TMA producer: A/B tiles (128-byte rows, 128B swizzle; one 16 KB
+//               and one 16/32 KB box per stage) and the scale-factor atoms (plain
+//               bulk copies) into a STAGES-deep shared-memory ring; the LoRA
+//               operands once per tile.
+//   warp 1      TMEM allocator and MMA issuer (one thread): MMAs only;
+//               tcgen05.commit frees ring slots and publishes the accumulator.
+//   warps 2-5   scale staging: shared -> TMEM with tcgen05.st (one warp per TMEM
+//               lane quarter).  A tcgen05.cp per atom on the MMA issuer's pipe
+//               cost ~35 extra cycles per copy beyond one per MMA; TMEM stores
+//               from other warps do not slow the MMAs.
+//   warps 6-13  epilogue: TMEM -> registers (tcgen05.ld), scale, optional addend,
+//               BF16 cast, global store, optional amax.
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -36,6 +40,9 @@ namespace pact {
 __device__ unsigned g_pact_status;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+// FP4 elements of K per ring stage: 128-byte tile rows, so each stage moves one
+// 16 KB A box and one 32 KB B box (TMA throughput grows with box size).
+constexpr int kStageK = 256;
 
 template <int BN, int BK, int STAGES, int RPE>
 struct GemmCfg {
@@ -48,30 +55,56 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = KSUB * 512;
   static constexpr int SFB_BYTES = NRB * KSUB * 512;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int LCH_BYTES = RPE * 2 > 128 ? 128 : RPE * 2;  // row bytes of a chunk
-  static constexpr int NLCH = RPE * 2 / LCH_BYTES;                    // LoRA operand chunks
-  static constexpr int LA_CHUNK = BM * LCH_BYTES;
-  static constexpr int LB_CHUNK = BN * LCH_BYTES;
+  // LoRA operands: LA [BM, RPE] = the down-projection output as a hi|lo BF16 pair,
+  // LB [BN, RP] = the up-projection (RP = RPE/2 columns), read by both the hi and the
+  // lo MMAs.  Each is loaded in chunks of at most 64 columns (128-byte rows).
+  static constexpr int RP = RPE / 2;
+  static constexpr int LA_CH = RPE * 2 > 128 ? 128 : RPE * 2;  // row bytes of an LA chunk
+  static constexpr int LB_CH = RP * 2 > 128 ? 128 : RP * 2;
+  static constexpr int NLA = RPE * 2 / LA_CH;
+  static constexpr int NLB = RP * 2 / LB_CH;
+  static constexpr int LA_CHUNK = BM * LA_CH;
+  static constexpr int LB_CHUNK = BN * LB_CH;
   static constexpr int LA_OFF = STAGES * STAGE_BYTES;
-  static constexpr int LA_BYTES = NLCH * LA_CHUNK;
+  static constexpr int LA_BYTES = NLA * LA_CHUNK;
   static constexpr int LB_OFF = LA_OFF + LA_BYTES;
-  static constexpr int LB_BYTES = NLCH * LB_CHUNK;
-  static constexpr int BAR_OFF = LB_OFF + LB_BYTES;
+  static constexpr int LB_BYTES = NLB * LB_CHUNK;
+  // Epilogue staging for TMA stores: per epilogue warp NSTG buffers of 32 rows x 32
+  // BF16 columns (2 KB); double-buffered when shared memory allows.
+  static constexpr int STG_OFF = LB_OFF + LB_BYTES;
+  static constexpr int STG_BUF = 2048;
+  static constexpr int NSTG = (STG_OFF + 2 * 8 * STG_BUF + 256 + 1024 <= 232448) ? 2 : 1;
+  static constexpr int BAR_OFF = STG_OFF + NSTG * 8 * STG_BUF;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
   static constexpr uint32_t AB_SWZ = ROWB == 128 ? 2u : 4u;  // 128B or 64B swizzle
   static constexpr uint32_t AB_SBO = 8 * ROWB;                // 8-row swizzle atom
-  static constexpr uint32_t L_SWZ = LCH_BYTES == 64 ? 4u : 2u;    // 64B or 128B swizzle
-  static constexpr uint32_t L_SBO = 8 * LCH_BYTES;
-  static constexpr int L_STEPS_PER_CH = LCH_BYTES / 32;            // K=16 BF16 steps
+  static constexpr uint32_t swz_mode(int row_bytes) {  // 32B -> 6, 64B -> 4, 128B -> 2
+    return row_bytes == 32 ? 6u : (row_bytes == 64 ? 4u : 2u);
+  }
+  static constexpr uint32_t LA_SWZ = swz_mode(LA_CH), LB_SWZ = swz_mode(LB_CH);
+  static constexpr uint32_t LA_SBO = 8 * LA_CH, LB_SBO = 8 * LB_CH;  // 8-row swizzle atoms
+  static constexpr int LA_STEPS = LA_CH / 32, LB_STEPS = LB_CH / 32;  // K=16 BF16 per step
   static constexpr int SF_BASE = 256;                          // TMEM column
   static constexpr int SF_COLS = 4 * KSUB * (1 + NRB);         // per stage
   static constexpr uint32_t TMEM_COLS = 512;
+  // warp 0 TMA, warp 1 MMA, warps 2-5 scale-factor staging, warps 6-13 epilogue
+  static constexpr int THREADS = 448;
+  static constexpr int SF_WARP0 = 2;
+  static constexpr int EPI_WARP0 = 6;
+  static constexpr int EPI_THREADS = 256;
+  static constexpr int EPI_COLS = BN / 2;    // accumulator columns per epilogue warp
+  static constexpr int SFA_TCOLS = 4 * KSUB;        // TMEM columns of a stage's A scales
+  static constexpr int SFB_TCOLS = 4 * KSUB * NRB;  // ... and B scales
+  static_assert(SFA_TCOLS == 16 && (SFB_TCOLS == 16 || SFB_TCOLS == 32), "SF staging shapes");
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(BK == 128 || BK == 256, "BK");
   static_assert(RPE == 32 || RPE == 64 || RPE == 128, "RPE");
   static_assert(SF_BASE + STAGES * SF_COLS <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(STAGE_BYTES % 1024 == 0 && LA_OFF % 1024 == 0 && LB_OFF % 1024 == 0, "align");
+  static_assert(STAGE_BYTES % 1024 == 0 && LA_OFF % 1024 == 0 && LB_OFF % 1024 == 0 &&
+                    STG_OFF % 1024 == 0,
+                "align");
+  static_assert((3 * STAGES + 5) * 8 <= 200, "barrier area");
 };
 
 // Instruction descriptors (M = 128, K-major A and B, dense).
@@ -92,10 +125,11 @@ __device__ __forceinline__ void raise_error(volatile uint32_t* abort_flag, unsig
 }
 
 template <int BN, int BK, int STAGES, int RPE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(448, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmLA,
-                 const __grid_constant__ CUtensorMap tmLB, const GemmParams p) {
+                 const __grid_constant__ CUtensorMap tmLB,
+                 const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
   using C = GemmCfg<BN, BK, STAGES, RPE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -107,6 +141,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t acc_full = lora_full + 16;
   const uint32_t acc_empty = lora_full + 24;
   const uint32_t final_bar = lora_full + 32;
+  const uint32_t sf_full0 = lora_full + 40;  // STAGES barriers: a stage's scales are in TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 200);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 204);
 
@@ -123,14 +158,16 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(lora_full, 1);
     mbar_init(lora_empty, 1);
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    mbar_init(acc_empty, C::EPI_THREADS);
     mbar_init(final_bar, 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(sf_full0 + 8 * s, 128);
     *abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmOut);
     if (p.lora_steps) {
       prefetch_tensormap(&tmLA);
       prefetch_tensormap(&tmLB);
@@ -162,10 +199,11 @@ __global__ void __launch_bounds__(192, 1)
           }
           mbar_expect_tx(lora_full, C::LA_BYTES + C::LB_BYTES);
 #pragma unroll
-          for (int c = 0; c < C::NLCH; ++c) {
+          for (int c = 0; c < C::NLA; ++c)
             tma_load_2d(base + C::LA_OFF + c * C::LA_CHUNK, &tmLA, 64 * c, m0, lora_full);
+#pragma unroll
+          for (int c = 0; c < C::NLB; ++c)
             tma_load_2d(base + C::LB_OFF + c * C::LB_CHUNK, &tmLB, 64 * c, n0, lora_full);
-          }
           lpend = 1u;
           lpend_par = lphase;
           lphase ^= 1u;
@@ -228,12 +266,15 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after();
           for (int j = 0; j < p.lora_steps; ++j) {
-            const int ch = j / C::L_STEPS_PER_CH;
-            const uint32_t off = 32u * (uint32_t)(j % C::L_STEPS_PER_CH);
-            const uint64_t da =
-                smem_desc(base + C::LA_OFF + ch * C::LA_CHUNK + off, 16, C::L_SBO, C::L_SWZ);
-            const uint64_t db =
-                smem_desc(base + C::LB_OFF + ch * C::LB_CHUNK + off, 16, C::L_SBO, C::L_SWZ);
+            // step j reads columns [16j, 16j+16) of LA (hi then lo) and the same
+            // up-projection columns [16(j mod RP/16), ...) of LB for both halves
+            const int jb = j % (C::RP / 16);
+            const uint64_t da = smem_desc(base + C::LA_OFF + (j / C::LA_STEPS) * C::LA_CHUNK +
+                                              32u * (uint32_t)(j % C::LA_STEPS),
+                                          16, C::LA_SBO, C::LA_SWZ);
+            const uint64_t db = smem_desc(base + C::LB_OFF + (jb / C::LB_STEPS) * C::LB_CHUNK +
+                                              32u * (uint32_t)(jb % C::LB_STEPS),
+                                          16, C::LB_SBO, C::LB_SWZ);
             mma_bf16(tmem, da, db, idesc_l, accum);
             accum = 1;
           }
@@ -241,23 +282,14 @@ __global__ void __launch_bounds__(192, 1)
           lphase ^= 1u;
         }
         for (int ks = 0; ks < nks; ++ks) {
-          if (!mbar_wait(bar0 + 8 * stage, phase, kWaitLimitNs, abort_flag)) {
+          // the stage's A/B tiles are in shared memory and its scales in TMEM
+          if (!mbar_wait(sf_full0 + 8 * stage, phase, kWaitLimitNs, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sb = base + stage * C::STAGE_BYTES;
-          const uint32_t sfa_s = sb + C::A_BYTES + C::B_BYTES;
-          const uint32_t sfb_s = sfa_s + C::SFA_BYTES;
           const uint32_t tsf = tmem + C::SF_BASE + stage * C::SF_COLS;
-#pragma unroll
-          for (int j = 0; j < C::KSUB; ++j) {
-            tmem_cp_sf_atom(tsf + 4 * j, smem_desc(sfa_s + 512 * j, 16, 128, 0));
-#pragma unroll
-            for (int rb = 0; rb < C::NRB; ++rb)
-              tmem_cp_sf_atom(tsf + 4 * C::KSUB + (j * C::NRB + rb) * 4,
-                              smem_desc(sfb_s + rb * C::KSUB * 512 + 512 * j, 16, 128, 0));
-          }
           const int ksub = min(C::KSUB, (p.K - ks * BK) / 64);
           for (int j = 0; j < ksub; ++j) {
             const uint64_t da = smem_desc(sb + 32 * j, 16, C::AB_SBO, C::AB_SWZ);
@@ -280,13 +312,77 @@ __global__ void __launch_bounds__(192, 1)
       mma_commit(final_bar);
       mbar_wait(final_bar, 0, kWaitLimitNs, nullptr);
     }
+  } else if (warp < C::EPI_WARP0) {
+    // ------------------------------------------------------------ scale staging
+    // One warp per TMEM lane quarter.  When a stage lands, each lane reads row
+    // `lane` (16 bytes) of every 512-byte scale atom in shared memory and writes it
+    // as 4 consecutive TMEM columns of its lane: the same image a 32x128b.warpx4
+    // copy makes (every lane quarter holds the whole atom), written with plain
+    // TMEM stores so that the MMA issuer's tensor pipe carries only MMAs.
+    const uint32_t q = (uint32_t)(warp & 3);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int ks = 0; ks < nks; ++ks) {
+        if (!mbar_wait(bar0 + 8 * stage, phase, kWaitLimitNs, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sfa_p = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+        const uint8_t* sfb_p = sfa_p + C::SFA_BYTES;
+        uint32_t va[C::SFA_TCOLS], vb[C::SFB_TCOLS];
+#pragma unroll
+        for (int j = 0; j < C::KSUB; ++j) {
+          const uint4 a = *reinterpret_cast<const uint4*>(sfa_p + 512 * j + 16 * lane);
+          va[4 * j] = a.x;
+          va[4 * j + 1] = a.y;
+          va[4 * j + 2] = a.z;
+          va[4 * j + 3] = a.w;
+#pragma unroll
+          for (int rb = 0; rb < C::NRB; ++rb) {
+            const uint4 b =
+                *reinterpret_cast<const uint4*>(sfb_p + rb * C::KSUB * 512 + 512 * j + 16 * lane);
+            const int c = 4 * (j * C::NRB + rb);
+            vb[c] = b.x;
+            vb[c + 1] = b.y;
+            vb[c + 2] = b.z;
+            vb[c + 3] = b.w;
+          }
+        }
+        const uint32_t tsf = tmem + (q * 32u << 16) + C::SF_BASE + stage * C::SF_COLS;
+        tmem_st16(tsf, va);
+        if constexpr (C::SFB_TCOLS == 32)
+          tmem_st32(tsf + C::SFA_TCOLS, vb);
+        else
+          tmem_st16(tsf + C::SFA_TCOLS, vb);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(sf_full0 + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_SF);
   } else {
     // ------------------------------------------------------------ epilogue
+    // Two warps per TMEM lane quarter, each owning half of the tile's columns.  A
+    // warp drains and stores the first half of its share, drains the second half,
+    // releases the accumulator to the MMA issuer, and then stores the rest, so the
+    // next tile's mainloop runs under most of this tile's stores.  Each 32x32 BF16
+    // block (row per lane) goes to a shared staging buffer and out with one TMA
+    // store, which also clips rows >= M; rows past M are never read from addend.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int ew = warp - C::EPI_WARP0;
+    const int c0 = (ew >> 2) * C::EPI_COLS;
+    const uint32_t stg = base + C::STG_OFF + (uint32_t)(ew * C::NSTG * C::STG_BUF);
     const float ga = *p.ga, gb = *p.gb;
     const float s_main = (ga > 0.0f && gb > 0.0f) ? __fmul_rn(ga, gb) : 1.0f;
     uint32_t amax = 0;
     uint32_t aphase = 0;
+    uint32_t nstore = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const int m0 = (tile % p.num_m) * C::BM;
       const int n0 = (tile / p.num_m) * BN;
@@ -297,19 +393,26 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const int m = m0 + q * 32 + lane;
       const bool row_ok = m < p.M;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
+#pragma unroll
+      for (int half = 0; half < C::EPI_COLS / 64; ++half) {
+        uint32_t v[64];
+        const int cb = c0 + 64 * half;
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)cb, v);
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cb + 32), v + 32);
         tmem_ld_wait();
-        const int n = n0 + c;
-        if (row_ok && n < p.N) {
+        if (half == C::EPI_COLS / 64 - 1) {  // the whole share is in registers
+          tc_fence_before();
+          mbar_arrive(acc_empty);
+        }
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          const int n = n0 + cb + c;
+          if (n >= p.N) continue;  // uniform across the warp (N % 32 == 0)
           float f[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[i]), s_main);
-          const size_t off = (size_t)m * p.N + n;
-          if (p.addend) {
-            const uint4* ad = reinterpret_cast<const uint4*>(p.addend + off);
+          for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[c + i]), s_main);
+          if (p.addend && row_ok) {
+            const uint4* ad = reinterpret_cast<const uint4*>(p.addend + (size_t)m * p.N + n);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               float r8[8];
@@ -322,18 +425,29 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-            amax = max(amax, max((w[i] & 0x7FFFu) << 16, (w[i] >> 16 & 0x7FFFu) << 16));
+            if (row_ok)
+              amax = max(amax, max((w[i] & 0x7FFFu) << 16, (w[i] >> 16 & 0x7FFFu) << 16));
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.out + off);
+          // staging buffer nstore % NSTG: wait until its previous store has read it
+          const uint32_t buf = stg + (nstore % C::NSTG) * C::STG_BUF;
+          if (nstore >= (uint32_t)C::NSTG && lane == 0) bulk_wait_read<C::NSTG - 1>();
+          __syncwarp();
+          uint4* sp = reinterpret_cast<uint4*>(smem + (buf - base) + 64 * lane);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            sp[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmOut, buf, n, m0 + q * 32);
+            bulk_commit();
+          }
+          ++nstore;
         }
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty);
       aphase ^= 1u;
     }
+    if (lane == 0) bulk_wait_all();
     if (p.out_amax) {
       amax = __reduce_max_sync(0xFFFFFFFFu, amax);
       if (lane == 0 && amax) atomicMax(p.out_amax, amax);
@@ -366,20 +480,24 @@ static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
   const int ntiles = L.p.num_m * L.p.num_n;
   const int grid = ntiles < L.num_sms ? ntiles : L.num_sms;
   note_launch();
-  kern<<<grid, 192, C::SMEM_BYTES, stream>>>(L.tmA, L.tmB, L.tmLA, L.tmLB, L.p);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(L.tmA, L.tmB, L.tmLA, L.tmLB, L.tmOut, L.p);
   return cudaGetLastError();
 }
 
 int gemm_block_n(int64_t N, int rpe) { return (N % 256 == 0 && rpe <= 64) ? 256 : 128; }
 
+int gemm_stage_row_bytes() { return kStageK / 2; }
+
+// Ring depth per configuration: as many 64-byte-row stages as shared memory holds
+// next to the LoRA operands.
 cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream) {
   if (bn == 256) {
-    if (rpe == 32) return launch_cfg<256, 256, 3, 32>(L, stream);
-    return launch_cfg<256, 256, 3, 64>(L, stream);
+    if (rpe == 32) return launch_cfg<256, kStageK, 3, 32>(L, stream);
+    return launch_cfg<256, kStageK, 3, 64>(L, stream);
   }
-  if (rpe == 32) return launch_cfg<128, 256, 4, 32>(L, stream);
-  if (rpe == 64) return launch_cfg<128, 256, 4, 64>(L, stream);
-  return launch_cfg<128, 256, 4, 128>(L, stream);
+  if (rpe == 32) return launch_cfg<128, kStageK, 5, 32>(L, stream);
+  if (rpe == 64) return launch_cfg<128, kStageK, 5, 64>(L, stream);
+  return launch_cfg<128, kStageK, 4, 128>(L, stream);
 }
 
 cudaError_t status_word_ptr(unsigned** ptr) {

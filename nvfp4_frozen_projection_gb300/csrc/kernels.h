@@ -13,6 +13,7 @@ enum : unsigned {
   PACT_DEV_ROLE_TMA = 1u << 8,
   PACT_DEV_ROLE_MMA = 1u << 9,
   PACT_DEV_ROLE_EPI = 1u << 10,
+  PACT_DEV_ROLE_SF = 1u << 11,
 };
 
 // Counts one kernel launch (pact_launch_count); called before every <<<>>>.
@@ -37,7 +38,7 @@ struct GemmParams {
 };
 
 struct GemmLaunch {
-  CUtensorMap tmA, tmB, tmLA, tmLB;
+  CUtensorMap tmA, tmB, tmLA, tmLB, tmOut;
   GemmParams p;
   int num_sms;
 };
@@ -45,6 +46,9 @@ struct GemmLaunch {
 // Tile width (128 or 256) for an output of N columns and a LoRA operand of rpe
 // columns, and the launcher.
 int gemm_block_n(int64_t N, int rpe);
+// Bytes of K per A/B tile row in one ring stage (the TMA box width; 64 -> 64B
+// swizzle, 128 -> 128B swizzle).
+int gemm_stage_row_bytes();
 cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream);
 cudaError_t status_word_ptr(unsigned** ptr);
 

@@ -10,8 +10,9 @@
 //
 // The result v = f * T is stored as BF16 [M, 2 RP] (RP = r rounded up to 16, 32 or
 // 64, zero padded): columns [0, RP) hold hi = bf16(v) and [RP, 2 RP) hold
-// lo = bf16(v - hi), and the right operand is stored twice ([B^T | B^T] or
-// [A | A]), so the fused BF16 LoRA product hi B + lo B carries v to about 16 bits
+// lo = bf16(v - hi); the GEMM multiplies both halves by the same right operand
+// ([N, RP] = B^T or [K, RP] = A, zero padded), so the fused BF16 LoRA product
+// hi B + lo B carries v to about 16 bits
 // (a single BF16 rounding of v costs up to 2^-9 |v| |B| per term, more than the
 // output tolerance allows).  f is chosen so that the GEMM epilogue's single
 // scale s = g_a g_w turns the fused product into the LoRA term:
@@ -87,8 +88,22 @@ __device__ __forceinline__ void reduce_and_store(float (*acc)[4], float* red, in
   }
 }
 
+// One padded right-operand row for the fused GEMM: the row's r adapter values,
+// zero padded to RP (the GEMM multiplies it by both halves of the left operand).
+template <int RP>
+__device__ __forceinline__ void store_row(uint16_t* out_row, const uint16_t* v) {
+  uint4* o = reinterpret_cast<uint4*>(out_row);
+#pragma unroll
+  for (int i = 0; i < RP / 8; ++i)
+    o[i] = make_uint4((uint32_t)v[8 * i] | ((uint32_t)v[8 * i + 1] << 16),
+                      (uint32_t)v[8 * i + 2] | ((uint32_t)v[8 * i + 3] << 16),
+                      (uint32_t)v[8 * i + 4] | ((uint32_t)v[8 * i + 5] << 16),
+                      (uint32_t)v[8 * i + 6] | ((uint32_t)v[8 * i + 7] << 16));
+}
+
 // T' = f * (X~ A): x_codes [M, K/2], x_sf (128x4 atoms), A [K, r] row-major.
-// Extra CTAs (blockIdx.x >= row CTAs) write Bt [N, RP] = B^T zero padded.
+// The first tcta CTAs write Bt [N, RP] = B^T zero padded (one row per thread, reads of
+// B coalesced along N); the rest own 16 rows of X each.
 template <int RP>
 __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict__ xc,
                                                        const uint8_t* __restrict__ xsf,
@@ -98,23 +113,22 @@ __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict
                                                        const uint16_t* __restrict__ B, int r,
                                                        float scale, int64_t N,
                                                        uint16_t* __restrict__ t_out,
-                                                       uint16_t* __restrict__ bt_out,
-                                                       int row_ctas) {
+                                                       uint16_t* __restrict__ bt_out, int tcta) {
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * RP];
-  if ((int)blockIdx.x >= row_ctas) {
-    const int64_t total = N * 2 * RP;
-    for (int64_t e = (int64_t)(blockIdx.x - row_ctas) * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)(gridDim.x - row_ctas) * blockDim.x) {
-      const int64_t n = e / (2 * RP);
-      const int j = (int)(e - n * 2 * RP) % RP;
-      bt_out[e] = j < r ? B[(int64_t)j * N + n] : (uint16_t)0;
+  if ((int)blockIdx.x < tcta) {
+    const int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (n < N) {
+      uint16_t v[RP];
+#pragma unroll
+      for (int j = 0; j < RP; ++j) v[j] = j < r ? B[(int64_t)j * N + n] : (uint16_t)0;
+      store_row<RP>(bt_out + n * RP, v);
     }
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t m0 = (int64_t)blockIdx.x * 16;
+  const int64_t m0 = (int64_t)(blockIdx.x - tcta) * 16;
   const int64_t ra = m0 + g, rb = m0 + g + 8;
   const bool va = ra < M, vb = rb < M;
   const int64_t c16p = K >> 4;
@@ -122,11 +136,12 @@ __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict
 #pragma unroll
   for (int jn = 0; jn < NT; ++jn) acc[jn][0] = acc[jn][1] = acc[jn][2] = acc[jn][3] = 0.0f;
 
-  const int64_t nchunks = K >> 6;
-  for (int64_t ch = warp; ch < nchunks; ch += 8) {
-    const int64_t blk = ch * 4 + c;  // block index along K
-    uint2 qa = make_uint2(0, 0), qb = make_uint2(0, 0);
-    uint32_t sa = 0, sb = 0;
+  // chunk ch of 64 along K: lane (g, c) holds block 4ch + c of rows g and g+8
+  auto load = [&](int64_t ch, uint2& qa, uint2& qb, uint32_t& sa, uint32_t& sb) {
+    const int64_t blk = ch * 4 + c;
+    qa = make_uint2(0, 0);
+    qb = make_uint2(0, 0);
+    sa = sb = 0;
     if (va) {
       qa = *reinterpret_cast<const uint2*>(xc + ra * (K >> 1) + blk * 8);
       sa = xsf[sf_offset(ra, blk, c16p)];
@@ -135,9 +150,18 @@ __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict
       qb = *reinterpret_cast<const uint2*>(xc + rb * (K >> 1) + blk * 8);
       sb = xsf[sf_offset(rb, blk, c16p)];
     }
+  };
+  const int64_t nchunks = K >> 6;
+  uint2 qa, qb;
+  uint32_t sa, sb;
+  if (warp < nchunks) load(warp, qa, qb, sa, sb);
+  for (int64_t ch = warp; ch < nchunks; ch += 8) {
+    uint2 nqa, nqb;
+    uint32_t nsa, nsb;
+    if (ch + 8 < nchunks) load(ch + 8, nqa, nqb, nsa, nsb);  // prefetch the next chunk
     const __half2 sca = __half2half2(__float2half_rn(e4m3_to_f32(sa)));
     const __half2 scb = __half2half2(__float2half_rn(e4m3_to_f32(sb)));
-    const int64_t kbase = blk * 16;
+    const int64_t kbase = (ch * 4 + c) * 16;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const uint32_t wa = (s < 2 ? qa.x : qa.y) >> (16 * (s & 1));
@@ -160,6 +184,10 @@ __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict
         mma_bf16_16816(acc[jn], a, b);
       }
     }
+    qa = nqa;
+    qb = nqb;
+    sa = nsa;
+    sb = nsb;
   }
   const float ga = *gx, gb = *gw;
   const bool normal = __fmul_rn(ga, gb) > 0.0f;
@@ -168,7 +196,7 @@ __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict
 }
 
 // U' = f * (dY B^T): dy [M, N] BF16, B [r, N] row-major.
-// Extra CTAs write Ap [K, RP] = A zero padded.
+// The first tcta CTAs write Ap [K, RP] = A zero padded; the rest own 16 rows of dY each.
 template <int RP>
 __global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restrict__ dy,
                                                          const float* __restrict__ gdy,
@@ -178,45 +206,52 @@ __global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restr
                                                          const uint16_t* __restrict__ B, int r,
                                                          float scale, int64_t K,
                                                          uint16_t* __restrict__ u_out,
-                                                         uint16_t* __restrict__ ap_out,
-                                                         int row_ctas) {
+                                                         uint16_t* __restrict__ ap_out, int tcta) {
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * RP];
-  if ((int)blockIdx.x >= row_ctas) {
-    const int64_t total = K * 2 * RP;
-    for (int64_t e = (int64_t)(blockIdx.x - row_ctas) * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)(gridDim.x - row_ctas) * blockDim.x) {
-      const int64_t k = e / (2 * RP);
-      const int j = (int)(e - k * 2 * RP) % RP;
-      ap_out[e] = j < r ? A[k * r + j] : (uint16_t)0;
+  if ((int)blockIdx.x < tcta) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < K) {
+      uint16_t v[RP];
+#pragma unroll
+      for (int j = 0; j < RP; ++j) v[j] = j < r ? A[k * r + j] : (uint16_t)0;
+      store_row<RP>(ap_out + k * RP, v);
     }
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t m0 = (int64_t)blockIdx.x * 16;
+  const int64_t m0 = (int64_t)(blockIdx.x - tcta) * 16;
   const int64_t ra = m0 + g, rb = m0 + g + 8;
   const bool va = ra < M, vb = rb < M;
   float acc[NT][4];
 #pragma unroll
   for (int jn = 0; jn < NT; ++jn) acc[jn][0] = acc[jn][1] = acc[jn][2] = acc[jn][3] = 0.0f;
 
-  const int64_t nchunks = N >> 6;
-  for (int64_t ch = warp; ch < nchunks; ch += 8) {
+  // chunk ch of 64 along N: lane (g, c) holds elements 16c .. 16c+15 of rows g, g+8
+  auto load = [&](int64_t ch, uint4* x) {
     const int64_t n0 = ch * 64 + 16 * c;
-    uint4 xa0 = make_uint4(0, 0, 0, 0), xa1 = xa0, xb0 = xa0, xb1 = xa0;
+    x[0] = x[1] = x[2] = x[3] = make_uint4(0, 0, 0, 0);
     if (va) {
       const uint4* p = reinterpret_cast<const uint4*>(dy + ra * N + n0);
-      xa0 = p[0];
-      xa1 = p[1];
+      x[0] = ldg_stream(p);
+      x[1] = ldg_stream(p + 1);
     }
     if (vb) {
       const uint4* p = reinterpret_cast<const uint4*>(dy + rb * N + n0);
-      xb0 = p[0];
-      xb1 = p[1];
+      x[2] = ldg_stream(p);
+      x[3] = ldg_stream(p + 1);
     }
-    const uint32_t wa[8] = {xa0.x, xa0.y, xa0.z, xa0.w, xa1.x, xa1.y, xa1.z, xa1.w};
-    const uint32_t wb[8] = {xb0.x, xb0.y, xb0.z, xb0.w, xb1.x, xb1.y, xb1.z, xb1.w};
+  };
+  const int64_t nchunks = N >> 6;
+  uint4 x[4];
+  if (warp < nchunks) load(warp, x);
+  for (int64_t ch = warp; ch < nchunks; ch += 8) {
+    uint4 nx[4];
+    if (ch + 8 < nchunks) load(ch + 8, nx);  // prefetch the next chunk
+    const int64_t n0 = ch * 64 + 16 * c;
+    const uint32_t wa[8] = {x[0].x, x[0].y, x[0].z, x[0].w, x[1].x, x[1].y, x[1].z, x[1].w};
+    const uint32_t wb[8] = {x[2].x, x[2].y, x[2].z, x[2].w, x[3].x, x[3].y, x[3].z, x[3].w};
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       uint32_t a[4] = {wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1]};
@@ -232,6 +267,8 @@ __global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restr
         mma_bf16_16816(acc[jn], a, b);
       }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = nx[i];
   }
   const float ga = *gdy, gb = *gw;
   const float s_main = __fmul_rn(ga, gb);
@@ -243,25 +280,25 @@ template <int RP>
 static cudaError_t fwd_rp(const uint8_t* xc, const uint8_t* xsf, const float* gx,
                           const float* gw, int64_t M, int64_t K, const uint16_t* A,
                           const uint16_t* B, int r, float scale, int64_t N, uint16_t* t_out,
-                          uint16_t* bt_out, int num_sms, cudaStream_t stream) {
+                          uint16_t* bt_out, int, cudaStream_t stream) {
   const int row_ctas = (int)((M + 15) / 16);
-  const int extra = (int)((N * RP + 255) / 256) < num_sms ? (int)((N * RP + 255) / 256) : num_sms;
+  const int tcta = (int)((N + 255) / 256);
   note_launch();
-  k_lora_down_fwd<RP><<<row_ctas + extra, 256, 0, stream>>>(xc, xsf, gx, gw, M, K, A, B, r,
-                                                            scale, N, t_out, bt_out, row_ctas);
+  k_lora_down_fwd<RP><<<tcta + row_ctas, 256, 0, stream>>>(xc, xsf, gx, gw, M, K, A, B, r,
+                                                           scale, N, t_out, bt_out, tcta);
   return cudaGetLastError();
 }
 
 template <int RP>
 static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* gw, int64_t M,
                             int64_t N, const uint16_t* A, const uint16_t* B, int r, float scale,
-                            int64_t K, uint16_t* u_out, uint16_t* ap_out, int num_sms,
+                            int64_t K, uint16_t* u_out, uint16_t* ap_out, int,
                             cudaStream_t stream) {
   const int row_ctas = (int)((M + 15) / 16);
-  const int extra = (int)((K * RP + 255) / 256) < num_sms ? (int)((K * RP + 255) / 256) : num_sms;
+  const int tcta = (int)((K + 255) / 256);
   note_launch();
-  k_lora_down_dgrad<RP><<<row_ctas + extra, 256, 0, stream>>>(dy, gdy, gw, M, N, A, B, r, scale,
-                                                              K, u_out, ap_out, row_ctas);
+  k_lora_down_dgrad<RP><<<tcta + row_ctas, 256, 0, stream>>>(dy, gdy, gw, M, N, A, B, r, scale,
+                                                             K, u_out, ap_out, tcta);
   return cudaGetLastError();
 }
 

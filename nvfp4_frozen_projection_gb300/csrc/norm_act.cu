@@ -271,11 +271,12 @@ __global__ void __launch_bounds__(256) k_silu_bwd(
       float rg[2], ru[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
+        // tolerance-checked BF16 gradient: fast exp and division are enough here
         const float gk = gv[i + k], uk = uv[i + k], dk = d[i + k];
-        const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, pexp(-gk)));
-        const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(gk, __fsub_rn(1.0f, sg))));
-        rg[k] = __fmul_rn(__fmul_rn(dk, uk), dsilu);
-        ru[k] = __fmul_rn(dk, __fmul_rn(gk, sg));
+        const float sg = __fdividef(1.0f, 1.0f + __expf(-gk));
+        const float dsilu = sg * fmaf(gk, 1.0f - sg, 1.0f);
+        rg[k] = (dk * uk) * dsilu;
+        ru[k] = dk * (gk * sg);
       }
       og[i / 2] = pack_bf16x2(rg[0], rg[1]);
       ou[i / 2] = pack_bf16x2(ru[0], ru[1]);
@@ -300,27 +301,39 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
     const uint16_t* __restrict__ gamma, const float* __restrict__ rstd,
     const uint16_t* __restrict__ dy, const uint16_t* dres, int64_t M, int64_t H,
     uint16_t* dx) {
+  // The row's codes, scales and dy stay in registers between the reduction and the
+  // output pass.  sum(dn * n) = sum(dy * gamma * yhat / gamma) = sum(dy * yhat), so
+  // the reduction needs no division; the output pass divides by gamma with the
+  // fast approximate division (the result is a tolerance-checked BF16 gradient).
   const int lane = threadIdx.x & 31;
   const int nb = (int)(H >> 4);
   const float g = *yg;
   for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < M;
        row += (int64_t)gridDim.x * 8) {
-    float dot = 0.0f;
+    uint2 cw[BPL];
+    uint32_t sb[BPL];
+    uint4 dv[BPL][2];
 #pragma unroll
     for (int j = 0; j < BPL; ++j) {
       const int b = lane + 32 * j;
       if (b < nb) {
-        float yv[16], gm[16], d[16];
-        dequant16(*reinterpret_cast<const uint2*>(yc + row * (H >> 1) + b * 8),
-                  ysf[sf_offset(row, b, nb)], g, yv);
-        const uint4* gp = reinterpret_cast<const uint4*>(gamma + b * 16);
-        bf16x8_to_f32(__ldg(gp), gm);
-        bf16x8_to_f32(__ldg(gp + 1), gm + 8);
+        cw[j] = *reinterpret_cast<const uint2*>(yc + row * (H >> 1) + b * 8);
+        sb[j] = ysf[sf_offset(row, b, nb)];
         const uint4* dp = reinterpret_cast<const uint4*>(dy + row * H + b * 16);
-        bf16x8_to_f32(__ldg(dp), d);
-        bf16x8_to_f32(__ldg(dp + 1), d + 8);
+        dv[j][0] = ldg_stream(dp);
+        dv[j][1] = ldg_stream(dp + 1);
+      }
+    }
+    float dot = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dot += (d[i] * gm[i]) * (yv[i] / gm[i]);
+    for (int j = 0; j < BPL; ++j) {
+      if (lane + 32 * j < nb) {
+        float yv[16], d[16];
+        dequant16(cw[j], sb[j], g, yv);
+        bf16x8_to_f32(dv[j][0], d);
+        bf16x8_to_f32(dv[j][1], d + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dot = fmaf(d[i], yv[i], dot);
       }
     }
 #pragma unroll
@@ -332,14 +345,12 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
       const int b = lane + 32 * j;
       if (b < nb) {
         float yv[16], gm[16], d[16], r[16];
-        dequant16(*reinterpret_cast<const uint2*>(yc + row * (H >> 1) + b * 8),
-                  ysf[sf_offset(row, b, nb)], g, yv);
+        dequant16(cw[j], sb[j], g, yv);
         const uint4* gp = reinterpret_cast<const uint4*>(gamma + b * 16);
         bf16x8_to_f32(__ldg(gp), gm);
         bf16x8_to_f32(__ldg(gp + 1), gm + 8);
-        const uint4* dp = reinterpret_cast<const uint4*>(dy + row * H + b * 16);
-        bf16x8_to_f32(__ldg(dp), d);
-        bf16x8_to_f32(__ldg(dp + 1), d + 8);
+        bf16x8_to_f32(dv[j][0], d);
+        bf16x8_to_f32(dv[j][1], d + 8);
         if (dres) {
           const uint4* rp = reinterpret_cast<const uint4*>(dres + row * H + b * 16);
           bf16x8_to_f32(rp[0], r);
@@ -351,9 +362,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
           float v[2];
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            const float n = yv[i + k] / gm[i + k];
-            const float dn = d[i + k] * gm[i + k];
-            v[k] = rs * (dn - n * c);
+            const float n = __fdividef(yv[i + k], gm[i + k]);
+            v[k] = rs * fmaf(d[i + k], gm[i + k], -n * c);
             if (dres) v[k] += r[i + k];
           }
           o[i / 2] = pack_bf16x2(v[0], v[1]);
