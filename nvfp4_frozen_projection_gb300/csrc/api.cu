@@ -192,6 +192,8 @@ int pact_quant_nvfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const
   if (rc) return rc;
   if (!x) return fail(PACT_ERR_INVALID_ARG, "x is null");
   if (M < 1 || K < 64 || K % 64) return fail(PACT_ERR_SHAPE, "need M >= 1 and K %% 64 == 0");
+  if (pad_to(M, 128) * (K / 64) >= (int64_t)1 << 31)
+    return fail(PACT_ERR_SHAPE, "tensor too large: pad128(M) * K / 64 must be < 2^31");
   if (ldx < K || ldx % 8) return fail(PACT_ERR_SHAPE, "need ldx >= K and ldx %% 8 == 0");
   if (!aligned(x, 16)) return fail(PACT_ERR_ALIGN, "x must be 16-byte aligned");
   if ((rc = check_nvfp4(out, "out", M, K, 16))) return rc;
@@ -237,11 +239,13 @@ int pact_pack_weight_bwd(const float* W, int64_t N, int64_t K, pact_nvfp4* out_b
 
 // ---------------------------------------------------------------- LoRA linear
 // Workspace: the LoRA left operand [M, 2 rp] (hi|lo BF16 pair) and the padded right
-// operand [rows, rp], both BF16.
-size_t pact_lora_linear_fwd_workspace_size(int64_t M, int64_t N, int64_t, int r) {
-  if (M < 1 || N < 1 || r < 1 || r > 64) return 0;
+// operand [rows, rp], both BF16; the forward also keeps A^T [rp, K] for its
+// down-projection.
+size_t pact_lora_linear_fwd_workspace_size(int64_t M, int64_t N, int64_t K, int r) {
+  if (M < 1 || N < 1 || K < 1 || r < 1 || r > 64) return 0;
   const int rp = rp_for(r);
-  return align256((size_t)M * 2 * rp * 2) + align256((size_t)N * rp * 2);
+  return align256((size_t)M * 2 * rp * 2) + align256((size_t)N * rp * 2) +
+         align256((size_t)K * rp * 2);
 }
 
 size_t pact_lora_linear_dgrad_workspace_size(int64_t M, int64_t, int64_t K, int r) {
@@ -346,9 +350,10 @@ int pact_lora_linear_fwd(const pact_nvfp4* xq, const pact_nvfp4* w_fwd, const ui
   const int rp = rp_for(r);
   uint16_t* t = (uint16_t*)ws;
   uint16_t* bt = (uint16_t*)((char*)ws + align256((size_t)M * 2 * rp * 2));
+  uint16_t* at = (uint16_t*)((char*)bt + align256((size_t)N * rp * 2));
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = launch_lora_down_fwd((const uint8_t*)xq->codes, (const uint8_t*)xq->sf, xq->g,
-                                       w_fwd->g, M, K, A, B, r, rp, scale, N, t, bt, d->sms, s);
+                                       w_fwd->g, M, K, A, B, r, rp, scale, N, t, bt, at, s);
   if (e != cudaSuccess) return cuda_fail(e, "lora down launch");
   return run_gemm(d, xq, w_fwd, M, N, K, t, bt, 2 * rp, residual_opt, y, out_amax_opt, s);
 }
@@ -375,7 +380,7 @@ int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact
   uint16_t* ap = (uint16_t*)((char*)ws + align256((size_t)M * 2 * rp * 2));
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = launch_lora_down_dgrad(dy, dyq->g, w_bwd->g, M, N, A, B, r, rp, scale, K, u, ap,
-                                         d->sms, s);
+                                         s);
   if (e != cudaSuccess) return cuda_fail(e, "lora down launch");
   return run_gemm(d, dyq, w_bwd, M, K, N, u, ap, 2 * rp, accumulate ? dx : nullptr, dx, nullptr,
                   s);
@@ -413,6 +418,8 @@ int pact_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I, const floa
   if (rc) return rc;
   if (!gateup) return fail(PACT_ERR_INVALID_ARG, "gateup is null");
   if (M < 1 || I < 64 || I % 64) return fail(PACT_ERR_SHAPE, "need M >= 1 and I %% 64 == 0");
+  if (pad_to(M, 128) * (I / 16) >= (int64_t)1 << 31)
+    return fail(PACT_ERR_SHAPE, "tensor too large: pad128(M) * I / 16 must be < 2^31");
   if (!aligned(gateup, 16)) return fail(PACT_ERR_ALIGN, "gateup must be 16-byte aligned");
   if ((rc = check_nvfp4(hq, "hq", M, I, 16)) || (rc = check_nvfp4(gate_q, "gate_q", M, I, 16)) ||
       (rc = check_nvfp4(up_q, "up_q", M, I, 16)))
@@ -436,6 +443,8 @@ int pact_silu_mul_bwd(const pact_nvfp4* gate_q, const pact_nvfp4* up_q, const ui
     return fail(PACT_ERR_INVALID_ARG, "gate_q, up_q, dh and dgateup are required");
   const int64_t M = gate_q->rows, I = gate_q->cols;
   if (M < 1 || I < 64 || I % 64) return fail(PACT_ERR_SHAPE, "need M >= 1 and I %% 64 == 0");
+  if (pad_to(M, 128) * (I / 16) >= (int64_t)1 << 31)
+    return fail(PACT_ERR_SHAPE, "tensor too large: pad128(M) * I / 16 must be < 2^31");
   if ((rc = check_nvfp4(gate_q, "gate_q", M, I, 16)) || (rc = check_nvfp4(up_q, "up_q", M, I, 16)))
     return rc;
   if (!aligned(dh, 16) || !aligned(dgateup, 16))

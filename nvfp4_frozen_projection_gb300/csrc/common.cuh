@@ -23,6 +23,25 @@ __host__ __device__ __forceinline__ int64_t pad_to(int64_t x, int64_t m) {
   return (x + m - 1) / m * m;
 }
 
+// n / d for n < 2^31 by a multiply-high and a shift (Granlund and Montgomery's
+// division by invariant integers): p = 31 + ceil(log2 d), m = ceil(2^p / d).
+struct FastDiv {
+  uint32_t d, m, s;
+  __host__ static FastDiv make(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint64_t p2 = 1ull << (31 + l);
+    FastDiv f;
+    f.d = d;
+    f.m = (uint32_t)((p2 + d - 1) / d);
+    f.s = l - 1;  // (n * m) >> (31 + l) == umulhi(n, m) >> (l - 1) for l >= 1
+    return f;
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    return d == 1 ? n : (__umulhi(n, m) >> s);
+  }
+};
+
 // Byte offset of the E4M3 scale of (row r, block c) in the 128x4-atom layout read
 // by the block-scaled tensor-core MMA (c16p = pad4(cols/16)).
 __host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t c16p) {
@@ -58,11 +77,31 @@ __device__ __forceinline__ uint32_t e2m1x2_mag(float lo, float hi) {
 
 __device__ __forceinline__ uint32_t sign_bit(float x) { return __float_as_uint(x) >> 31; }
 
+// Two E2M1 codes (one byte, first element in the low nibble) -> two floats, exact.
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h2)
+      : "r"(byte));
+  return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+
 // Encode 8 FP32 values that share the block decode step t (with rcp = 1/t) into
 // 8 E2M1 codes packed in a uint32 (element 0 in bits 0..3).  Signed-zero codes
-// when t == 0 or the element is zero.
+// when t == 0 or the element is zero.  With t > 0 and a finite rcp a zero element
+// already encodes as a zero magnitude; the masked path covers rcp = inf (a
+// subnormal t), where 0 * inf would otherwise be NaN.
 __device__ __forceinline__ uint32_t encode8(const float* x, float t, float rcp) {
   uint32_t w = 0;
+  if (t > 0.0f && rcp <= 3.4028234663852886e38f) {
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      const uint32_t mag = e2m1x2_mag(__fmul_rn(fabsf(x[i]), rcp), __fmul_rn(fabsf(x[i + 1]), rcp));
+      const uint32_t sg = ((__float_as_uint(x[i]) >> 28) & 8u) | ((__float_as_uint(x[i + 1]) >> 24) & 0x80u);
+      w |= (mag | sg) << (4 * i);
+    }
+    return w;
+  }
 #pragma unroll
   for (int i = 0; i < 8; i += 2) {
     float a0 = fabsf(x[i]), a1 = fabsf(x[i + 1]);
@@ -73,6 +112,19 @@ __device__ __forceinline__ uint32_t encode8(const float* x, float t, float rcp) 
     w |= b << (4 * i);
   }
   return w;
+}
+
+// Dequantise one block of 16 codes (8 bytes) with decode step s = e4m3(scale) * g.
+__device__ __forceinline__ void dequant16_f32(uint2 cw, float s, float* out) {
+  const uint32_t w[2] = {cw.x, cw.y};
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 f = e2m1x2_to_f32x2((w[h] >> (8 * b)) & 0xFFu);
+      out[8 * h + 2 * b] = f.x * s;
+      out[8 * h + 2 * b + 1] = f.y * s;
+    }
 }
 
 // Per-tensor scale and its block-scale divisor.
@@ -172,9 +224,27 @@ __device__ __forceinline__ float pexp(float x) {
   return scale_pow2(p, (int)n);
 }
 
+// pexp for |x| <= 87: the same operations without the range checks (n stays in
+// [-126, 126], so 2^n is a normal number and the final product is exact or
+// correctly rounded exactly as in pexp).
+__device__ __forceinline__ float pexp_mid(float x) {
+  float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
+  float f = __fmaf_rn(-n, 0x1.62e400p-1f, x);
+  f = __fmaf_rn(-n, 0x1.7f7d1cp-20f, f);
+  float p = 0x1.a01a02p-13f;
+  p = __fmaf_rn(p, f, 0x1.6c16c2p-10f);
+  p = __fmaf_rn(p, f, 0x1.111112p-7f);
+  p = __fmaf_rn(p, f, 0x1.555556p-5f);
+  p = __fmaf_rn(p, f, 0x1.555556p-3f);
+  p = __fmaf_rn(p, f, 0x1.000000p-1f);
+  p = __fmaf_rn(p, f, 1.0f);
+  p = __fmaf_rn(p, f, 1.0f);
+  return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+}
+
 // h = (g / (1 + exp(-g))) * u, FP32, fixed order.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-  float e = pexp(-g);
+  float e = fabsf(g) <= 87.0f ? pexp_mid(-g) : pexp(-g);
   float den = __fadd_rn(1.0f, e);
   float s = __fdiv_rn(g, den);
   return __fmul_rn(s, u);

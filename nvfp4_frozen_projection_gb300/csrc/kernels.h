@@ -61,16 +61,17 @@ cudaError_t launch_pack_weight(const float* W, int64_t N, int64_t K, int backwar
 
 // LoRA down-projections (BF16 tensor cores, FP32 accumulate), written pre-scaled
 // as the left LoRA operand [M, 2 rp] (hi/lo BF16 pair) of the fused GEMM, plus
-// the padded right operand [rows, 2 rp] (stored twice).
+// the padded right operand [rows, rp].  The forward also needs at_ws [rp, K] of
+// workspace for the transposed adapter.
 cudaError_t launch_lora_down_fwd(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
                                  const float* gw, int64_t M, int64_t K, const uint16_t* A,
                                  const uint16_t* B, int r, int rp, float scale, int64_t N,
-                                 uint16_t* t_out, uint16_t* bt_out, int num_sms,
+                                 uint16_t* t_out, uint16_t* bt_out, uint16_t* at_ws,
                                  cudaStream_t stream);
 cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const float* gw,
                                    int64_t M, int64_t N, const uint16_t* A, const uint16_t* B,
                                    int r, int rp, float scale, int64_t K, uint16_t* u_out,
-                                   uint16_t* ap_out, int num_sms, cudaStream_t stream);
+                                   uint16_t* ap_out, cudaStream_t stream);
 
 cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M,
                                  int64_t H, float eps, uint8_t* codes, uint8_t* sf, float* g,

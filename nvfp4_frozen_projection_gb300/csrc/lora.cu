@@ -101,34 +101,61 @@ __device__ __forceinline__ void store_row(uint16_t* out_row, const uint16_t* v) 
                       (uint32_t)v[8 * i + 6] | ((uint32_t)v[8 * i + 7] << 16));
 }
 
-// T' = f * (X~ A): x_codes [M, K/2], x_sf (128x4 atoms), A [K, r] row-major.
-// The first tcta CTAs write Bt [N, RP] = B^T zero padded (one row per thread, reads of
-// B coalesced along N); the rest own 16 rows of X each.
+// Prep: the small adapter layouts the two kernels below and the fused GEMM read.
+//   fwd:   At [RP, K] = A^T zero padded (the down-projection's B fragments become
+//          single 8-byte loads), Bt [N, RP] = B^T zero padded (GEMM right operand)
+//   dgrad: Ap [K, RP] = A zero padded (GEMM right operand)
+// One thread per output row; reads are coalesced along the long dimension.
+template <int RP>
+__global__ void __launch_bounds__(256) k_lora_prep(const uint16_t* __restrict__ A,
+                                                   const uint16_t* __restrict__ B, int r,
+                                                   int64_t K, int64_t N, int fwd,
+                                                   uint16_t* __restrict__ at_out,
+                                                   uint16_t* __restrict__ rhs_out) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (fwd) {
+    if (t < N) {  // Bt row n
+      uint16_t v[RP];
+#pragma unroll
+      for (int j = 0; j < RP; ++j) v[j] = j < r ? B[(int64_t)j * N + t] : (uint16_t)0;
+      store_row<RP>(rhs_out + t * RP, v);
+    } else if (t < N + K) {  // At column k: element (j, k) for every j
+      const int64_t k = t - N;
+#pragma unroll 4
+      for (int j = 0; j < RP; ++j) at_out[(int64_t)j * K + k] = j < r ? A[k * r + j] : (uint16_t)0;
+    }
+  } else if (t < K) {  // Ap row k
+    uint16_t v[RP];
+#pragma unroll
+    for (int j = 0; j < RP; ++j) v[j] = j < r ? A[t * r + j] : (uint16_t)0;
+    store_row<RP>(rhs_out + t * RP, v);
+  }
+}
+
+// T' = f * (X~ A): x_codes [M, K/2], x_sf (128x4 atoms), At [RP, K].  A CTA owns 16
+// rows; warp w takes the 64-wide K chunks w, w+8, ... with two chunks of codes in
+// flight ahead of the one it multiplies.  E2M1 pairs are decoded through a
+// 256-entry byte -> BF16x2 table in shared memory and scaled by the block's E4M3
+// scale with one exact BF16x2 multiply.
 template <int RP>
 __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict__ xc,
                                                        const uint8_t* __restrict__ xsf,
                                                        const float* __restrict__ gx,
                                                        const float* __restrict__ gw, int64_t M,
-                                                       int64_t K, const uint16_t* __restrict__ A,
-                                                       const uint16_t* __restrict__ B, int r,
-                                                       float scale, int64_t N,
-                                                       uint16_t* __restrict__ t_out,
-                                                       uint16_t* __restrict__ bt_out, int tcta) {
+                                                       int64_t K, const uint16_t* __restrict__ At,
+                                                       int r, float scale,
+                                                       uint16_t* __restrict__ t_out) {
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * RP];
-  if ((int)blockIdx.x < tcta) {
-    const int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (n < N) {
-      uint16_t v[RP];
-#pragma unroll
-      for (int j = 0; j < RP; ++j) v[j] = j < r ? B[(int64_t)j * N + n] : (uint16_t)0;
-      store_row<RP>(bt_out + n * RP, v);
-    }
-    return;
+  __shared__ uint32_t dec[256];
+  {
+    const float2 f = e2m1x2_to_f32x2(threadIdx.x);
+    dec[threadIdx.x] = pack_bf16x2(f.x, f.y);
   }
+  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t m0 = (int64_t)(blockIdx.x - tcta) * 16;
+  const int64_t m0 = (int64_t)blockIdx.x * 16;
   const int64_t ra = m0 + g, rb = m0 + g + 8;
   const bool va = ra < M, vb = rb < M;
   const int64_t c16p = K >> 4;
@@ -136,58 +163,59 @@ __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict
 #pragma unroll
   for (int jn = 0; jn < NT; ++jn) acc[jn][0] = acc[jn][1] = acc[jn][2] = acc[jn][3] = 0.0f;
 
+  struct Chunk {
+    uint2 qa, qb;
+    uint32_t sa, sb;
+  };
   // chunk ch of 64 along K: lane (g, c) holds block 4ch + c of rows g and g+8
-  auto load = [&](int64_t ch, uint2& qa, uint2& qb, uint32_t& sa, uint32_t& sb) {
+  auto load = [&](int64_t ch, Chunk& q) {
     const int64_t blk = ch * 4 + c;
-    qa = make_uint2(0, 0);
-    qb = make_uint2(0, 0);
-    sa = sb = 0;
+    q.qa = q.qb = make_uint2(0, 0);
+    q.sa = q.sb = 0;
     if (va) {
-      qa = *reinterpret_cast<const uint2*>(xc + ra * (K >> 1) + blk * 8);
-      sa = xsf[sf_offset(ra, blk, c16p)];
+      q.qa = __ldg(reinterpret_cast<const uint2*>(xc + ra * (K >> 1) + blk * 8));
+      q.sa = xsf[sf_offset(ra, blk, c16p)];
     }
     if (vb) {
-      qb = *reinterpret_cast<const uint2*>(xc + rb * (K >> 1) + blk * 8);
-      sb = xsf[sf_offset(rb, blk, c16p)];
+      q.qb = __ldg(reinterpret_cast<const uint2*>(xc + rb * (K >> 1) + blk * 8));
+      q.sb = xsf[sf_offset(rb, blk, c16p)];
     }
   };
   const int64_t nchunks = K >> 6;
-  uint2 qa, qb;
-  uint32_t sa, sb;
-  if (warp < nchunks) load(warp, qa, qb, sa, sb);
+  Chunk q0, q1;
+  if (warp < nchunks) load(warp, q0);
+  if (warp + 8 < nchunks) load(warp + 8, q1);
   for (int64_t ch = warp; ch < nchunks; ch += 8) {
-    uint2 nqa, nqb;
-    uint32_t nsa, nsb;
-    if (ch + 8 < nchunks) load(ch + 8, nqa, nqb, nsa, nsb);  // prefetch the next chunk
-    const __half2 sca = __half2half2(__float2half_rn(e4m3_to_f32(sa)));
-    const __half2 scb = __half2half2(__float2half_rn(e4m3_to_f32(sb)));
+    Chunk q2;
+    if (ch + 16 < nchunks) load(ch + 16, q2);  // two chunks ahead
+    const __nv_bfloat162 sca = __float2bfloat162_rn(e4m3_to_f32(q0.sa));
+    const __nv_bfloat162 scb = __float2bfloat162_rn(e4m3_to_f32(q0.sb));
     const int64_t kbase = (ch * 4 + c) * 16;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-      const uint32_t wa = (s < 2 ? qa.x : qa.y) >> (16 * (s & 1));
-      const uint32_t wb = (s < 2 ? qb.x : qb.y) >> (16 * (s & 1));
+      const uint32_t wa = (s < 2 ? q0.qa.x : q0.qa.y) >> (16 * (s & 1));
+      const uint32_t wb = (s < 2 ? q0.qb.x : q0.qb.y) >> (16 * (s & 1));
       uint32_t a[4];
-      a[0] = e2m1x2_scaled_bf16x2(wa & 0xFFu, sca);         // row g,   k 4s, 4s+1
-      a[1] = e2m1x2_scaled_bf16x2(wb & 0xFFu, scb);         // row g+8, k 4s, 4s+1
-      a[2] = e2m1x2_scaled_bf16x2((wa >> 8) & 0xFFu, sca);  // row g,   k 4s+2, 4s+3
-      a[3] = e2m1x2_scaled_bf16x2((wb >> 8) & 0xFFu, scb);  // row g+8, k 4s+2, 4s+3
+      __nv_bfloat162 t;
+      t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[wa & 0xFFu]), sca);
+      a[0] = *reinterpret_cast<uint32_t*>(&t);  // row g,   k 4s, 4s+1
+      t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[wb & 0xFFu]), scb);
+      a[1] = *reinterpret_cast<uint32_t*>(&t);  // row g+8, k 4s, 4s+1
+      t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[(wa >> 8) & 0xFFu]), sca);
+      a[2] = *reinterpret_cast<uint32_t*>(&t);  // row g,   k 4s+2, 4s+3
+      t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[(wb >> 8) & 0xFFu]), scb);
+      a[3] = *reinterpret_cast<uint32_t*>(&t);  // row g+8, k 4s+2, 4s+3
       const int64_t k = kbase + 4 * s;
 #pragma unroll
       for (int jn = 0; jn < NT; ++jn) {
-        const int col = jn * 8 + g;
-        uint32_t b[2] = {0u, 0u};
-        if (col < r) {
-          const uint16_t* ap = A + k * r + col;
-          b[0] = (uint32_t)ap[0] | ((uint32_t)ap[r] << 16);
-          b[1] = (uint32_t)ap[2 * r] | ((uint32_t)ap[3 * r] << 16);
-        }
+        // At rows >= r are zero, so no bounds test on the adapter column is needed
+        const uint2 bb = __ldg(reinterpret_cast<const uint2*>(At + (int64_t)(jn * 8 + g) * K + k));
+        const uint32_t b[2] = {bb.x, bb.y};
         mma_bf16_16816(acc[jn], a, b);
       }
     }
-    qa = nqa;
-    qb = nqb;
-    sa = nsa;
-    sb = nsb;
+    q0 = q1;
+    q1 = q2;
   }
   const float ga = *gx, gb = *gw;
   const bool normal = __fmul_rn(ga, gb) > 0.0f;
@@ -195,33 +223,21 @@ __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict
   reduce_and_store<RP>(acc, red, m0, M, f, t_out);
 }
 
-// U' = f * (dY B^T): dy [M, N] BF16, B [r, N] row-major.
-// The first tcta CTAs write Ap [K, RP] = A zero padded; the rest own 16 rows of dY each.
+// U' = f * (dY B^T): dy [M, N] BF16, B [r, N] row-major.  A CTA owns 16 rows; warp
+// w takes the 64-wide N chunks w, w+8, ... with two chunks in flight ahead.
 template <int RP>
 __global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restrict__ dy,
                                                          const float* __restrict__ gdy,
                                                          const float* __restrict__ gw,
                                                          int64_t M, int64_t N,
-                                                         const uint16_t* __restrict__ A,
                                                          const uint16_t* __restrict__ B, int r,
-                                                         float scale, int64_t K,
-                                                         uint16_t* __restrict__ u_out,
-                                                         uint16_t* __restrict__ ap_out, int tcta) {
+                                                         float scale,
+                                                         uint16_t* __restrict__ u_out) {
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * RP];
-  if ((int)blockIdx.x < tcta) {
-    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k < K) {
-      uint16_t v[RP];
-#pragma unroll
-      for (int j = 0; j < RP; ++j) v[j] = j < r ? A[k * r + j] : (uint16_t)0;
-      store_row<RP>(ap_out + k * RP, v);
-    }
-    return;
-  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t m0 = (int64_t)(blockIdx.x - tcta) * 16;
+  const int64_t m0 = (int64_t)blockIdx.x * 16;
   const int64_t ra = m0 + g, rb = m0 + g + 8;
   const bool va = ra < M, vb = rb < M;
   float acc[NT][4];
@@ -244,14 +260,15 @@ __global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restr
     }
   };
   const int64_t nchunks = N >> 6;
-  uint4 x[4];
-  if (warp < nchunks) load(warp, x);
+  uint4 x0[4], x1[4];
+  if (warp < nchunks) load(warp, x0);
+  if (warp + 8 < nchunks) load(warp + 8, x1);
   for (int64_t ch = warp; ch < nchunks; ch += 8) {
-    uint4 nx[4];
-    if (ch + 8 < nchunks) load(ch + 8, nx);  // prefetch the next chunk
+    uint4 x2[4];
+    if (ch + 16 < nchunks) load(ch + 16, x2);  // two chunks ahead
     const int64_t n0 = ch * 64 + 16 * c;
-    const uint32_t wa[8] = {x[0].x, x[0].y, x[0].z, x[0].w, x[1].x, x[1].y, x[1].z, x[1].w};
-    const uint32_t wb[8] = {x[2].x, x[2].y, x[2].z, x[2].w, x[3].x, x[3].y, x[3].z, x[3].w};
+    const uint32_t wa[8] = {x0[0].x, x0[0].y, x0[0].z, x0[0].w, x0[1].x, x0[1].y, x0[1].z, x0[1].w};
+    const uint32_t wb[8] = {x0[2].x, x0[2].y, x0[2].z, x0[2].w, x0[3].x, x0[3].y, x0[3].z, x0[3].w};
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       uint32_t a[4] = {wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1]};
@@ -260,7 +277,7 @@ __global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restr
         const int col = jn * 8 + g;
         uint32_t b[2] = {0u, 0u};
         if (col < r) {
-          const uint2 bb = *reinterpret_cast<const uint2*>(B + (int64_t)col * N + n0 + 4 * s);
+          const uint2 bb = __ldg(reinterpret_cast<const uint2*>(B + (int64_t)col * N + n0 + 4 * s));
           b[0] = bb.x;
           b[1] = bb.y;
         }
@@ -268,7 +285,10 @@ __global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restr
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = nx[i];
+    for (int i = 0; i < 4; ++i) {
+      x0[i] = x1[i];
+      x1[i] = x2[i];
+    }
   }
   const float ga = *gdy, gb = *gw;
   const float s_main = __fmul_rn(ga, gb);
@@ -280,52 +300,49 @@ template <int RP>
 static cudaError_t fwd_rp(const uint8_t* xc, const uint8_t* xsf, const float* gx,
                           const float* gw, int64_t M, int64_t K, const uint16_t* A,
                           const uint16_t* B, int r, float scale, int64_t N, uint16_t* t_out,
-                          uint16_t* bt_out, int, cudaStream_t stream) {
-  const int row_ctas = (int)((M + 15) / 16);
-  const int tcta = (int)((N + 255) / 256);
+                          uint16_t* bt_out, uint16_t* at_ws, cudaStream_t stream) {
   note_launch();
-  k_lora_down_fwd<RP><<<tcta + row_ctas, 256, 0, stream>>>(xc, xsf, gx, gw, M, K, A, B, r,
-                                                           scale, N, t_out, bt_out, tcta);
+  k_lora_prep<RP><<<(int)((N + K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 1, at_ws,
+                                                                    bt_out);
+  note_launch();
+  k_lora_down_fwd<RP><<<(int)((M + 15) / 16), 256, 0, stream>>>(xc, xsf, gx, gw, M, K, at_ws, r,
+                                                                 scale, t_out);
   return cudaGetLastError();
 }
 
 template <int RP>
 static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* gw, int64_t M,
                             int64_t N, const uint16_t* A, const uint16_t* B, int r, float scale,
-                            int64_t K, uint16_t* u_out, uint16_t* ap_out, int,
-                            cudaStream_t stream) {
-  const int row_ctas = (int)((M + 15) / 16);
-  const int tcta = (int)((K + 255) / 256);
+                            int64_t K, uint16_t* u_out, uint16_t* ap_out, cudaStream_t stream) {
   note_launch();
-  k_lora_down_dgrad<RP><<<tcta + row_ctas, 256, 0, stream>>>(dy, gdy, gw, M, N, A, B, r, scale,
-                                                             K, u_out, ap_out, tcta);
+  k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
+  note_launch();
+  k_lora_down_dgrad<RP><<<(int)((M + 15) / 16), 256, 0, stream>>>(dy, gdy, gw, M, N, B, r, scale,
+                                                                   u_out);
   return cudaGetLastError();
 }
 
 cudaError_t launch_lora_down_fwd(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
                                  const float* gw, int64_t M, int64_t K, const uint16_t* A,
                                  const uint16_t* B, int r, int rp, float scale, int64_t N,
-                                 uint16_t* t_out, uint16_t* bt_out, int num_sms,
+                                 uint16_t* t_out, uint16_t* bt_out, uint16_t* at_ws,
                                  cudaStream_t stream) {
   if (rp == 16)
-    return fwd_rp<16>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, t_out, bt_out, num_sms,
+    return fwd_rp<16>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, t_out, bt_out, at_ws,
                       stream);
   if (rp == 32)
-    return fwd_rp<32>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, t_out, bt_out, num_sms,
+    return fwd_rp<32>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, t_out, bt_out, at_ws,
                       stream);
-  return fwd_rp<64>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, t_out, bt_out, num_sms,
-                    stream);
+  return fwd_rp<64>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, t_out, bt_out, at_ws, stream);
 }
 
 cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const float* gw,
                                    int64_t M, int64_t N, const uint16_t* A, const uint16_t* B,
                                    int r, int rp, float scale, int64_t K, uint16_t* u_out,
-                                   uint16_t* ap_out, int num_sms, cudaStream_t stream) {
-  if (rp == 16)
-    return dgrad_rp<16>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, num_sms, stream);
-  if (rp == 32)
-    return dgrad_rp<32>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, num_sms, stream);
-  return dgrad_rp<64>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, num_sms, stream);
+                                   uint16_t* ap_out, cudaStream_t stream) {
+  if (rp == 16) return dgrad_rp<16>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, stream);
+  if (rp == 32) return dgrad_rp<32>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, stream);
+  return dgrad_rp<64>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, stream);
 }
 
 }  // namespace pact

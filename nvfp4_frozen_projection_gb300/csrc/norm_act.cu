@@ -147,13 +147,14 @@ __global__ void __launch_bounds__(256) k_rmsnorm_encode(
 // ============================================================== SiLU-multiply
 // Pass 1: amax of h, gate and up.  One thread per block of 16 columns.
 __global__ void __launch_bounds__(256) k_silu_amax(const uint16_t* __restrict__ gu, int64_t M,
-                                                   int64_t I, unsigned* __restrict__ amax3) {
-  const int64_t bpr = I >> 4;
-  const int64_t total = M * bpr;
+                                                   int64_t I, FastDiv bpr_div,
+                                                   unsigned* __restrict__ amax3) {
+  const uint32_t bpr = (uint32_t)(I >> 4);
+  const uint32_t total = (uint32_t)M * bpr;
   uint32_t ah = 0, ag = 0, au = 0;
-  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = it / bpr, b = it - row * bpr;
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += gridDim.x * blockDim.x) {
+    const int64_t row = bpr_div.div(it), b = it - (uint32_t)row * bpr;
     const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2 * I + b * 16);
     const uint4* up = reinterpret_cast<const uint4*>(gu + row * 2 * I + I + b * 16);
     const uint4 g0 = ldg_stream(gp), g1 = ldg_stream(gp + 1);
@@ -181,7 +182,7 @@ struct SiluOut {
 };
 
 __global__ void __launch_bounds__(256) k_silu_encode(const uint16_t* __restrict__ gu, int64_t M,
-                                                     int64_t Mpad, int64_t I,
+                                                     int64_t Mpad, int64_t I, FastDiv bpr_div,
                                                      const float* __restrict__ amax3_opt,
                                                      const unsigned* __restrict__ amax3,
                                                      SiluOut out) {
@@ -191,11 +192,11 @@ __global__ void __launch_bounds__(256) k_silu_encode(const uint16_t* __restrict_
     ts[k] = tensor_scale(amax3_opt ? amax3_opt[k] : __uint_as_float(amax3[k]));
     if (blockIdx.x == 0 && threadIdx.x == 0) *out.g[k] = ts[k].g;
   }
-  const int64_t bpr = I >> 4;
-  const int64_t total = Mpad * bpr;
-  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = it / bpr, b = it - row * bpr;
+  const uint32_t bpr = (uint32_t)(I >> 4);
+  const uint32_t total = (uint32_t)Mpad * bpr;
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += gridDim.x * blockDim.x) {
+    const int64_t row = bpr_div.div(it), b = it - (uint32_t)row * bpr;
     const int64_t so = sf_offset(row, b, bpr);
     if (row >= M) {
 #pragma unroll
@@ -228,40 +229,25 @@ __global__ void __launch_bounds__(256) k_silu_encode(const uint16_t* __restrict_
 }
 
 // ============================================================== backward kernels
-// Dequantise one block of 16 (codes: 8 bytes) in FP32.
-__device__ __forceinline__ void dequant16(uint2 cw, uint32_t sfb, float g, float* out) {
-  const float s = __fmul_rn(e4m3_to_f32(sfb), g);
-  const uint32_t w[2] = {cw.x, cw.y};
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t q = (w[h] >> (4 * i)) & 0xFu;
-      // magnitudes {0, .5, 1, 1.5} = i/2 for i < 4; {2, 3, 4, 6} = 2^(i/2-1) * (1 or 1.5)
-      const uint32_t i7 = q & 7u;
-      const float mag = i7 < 4u ? 0.5f * (float)i7
-                                : (float)(1u << ((i7 >> 1) - 1u)) * ((i7 & 1u) ? 1.5f : 1.0f);
-      out[8 * h + i] = __fmul_rn((q & 8u) ? -mag : mag, s);
-    }
-}
-
 // SiLU-multiply backward; one thread per block of 16 columns.
 __global__ void __launch_bounds__(256) k_silu_bwd(
     const uint8_t* __restrict__ gc, const uint8_t* __restrict__ gsf, const float* __restrict__ gg,
     const uint8_t* __restrict__ uc, const uint8_t* __restrict__ usf, const float* __restrict__ ug,
-    const uint16_t* __restrict__ dh, int64_t M, int64_t I, uint16_t* __restrict__ dgu,
-    unsigned* __restrict__ out_amax) {
-  const int64_t bpr = I >> 4;
-  const int64_t total = M * bpr;
+    const uint16_t* __restrict__ dh, int64_t M, int64_t I, FastDiv bpr_div,
+    uint16_t* __restrict__ dgu, unsigned* __restrict__ out_amax) {
+  const uint32_t bpr = (uint32_t)(I >> 4);
+  const uint32_t total = (uint32_t)M * bpr;
   const float g_gate = *gg, g_up = *ug;
   uint32_t amax = 0;
-  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = it / bpr, b = it - row * bpr;
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += gridDim.x * blockDim.x) {
+    const int64_t row = bpr_div.div(it), b = it - (uint32_t)row * bpr;
     const int64_t so = sf_offset(row, b, bpr);
     float gv[16], uv[16], d[16];
-    dequant16(*reinterpret_cast<const uint2*>(gc + row * (I >> 1) + b * 8), gsf[so], g_gate, gv);
-    dequant16(*reinterpret_cast<const uint2*>(uc + row * (I >> 1) + b * 8), usf[so], g_up, uv);
+    dequant16_f32(*reinterpret_cast<const uint2*>(gc + row * (I >> 1) + b * 8),
+                  e4m3_to_f32(gsf[so]) * g_gate, gv);
+    dequant16_f32(*reinterpret_cast<const uint2*>(uc + row * (I >> 1) + b * 8),
+                  e4m3_to_f32(usf[so]) * g_up, uv);
     const uint4* dp = reinterpret_cast<const uint4*>(dh + row * I + b * 16);
     bf16x8_to_f32(ldg_stream(dp), d);
     bf16x8_to_f32(ldg_stream(dp + 1), d + 8);
@@ -329,7 +315,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
     for (int j = 0; j < BPL; ++j) {
       if (lane + 32 * j < nb) {
         float yv[16], d[16];
-        dequant16(cw[j], sb[j], g, yv);
+        dequant16_f32(cw[j], e4m3_to_f32(sb[j]) * g, yv);
         bf16x8_to_f32(dv[j][0], d);
         bf16x8_to_f32(dv[j][1], d + 8);
 #pragma unroll
@@ -345,7 +331,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
       const int b = lane + 32 * j;
       if (b < nb) {
         float yv[16], gm[16], d[16], r[16];
-        dequant16(cw[j], sb[j], g, yv);
+        dequant16_f32(cw[j], e4m3_to_f32(sb[j]) * g, yv);
         const uint4* gp = reinterpret_cast<const uint4*>(gamma + b * 16);
         bf16x8_to_f32(__ldg(gp), gm);
         bf16x8_to_f32(__ldg(gp + 1), gm + 8);
@@ -433,8 +419,8 @@ cudaError_t launch_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I,
     cudaError_t e = cudaMemsetAsync(ws_amax3, 0, 3 * sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
     note_launch();
-    k_silu_amax<<<blocks_for(M * (I / 16), 256, num_sms * 8), 256, 0, stream>>>(gateup, M, I,
-                                                                                 ws_amax3);
+    k_silu_amax<<<blocks_for(M * (I / 16), 256, num_sms * 8), 256, 0, stream>>>(
+        gateup, M, I, FastDiv::make((uint32_t)(I / 16)), ws_amax3);
   }
   SiluOut o;
   for (int k = 0; k < 3; ++k) {
@@ -445,7 +431,7 @@ cudaError_t launch_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I,
   const int64_t Mpad = pad_to(M, 128);
   note_launch();
   k_silu_encode<<<blocks_for(Mpad * (I / 16), 256, num_sms * 16), 256, 0, stream>>>(
-      gateup, M, Mpad, I, amax3_opt, ws_amax3, o);
+      gateup, M, Mpad, I, FastDiv::make((uint32_t)(I / 16)), amax3_opt, ws_amax3, o);
   return cudaGetLastError();
 }
 
@@ -459,7 +445,7 @@ cudaError_t launch_silu_mul_bwd(const uint8_t* gc, const uint8_t* gsf, const flo
   }
   note_launch();
   k_silu_bwd<<<blocks_for(M * (I / 16), 256, num_sms * 16), 256, 0, stream>>>(
-      gc, gsf, gg, uc, usf, ug, dh, M, I, dgu, out_amax);
+      gc, gsf, gg, uc, usf, ug, dh, M, I, FastDiv::make((uint32_t)(I / 16)), dgu, out_amax);
   return cudaGetLastError();
 }
 

@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(256) k_amax_f32(const float* __restrict__ w, i
 // pad128(M)) write zero scale words so the padded scale array is fully defined.
 __global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__ x, int64_t M,
                                                     int64_t K, int64_t ldx, int64_t Mpad,
+                                                    FastDiv chunks_div,
                                                     const float* __restrict__ amax_opt,
                                                     const unsigned* __restrict__ amax_bits,
                                                     uint8_t* __restrict__ codes,
@@ -68,18 +69,18 @@ __global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__
   const float amax = amax_opt ? *amax_opt : __uint_as_float(*amax_bits);
   const TensorScale ts = tensor_scale(amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
-  const int64_t chunks = K >> 6;
-  const int64_t total = Mpad * chunks;
+  const uint32_t chunks = (uint32_t)(K >> 6);
+  const uint32_t total = (uint32_t)Mpad * chunks;  // < 2^31 (checked by the caller)
   const int64_t c16p = K >> 4;
-  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = it / chunks, ch = it - r * chunks;
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += gridDim.x * blockDim.x) {
+    const uint32_t r = chunks_div.div(it), ch = it - r * chunks;
     uint32_t sfw = 0;
     if (r < M) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + r * ldx + ch * 64);
+      const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * ldx + ch * 64);
       uint4 v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = ldg_stream(src + i);
+      for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i);
       uint32_t w[8];
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__
         w[2 * b + 1] = encode8(f + 8, t, rcp);
         sfw |= s << (8 * b);
       }
-      uint4* dst = reinterpret_cast<uint4*>(codes + r * (K >> 1) + ch * 32);
+      uint4* dst = reinterpret_cast<uint4*>(codes + (int64_t)r * (K >> 1) + ch * 32);
       dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
       dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
@@ -174,7 +175,7 @@ cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
   const int64_t Mpad = pad_to(M, 128);
   note_launch();
   k_quant_bf16<<<grid_for(Mpad * (K / 64), 256, num_sms * 16), 256, 0, stream>>>(
-      x, M, K, ldx, Mpad, amax_opt, ws_amax, codes, sf, g);
+      x, M, K, ldx, Mpad, FastDiv::make((uint32_t)(K / 64)), amax_opt, ws_amax, codes, sf, g);
   return cudaGetLastError();
 }
 

@@ -54,8 +54,9 @@ def test_host_helpers_without_gpu(lib):
     assert so.pact_nvfp4_sf_bytes(1, 64) == 128 * 4
     so.pact_lora_linear_fwd_workspace_size.restype = ctypes.c_size_t
     so.pact_lora_linear_fwd_workspace_size.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int]
-    # LoRA left operand is a hi/lo BF16 pair (2 x 16 columns), right operand 16 columns
-    assert so.pact_lora_linear_fwd_workspace_size(4096, 3072, 3072, 16) == 4096 * 64 + 3072 * 32
+    # LoRA left operand is a hi/lo BF16 pair (2 x 16 columns), right operand 16 columns,
+    # and the transposed adapter A^T [16, K]
+    assert so.pact_lora_linear_fwd_workspace_size(4096, 3072, 3072, 16) == 4096 * 64 + 3072 * 32 + 3072 * 32
     assert so.pact_lora_linear_fwd_workspace_size(4096, 3072, 3072, 65) == 0
     so.pact_version.restype = ctypes.c_char_p
     assert b"sm_103a" in so.pact_version()
