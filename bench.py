@@ -111,41 +111,13 @@ class ClockSampler:
 
 # --------------------------------------------------------------------- oracle leg
 def oracle_stack_sample(d, packs, rows: int):
-    """The oracle run over the first `rows` tokens of the layer-3b step (same call
-    sequence as the GPU step; activations rounded to BF16 where the GPU stores
-    BF16).  Returns the GEMM FLOPs of the sample."""
-    import oracle as orc
-    b = wl.bf16_round
-    sl = slice(0, rows)
-    x, attn, dy = d["x"][sl], d["attn"][sl], d["dy"][sl]
-    dq, dk, dv = d["dq"][sl], d["dk"][sl], d["dv"][sl]
-    P = {k: d[k] for k in ("q", "k", "v", "o", "gate_up", "down")}
-
-    def fwd(name, xq, residual=None):
-        p = P[name]
-        return orc.lora_linear_fwd(xq, packs[name][0], p.A, p.B, p.alpha, residual=residual)
-
-    def dgrad(name, gq, g, prev=None):
-        p = P[name]
-        return orc.lora_linear_dgrad(gq, g, packs[name][1], p.A, p.B, p.alpha, dx_prev=prev)
-
-    xq1, rstd1 = orc.rmsnorm_quant(x, d["gamma1"], d["eps"])
-    for n in ("q", "k", "v"):
-        fwd(n, xq1)
-    h1 = b(fwd("o", orc.quantize(attn), residual=x))
-    xq2, rstd2 = orc.rmsnorm_quant(h1, d["gamma2"], d["eps"])
-    gu = b(fwd("gate_up", xq2))
-    hq, gq, uq = orc.silu_mul_quant(gu)
-    fwd("down", hq, residual=h1)
-    dh = b(dgrad("down", orc.quantize(dy), dy))
-    dgu = b(orc.silu_mul_bwd(gq, uq, dh))
-    dxn2 = b(dgrad("gate_up", orc.quantize(dgu), dgu))
-    dh1 = b(orc.rmsnorm_bwd(xq2, d["gamma2"], rstd2, dxn2, dres=dy))
-    dgrad("o", orc.quantize(dh1), dh1)
-    dxn1 = b(dgrad("q", orc.quantize(dq), dq))
-    dxn1 = b(dgrad("k", orc.quantize(dk), dk, dxn1))
-    dxn1 = b(dgrad("v", orc.quantize(dv), dv, dxn1))
-    orc.rmsnorm_bwd(xq1, d["gamma1"], rstd1, dxn1, dres=dh1)
+    """The oracle chain of the layer-3b step (the same call sequence as the GPU
+    step) over the first `rows` tokens.  Returns the GEMM FLOPs of the sample."""
+    from oracle import chain
+    sub = dict(d)
+    for k in ("x", "attn", "dy", "dq", "dk", "dv"):
+        sub[k] = d[k][:rows]
+    chain.decoder_layer(sub, packs)
     return wl.gemm_flops_per_step(5, m=rows)
 
 
@@ -206,17 +178,9 @@ def run_reference(args):
 # --------------------------------------------------------------------- GPU leg
 def build_stack(d, dev):
     import nvfp4_frozen_projection_gb300 as pk
-    from nvfp4_frozen_projection_gb300.stack import DecoderProjectionStack, LoraLinear
+    from nvfp4_frozen_projection_gb300.stack import DecoderProjectionStack
 
-    def t32(a):
-        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
-
-    proj = {}
-    for k in ("q", "k", "v", "o", "gate_up", "down"):
-        p = d[k]
-        proj[k] = LoraLinear(t32(p.W), t32(p.A).bfloat16(), t32(p.B).bfloat16(), p.scale)
-    stack = DecoderProjectionStack(d["x"].shape[0], proj, t32(d["gamma1"]).bfloat16(),
-                                   t32(d["gamma2"]).bfloat16(), float(d["eps"]))
+    stack = DecoderProjectionStack.from_workload(d, dev)
     torch.cuda.synchronize()
     pk.pact_check_status()
     return stack
@@ -285,6 +249,24 @@ def time_call(fn, reps):
     return statistics.mean(b.elapsed_time(e) for b, e in evs)
 
 
+# ------------------------------------------------------------------ multi-rank
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time: every rank runs an independent replica of the step
+    (no data-path collective), so the job takes as long as its slowest rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Units processed by all ranks per second (weak scaling: each rank does the
+    same fixed amount of work)."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -338,9 +320,14 @@ def main():
         with torch.cuda.graph(graph):
             step()
         launches_per_step = pk.pact_launch_count() - n0
+        # the two replays before the timed region are what a profiler started with
+        # collection off (ncu --profile-from-start off) records
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
         for _ in range(2):
             graph.replay()
         torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
         run = graph.replay
     else:
         step()
@@ -366,15 +353,11 @@ def main():
     ms = t_begin.elapsed_time(t_end) / args.steps
     clocks = clk.summary()
     pk.pact_check_status()
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dev)
 
     flops = stack.gemm_flops()
-    value = flops * world / (ms * 1e-3) / 1e12
-    tokens_per_s = stack.m * world / (ms * 1e-3)
+    value = job_throughput(flops, world, ms) / 1e12
+    tokens_per_s = job_throughput(stack.m, world, ms)
 
     # ---------------- end to end: pinned host inputs in, result (dx) out, per step
     host_out = torch.empty_like(stack.dx, device="cpu").pin_memory()
@@ -390,7 +373,7 @@ def main():
     e_end.record()
     torch.cuda.synchronize()
     barrier()
-    ms_e2e = e_begin.elapsed_time(e_end) / args.steps
+    ms_e2e = max_over_ranks(e_begin.elapsed_time(e_end) / args.steps, dev)
     h2d = sum(h.numel() * h.element_size() for h in host_in)
     d2h = host_out.numel() * host_out.element_size()
 
@@ -423,7 +406,7 @@ def main():
                    "l2": "no flush: one step moves several GB through HBM (L2 is 129 MB)",
                    "graph": graph is not None, "parallelism": f"replicas x{world}"},
         "clocks": clocks,
-        "e2e": {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_throughput(flops, world, ms_e2e) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "gpu_launches": int(launches_per_step) * args.steps,
         "layer_tokens_per_s": tokens_per_s,

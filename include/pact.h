@@ -256,6 +256,15 @@ int pact_test_pexp(const float* x, float* y, int64_t n, pact_stream_t stream);
 uint64_t pact_launch_count(void);
 int pact_profile_next_gemm(void* begin_event, void* end_event);
 
+/*
+ * Test of the failure path (no counterpart in the method).  Launches one thread
+ * that waits, with the bounded wait the GEMM kernels use, on a barrier that nothing
+ * completes; after limit_us microseconds (1 .. 2e6) it records a timeout in the
+ * device status word and returns.  pact_check_status() then reports
+ * PACT_ERR_TIMEOUT, and the context stays usable.
+ */
+int pact_test_wait_timeout(uint32_t limit_us, pact_stream_t stream);
+
 /* Synchronises the stream, then returns and clears the device status word:
  * PACT_OK, PACT_ERR_TIMEOUT or PACT_ERR_DEVICE_STATUS.  For tests and debugging. */
 int pact_check_status(pact_stream_t stream);

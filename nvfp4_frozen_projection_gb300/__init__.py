@@ -22,7 +22,7 @@ __all__ = [
     "pact_lora_linear_fwd", "pact_lora_linear_fwd_noalloc", "pact_lora_linear_dgrad",
     "pact_rmsnorm_quant",
     "pact_silu_mul_quant", "pact_silu_mul_bwd", "pact_rmsnorm_bwd", "pact_test_pexp",
-    "pact_check_status", "pact_device_supported", "pact_launch_count", "pact_profile_next_gemm",
+    "pact_test_wait_timeout", "pact_check_status", "pact_device_supported", "pact_launch_count", "pact_profile_next_gemm",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +69,7 @@ _SIGNATURES = {
     "pact_silu_mul_bwd": (_int, [_SP, _SP, _vp, _vp, _vp, _vp]),
     "pact_rmsnorm_bwd": (_int, [_SP, _vp, _vp, _vp, _vp, _vp, _vp]),
     "pact_test_pexp": (_int, [_vp, _vp, _i64, _vp]),
+    "pact_test_wait_timeout": (_int, [ctypes.c_uint32, _vp]),
     "pact_check_status": (_int, [_vp]),
     "pact_launch_count": (ctypes.c_uint64, []),
     "pact_profile_next_gemm": (_int, [_vp, _vp]),
@@ -337,6 +338,12 @@ def pact_test_pexp(x: torch.Tensor) -> torch.Tensor:
     y = torch.empty_like(x)
     _check(lib.pact_test_pexp(_ptr(x), _ptr(y), x.numel(), _stream()))
     return y
+
+
+def pact_test_wait_timeout(limit_us: int = 1000) -> None:
+    """Launch a kernel whose bounded wait runs out after limit_us microseconds; the
+    next pact_check_status() raises PactError with code PACT_ERR_TIMEOUT (6)."""
+    _check(load_library().pact_test_wait_timeout(int(limit_us), _stream()))
 
 
 def pact_check_status() -> None:

@@ -477,6 +477,16 @@ int pact_rmsnorm_bwd(const pact_nvfp4* yq, const uint16_t* gamma, const float* r
   return e == cudaSuccess ? PACT_OK : cuda_fail(e, "rmsnorm bwd launch");
 }
 
+int pact_test_wait_timeout(uint32_t limit_us, pact_stream_t stream) {
+  DeviceInfo* d;
+  int rc = device_info(&d);
+  if (rc) return rc;
+  if (limit_us == 0 || limit_us > 2000000)
+    return fail(PACT_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");
+  cudaError_t e = launch_wait_timeout((uint64_t)limit_us * 1000ull, (cudaStream_t)stream);
+  return e == cudaSuccess ? PACT_OK : cuda_fail(e, "wait-timeout launch");
+}
+
 int pact_test_pexp(const float* x, float* y, int64_t n, pact_stream_t stream) {
   DeviceInfo* d;
   int rc = device_info(&d);

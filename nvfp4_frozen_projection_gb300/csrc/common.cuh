@@ -65,8 +65,9 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu)));
 }
 
-// Two non-negative magnitudes -> E2M1 magnitude codes (RN, satfinite at 6):
-// lo in bits 0..3, hi in bits 4..7.
+// Two values -> E2M1 codes (RN, satfinite at 6): lo in bits 0..3, hi in bits 4..7.
+// The sign bit follows the input, also when it rounds to zero (-0.1 -> 0x8,
+// -0.0 -> 0x8; checked on GB300), matching the oracle's sign rule.
 __device__ __forceinline__ uint32_t e2m1x2_mag(float lo, float hi) {
   uint32_t r;
   asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
@@ -94,12 +95,10 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
 __device__ __forceinline__ uint32_t encode8(const float* x, float t, float rcp) {
   uint32_t w = 0;
   if (t > 0.0f && rcp <= 3.4028234663852886e38f) {
+    // x * rcp keeps the sign of x (rcp > 0) and the convert keeps it on zeros
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-      const uint32_t mag = e2m1x2_mag(__fmul_rn(fabsf(x[i]), rcp), __fmul_rn(fabsf(x[i + 1]), rcp));
-      const uint32_t sg = ((__float_as_uint(x[i]) >> 28) & 8u) | ((__float_as_uint(x[i + 1]) >> 24) & 0x80u);
-      w |= (mag | sg) << (4 * i);
-    }
+    for (int i = 0; i < 8; i += 2)
+      w |= e2m1x2_mag(__fmul_rn(x[i], rcp), __fmul_rn(x[i + 1], rcp)) << (4 * i);
     return w;
   }
 #pragma unroll

@@ -500,6 +500,30 @@ cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, cudaStream_t
   return launch_cfg<128, kStageK, 4, 128>(L, stream);
 }
 
+// Test of the bounded-wait path: one thread waits on an mbarrier that nothing
+// arrives at, with the same wait routine the GEMM uses and a limit of limit_ns.
+// When it gives up it records the timeout in the status word and returns, so the
+// context stays usable.
+__global__ void k_wait_timeout(uint64_t limit_ns, unsigned* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t never;
+  if (threadIdx.x == 0) {
+    never = 0u;
+    mbar_init(smem_addr(&bar), 1);
+    fence_mbar_init();
+    if (!mbar_wait(smem_addr(&bar), 0, limit_ns, &never)) atomicOr(status, PACT_DEV_TIMEOUT);
+  }
+}
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+  unsigned* status = nullptr;
+  cudaError_t e = status_word_ptr(&status);
+  if (e != cudaSuccess) return e;
+  note_launch();
+  k_wait_timeout<<<1, 32, 0, stream>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
 cudaError_t status_word_ptr(unsigned** ptr) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_pact_status);
 }

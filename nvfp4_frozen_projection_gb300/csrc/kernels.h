@@ -51,6 +51,7 @@ int gemm_block_n(int64_t N, int rpe);
 int gemm_stage_row_bytes();
 cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream);
 cudaError_t status_word_ptr(unsigned** ptr);
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 
 cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
                               const float* amax_opt, uint8_t* codes, uint8_t* sf, float* g,

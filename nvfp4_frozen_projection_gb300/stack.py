@@ -13,6 +13,7 @@ CUDA graph and replayed.
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 from . import (NVFP4, pact_lora_linear_dgrad, pact_lora_linear_fwd, pact_pack_weight_bwd,
@@ -121,6 +122,22 @@ class DecoderProjectionStack:
         p["v"].dgrad(self.dvq, dv, self.dxn1, accumulate=True)
         pact_rmsnorm_bwd(self.xq1, self.gamma1, self.rstd1, self.dxn1, dres=self.dh1, dx=self.dx)
         return self.dx
+
+    @classmethod
+    def from_workload(cls, d: dict, device) -> "DecoderProjectionStack":
+        """Build the stack from host arrays: d holds x (for M), gamma1, gamma2, eps and
+        projections q, k, v, o, gate_up, down with FP32 W [d_out, d_in], adapters A
+        [d_in, r], B [r, d_out] (BF16 values) and alpha, r.  Weights are packed here."""
+        def t32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+
+        proj = {}
+        for k in ("q", "k", "v", "o", "gate_up", "down"):
+            p = d[k]
+            proj[k] = LoraLinear(t32(p.W), t32(p.A).bfloat16(), t32(p.B).bfloat16(),
+                                 float(p.alpha) / float(p.r))
+        return cls(d["x"].shape[0], proj, t32(d["gamma1"]).bfloat16(),
+                   t32(d["gamma2"]).bfloat16(), float(d["eps"]))
 
     def gemm_flops(self) -> float:
         """2*M*N*K over the 14 frozen-projection GEMMs of one forward + dgrad pass."""
