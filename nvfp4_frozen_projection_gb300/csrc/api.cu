@@ -264,14 +264,15 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
   const int bn = gemm_block_n(Nout, rpe);
+  const int cm = gemm_cluster_m(M);  // each CTA of a cluster loads bn / cm rows of B
   int rc;
   const uint32_t rowb = (uint32_t)gemm_stage_row_bytes();
   const CUtensorMapSwizzle absw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   if ((rc = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->codes, Kr / 2, M, rowb, 128,
                      absw)))
     return rc;
-  if ((rc = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b->codes, Kr / 2, Nout, rowb, bn,
-                     absw)))
+  if ((rc = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b->codes, Kr / 2, Nout, rowb,
+                     bn / cm, absw)))
     return rc;
   // LoRA operands: la [M, rpe] (hi|lo pair), lb [Nout, rpe/2]; boxes of at most 64
   // columns (128-byte rows), swizzled by their row width.
@@ -287,9 +288,10 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   if ((rc = make_map(&L.tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lb, rp, Nout, bbox, bn,
                      lsw(bbox))))
     return rc;
-  // output: 32 x 32 BF16 blocks written by TMA stores from the epilogue
+  // output: 32 x 32 BF16 blocks written by TMA stores from the epilogue's 64-byte
+  // swizzled staging buffers
   if ((rc = make_map(&L.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, Nout, M, 32, 32,
-                     CU_TENSOR_MAP_SWIZZLE_NONE)))
+                     CU_TENSOR_MAP_SWIZZLE_64B)))
     return rc;
   GemmParams& p = L.p;
   p.sfa = (const uint8_t*)a->sf;
@@ -315,7 +317,7 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
   g_prof_begin = g_prof_end = nullptr;
   if (pb && cudaEventRecord(pb, stream) != cudaSuccess) return cuda_fail(cudaGetLastError(), "event");
-  cudaError_t e = launch_gemm_nvfp4(L, bn, rpe, stream);
+  cudaError_t e = launch_gemm_nvfp4(L, bn, rpe, cm, stream);
   if (e == cudaSuccess && pe && cudaEventRecord(pe, stream) != cudaSuccess)
     return cuda_fail(cudaGetLastError(), "event");
   return e == cudaSuccess ? PACT_OK : cuda_fail(e, "gemm launch");

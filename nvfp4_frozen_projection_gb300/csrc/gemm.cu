@@ -41,9 +41,13 @@ __device__ unsigned g_pact_status;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 // FP4 elements of K per ring stage: 128-byte tile rows, so each stage moves one
-// 16 KB A box and one 32 KB B box (TMA throughput grows with box size).
+// 16 KB A box and one 32 KB B box (TMA throughput grows with box size; 64-byte
+// rows measured slower even with twice the ring depth).
 constexpr int kStageK = 256;
 
+// Shared memory: [ring: STAGES x (A | B | SFA | SFB)] [LA] [LB] [epilogue staging]
+// [barriers].  A stage's scale factors travel with its A/B tiles (loaded after
+// them, on the same barrier): issuing them apart or ahead measured slower.
 template <int BN, int BK, int STAGES, int RPE>
 struct GemmCfg {
   static constexpr int BM = 128;
@@ -70,12 +74,13 @@ struct GemmCfg {
   static constexpr int LB_OFF = LA_OFF + LA_BYTES;
   static constexpr int LB_BYTES = NLB * LB_CHUNK;
   // Epilogue staging for TMA stores: per epilogue warp NSTG buffers of 32 rows x 32
-  // BF16 columns (2 KB); double-buffered when shared memory allows.
+  // BF16 columns (2 KB, 64-byte swizzled rows); double-buffered when shared memory
+  // allows.
   static constexpr int STG_OFF = LB_OFF + LB_BYTES;
   static constexpr int STG_BUF = 2048;
-  static constexpr int NSTG = (STG_OFF + 2 * 8 * STG_BUF + 256 + 1024 <= 232448) ? 2 : 1;
+  static constexpr int NSTG = (STG_OFF + 2 * 8 * STG_BUF + 512 + 1024 <= 232448) ? 2 : 1;
   static constexpr int BAR_OFF = STG_OFF + NSTG * 8 * STG_BUF;
-  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // + barriers + alignment slack
   static constexpr uint32_t AB_SWZ = ROWB == 128 ? 2u : 4u;  // 128B or 64B swizzle
   static constexpr uint32_t AB_SBO = 8 * ROWB;                // 8-row swizzle atom
   static constexpr uint32_t swz_mode(int row_bytes) {  // 32B -> 6, 64B -> 4, 128B -> 2
@@ -95,7 +100,12 @@ struct GemmCfg {
   static constexpr int EPI_COLS = BN / 2;    // accumulator columns per epilogue warp
   static constexpr int SFA_TCOLS = 4 * KSUB;        // TMEM columns of a stage's A scales
   static constexpr int SFB_TCOLS = 4 * KSUB * NRB;  // ... and B scales
-  static_assert(SFA_TCOLS == 16 && (SFB_TCOLS == 16 || SFB_TCOLS == 32), "SF staging shapes");
+  // barriers (8 bytes each): full[S], empty[S], sf_full[S] (the stage's scales are
+  // in TMEM), then lora_full, lora_empty, acc_full, acc_empty, final
+  static constexpr int NBARS = 3 * STAGES + 5;
+  static_assert((SFA_TCOLS == 8 || SFA_TCOLS == 16) &&
+                    (SFB_TCOLS == 8 || SFB_TCOLS == 16 || SFB_TCOLS == 32),
+                "SF staging shapes");
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(BK == 128 || BK == 256, "BK");
   static_assert(RPE == 32 || RPE == 64 || RPE == 128, "RPE");
@@ -104,7 +114,7 @@ struct GemmCfg {
   static_assert(STAGE_BYTES % 1024 == 0 && LA_OFF % 1024 == 0 && LB_OFF % 1024 == 0 &&
                     STG_OFF % 1024 == 0,
                 "align");
-  static_assert((3 * STAGES + 5) * 8 <= 200, "barrier area");
+  static_assert(NBARS * 8 <= 504, "barrier area");
 };
 
 // Instruction descriptors (M = 128, K-major A and B, dense).
@@ -124,7 +134,11 @@ __device__ __forceinline__ void raise_error(volatile uint32_t* abort_flag, unsig
   atomicOr(status, code);
 }
 
-template <int BN, int BK, int STAGES, int RPE>
+// CM = CTAs per cluster along M (1 or 2).  With CM = 2 the two CTAs of a cluster
+// compute the tiles (m, n) and (m + 1, n) in lock step: each loads half of the
+// shared B tile and multicasts it to both, so every B byte leaves L2 once per pair,
+// and a stage is refilled only after both CTAs' MMAs released it.
+template <int BN, int BK, int STAGES, int RPE, int CM>
 __global__ void __launch_bounds__(448, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmLA,
@@ -136,31 +150,42 @@ __global__ void __launch_bounds__(448, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t bar0 = base + C::BAR_OFF;
-  const uint32_t lora_full = bar0 + 8 * (2 * STAGES);
+  const uint32_t full0 = bar0, empty0 = bar0 + 8 * STAGES;
+  const uint32_t sf_full0 = bar0 + 8 * (2 * STAGES);
+  const uint32_t lora_full = sf_full0 + 8 * STAGES;
   const uint32_t lora_empty = lora_full + 8;
   const uint32_t acc_full = lora_full + 16;
   const uint32_t acc_empty = lora_full + 24;
   const uint32_t final_bar = lora_full + 32;
-  const uint32_t sf_full0 = lora_full + 40;  // STAGES barriers: a stage's scales are in TMEM
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 200);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 204);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 504);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 508);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ntiles = p.num_m * p.num_n;
   const int nks = (p.K + BK - 1) / BK;
   const int rb_total = (p.N + 127) / 128;
+  // work units: CM vertically adjacent tiles sharing one B tile; unit u covers
+  // m-tiles CM*(u % num_mc) + [0, CM) and n-tile u / num_mc
+  const uint32_t crank = CM > 1 ? cluster_ctarank() : 0u;
+  const int num_mc = (p.num_m + CM - 1) / CM;
+  const int nunits = num_mc * p.num_n;
+  const int unit0 = (int)blockIdx.x / CM, nclusters = (int)gridDim.x / CM;
+  auto tile_mt = [&](int u) { return (u % num_mc) * CM + (int)crank; };
+  auto tile_n0 = [&](int u) { return (u / num_mc) * BN; };
+  // this CTA's K steps over all its units, as one sequence of "fills"
+  const int my_units = unit0 < nunits ? (nunits - unit0 + nclusters - 1) / nclusters : 0;
+  const int nfills = my_units * nks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar0 + 8 * s, 1);
-      mbar_init(bar0 + 8 * (STAGES + s), 1);
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CM);
+      mbar_init(sf_full0 + 8 * s, 128);
     }
     mbar_init(lora_full, 1);
     mbar_init(lora_empty, 1);
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, C::EPI_THREADS);
     mbar_init(final_bar, 1);
-    for (int s = 0; s < STAGES; ++s) mbar_init(sf_full0 + 8 * s, 128);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -179,19 +204,23 @@ __global__ void __launch_bounds__(448, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CM > 1) cluster_sync();  // peers' barriers are initialised
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, lphase = 0;
+      // Everything per tile is computed once per tile: the per-stage path between
+      // an empty barrier completing and the next copies being issued stays short.
       uint32_t pend = 0, pend_par = 0, lpend = 0, lpend_par = 0;
+      uint32_t lphase = 0, phase = 0;
+      int stage = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % p.num_m) * C::BM;
-        const int n0 = (tile / p.num_m) * BN;
+      for (int u = unit0; u < nunits && ok; u += nclusters) {
+        const int mt = tile_mt(u);
+        const int m0 = mt * C::BM;
+        const int n0 = tile_n0(u);
         if (p.lora_steps) {
           if (!mbar_wait(lora_empty, lphase ^ 1u, kWaitLimitNs, abort_flag)) {
             ok = false;
@@ -208,26 +237,33 @@ __global__ void __launch_bounds__(448, 1)
           lpend_par = lphase;
           lphase ^= 1u;
         }
+        // a CTA whose m-tile lies past M (odd tile count) computes on zero-filled A
+        // and stores nothing; its scale reads stay inside the last row atom
+        const uint8_t* sfa_t = p.sfa + (size_t)min(mt, p.num_m - 1) * (p.k16p / 4) * 512;
+        const uint8_t* sfb_t = p.sfb + (size_t)(n0 / 128) * (p.k16p / 4) * 512;
+        const size_t sfb_rb = (size_t)(p.k16p / 4) * 512;  // one 128-row block of B scales
         const int nrb = min(C::NRB, rb_total - n0 / 128);
+        const int nb = n0 + (int)crank * (BN / CM);
         for (int ks = 0; ks < nks; ++ks) {
-          const uint32_t fb = bar0 + 8 * stage;
-          if (!mbar_wait(bar0 + 8 * (STAGES + stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs, abort_flag)) {
             ok = false;
             break;
           }
           const int ksub = min(C::KSUB, (p.K - ks * BK) / 64);
+          const uint32_t fb = full0 + 8 * stage;
           const uint32_t sb = base + stage * C::STAGE_BYTES;
           mbar_expect_tx(fb, C::A_BYTES + C::B_BYTES + (uint32_t)(ksub * 512 * (1 + nrb)));
           tma_load_2d(sb, &tmA, ks * C::ROWB, m0, fb);
-          tma_load_2d(sb + C::A_BYTES, &tmB, ks * C::ROWB, n0, fb);
-          const size_t katom = (size_t)ks * C::KSUB;
-          bulk_load(sb + C::A_BYTES + C::B_BYTES,
-                    p.sfa + ((size_t)(m0 / 128) * (p.k16p / 4) + katom) * 512,
-                    (uint32_t)(ksub * 512), fb);
+          if constexpr (CM > 1)
+            tma_load_2d_mc(sb + C::A_BYTES + crank * (C::B_BYTES / CM), &tmB, ks * C::ROWB, nb,
+                           fb, (uint16_t)((1u << CM) - 1u));
+          else
+            tma_load_2d(sb + C::A_BYTES, &tmB, ks * C::ROWB, n0, fb);
+          const size_t koff = (size_t)ks * C::KSUB * 512;
+          bulk_load(sb + C::A_BYTES + C::B_BYTES, sfa_t + koff, (uint32_t)(ksub * 512), fb);
           for (int rb = 0; rb < nrb; ++rb)
             bulk_load(sb + C::A_BYTES + C::B_BYTES + C::SFA_BYTES + rb * C::KSUB * 512,
-                      p.sfb + ((size_t)(n0 / 128 + rb) * (p.k16p / 4) + katom) * 512,
-                      (uint32_t)(ksub * 512), fb);
+                      sfb_t + rb * sfb_rb + koff, (uint32_t)(ksub * 512), fb);
           pend |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -240,19 +276,29 @@ __global__ void __launch_bounds__(448, 1)
         raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_TMA);
         // let copies already in flight land before the CTA can exit
         for (int s = 0; s < STAGES; ++s)
-          if (pend & (1u << s)) mbar_wait(bar0 + 8 * s, (pend_par >> s) & 1u, 10000000ull, nullptr);
+          if (pend & (1u << s)) mbar_wait(full0 + 8 * s, (pend_par >> s) & 1u, 10000000ull, nullptr);
         if (lpend) mbar_wait(lora_full, lpend_par, 10000000ull, nullptr);
+      } else if constexpr (CM > 1) {
+        // the peer's MMA commits arrive on this CTA's empty barriers: wait for the
+        // release of the last STAGES loads before the CTA may exit
+        for (int i = 0; i < STAGES; ++i) {
+          mbar_wait(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs, abort_flag);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      uint32_t lphase = 0, aphase = 0, phase = 0;
       int stage = 0;
-      uint32_t phase = 0, lphase = 0, aphase = 0;
       bool ok = true;
       const uint32_t idesc = idesc_nvf4(BN);
       const uint32_t idesc_l = idesc_bf16(BN);
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int u = unit0; u < nunits && ok; u += nclusters) {
         if (!mbar_wait(acc_empty, aphase ^ 1u, kWaitLimitNs, abort_flag)) {
           ok = false;
           break;
@@ -297,7 +343,10 @@ __global__ void __launch_bounds__(448, 1)
             mma_nvf4(tmem, da, db, idesc, tsf + 4 * j, tsf + 4 * C::KSUB + j * C::NRB * 4, accum);
             accum = 1;
           }
-          mma_commit(bar0 + 8 * (STAGES + stage));
+          if constexpr (CM > 1)
+            mma_commit_mc(empty0 + 8 * stage, (uint16_t)((1u << CM) - 1u));
+          else
+            mma_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -312,68 +361,71 @@ __global__ void __launch_bounds__(448, 1)
       mma_commit(final_bar);
       mbar_wait(final_bar, 0, kWaitLimitNs, nullptr);
     }
-  } else if (warp < C::EPI_WARP0) {
+  } else if (warp >= C::SF_WARP0 && warp < C::SF_WARP0 + 4) {
     // ------------------------------------------------------------ scale staging
-    // One warp per TMEM lane quarter.  When a stage lands, each lane reads row
-    // `lane` (16 bytes) of every 512-byte scale atom in shared memory and writes it
-    // as 4 consecutive TMEM columns of its lane: the same image a 32x128b.warpx4
-    // copy makes (every lane quarter holds the whole atom), written with plain
-    // TMEM stores so that the MMA issuer's tensor pipe carries only MMAs.
+    // One warp per TMEM lane quarter q.  A 512-byte scale atom holds rows r, r+32,
+    // r+64, r+96 in its 16-byte row r (4 bytes = 4 blocks each).  The MMA reads the
+    // A scales of tile row 32q + r from TMEM lane 32q + r, column q of the atom's 4
+    // columns, and the B scales of every row from lane 32q + (row mod 32) of the
+    // lane quarter it computes in, all 4 columns (the atom image itself, in every
+    // quarter).  So lane r of warp q loads only 4 bytes of every A atom (columns
+    // nobody reads get copies) and the 16-byte rows of the B atoms: 18 KB of
+    // shared-memory reads per stage instead of 24 KB, which matters because
+    // shared-memory bandwidth is what this pipeline is short of.  Plain TMEM stores
+    // keep the MMA issuer's tensor pipe for MMAs only.  The stage's TMEM slot is
+    // free again once its full barrier completes: the producer only refills a stage
+    // after the MMAs that read it have completed.
     const uint32_t q = (uint32_t)(warp & 3);
+    bool ok = true;
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      for (int ks = 0; ks < nks; ++ks) {
-        if (!mbar_wait(bar0 + 8 * stage, phase, kWaitLimitNs, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* sfa_p = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
-        const uint8_t* sfb_p = sfa_p + C::SFA_BYTES;
-        uint32_t va[C::SFA_TCOLS], vb[C::SFB_TCOLS];
+    for (int f = 0; f < nfills; ++f) {
+      if (!mbar_wait(full0 + 8 * stage, phase, kWaitLimitNs, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* sf_p = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES + 16 * lane;
+      uint32_t va[C::SFA_TCOLS], vb[C::SFB_TCOLS];
 #pragma unroll
-        for (int j = 0; j < C::KSUB; ++j) {
-          const uint4 a = *reinterpret_cast<const uint4*>(sfa_p + 512 * j + 16 * lane);
-          va[4 * j] = a.x;
-          va[4 * j + 1] = a.y;
-          va[4 * j + 2] = a.z;
-          va[4 * j + 3] = a.w;
+      for (int j = 0; j < C::KSUB; ++j) {
+        const uint32_t a = *reinterpret_cast<const uint32_t*>(sf_p + 512 * j + 4 * q);
 #pragma unroll
-          for (int rb = 0; rb < C::NRB; ++rb) {
-            const uint4 b =
-                *reinterpret_cast<const uint4*>(sfb_p + rb * C::KSUB * 512 + 512 * j + 16 * lane);
-            const int c = 4 * (j * C::NRB + rb);
-            vb[c] = b.x;
-            vb[c + 1] = b.y;
-            vb[c + 2] = b.z;
-            vb[c + 3] = b.w;
-          }
+        for (int i = 0; i < 4; ++i) va[4 * j + i] = a;
+#pragma unroll
+        for (int rb = 0; rb < C::NRB; ++rb) {
+          const int c = 4 * (j * C::NRB + rb);
+          const uint4 b =
+              *reinterpret_cast<const uint4*>(sf_p + C::SFA_BYTES + rb * C::KSUB * 512 + 512 * j);
+          vb[c] = b.x;
+          vb[c + 1] = b.y;
+          vb[c + 2] = b.z;
+          vb[c + 3] = b.w;
         }
-        const uint32_t tsf = tmem + (q * 32u << 16) + C::SF_BASE + stage * C::SF_COLS;
-        tmem_st16(tsf, va);
-        if constexpr (C::SFB_TCOLS == 32)
-          tmem_st32(tsf + C::SFA_TCOLS, vb);
-        else
-          tmem_st16(tsf + C::SFA_TCOLS, vb);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(sf_full0 + 8 * stage);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      }
+      tc_fence_after();
+      const uint32_t tsf = tmem + (q * 32u << 16) + C::SF_BASE + stage * C::SF_COLS;
+      tmem_st<C::SFA_TCOLS>(tsf, va);
+      tmem_st<C::SFB_TCOLS>(tsf + C::SFA_TCOLS, vb);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(sf_full0 + 8 * stage);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
     if (!ok) raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_SF);
-  } else {
+  } else if (warp >= C::EPI_WARP0) {
     // ------------------------------------------------------------ epilogue
-    // Two warps per TMEM lane quarter, each owning half of the tile's columns.  A
-    // warp drains and stores the first half of its share, drains the second half,
-    // releases the accumulator to the MMA issuer, and then stores the rest, so the
-    // next tile's mainloop runs under most of this tile's stores.  Each 32x32 BF16
-    // block (row per lane) goes to a shared staging buffer and out with one TMA
-    // store, which also clips rows >= M; rows past M are never read from addend.
+    // Two warps per TMEM lane quarter, each owning half of the tile's columns.  The
+    // MMA issuer has one accumulator, so the next tile's mainloop waits for this
+    // drain: a warp loads its share 32 columns at a time and turns each slice into
+    // rounded BF16 (scaled, plus the addend) at once, so the whole share fits in
+    // registers and the accumulator is released right after the last load.  The
+    // addend share is fetched, as BF16, while the mainloop still runs.  Then each
+    // 32x32 BF16 block (row per lane) goes to a shared staging buffer and out with
+    // one TMA store, which also clips rows >= M; rows past M never read addend.
+    constexpr int NCH = C::EPI_COLS / 32;
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ew = warp - C::EPI_WARP0;
     const int c0 = (ew >> 2) * C::EPI_COLS;
@@ -383,67 +435,85 @@ __global__ void __launch_bounds__(448, 1)
     uint32_t amax = 0;
     uint32_t aphase = 0;
     uint32_t nstore = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const int m0 = (tile % p.num_m) * C::BM;
-      const int n0 = (tile / p.num_m) * BN;
+    for (int u = unit0; u < nunits; u += nclusters) {
+      const int m0 = tile_mt(u) * C::BM;
+      const int n0 = tile_n0(u);
+      const int m = m0 + q * 32 + lane;
+      const bool row_ok = m < p.M;
+      // the 32-row block is wholly past M (ragged or padding tile): nothing to store
+      const bool blk_live = m0 + q * 32 < p.M;
+      // out[ch] first holds the addend slice ch (packed BF16), then the result
+      uint32_t out[NCH][16];
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int n = n0 + c0 + 32 * ch;
+        if (p.addend && row_ok && n < p.N) {
+          const uint4* ad = reinterpret_cast<const uint4*>(p.addend + (size_t)m * p.N + n);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 a4 = ad[k];
+            out[ch][4 * k] = a4.x;
+            out[ch][4 * k + 1] = a4.y;
+            out[ch][4 * k + 2] = a4.z;
+            out[ch][4 * k + 3] = a4.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) out[ch][i] = 0u;
+        }
+      }
       if (!mbar_wait(acc_full, aphase, kWaitLimitNs, abort_flag)) {
         raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_EPI);
         break;
       }
       tc_fence_after();
-      const int m = m0 + q * 32 + lane;
-      const bool row_ok = m < p.M;
 #pragma unroll
-      for (int half = 0; half < C::EPI_COLS / 64; ++half) {
-        uint32_t v[64];
-        const int cb = c0 + 64 * half;
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)cb, v);
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cb + 32), v + 32);
+      for (int ch = 0; ch < NCH; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c0 + 32 * ch), v);
         tmem_ld_wait();
-        if (half == C::EPI_COLS / 64 - 1) {  // the whole share is in registers
-          tc_fence_before();
-          mbar_arrive(acc_empty);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float lo = __fmul_rn(__uint_as_float(v[2 * i]), s_main);
+          float hi = __fmul_rn(__uint_as_float(v[2 * i + 1]), s_main);
+          if (p.addend) {  // an absent addend slice is zeros: x + 0 = x for x != -0
+            lo = __fadd_rn(lo, __uint_as_float(out[ch][i] << 16));
+            hi = __fadd_rn(hi, __uint_as_float(out[ch][i] & 0xFFFF0000u));
+          }
+          out[ch][i] = pack_bf16x2(lo, hi);
         }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          const int n = n0 + cb + c;
-          if (n >= p.N) continue;  // uniform across the warp (N % 32 == 0)
-          float f[32];
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int n = n0 + c0 + 32 * ch;
+        if (n >= p.N || !blk_live) continue;  // uniform across the warp (N % 32 == 0)
+        if (row_ok) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[c + i]), s_main);
-          if (p.addend && row_ok) {
-            const uint4* ad = reinterpret_cast<const uint4*>(p.addend + (size_t)m * p.N + n);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float r8[8];
-              bf16x8_to_f32(ad[k], r8);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) f[8 * k + i] = __fadd_rn(f[8 * k + i], r8[i]);
-            }
-          }
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-            if (row_ok)
-              amax = max(amax, max((w[i] & 0x7FFFu) << 16, (w[i] >> 16 & 0x7FFFu) << 16));
-          }
-          // staging buffer nstore % NSTG: wait until its previous store has read it
-          const uint32_t buf = stg + (nstore % C::NSTG) * C::STG_BUF;
-          if (nstore >= (uint32_t)C::NSTG && lane == 0) bulk_wait_read<C::NSTG - 1>();
-          __syncwarp();
-          uint4* sp = reinterpret_cast<uint4*>(smem + (buf - base) + 64 * lane);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            sp[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmOut, buf, n, m0 + q * 32);
-            bulk_commit();
-          }
-          ++nstore;
+          for (int i = 0; i < 16; ++i)
+            amax = max(amax, max((out[ch][i] & 0x7FFFu) << 16, (out[ch][i] >> 16 & 0x7FFFu) << 16));
         }
+        // staging buffer nstore % NSTG: wait until its previous store has read it
+        const uint32_t buf = stg + (nstore % C::NSTG) * C::STG_BUF;
+        if (nstore >= (uint32_t)C::NSTG && lane == 0) bulk_wait_read<C::NSTG - 1>();
+        __syncwarp();
+        // 64-byte swizzle (the store's tensor map says the same): 16-byte chunk k
+        // of row r sits at chunk k ^ ((r / 2) % 4), which spreads a store
+        // instruction's 32 rows over all banks
+        uint8_t* row = smem + (buf - base) + 64 * lane;
+        const uint32_t sw = (uint32_t)(lane >> 1) & 3u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(row + 16 * (k ^ sw)) =
+              make_uint4(out[ch][4 * k], out[ch][4 * k + 1], out[ch][4 * k + 2], out[ch][4 * k + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmOut, buf, n, m0 + q * 32);
+          bulk_commit();
+        }
+        ++nstore;
       }
       aphase ^= 1u;
     }
@@ -457,6 +527,7 @@ __global__ void __launch_bounds__(448, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if constexpr (CM > 1) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -464,40 +535,87 @@ __global__ void __launch_bounds__(448, 1)
 }
 
 // ---------------------------------------------------------------- host side
-template <int BN, int BK, int STAGES, int RPE>
+template <int BN, int BK, int STAGES, int RPE, int CM>
 static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
   using C = GemmCfg<BN, BK, STAGES, RPE>;
-  auto kern = k_gemm_nvfp4<BN, BK, STAGES, RPE>;
-  static bool attr_set[64] = {};
+  auto kern = k_gemm_nvfp4<BN, BK, STAGES, RPE, CM>;
+  // per device: shared-memory attribute set, and how many clusters fit at once
+  static int max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters[dev] == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    int n = L.num_sms / CM;
+    if (CM > 1) {
+      cfg.gridDim = dim3(L.num_sms / CM * CM);
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n < 1) return cudaErrorInvalidConfiguration;
+    }
+    max_clusters[dev] = n;
   }
-  const int ntiles = L.p.num_m * L.p.num_n;
-  const int grid = ntiles < L.num_sms ? ntiles : L.num_sms;
+  const int num_mc = (L.p.num_m + CM - 1) / CM;
+  const int units = num_mc * L.p.num_n;
+  const int clusters = units < max_clusters[dev] ? units : max_clusters[dev];
+  cfg.gridDim = dim3(clusters * CM);
   note_launch();
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(L.tmA, L.tmB, L.tmLA, L.tmLB, L.tmOut, L.p);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmLA, L.tmLB, L.tmOut, L.p);
 }
 
 int gemm_block_n(int64_t N, int rpe) { return (N % 256 == 0 && rpe <= 64) ? 256 : 128; }
 
+#ifndef PACT_GEMM_CM
+#define PACT_GEMM_CM 2
+#endif
+int gemm_cluster_m(int64_t M) { return (PACT_GEMM_CM > 1 && M > 128) ? 2 : 1; }
+
 int gemm_stage_row_bytes() { return kStageK / 2; }
 
-// Ring depth per configuration: as many 64-byte-row stages as shared memory holds
-// next to the LoRA operands.
-cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream) {
+// Ring depth: as many stages as shared memory holds next to the LoRA operands and
+// one staging buffer per epilogue warp, within the TMEM left for scale factors, at
+// most 10.
+template <int BN, int BK, int RPE>
+constexpr int ring_stages() {
+  constexpr int stage = 128 * BK / 2 + BN * BK / 2 + (BK / 64) * 512 * (1 + BN / 128);
+  constexpr int fixed = 128 * RPE * 2 + BN * (RPE / 2) * 2 + 8 * 2048 + 1536;
+  constexpr int by_smem = (232448 - fixed) / stage;
+  constexpr int by_tmem = 256 / (4 * (BK / 64) * (1 + BN / 128));
+  constexpr int s = by_smem < by_tmem ? by_smem : by_tmem;
+  return s < 10 ? s : 10;
+}
+
+template <int BN, int RPE, int CM>
+static cudaError_t launch_one(const GemmLaunch& L, cudaStream_t stream) {
+  return launch_cfg<BN, kStageK, ring_stages<BN, kStageK, RPE>(), RPE, CM>(L, stream);
+}
+
+template <int CM>
+static cudaError_t launch_cm(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream) {
   if (bn == 256) {
-    if (rpe == 32) return launch_cfg<256, kStageK, 3, 32>(L, stream);
-    return launch_cfg<256, kStageK, 3, 64>(L, stream);
+    if (rpe == 32) return launch_one<256, 32, CM>(L, stream);
+    return launch_one<256, 64, CM>(L, stream);
   }
-  if (rpe == 32) return launch_cfg<128, kStageK, 5, 32>(L, stream);
-  if (rpe == 64) return launch_cfg<128, kStageK, 5, 64>(L, stream);
-  return launch_cfg<128, kStageK, 4, 128>(L, stream);
+  if (rpe == 32) return launch_one<128, 32, CM>(L, stream);
+  if (rpe == 64) return launch_one<128, 64, CM>(L, stream);
+  return launch_one<128, 128, CM>(L, stream);
+}
+
+cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, int cm, cudaStream_t stream) {
+  return cm == 2 ? launch_cm<2>(L, bn, rpe, stream) : launch_cm<1>(L, bn, rpe, stream);
 }
 
 // Test of the bounded-wait path: one thread waits on an mbarrier that nothing

@@ -46,10 +46,12 @@ struct GemmLaunch {
 // Tile width (128 or 256) for an output of N columns and a LoRA operand of rpe
 // columns, and the launcher.
 int gemm_block_n(int64_t N, int rpe);
+// CTAs per cluster along M (2: pairs share each B tile by multicast), for M rows.
+int gemm_cluster_m(int64_t M);
 // Bytes of K per A/B tile row in one ring stage (the TMA box width; 64 -> 64B
 // swizzle, 128 -> 128B swizzle).
 int gemm_stage_row_bytes();
-cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream);
+cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, int cm, cudaStream_t stream);
 cudaError_t status_word_ptr(unsigned** ptr);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 
