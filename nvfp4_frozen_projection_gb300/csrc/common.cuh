@@ -148,6 +148,49 @@ __device__ __forceinline__ uint32_t block_scale(float amax_blk, TensorScale ts, 
   return s;
 }
 
+// Per-tensor table of a block's decode step t = RN(e4m3(s) g) and rcp = RN(1/t)
+// (0 for t = 0) for every scale byte an encoder can produce (0 .. 0x7E, 0x7F for a
+// NaN), kept in shared memory and filled once per CTA: it replaces the division
+// 1/t of block_scale.  The scale byte itself comes from q = amax * RN(1/d): q is
+// within 2^-22.4 of RN(amax / d) (relative), so when q (1 - 2^-21) and q (1 + 2^-21)
+// round to the same E4M3 byte, so does RN(amax / d) (the rounding is monotonic);
+// otherwise the exact division decides.  E4M3 thresholds lie at 2^-10 and above,
+// so subnormal quotients never reach the check's margin.
+struct ScaleTable {
+  float t[128];
+  float rcp[128];
+  float rcp_d;  // RN(1/d), or 0 when the fast quotient may not be used
+};
+
+// Fill the table (all threads of the CTA; the caller synchronises afterwards).
+__device__ __forceinline__ void scale_table_init(ScaleTable* tab, TensorScale ts) {
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+    const float t = __fmul_rn(e4m3_to_f32((uint32_t)i), ts.g);
+    tab->t[i] = t;
+    tab->rcp[i] = (t == 0.0f) ? 0.0f : __fdiv_rn(1.0f, t);
+  }
+  if (threadIdx.x == 0) {
+    const float r = ts.d > 0.0f ? __fdiv_rn(1.0f, ts.d) : 0.0f;
+    tab->rcp_d = (r > 0.0f && r <= 3.4028234663852886e38f) ? r : 0.0f;
+  }
+}
+
+// block_scale() with the table: the same byte, t and rcp.
+__device__ __forceinline__ uint32_t block_scale_tab(float amax_blk, TensorScale ts,
+                                                    const ScaleTable* tab, float* t, float* rcp) {
+  uint32_t s = 0;
+  if (ts.g != 0.0f) {
+    const float rd = tab->rcp_d;
+    const float q = __fmul_rn(amax_blk, rd);
+    s = e4m3_from_f32(__fmul_rn(q, 1.0f - 0x1p-21f));
+    if (rd == 0.0f || s != e4m3_from_f32(__fmul_rn(q, 1.0f + 0x1p-21f)))
+      s = e4m3_from_f32(__fdiv_rn(amax_blk, ts.d));
+  }
+  *t = tab->t[s & 0x7Fu];
+  *rcp = tab->rcp[s & 0x7Fu];
+  return s;
+}
+
 // ------------------------------------------------------------------ bf16
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -247,6 +290,37 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   float den = __fadd_rn(1.0f, e);
   float s = __fdiv_rn(g, den);
   return __fmul_rn(s, u);
+}
+
+// A fast stand-in for silu_mul, used only to decide where the exact value is
+// needed: h ~ g * u / (1 + e) with e = 2^y, y = -g log2(e), from the hardware
+// base-2 exponential and reciprocal (flush-to-zero forms).  The rounding error of
+// y (up to 115.5 * 2^-24 for |g| <= 80) is split off with a fused multiply-add
+// (together with the low part of log2(e)) and applied to the exponential as
+// e (1 + dy ln 2), so what remains is the two approximations (about 2^-22 and
+// 2^-23), four roundings and silu_mul's own distance to the true value (about 4
+// units): below 2^-20.5 relative for finite inputs with |g| zero or in [2^-60, 80]
+// and a normal result (every intermediate is normal there: 1 + e <= 2^116 and
+// |g| / (1 + e) >= 2^-110).  kSiluRel keeps a margin of more than 5 over that.
+// A subnormal h may flush to a zero of the same sign.
+constexpr float kSiluRel = 0x1p-18f;
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float silu_mul_fast(float g, float u) {
+  const float ng = -g;
+  const float y = __fmul_rn(ng, 0x1.715476p+0f);                            // RN(-g log2 e)
+  const float dy = __fmaf_rn(ng, 0x1.4ae0c0p-26f, __fmaf_rn(ng, 0x1.715476p+0f, -y));
+  const float e0 = ex2_ftz(y);
+  const float e = __fmaf_rn(e0, __fmul_rn(dy, 0x1.62e430p-1f), e0);          // e0 (1 + dy ln 2)
+  return __fmul_rn(__fmul_rn(g, rcp_ftz(__fadd_rn(1.0f, e))), u);
 }
 
 }  // namespace pact

@@ -52,31 +52,36 @@ __device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, __half2 
   return pack_bf16x2(f.x, f.y);
 }
 
-// Sums the 8 warps' partial products and stores f * T as a BF16 pair per element:
-// out[m, j] = hi = bf16(v), out[m, RP + j] = lo = bf16(v - hi), so that the fused
-// GEMM's BF16 LoRA product sees v to about 16 significant bits.
-template <int RP>
-__device__ __forceinline__ void reduce_and_store(float (*acc)[4], float* red, int64_t m0,
+// Sums the 8 warps' partial products (fixed order) and stores f * T as a BF16
+// pair per element: out[m, j] = hi = bf16(v), out[m, RP + j] = lo = bf16(v - hi),
+// so that the fused GEMM's BF16 LoRA product sees v to about 16 significant bits.
+// acc[g][jn][*] is the m16n8 accumulator of row group g (rows 16g + lane/4 and
+// 16g + lane/4 + 8) and columns 8 jn + 2 (lane % 4) + {0, 1}.
+template <int RP, int G>
+__device__ __forceinline__ void reduce_and_store(float (*acc)[RP / 8][4], float* red, int64_t m0,
                                                  int64_t M, float f, uint16_t* out) {
-  constexpr int NT = RP / 8;
+  constexpr int NT = RP / 8, ROWS = 16 * G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  // red[warp][row 0..15][col 0..RP)
+  // red[warp][row 0..ROWS)[col 0..RP)
 #pragma unroll
-  for (int jn = 0; jn < NT; ++jn) {
-    float* r0 = red + (warp * 16 + g) * RP + jn * 8 + 2 * c;
-    float* r1 = red + (warp * 16 + g + 8) * RP + jn * 8 + 2 * c;
-    r0[0] = acc[jn][0];
-    r0[1] = acc[jn][1];
-    r1[0] = acc[jn][2];
-    r1[1] = acc[jn][3];
+  for (int gi = 0; gi < G; ++gi) {
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn) {
+      float* r0 = red + (warp * ROWS + 16 * gi + g) * RP + jn * 8 + 2 * c;
+      float* r1 = r0 + 8 * RP;
+      r0[0] = acc[gi][jn][0];
+      r0[1] = acc[gi][jn][1];
+      r1[0] = acc[gi][jn][2];
+      r1[1] = acc[gi][jn][3];
+    }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < 16 * RP; e += blockDim.x) {
+  for (int e = threadIdx.x; e < ROWS * RP; e += blockDim.x) {
     const int row = e / RP, col = e - row * RP;
     float s = 0.0f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) s += red[(w * 16 + row) * RP + col];
+    for (int w = 0; w < 8; ++w) s += red[(w * ROWS + row) * RP + col];
     const int64_t m = m0 + row;
     if (m < M) {
       const float v = s * f;
@@ -132,21 +137,29 @@ __global__ void __launch_bounds__(256) k_lora_prep(const uint16_t* __restrict__ 
   }
 }
 
-// T' = f * (X~ A): x_codes [M, K/2], x_sf (128x4 atoms), At [RP, K].  A CTA owns 16
-// rows; warp w takes the 64-wide K chunks w, w+8, ... with two chunks of codes in
-// flight ahead of the one it multiplies.  E2M1 pairs are decoded through a
-// 256-entry byte -> BF16x2 table in shared memory and scaled by the block's E4M3
-// scale with one exact BF16x2 multiply.
-template <int RP>
-__global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict__ xc,
+// Both down-projections are skinny GEMMs ([M, K] x [K, RP]) bound by reading
+// their left operand once.  A CTA owns 16 G rows (G = 2 row groups of 16 when
+// RP <= 32, else 1); its 8 warps split K into interleaved chunks of 64 bytes per
+// row and reduce through shared memory in a fixed order.  Inside a chunk, lane
+// (g, c) = (lane / 4, lane % 4) loads 16 contiguous bytes of rows g and g + 8 of
+// every row group (a warp instruction covers 8 rows x 64 bytes), and the m16n8k16
+// MMAs take the chunk's K elements in a permuted order, the same on both operands:
+// step s gives lane c the elements [4s, 4s + 4) of its own 16-byte piece.  The next
+// chunk's loads are in flight while the current one is multiplied.
+
+// T' = f * (X~ A): x_codes [M, K/2], x_sf (128x4 atoms), At [RP, K].  A chunk is
+// 128 codes of a row: lane c holds blocks 2c and 2c + 1 (32 codes, 16 bytes).  E2M1
+// pairs are decoded through a 256-entry byte -> BF16x2 table in shared memory and
+// scaled by their block's E4M3 scale with one exact BF16x2 multiply.
+template <int RP, int G>
+__global__ void __launch_bounds__(256, 2) k_lora_down_fwd(const uint8_t* __restrict__ xc,
                                                        const uint8_t* __restrict__ xsf,
                                                        const float* __restrict__ gx,
                                                        const float* __restrict__ gw, int64_t M,
                                                        int64_t K, const uint16_t* __restrict__ At,
-                                                       int r, float scale,
-                                                       uint16_t* __restrict__ t_out) {
+                                                       float scale, uint16_t* __restrict__ t_out) {
   constexpr int NT = RP / 8;
-  __shared__ float red[8 * 16 * RP];
+  __shared__ float red[8 * 16 * G * RP];
   __shared__ uint32_t dec[256];
   {
     const float2 f = e2m1x2_to_f32x2(threadIdx.x);
@@ -155,78 +168,96 @@ __global__ void __launch_bounds__(256) k_lora_down_fwd(const uint8_t* __restrict
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t m0 = (int64_t)blockIdx.x * 16;
-  const int64_t ra = m0 + g, rb = m0 + g + 8;
-  const bool va = ra < M, vb = rb < M;
-  const int64_t c16p = K >> 4;
-  float acc[NT][4];
+  const int64_t m0 = (int64_t)blockIdx.x * (16 * G);
+  const int64_t c16p = pad_to(K >> 4, 4);
+  const int64_t row_bytes = K >> 1;
+  const int nch = (int)((K + 127) >> 7);
+  // in a final half chunk (K % 128 == 64) lanes 2 and 3 have nothing to load
+  const bool half_tail = (K & 127) != 0;
+  float acc[G][NT][4];
 #pragma unroll
-  for (int jn = 0; jn < NT; ++jn) acc[jn][0] = acc[jn][1] = acc[jn][2] = acc[jn][3] = 0.0f;
+  for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn) acc[gi][jn][0] = acc[gi][jn][1] = acc[gi][jn][2] = acc[gi][jn][3] = 0.0f;
 
   struct Chunk {
-    uint2 qa, qb;
-    uint32_t sa, sb;
+    uint4 q[G][2];      // codes of rows g, g + 8 of each group
+    uint32_t sc[G][2];  // the two block scales (2 bytes) of those rows
   };
-  // chunk ch of 64 along K: lane (g, c) holds block 4ch + c of rows g and g+8
-  auto load = [&](int64_t ch, Chunk& q) {
-    const int64_t blk = ch * 4 + c;
-    q.qa = q.qb = make_uint2(0, 0);
-    q.sa = q.sb = 0;
-    if (va) {
-      q.qa = __ldg(reinterpret_cast<const uint2*>(xc + ra * (K >> 1) + blk * 8));
-      q.sa = xsf[sf_offset(ra, blk, c16p)];
-    }
-    if (vb) {
-      q.qb = __ldg(reinterpret_cast<const uint2*>(xc + rb * (K >> 1) + blk * 8));
-      q.sb = xsf[sf_offset(rb, blk, c16p)];
-    }
-  };
-  const int64_t nchunks = K >> 6;
-  Chunk q0, q1;
-  if (warp < nchunks) load(warp, q0);
-  if (warp + 8 < nchunks) load(warp + 8, q1);
-  for (int64_t ch = warp; ch < nchunks; ch += 8) {
-    Chunk q2;
-    if (ch + 16 < nchunks) load(ch + 16, q2);  // two chunks ahead
-    const __nv_bfloat162 sca = __float2bfloat162_rn(e4m3_to_f32(q0.sa));
-    const __nv_bfloat162 scb = __float2bfloat162_rn(e4m3_to_f32(q0.sb));
-    const int64_t kbase = (ch * 4 + c) * 16;
+  auto load = [&](int ch, Chunk& x) {
+    const bool live = !(half_tail && ch == nch - 1 && c >= 2);
+    const int64_t blk = (int64_t)ch * 8 + 2 * c;  // first of the lane's two blocks
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const uint32_t wa = (s < 2 ? q0.qa.x : q0.qa.y) >> (16 * (s & 1));
-      const uint32_t wb = (s < 2 ? q0.qb.x : q0.qb.y) >> (16 * (s & 1));
-      uint32_t a[4];
-      __nv_bfloat162 t;
-      t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[wa & 0xFFu]), sca);
-      a[0] = *reinterpret_cast<uint32_t*>(&t);  // row g,   k 4s, 4s+1
-      t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[wb & 0xFFu]), scb);
-      a[1] = *reinterpret_cast<uint32_t*>(&t);  // row g+8, k 4s, 4s+1
-      t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[(wa >> 8) & 0xFFu]), sca);
-      a[2] = *reinterpret_cast<uint32_t*>(&t);  // row g,   k 4s+2, 4s+3
-      t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[(wb >> 8) & 0xFFu]), scb);
-      a[3] = *reinterpret_cast<uint32_t*>(&t);  // row g+8, k 4s+2, 4s+3
-      const int64_t k = kbase + 4 * s;
+    for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t r = m0 + 16 * gi + g + 8 * h;
+        x.q[gi][h] = make_uint4(0u, 0u, 0u, 0u);
+        x.sc[gi][h] = 0u;
+        if (live && r < M) {
+          x.q[gi][h] = ldg_stream(reinterpret_cast<const uint4*>(xc + r * row_bytes + blk * 8));
+          x.sc[gi][h] = *reinterpret_cast<const uint16_t*>(xsf + sf_offset(r, blk, c16p));
+        }
+      }
+  };
+  Chunk x0, x1;
+  if (warp < nch) load(warp, x0);
+  for (int ch = warp; ch < nch; ch += 8) {
+    if (ch + 8 < nch) load(ch + 8, x1);
+    const bool live = !(half_tail && ch == nch - 1 && c >= 2);
+    __nv_bfloat162 scl[G][2][2];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        scl[gi][h][0] = __float2bfloat162_rn(e4m3_to_f32(x0.sc[gi][h] & 0xFFu));
+        scl[gi][h][1] = __float2bfloat162_rn(e4m3_to_f32(x0.sc[gi][h] >> 8));
+      }
+    const int64_t kb = (int64_t)ch * 128 + 32 * c;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t bfr[NT][2];
 #pragma unroll
       for (int jn = 0; jn < NT; ++jn) {
-        // At rows >= r are zero, so no bounds test on the adapter column is needed
-        const uint2 bb = __ldg(reinterpret_cast<const uint2*>(At + (int64_t)(jn * 8 + g) * K + k));
-        const uint32_t b[2] = {bb.x, bb.y};
-        mma_bf16_16816(acc[jn], a, b);
+        // At rows >= r are zero; a dead lane of a half chunk multiplies zeros
+        uint2 bb = make_uint2(0u, 0u);
+        if (live) bb = __ldg(reinterpret_cast<const uint2*>(At + (int64_t)(jn * 8 + g) * K + kb + 4 * s));
+        bfr[jn][0] = bb.x;
+        bfr[jn][1] = bb.y;
+      }
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        uint32_t a[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t word = (s < 4 ? (s < 2 ? x0.q[gi][h].x : x0.q[gi][h].y)
+                                       : (s < 6 ? x0.q[gi][h].z : x0.q[gi][h].w)) >>
+                                (16 * (s & 1));
+          __nv_bfloat162 t;
+          t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[word & 0xFFu]), scl[gi][h][s >> 2]);
+          a[h] = *reinterpret_cast<uint32_t*>(&t);  // elements 4s, 4s+1
+          t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[(word >> 8) & 0xFFu]),
+                      scl[gi][h][s >> 2]);
+          a[2 + h] = *reinterpret_cast<uint32_t*>(&t);  // elements 4s+2, 4s+3
+        }
+#pragma unroll
+        for (int jn = 0; jn < NT; ++jn) mma_bf16_16816(acc[gi][jn], a, bfr[jn]);
       }
     }
-    q0 = q1;
-    q1 = q2;
+    x0 = x1;
   }
   const float ga = *gx, gb = *gw;
   const bool normal = __fmul_rn(ga, gb) > 0.0f;
   const float f = normal ? __fdiv_rn(scale, gb) : __fmul_rn(scale, ga);
-  reduce_and_store<RP>(acc, red, m0, M, f, t_out);
+  reduce_and_store<RP, G>(acc, red, m0, M, f, t_out);
 }
 
-// U' = f * (dY B^T): dy [M, N] BF16, B [r, N] row-major.  A CTA owns 16 rows; warp
-// w takes the 64-wide N chunks w, w+8, ... with two chunks in flight ahead.
-template <int RP>
-__global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restrict__ dy,
+// U' = f * (dY B^T): dy [M, N] BF16, B [r, N] row-major.  A chunk is 32 elements
+// of a row: lane c holds elements [8c, 8c + 8) (16 bytes).  N is long here (up to
+// 2 x the intermediate size), so two chunks are in flight ahead of the one being
+// multiplied.
+template <int RP, int G>
+__global__ void __launch_bounds__(256, 2) k_lora_down_dgrad(const uint16_t* __restrict__ dy,
                                                          const float* __restrict__ gdy,
                                                          const float* __restrict__ gw,
                                                          int64_t M, int64_t N,
@@ -234,66 +265,64 @@ __global__ void __launch_bounds__(256) k_lora_down_dgrad(const uint16_t* __restr
                                                          float scale,
                                                          uint16_t* __restrict__ u_out) {
   constexpr int NT = RP / 8;
-  __shared__ float red[8 * 16 * RP];
+  __shared__ float red[8 * 16 * G * RP];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t m0 = (int64_t)blockIdx.x * 16;
-  const int64_t ra = m0 + g, rb = m0 + g + 8;
-  const bool va = ra < M, vb = rb < M;
-  float acc[NT][4];
+  const int64_t m0 = (int64_t)blockIdx.x * (16 * G);
+  const int nch = (int)(N >> 5);
+  float acc[G][NT][4];
 #pragma unroll
-  for (int jn = 0; jn < NT; ++jn) acc[jn][0] = acc[jn][1] = acc[jn][2] = acc[jn][3] = 0.0f;
+  for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn) acc[gi][jn][0] = acc[gi][jn][1] = acc[gi][jn][2] = acc[gi][jn][3] = 0.0f;
 
-  // chunk ch of 64 along N: lane (g, c) holds elements 16c .. 16c+15 of rows g, g+8
-  auto load = [&](int64_t ch, uint4* x) {
-    const int64_t n0 = ch * 64 + 16 * c;
-    x[0] = x[1] = x[2] = x[3] = make_uint4(0, 0, 0, 0);
-    if (va) {
-      const uint4* p = reinterpret_cast<const uint4*>(dy + ra * N + n0);
-      x[0] = ldg_stream(p);
-      x[1] = ldg_stream(p + 1);
-    }
-    if (vb) {
-      const uint4* p = reinterpret_cast<const uint4*>(dy + rb * N + n0);
-      x[2] = ldg_stream(p);
-      x[3] = ldg_stream(p + 1);
-    }
-  };
-  const int64_t nchunks = N >> 6;
-  uint4 x0[4], x1[4];
-  if (warp < nchunks) load(warp, x0);
-  if (warp + 8 < nchunks) load(warp + 8, x1);
-  for (int64_t ch = warp; ch < nchunks; ch += 8) {
-    uint4 x2[4];
-    if (ch + 16 < nchunks) load(ch + 16, x2);  // two chunks ahead
-    const int64_t n0 = ch * 64 + 16 * c;
-    const uint32_t wa[8] = {x0[0].x, x0[0].y, x0[0].z, x0[0].w, x0[1].x, x0[1].y, x0[1].z, x0[1].w};
-    const uint32_t wb[8] = {x0[2].x, x0[2].y, x0[2].z, x0[2].w, x0[3].x, x0[3].y, x0[3].z, x0[3].w};
+  auto load = [&](int ch, uint4 (&x)[G][2]) {
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      uint32_t a[4] = {wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1]};
+    for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t row = m0 + 16 * gi + g + 8 * h;
+        x[gi][h] = row < M ? ldg_stream(reinterpret_cast<const uint4*>(dy + row * N + (int64_t)ch * 32 + 8 * c))
+                           : make_uint4(0u, 0u, 0u, 0u);
+      }
+  };
+  uint4 x0[G][2], x1[G][2], x2[G][2];
+  if (warp < nch) load(warp, x0);
+  if (warp + 8 < nch) load(warp + 8, x1);
+  for (int ch = warp; ch < nch; ch += 8) {
+    if (ch + 16 < nch) load(ch + 16, x2);
+    const int64_t n0 = (int64_t)ch * 32 + 8 * c;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      uint32_t bfr[NT][2];
 #pragma unroll
       for (int jn = 0; jn < NT; ++jn) {
         const int col = jn * 8 + g;
-        uint32_t b[2] = {0u, 0u};
-        if (col < r) {
-          const uint2 bb = __ldg(reinterpret_cast<const uint2*>(B + (int64_t)col * N + n0 + 4 * s));
-          b[0] = bb.x;
-          b[1] = bb.y;
-        }
-        mma_bf16_16816(acc[jn], a, b);
+        uint2 bb = make_uint2(0u, 0u);
+        if (col < r) bb = __ldg(reinterpret_cast<const uint2*>(B + (int64_t)col * N + n0 + 4 * s));
+        bfr[jn][0] = bb.x;
+        bfr[jn][1] = bb.y;
+      }
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        const uint32_t a[4] = {s ? x0[gi][0].z : x0[gi][0].x, s ? x0[gi][1].z : x0[gi][1].x,
+                               s ? x0[gi][0].w : x0[gi][0].y, s ? x0[gi][1].w : x0[gi][1].y};
+#pragma unroll
+        for (int jn = 0; jn < NT; ++jn) mma_bf16_16816(acc[gi][jn], a, bfr[jn]);
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x0[i] = x1[i];
-      x1[i] = x2[i];
-    }
+    for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        x0[gi][h] = x1[gi][h];
+        x1[gi][h] = x2[gi][h];
+      }
   }
   const float ga = *gdy, gb = *gw;
   const float s_main = __fmul_rn(ga, gb);
   const float f = s_main > 0.0f ? __fdiv_rn(scale, s_main) : scale;
-  reduce_and_store<RP>(acc, red, m0, M, f, u_out);
+  reduce_and_store<RP, G>(acc, red, m0, M, f, u_out);
 }
 
 template <int RP>
@@ -301,12 +330,13 @@ static cudaError_t fwd_rp(const uint8_t* xc, const uint8_t* xsf, const float* gx
                           const float* gw, int64_t M, int64_t K, const uint16_t* A,
                           const uint16_t* B, int r, float scale, int64_t N, uint16_t* t_out,
                           uint16_t* bt_out, uint16_t* at_ws, cudaStream_t stream) {
+  constexpr int G = RP <= 32 ? 2 : 1;
   note_launch();
   k_lora_prep<RP><<<(int)((N + K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 1, at_ws,
                                                                     bt_out);
   note_launch();
-  k_lora_down_fwd<RP><<<(int)((M + 15) / 16), 256, 0, stream>>>(xc, xsf, gx, gw, M, K, at_ws, r,
-                                                                 scale, t_out);
+  k_lora_down_fwd<RP, G><<<(int)((M + 16 * G - 1) / (16 * G)), 256, 0, stream>>>(
+      xc, xsf, gx, gw, M, K, at_ws, scale, t_out);
   return cudaGetLastError();
 }
 
@@ -314,11 +344,12 @@ template <int RP>
 static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* gw, int64_t M,
                             int64_t N, const uint16_t* A, const uint16_t* B, int r, float scale,
                             int64_t K, uint16_t* u_out, uint16_t* ap_out, cudaStream_t stream) {
+  constexpr int G = RP <= 32 ? 2 : 1;
   note_launch();
   k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
   note_launch();
-  k_lora_down_dgrad<RP><<<(int)((M + 15) / 16), 256, 0, stream>>>(dy, gdy, gw, M, N, B, r, scale,
-                                                                   u_out);
+  k_lora_down_dgrad<RP, G><<<(int)((M + 16 * G - 1) / (16 * G)), 256, 0, stream>>>(
+      dy, gdy, gw, M, N, B, r, scale, u_out);
   return cudaGetLastError();
 }
 

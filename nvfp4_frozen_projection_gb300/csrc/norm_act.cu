@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(256) k_rmsnorm_encode(
   const int nb = (int)(H >> 4);
   const TensorScale ts = tensor_scale(__uint_as_float(*amax_bits));
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
+  __shared__ ScaleTable tab;
+  scale_table_init(&tab, ts);
+  __syncthreads();
   for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < Mpad;
        w += (int64_t)gridDim.x * 8) {
     const int64_t row = Mpad - 1 - w;
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_encode(
           am = max(am, __float_as_uint(f[i]) & 0x7FFFFFFFu);
         }
         float t, rcp;
-        const uint32_t s = block_scale(__uint_as_float(am), ts, &t, &rcp);
+        const uint32_t s = block_scale_tab(__uint_as_float(am), ts, &tab, &t, &rcp);
         uint2 cw;
         cw.x = encode8(f, t, rcp);
         cw.y = encode8(f + 8, t, rcp);
@@ -145,29 +148,140 @@ __global__ void __launch_bounds__(256) k_rmsnorm_encode(
 }
 
 // ============================================================== SiLU-multiply
-// Pass 1: amax of h, gate and up.  One thread per block of 16 columns.
-__global__ void __launch_bounds__(256) k_silu_amax(const uint16_t* __restrict__ gu, int64_t M,
-                                                   int64_t I, FastDiv bpr_div,
-                                                   unsigned* __restrict__ amax3) {
+// The exact h of element i (0..15) of a block held as two uint4 of BF16 gate and
+// up values, for a runtime i, without indexing a register array.  Called from
+// loops that are not unrolled: the exact recipe is long, and copies of it for
+// every element would not fit the instruction cache.
+__device__ __forceinline__ float silu_exact_at(const uint4& g0, const uint4& g1, const uint4& u0,
+                                               const uint4& u1, int i) {
+  auto word = [](const uint4& a, const uint4& b, int i) {
+    const uint4& v = i < 8 ? a : b;
+    const int k = (i & 7) >> 1;
+    const uint32_t w = k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+    return (i & 1) ? (w & 0xFFFF0000u) : (w << 16);
+  };
+  return silu_mul(__uint_as_float(word(g0, g1, i)), __uint_as_float(word(u0, u1, i)));
+}
+
+// Fast h for a block of 16 (gate values gf, up values uf) and its largest
+// magnitude.  The fast values are used only where silu_mul_fast's bound is
+// guaranteed for the whole block: every |gate| zero or in [2^-60, 80], every
+// input finite, and the block maximum between 2^-100 and 2^100;
+// silu_block_fast_ok says whether it is.
+__device__ __forceinline__ float silu_block_fast(const float* gf, const float* uf, float* hf) {
+  float am = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    hf[i] = silu_mul_fast(gf[i], uf[i]);
+    am = fmaxf(am, fabsf(hf[i]));
+  }
+  return am;
+}
+__device__ __forceinline__ bool silu_block_fast_ok(uint32_t gmax_bits, uint32_t umax_bits,
+                                                   bool tiny_gate, float am) {
+  return gmax_bits <= 0x42A00000u /* 80.0f */ && umax_bits < 0x7F800000u && !tiny_gate &&
+         am >= 0x1p-100f && am <= 0x1p+100f;
+}
+// Whether some gate value of the 8 BF16 values is nonzero but below 2^-60: there
+// g / (1 + exp(-g)) may leave the normal range and the fast quotient its bound,
+// while a large up value can still lift h far above the block's rounding
+// thresholds.  With every |g| zero or in [2^-60, 80] that quotient is zero or
+// normal.
+__device__ __forceinline__ bool bf16x8_has_tiny(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  bool t = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = w[i] & 0x7FFFu, hi = (w[i] >> 16) & 0x7FFFu;
+    t |= (lo - 1u) < (0x2180u - 1u);  // 0 < |x| < 2^-60 (bf16 bits of 2^-60: 0x2180)
+    t |= (hi - 1u) < (0x2180u - 1u);
+  }
+  return t;
+}
+
+// Pass 1: amax of h = silu(gate) * up, of gate and of up.  The exact recipe runs
+// only for blocks that may hold the maximum.  Each round the warp takes A, the
+// largest of its running value am and every lane's block maximum of fast values
+// (am_blk), and a lane evaluates its block exactly only if am_blk >= A (1 - 3r)
+// (r = kSiluRel); the block behind A always is, so A stays the fast value of an
+// exactly evaluated element y.  A block skipped this way holds nothing above
+// exact(y): exact <= fast (1 + r) < A (1 - 3r)(1 + r) < A (1 - 2r) <= exact(y), and
+// y's lane keeps exact(y) in its maximum.  So the largest exact value over the
+// evaluated blocks is the exact maximum, and only a few blocks per warp take the
+// exact path.  A block outside the fast bound is always evaluated exactly (its
+// exact maximum then enters A).  The loop advances by warps so that every lane
+// takes part in each round.
+__global__ void __launch_bounds__(256, 3) k_silu_amax(const uint16_t* __restrict__ gu, int64_t M,
+                                                      int64_t I, FastDiv bpr_div,
+                                                      unsigned* __restrict__ amax3) {
   const uint32_t bpr = (uint32_t)(I >> 4);
   const uint32_t total = (uint32_t)M * bpr;
+  const uint32_t lane = threadIdx.x & 31u;
+  const float keep = 1.0f - 3.0f * kSiluRel;
   uint32_t ah = 0, ag = 0, au = 0;
-  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += gridDim.x * blockDim.x) {
-    const int64_t row = bpr_div.div(it), b = it - (uint32_t)row * bpr;
-    const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2 * I + b * 16);
-    const uint4* up = reinterpret_cast<const uint4*>(gu + row * 2 * I + I + b * 16);
-    const uint4 g0 = ldg_stream(gp), g1 = ldg_stream(gp + 1);
-    const uint4 u0 = ldg_stream(up), u1 = ldg_stream(up + 1);
-    ag = max(ag, max(absmax_bf16x8_bits(g0), absmax_bf16x8_bits(g1)));
-    au = max(au, max(absmax_bf16x8_bits(u0), absmax_bf16x8_bits(u1)));
-    float gf[16], uf[16];
-    bf16x8_to_f32(g0, gf);
-    bf16x8_to_f32(g1, gf + 8);
-    bf16x8_to_f32(u0, uf);
-    bf16x8_to_f32(u1, uf + 8);
+  float am = 0.0f;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  // the next round's 64 bytes are loaded before this one is processed
+  uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0, n2 = n0, n3 = n0;
+  auto fetch = [&](uint32_t it) {
+    if (it < total) {
+      const int64_t row = bpr_div.div(it), b = it - (uint32_t)row * bpr;
+      const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2 * I + b * 16);
+      const uint4* up = reinterpret_cast<const uint4*>(gu + row * 2 * I + I + b * 16);
+      n0 = ldg_stream(gp);
+      n1 = ldg_stream(gp + 1);
+      n2 = ldg_stream(up);
+      n3 = ldg_stream(up + 1);
+    }
+  };
+  const uint32_t first = blockIdx.x * blockDim.x + (threadIdx.x & ~31u);
+  fetch(first + lane);
+  for (uint32_t w0 = first; w0 < total; w0 += stride) {
+    const uint32_t it = w0 + lane;
+    const bool act = it < total;
+    const uint4 g0 = n0, g1 = n1, u0 = n2, u1 = n3;
+    fetch(it + stride);
+    const uint32_t gb = max(absmax_bf16x8_bits(g0), absmax_bf16x8_bits(g1));
+    const uint32_t ub = max(absmax_bf16x8_bits(u0), absmax_bf16x8_bits(u1));
+    float am_blk = 0.0f;
+    bool ok = true;
+    float hf[16];
+    if (act) {
+      ag = max(ag, gb);
+      au = max(au, ub);
+      float gf[16], uf[16];
+      bf16x8_to_f32(g0, gf);
+      bf16x8_to_f32(g1, gf + 8);
+      bf16x8_to_f32(u0, uf);
+      bf16x8_to_f32(u1, uf + 8);
+      am_blk = silu_block_fast(gf, uf, hf);
+      ok = silu_block_fast_ok(gb, ub, bf16x8_has_tiny(g0) || bf16x8_has_tiny(g1), am_blk);
+    }
+    float A = fmaxf(am, ok ? am_blk : 0.0f);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ah = max(ah, __float_as_uint(silu_mul(gf[i], uf[i])) & 0x7FFFFFFFu);
+    for (int off = 16; off > 0; off >>= 1) A = fmaxf(A, __shfl_xor_sync(0xFFFFFFFFu, A, off));
+    float em = 0.0f;
+    if (act && (!ok || !(am_blk < A * keep))) {
+      // the elements that may reach A (every element of a block outside the bound)
+      uint32_t cand = 0xFFFFu;
+      if (ok) {
+        cand = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) cand |= (fabsf(hf[i]) < A * keep ? 0u : 1u) << i;
+      }
+      while (cand) {
+        const int i = __ffs(cand) - 1;
+        cand &= cand - 1;
+        const uint32_t xb = __float_as_uint(silu_exact_at(g0, g1, u0, u1, i)) & 0x7FFFFFFFu;
+        ah = max(ah, xb);
+        if (xb < 0x7F800000u) em = fmaxf(em, __uint_as_float(xb));
+      }
+    }
+    // a block outside the fast bound enters the running value with its exact maximum
+    float B = ok ? 0.0f : em;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) B = fmaxf(B, __shfl_xor_sync(0xFFFFFFFFu, B, off));
+    am = fmaxf(A, B);
   }
   block_max_atomic(ah, amax3 + 0);
   block_max_atomic(ag, amax3 + 1);
@@ -175,27 +289,67 @@ __global__ void __launch_bounds__(256) k_silu_amax(const uint16_t* __restrict__ 
 }
 
 // Pass 2: one thread per block of 16 columns of one row; encodes h, gate and up.
+// Fast values give the exact encoding of h wherever both roundings are certain:
+// the block scale when e4m3 of the fast block maximum over d, widened by
+// (1 -/+ 2r), rounds to one code; an element's code when its scaled fast value
+// widened by (1 -/+ 2r) rounds to one E2M1 code (the exact scaled value lies in
+// between, and both roundings are monotonic).  Elements that fail the second test
+// are encoded from their exact values; a block that fails the first, or lies
+// outside the fast bound, is encoded from exact values throughout.
 struct SiluOut {
   uint8_t* codes[3];
   uint8_t* sf[3];
   float* g[3];
 };
 
-__global__ void __launch_bounds__(256) k_silu_encode(const uint16_t* __restrict__ gu, int64_t M,
-                                                     int64_t Mpad, int64_t I, FastDiv bpr_div,
-                                                     const float* __restrict__ amax3_opt,
-                                                     const unsigned* __restrict__ amax3,
-                                                     SiluOut out) {
+// The E2M1 code of x as encode8 makes it for a block with decode step t and
+// rcp = 1/t (0 when t == 0).
+__device__ __forceinline__ uint32_t e2m1_code_of(float x, float t, float rcp) {
+  if (t > 0.0f && rcp <= 3.4028234663852886e38f) return e2m1x2_mag(__fmul_rn(x, rcp), 0.0f) & 0xFu;
+  const float a = fabsf(x);
+  const uint32_t mag = (t == 0.0f || a == 0.0f) ? 0u : (e2m1x2_mag(__fmul_rn(a, rcp), 0.0f) & 0x7u);
+  return mag | (sign_bit(x) << 3);
+}
+
+__global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restrict__ gu,
+                                                        int64_t M, int64_t Mpad, int64_t I,
+                                                        FastDiv bpr_div,
+                                                        const float* __restrict__ amax3_opt,
+                                                        const unsigned* __restrict__ amax3,
+                                                        SiluOut out) {
   TensorScale ts[3];
+  __shared__ ScaleTable tab[3];
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
     ts[k] = tensor_scale(amax3_opt ? amax3_opt[k] : __uint_as_float(amax3[k]));
     if (blockIdx.x == 0 && threadIdx.x == 0) *out.g[k] = ts[k].g;
+    scale_table_init(&tab[k], ts[k]);
   }
+  __syncthreads();
+  const float lo_f = 1.0f - 2.0f * kSiluRel, hi_f = 1.0f + 2.0f * kSiluRel;
+  const float rcp_d = tab[0].rcp_d;
   const uint32_t bpr = (uint32_t)(I >> 4);
   const uint32_t total = (uint32_t)Mpad * bpr;
-  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += gridDim.x * blockDim.x) {
+  const uint32_t stride = gridDim.x * blockDim.x;
+  // the next iteration's 64 bytes are loaded before this one is processed
+  uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0, n2 = n0, n3 = n0;
+  auto fetch = [&](uint32_t it) {
+    if (it < total) {
+      const int64_t row = bpr_div.div(it), b = it - (uint32_t)row * bpr;
+      if (row < M) {
+        const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2 * I + b * 16);
+        const uint4* up = reinterpret_cast<const uint4*>(gu + row * 2 * I + I + b * 16);
+        n0 = ldg_stream(gp);
+        n1 = ldg_stream(gp + 1);
+        n2 = ldg_stream(up);
+        n3 = ldg_stream(up + 1);
+      }
+    }
+  };
+  fetch(blockIdx.x * blockDim.x + threadIdx.x);
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += stride) {
+    const uint4 g0 = n0, g1 = n1, u0 = n2, u1 = n3;
+    fetch(it + stride);
     const int64_t row = bpr_div.div(it), b = it - (uint32_t)row * bpr;
     const int64_t so = sf_offset(row, b, bpr);
     if (row >= M) {
@@ -203,26 +357,74 @@ __global__ void __launch_bounds__(256) k_silu_encode(const uint16_t* __restrict_
       for (int k = 0; k < 3; ++k) out.sf[k][so] = 0;
       continue;
     }
-    const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2 * I + b * 16);
-    const uint4* up = reinterpret_cast<const uint4*>(gu + row * 2 * I + I + b * 16);
-    float v[3][16];
-    bf16x8_to_f32(ldg_stream(gp), v[1]);
-    bf16x8_to_f32(ldg_stream(gp + 1), v[1] + 8);
-    bf16x8_to_f32(ldg_stream(up), v[2]);
-    bf16x8_to_f32(ldg_stream(up + 1), v[2] + 8);
+    uint32_t w[2] = {0u, 0u};
+    uint32_t sh = 0;
+    {
+      // ---- h
+      float gf[16], uf[16], hf[16];
+      bf16x8_to_f32(g0, gf);
+      bf16x8_to_f32(g1, gf + 8);
+      bf16x8_to_f32(u0, uf);
+      bf16x8_to_f32(u1, uf + 8);
+      const float am_blk = silu_block_fast(gf, uf, hf);
+      bool fast = silu_block_fast_ok(max(absmax_bf16x8_bits(g0), absmax_bf16x8_bits(g1)),
+                                     max(absmax_bf16x8_bits(u0), absmax_bf16x8_bits(u1)),
+                                     bf16x8_has_tiny(g0) || bf16x8_has_tiny(g1), am_blk) &&
+                  ts[0].g > 0.0f;
+      float t = 0.0f, rcp = 0.0f;
+      fast = fast && rcp_d > 0.0f;
+      if (fast) {
+        const float q = __fmul_rn(am_blk, rcp_d);
+        sh = e4m3_from_f32(__fmul_rn(q, lo_f));
+        fast = sh == e4m3_from_f32(__fmul_rn(q, hi_f));
+        t = tab[0].t[sh & 0x7Fu];
+        rcp = tab[0].rcp[sh & 0x7Fu];
+        fast = fast && t > 0.0f && rcp <= 3.4028234663852886e38f;
+      }
+      uint32_t redo = 0xFFFFu;
+      if (fast) {
+        redo = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[0][i] = silu_mul(v[1][i], v[2][i]);
+        for (int i = 0; i < 16; i += 2) {
+          const float x0 = __fmul_rn(hf[i], rcp), x1 = __fmul_rn(hf[i + 1], rcp);
+          const uint32_t cl = e2m1x2_mag(__fmul_rn(x0, lo_f), __fmul_rn(x1, lo_f));
+          const uint32_t ch = e2m1x2_mag(__fmul_rn(x0, hi_f), __fmul_rn(x1, hi_f));
+          const uint32_t d = cl ^ ch;
+          redo |= ((d & 0x0Fu) ? 1u : 0u) << i;
+          redo |= ((d & 0xF0u) ? 1u : 0u) << (i + 1);
+          w[i >> 3] |= cl << (4 * (i & 7));
+        }
+      } else {
+        // the exact block maximum and scale; every code from its exact value below
+        uint32_t em = 0;
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+          em = max(em, __float_as_uint(silu_exact_at(g0, g1, u0, u1, i)) & 0x7FFFFFFFu);
+        sh = block_scale_tab(__uint_as_float(em), ts[0], &tab[0], &t, &rcp);
+      }
+      while (redo) {
+        const int i = __ffs(redo) - 1;
+        redo &= redo - 1;
+        const uint32_t c = e2m1_code_of(silu_exact_at(g0, g1, u0, u1, i), t, rcp);
+        const int sh4 = 4 * (i & 7);
+        w[i >> 3] = (w[i >> 3] & ~(0xFu << sh4)) | (c << sh4);
+      }
+    }
+    *reinterpret_cast<uint2*>(out.codes[0] + row * (I >> 1) + b * 8) = make_uint2(w[0], w[1]);
+    out.sf[0][so] = (uint8_t)sh;
+    // ---- gate and up: their BF16 values are exact
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      uint32_t am = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) am = max(am, __float_as_uint(v[k][i]) & 0x7FFFFFFFu);
-      float t, rcp;
-      const uint32_t s = block_scale(__uint_as_float(am), ts[k], &t, &rcp);
-      uint2 cw;
-      cw.x = encode8(v[k], t, rcp);
-      cw.y = encode8(v[k] + 8, t, rcp);
-      *reinterpret_cast<uint2*>(out.codes[k] + row * (I >> 1) + b * 8) = cw;
+    for (int k = 1; k < 3; ++k) {
+      float v[16];
+      bf16x8_to_f32(k == 1 ? g0 : u0, v);
+      bf16x8_to_f32(k == 1 ? g1 : u1, v + 8);
+      const uint32_t am = max(absmax_bf16x8_bits(k == 1 ? g0 : u0), absmax_bf16x8_bits(k == 1 ? g1 : u1));
+      float tk, rk;
+      const uint32_t s = block_scale_tab(__uint_as_float(am), ts[k], &tab[k], &tk, &rk);
+      uint2 ck;
+      ck.x = encode8(v, tk, rk);
+      ck.y = encode8(v + 8, tk, rk);
+      *reinterpret_cast<uint2*>(out.codes[k] + row * (I >> 1) + b * 8) = ck;
       out.sf[k][so] = (uint8_t)s;
     }
   }

@@ -69,6 +69,9 @@ __global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__
   const float amax = amax_opt ? *amax_opt : __uint_as_float(*amax_bits);
   const TensorScale ts = tensor_scale(amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
+  __shared__ ScaleTable tab;
+  scale_table_init(&tab, ts);
+  __syncthreads();
   const uint32_t chunks = (uint32_t)(K >> 6);
   const uint32_t total = (uint32_t)Mpad * chunks;  // < 2^31 (checked by the caller)
   const int64_t c16p = K >> 4;
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__
         float amax_blk = __uint_as_float(
             max(absmax_bf16x8_bits(v[2 * b]), absmax_bf16x8_bits(v[2 * b + 1])));
         float t, rcp;
-        uint32_t s = block_scale(amax_blk, ts, &t, &rcp);
+        uint32_t s = block_scale_tab(amax_blk, ts, &tab, &t, &rcp);
         w[2 * b] = encode8(f, t, rcp);
         w[2 * b + 1] = encode8(f + 8, t, rcp);
         sfw |= s << (8 * b);

@@ -61,6 +61,39 @@ def test_silu_mul_quant_bit_exact(M, I):
     assert_nvfp4_equal(uq, ru, "up")
 
 
+@pytest.mark.parametrize("case", ["wide", "tiny_rows", "tiny_tensor", "tiny_gate"])
+def test_silu_mul_quant_adversarial(case):
+    """Inputs that push the kernel's fast-value shortcut to its exact fallbacks:
+    |gate| beyond 80, exact and signed zeros, products that underflow, blocks whose
+    decode step is zero or subnormal, and a whole tensor of tiny values."""
+    rng = np.random.default_rng({"wide": 11, "tiny_rows": 12, "tiny_tensor": 13,
+                                 "tiny_gate": 14}[case])
+    M, I = 257, 1024
+    g = rng.uniform(-100.0, 100.0, (M, I)).astype(np.float32)
+    u = rng.standard_normal((M, I)).astype(np.float32)
+    u[rng.random((M, I)) < 0.1] = 0.0
+    u[rng.random((M, I)) < 0.05] = -0.0
+    g[rng.random((M, I)) < 0.05] = -0.0
+    if case == "tiny_rows":
+        u[::7] *= np.float32(1e-37)   # h of these rows lands far below the tensor's scale
+        u[3::11] = np.float32(1e-38)
+    if case == "tiny_tensor":
+        u *= np.float32(1e-36)
+    if case == "tiny_gate":
+        # gate values near the bottom of the range against large up values: h stays
+        # ordinary while g / (1 + exp(-g)) is tiny
+        m = rng.random((M, I)) < 0.2
+        g[m] = rng.choice(np.array([1e-20, -1e-25, 3e-30, -1e-38, 2e-39], np.float32), m.sum())
+        u[m] = rng.choice(np.array([1e15, -3e20, 1e25, 7e30, -2e35], np.float32), m.sum())
+    gu = wl.bf16_round(np.concatenate([g, u], axis=1))
+    hq, gq, uq = pact_silu_mul_quant(bf16(gu))
+    pact_check_status()
+    rh, rg, ru = orc.silu_mul_quant(gu)
+    assert_nvfp4_equal(hq, rh, "h " + case)
+    assert_nvfp4_equal(gq, rg, "gate " + case)
+    assert_nvfp4_equal(uq, ru, "up " + case)
+
+
 def test_silu_mul_quant_full_size_and_amax_opt():
     """Workload 3's SiLU input shape [4096, 2 x 8192]; also the single-pass variant
     that takes precomputed amax values."""
