@@ -18,19 +18,25 @@
 // chunks.  s = g_a * g_b (or 1 when either per-tensor scale is zero, in which
 // case the NVFP4 operand is all zero).
 //
-// Structure: one persistent CTA per SM, 14 warps.
+// Structure: one persistent CTA per SM, 14 warps; CTAs pair up in clusters of two
+// along M (when M spans more than one tile) and share each B tile by multicast.
 //   warp 0      TMA producer: A/B tiles (128-byte rows, 128B swizzle; one 16 KB
-//               and one 16/32 KB box per stage) and the scale-factor atoms (plain
-//               bulk copies) into a STAGES-deep shared-memory ring; the LoRA
-//               operands once per tile.
+//               A box and half of the B tile per CTA, multicast to the pair) and
+//               the scale-factor atoms (plain bulk copies) into a STAGES-deep
+//               shared-memory ring; the LoRA operands once per tile.
 //   warp 1      TMEM allocator and MMA issuer (one thread): MMAs only;
-//               tcgen05.commit frees ring slots and publishes the accumulator.
+//               tcgen05.commit frees ring slots (in both CTAs of the pair) and
+//               publishes the accumulator.
 //   warps 2-5   scale staging: shared -> TMEM with tcgen05.st (one warp per TMEM
 //               lane quarter).  A tcgen05.cp per atom on the MMA issuer's pipe
 //               cost ~35 extra cycles per copy beyond one per MMA; TMEM stores
 //               from other warps do not slow the MMAs.
-//   warps 6-13  epilogue: TMEM -> registers (tcgen05.ld), scale, optional addend,
-//               BF16 cast, global store, optional amax.
+//   warps 6-13  epilogue: TMEM -> registers (tcgen05.ld) 32 columns at a time,
+//               each slice scaled, added to the prefetched addend and rounded to
+//               BF16 at once, so the single accumulator is released right after the
+//               last load; then swizzled staging and TMA stores, optional amax.
+// Tiles are visited in bands of M-units swept over all N-tiles (see unit_mn), so
+// a large A operand leaves DRAM once.
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -163,14 +169,33 @@ __global__ void __launch_bounds__(448, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nks = (p.K + BK - 1) / BK;
   const int rb_total = (p.N + 127) / 128;
-  // work units: CM vertically adjacent tiles sharing one B tile; unit u covers
-  // m-tiles CM*(u % num_mc) + [0, CM) and n-tile u / num_mc
+  // work units: CM vertically adjacent tiles (an M-unit) sharing one B tile.  The
+  // units are ordered in bands of band_mc M-units: a band is swept over every
+  // N-tile, M-units fastest, before the next band starts.  With one band (the
+  // whole M range) consecutive units share a B tile and all of A stays in L2
+  // across the sweeps; when A is too large for that, a narrower band keeps its
+  // rows in L2 while every B tile passes, so each byte of A leaves DRAM once.
   const uint32_t crank = CM > 1 ? cluster_ctarank() : 0u;
   const int num_mc = (p.num_m + CM - 1) / CM;
   const int nunits = num_mc * p.num_n;
   const int unit0 = (int)blockIdx.x / CM, nclusters = (int)gridDim.x / CM;
-  auto tile_mt = [&](int u) { return (u % num_mc) * CM + (int)crank; };
-  auto tile_n0 = [&](int u) { return (u / num_mc) * BN; };
+  const int band = p.band_mc;
+  auto unit_mn = [&](int u, int& mc, int& n) {
+    const int bi = u / (band * p.num_n), r = u - bi * band * p.num_n;
+    const int mc0 = bi * band, bm = min(band, num_mc - mc0);
+    n = r / bm;
+    mc = mc0 + (r - n * bm);
+  };
+  auto tile_mt = [&](int u) {
+    int mc, n;
+    unit_mn(u, mc, n);
+    return mc * CM + (int)crank;
+  };
+  auto tile_n0 = [&](int u) {
+    int mc, n;
+    unit_mn(u, mc, n);
+    return n * BN;
+  };
   // this CTA's K steps over all its units, as one sequence of "fills"
   const int my_units = unit0 < nunits ? (nunits - unit0 + nclusters - 1) / nclusters : 0;
   const int nfills = my_units * nks;
@@ -572,8 +597,17 @@ static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
   const int units = num_mc * L.p.num_n;
   const int clusters = units < max_clusters[dev] ? units : max_clusters[dev];
   cfg.gridDim = dim3(clusters * CM);
+  // one band while A (the codes of all M rows) fits comfortably in L2 next to the
+  // B tiles in flight; else bands just wide enough to keep every cluster busy
+  GemmParams p = L.p;
+  const double a_bytes = (double)p.num_m * 128.0 * (double)p.K * 0.5625;
+  p.band_mc = num_mc;
+  if (a_bytes > 32.0 * 1024 * 1024) {
+    const int b = (clusters + p.num_n - 1) / p.num_n;
+    p.band_mc = b < 1 ? 1 : (b > num_mc ? num_mc : b);
+  }
   note_launch();
-  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmLA, L.tmLB, L.tmOut, L.p);
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmLA, L.tmLB, L.tmOut, p);
 }
 
 int gemm_block_n(int64_t N, int rpe) { return (N % 256 == 0 && rpe <= 64) ? 256 : 128; }

@@ -35,6 +35,7 @@ struct GemmParams {
   int k16p;                // pad4(K/16)
   int num_m, num_n;        // tile grid
   int lora_steps;          // K=16 BF16 MMAs of the LoRA product per tile (0 = none)
+  int band_mc;             // tile order: bands of band_mc M-units, each swept over all N
 };
 
 struct GemmLaunch {

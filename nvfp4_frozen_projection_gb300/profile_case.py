@@ -1,0 +1,85 @@
+"""One libpact operation on seeded inputs, repeated a few times, for a profiler.
+
+    python -m nvfp4_frozen_projection_gb300.profile_case <case> [--m M] [--reps R]
+
+Cases (M = tokens; the other sizes are the Llama-3B layer's):
+  gemm-gate-up-dgrad  dX = dY W (NVFP4, K = 2 x 8192) + LoRA term, out 3072 wide
+  gemm-gate-up-fwd    Y = X W^T (NVFP4, 3072 -> 2 x 8192) + LoRA term
+  quant               NVFP4 quantisation of a BF16 [M, 3072] tensor
+  silu                SiLU-multiply -> NVFP4 of a BF16 [M, 2 x 8192] tensor
+  lora-down-fwd       the q projection's forward (down-projection + GEMM)
+
+The default M (4096) keeps every case's inputs above the 129 MB L2 and its device
+memory under 1 GB, which is the size a full ncu capture wants.  Each run exits 0
+only if the library's status word is clear.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import (pact_check_status, pact_lora_linear_dgrad, pact_lora_linear_fwd,
+               pact_pack_weight_bwd, pact_pack_weight_fwd, pact_quant_nvfp4,
+               pact_silu_mul_quant)
+
+HIDDEN, INTER = 3072, 8192
+
+
+def _lora(d_in, d_out, r, dev, gen):
+    W = torch.randn(d_out, d_in, device=dev, generator=gen) * 0.02
+    A = (torch.randn(d_in, r, device=dev, generator=gen) / d_in ** 0.5).bfloat16()
+    B = (torch.randn(r, d_out, device=dev, generator=gen) * 0.1).bfloat16()
+    return W, A, B
+
+
+def run(case: str, m: int, reps: int) -> None:
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    if case == "gemm-gate-up-dgrad":
+        W, A, B = _lora(HIDDEN, 2 * INTER, 32, dev, gen)
+        wb = pact_pack_weight_bwd(W)
+        dy = (torch.randn(m, 2 * INTER, device=dev, generator=gen) * 0.01).bfloat16()
+        dyq = pact_quant_nvfp4(dy)
+        dx = torch.empty(m, HIDDEN, dtype=torch.bfloat16, device=dev)
+        for _ in range(reps):
+            pact_lora_linear_dgrad(dyq, dy, wb, A, B, 2.0, dx=dx)
+    elif case in ("gemm-gate-up-fwd", "lora-down-fwd"):
+        n_out = 2 * INTER if case == "gemm-gate-up-fwd" else HIDDEN
+        r = 32 if case == "gemm-gate-up-fwd" else 16
+        W, A, B = _lora(HIDDEN, n_out, r, dev, gen)
+        wf = pact_pack_weight_fwd(W)
+        x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
+        xq = pact_quant_nvfp4(x)
+        y = torch.empty(m, n_out, dtype=torch.bfloat16, device=dev)
+        for _ in range(reps):
+            pact_lora_linear_fwd(xq, wf, A, B, 2.0, y=y)
+    elif case == "quant":
+        x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
+        q = pact_quant_nvfp4(x)
+        for _ in range(reps):
+            pact_quant_nvfp4(x, out=q)
+    elif case == "silu":
+        gu = torch.randn(m, 2 * INTER, device=dev, generator=gen).bfloat16()
+        outs = pact_silu_mul_quant(gu)
+        for _ in range(reps):
+            pact_silu_mul_quant(gu, outs=outs)
+    else:
+        raise SystemExit(f"unknown case {case!r}")
+    torch.cuda.synchronize()
+    pact_check_status()
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case")
+    ap.add_argument("--m", type=int, default=4096)
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args()
+    run(a.case, a.m, a.reps)
+    print("ok")
+
+
+if __name__ == "__main__":
+    main()
