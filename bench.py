@@ -42,6 +42,10 @@ from nvfp4_frozen_projection_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "NVFP4 LoRA-linear fwd+dgrad TFLOPS (% FP4 peak); quant GB/s; layer tokens/s"
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
+# DRAM bytes (read + write) of one full-size launch of the GEMM kernel, from a
+# one-pass ncu capture of profile_case at M = 8192 (profiles/gemm_nvfp4_gate_up.md);
+# they describe the kernel as of that capture.
+GEMM_TRAFFIC_BYTES = {"gate_up.dgrad": 195.53e6, "gate_up.fwd": 263.92e6}
 
 
 def peaks():
@@ -413,7 +417,8 @@ def main():
         "fp4_peak_frac_step": value / world / fp4_peak,
         "roofline": {"bound": "tensor", "kernel": f"k_gemm_nvfp4 ({dominant})",
                      "achieved": dk_["tflops"], "peak": fp4_peak, "unit": "TFLOP/s",
-                     "frac": dk_["tflops"] / fp4_peak, "traffic": None,
+                     "frac": dk_["tflops"] / fp4_peak,
+                     "traffic": GEMM_TRAFFIC_BYTES.get(dominant),
                      "peak_source": f"{src} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
         "gemm_kernels": {k: {"ms": round(v["ms"], 5), "tflops": round(v["tflops"], 1)}
                          for k, v in kern.items()},
