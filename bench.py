@@ -46,6 +46,11 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
 # one-pass ncu capture of profile_case at M = 8192 (profiles/gemm_nvfp4_gate_up.md);
 # they describe the kernel as of that capture.
 GEMM_TRAFFIC_BYTES = {"gate_up.dgrad": 195.53e6, "gate_up.fwd": 263.92e6}
+# (N, K) of each distinct frozen-projection GEMM of the layer-3b step (out = M x N)
+GEMM_SHAPES = {"q.fwd": (3072, 3072), "k.fwd": (1024, 3072), "o.fwd": (3072, 3072),
+               "gate_up.fwd": (16384, 3072), "down.fwd": (3072, 8192),
+               "down.dgrad": (8192, 3072), "gate_up.dgrad": (3072, 16384),
+               "q.dgrad": (3072, 3072), "k.dgrad": (3072, 1024)}
 
 
 def peaks():
@@ -209,9 +214,7 @@ def time_gemm_kernels(stack, inputs, reps):
         "k.dgrad": lambda: stack.p["k"].dgrad(stack.dkq, dk, stack.dxn1, accumulate=True),
     }
     m = stack.m
-    flops = {"q.fwd": (3072, 3072), "k.fwd": (1024, 3072), "o.fwd": (3072, 3072),
-             "gate_up.fwd": (16384, 3072), "down.fwd": (3072, 8192), "down.dgrad": (8192, 3072),
-             "gate_up.dgrad": (3072, 16384), "q.dgrad": (3072, 3072), "k.dgrad": (3072, 1024)}
+    flops = GEMM_SHAPES
     out = {}
     for name, fn in calls.items():
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -230,6 +233,30 @@ def time_gemm_kernels(stack, inputs, reps):
         n_, k_ = flops[name]
         f = 2.0 * m * n_ * k_
         out[name] = {"ms": ms, "tflops": f / (ms * 1e-3) / 1e12, "flops": f}
+    return out
+
+
+def time_bf16_comparator(m, shapes, reps):
+    """The same GEMM shapes as plain BF16 matmuls through torch (cuBLAS): the BF16
+    column of the pages' Table 1, for context.  shapes: name -> (N, K)."""
+    out = {}
+    for name, (n_, k_) in shapes.items():
+        a = torch.randn(m, k_, device="cuda", dtype=torch.bfloat16)
+        w = torch.randn(n_, k_, device="cuda", dtype=torch.bfloat16)
+        y = torch.empty(m, n_, device="cuda", dtype=torch.bfloat16)
+        for _ in range(3):
+            torch.matmul(a, w.t(), out=y)
+        torch.cuda.synchronize()
+        b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b.record()
+        for _ in range(reps):
+            torch.matmul(a, w.t(), out=y)
+        e.record()
+        torch.cuda.synchronize()
+        ms = b.elapsed_time(e) / reps
+        out[name] = {"ms": ms, "tflops": 2.0 * m * n_ * k_ / (ms * 1e-3) / 1e12}
+        del a, w, y
+    torch.cuda.empty_cache()
     return out
 
 
@@ -398,6 +425,7 @@ def main():
                      reps=10)
     s_bytes = m * stack.inter * (4 + 3 * (0.5 + 1 / 16))
     pk.pact_check_status()
+    bf16 = time_bf16_comparator(m, GEMM_SHAPES, reps=10)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -428,6 +456,11 @@ def main():
             "silu_mul_quant 8192x2x8192": {"ms": s_ms, "gbs": s_bytes / (s_ms * 1e-3) / 1e9},
             "hbm_peak_gbs": P["hbm_gbs"]},
         "quant_gbs": q_bytes / (q_ms * 1e-3) / 1e9,
+        # context: the same GEMM shapes as cuBLAS BF16 matmuls (no LoRA, no epilogue
+        # work), and the NVFP4 kernel's speedup over them
+        "bf16_comparator": {k: {"ms": round(v["ms"], 5), "tflops": round(v["tflops"], 1),
+                                "nvfp4_speedup": round(v["ms"] / kern[k]["ms"], 2)}
+                            for k, v in bf16.items()},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(d)

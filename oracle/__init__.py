@@ -266,6 +266,24 @@ def lora_linear_dgrad(dyq: Q, dy, wq_bwd: Q, A, B, alpha: float, dx_prev=None, r
     return dx
 
 
+def lora_adapter_grad(xq: Q, dy, A, B, alpha: float):
+    """Gradients of the LoRA adapters of one LoRA linear, FP64 ("PACT: NVFP4
+    Data-Flow LoRA Fine-Tuning on Consumer GPUs", Table 7 "LoRA branch": BF16 GEMMs
+    on the reconstructed shared input; BF16 gradients).  With s = alpha / r,
+    T = Xhat A and U = dY B^T:
+        dA = s Xhat^T U   [K, r]      dB = s T^T dY   [r, N]
+    Xhat is the exactly dequantised NVFP4 input the forward used; dY is the BF16
+    gradient of the layer output (the values the dgrad's LoRA term also uses)."""
+    xh = dequant(xq)
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    dy64 = np.asarray(dy, np.float64)
+    s = alpha / A.shape[1]
+    dA = s * (xh.T @ (dy64 @ B.T))
+    dB = s * ((xh @ A).T @ dy64)
+    return dA, dB
+
+
 # ---------------------------------------------------------------- RMSNorm
 EPS_DEFAULT = np.float32(1e-5)
 

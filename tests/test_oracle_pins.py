@@ -300,6 +300,52 @@ def test_fwd_dgrad_adjoint():
     assert lhs == pytest.approx(rhs, rel=1e-12)
 
 
+def test_adapter_grad_is_the_derivative_of_the_forward():
+    """The forward is linear in A and in B, so for any directions E_A, E_B
+    <fwd(A + E_A, B) - fwd(A, B), dY> == <dA, E_A> and likewise for B, exactly up to
+    FP64 rounding: the gradients are checked against the forward, not restated."""
+    rng = np.random.default_rng(21)
+    M, K, N, r, alpha = 9, 64, 48, 5, 10.0
+    W = (rng.standard_normal((N, K)) * 0.1).astype(np.float32)
+    wf, _ = orc.pack_weight(W)
+    xq = orc.quantize(rng.standard_normal((M, K)).astype(np.float32))
+    A = rng.standard_normal((K, r))
+    B = rng.standard_normal((r, N))
+    dy = rng.standard_normal((M, N))
+    dA, dB = orc.lora_adapter_grad(xq, dy, A, B, alpha)
+    assert dA.shape == (K, r) and dB.shape == (r, N)
+    loss = lambda A_, B_: float(np.sum(orc.lora_linear_fwd(xq, wf, A_, B_, alpha) * dy))
+    base = loss(A, B)
+    for _ in range(4):
+        EA = rng.standard_normal((K, r))
+        EB = rng.standard_normal((r, N))
+        assert loss(A + EA, B) - base == pytest.approx(float(np.sum(dA * EA)), rel=1e-9, abs=1e-9)
+        assert loss(A, B + EB) - base == pytest.approx(float(np.sum(dB * EB)), rel=1e-9, abs=1e-9)
+
+
+def test_adapter_grad_brute_force_and_zero_cases():
+    rng = np.random.default_rng(22)
+    M, K, N, r, alpha = 3, 16, 16, 2, 4.0
+    xq = orc.quantize(rng.integers(-3, 4, (M, K)).astype(np.float32))
+    xh = orc.dequant(xq)
+    A = rng.integers(-2, 3, (K, r)).astype(np.float64)
+    B = rng.integers(-2, 3, (r, N)).astype(np.float64)
+    dy = rng.integers(-2, 3, (M, N)).astype(np.float64)
+    dA, dB = orc.lora_adapter_grad(xq, dy, A, B, alpha)
+    s = alpha / r
+    for k in range(K):
+        for j in range(r):
+            want = s * sum(xh[m, k] * sum(dy[m, n] * B[j, n] for n in range(N)) for m in range(M))
+            assert dA[k, j] == pytest.approx(want, abs=1e-12)
+    for j in range(r):
+        for n in range(N):
+            want = s * sum(sum(xh[m, k] * A[k, j] for k in range(K)) * dy[m, n] for m in range(M))
+            assert dB[j, n] == pytest.approx(want, abs=1e-12)
+    dA0, _ = orc.lora_adapter_grad(xq, dy, A, np.zeros_like(B), alpha)
+    _, dB0 = orc.lora_adapter_grad(xq, dy, np.zeros_like(A), B, alpha)
+    assert not np.any(dA0) and not np.any(dB0)
+
+
 # ------------------------------------------------------------- SF swizzle
 def test_sf_layout_is_a_bijection_onto_padded_atoms():
     for R, C16 in ((1, 4), (130, 8), (256, 12), (64, 16)):
