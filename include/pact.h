@@ -178,6 +178,31 @@ int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact
                            pact_stream_t stream);
 
 /*
+ * LoRA adapter gradients (Table 7: LoRA branch "BF16 adapter gradients"; Figure 1,
+ * the trainable A, B beside the frozen NVFP4 projection).  With Xhat the dequantised
+ * NVFP4 input that the forward multiplied (the tensor retained for backward):
+ *   dA = scale * Xhat^T (dY B^T)      FP32 [K, r]
+ *   dB = scale * (Xhat A)^T dY        FP32 [r, N]
+ *   xq  NVFP4 [M, K] (the forward's xq);  dy BF16 [M, N] (the output gradient before
+ *       quantisation, as passed to pact_lora_linear_dgrad);  A BF16 [K, r];
+ *   B BF16 [r, N];  1 <= r <= 64;  scale = alpha / r;  N the output width.
+ *   dA, dB are overwritten (not accumulated).
+ * Arithmetic: dY B^T and Xhat A are formed in FP32 and carried as a hi + lo pair of
+ * BF16 values (about 16 significant bits); the products with Xhat (exact in BF16
+ * once the per-tensor scale is factored out) and dY accumulate in FP32 over row
+ * splits whose partial sums are added in a fixed order, so results are
+ * deterministic run to run.
+ * Rules: M >= 1, N and K multiples of 64; dy 16-byte, B 8-byte, dA and dB 4-byte
+ * aligned; xq codes/sf 16-byte aligned.  ws: pact_lora_adapter_grad_workspace_size()
+ * bytes, 256-byte aligned, owned by the caller and free again when the stream
+ * reaches the end of the call.  Errors are reported before any launch.
+ */
+size_t pact_lora_adapter_grad_workspace_size(int64_t M, int64_t N, int64_t K, int r);
+int pact_lora_adapter_grad(const pact_nvfp4* xq, const uint16_t* dy, const uint16_t* A,
+                           const uint16_t* B, int r, float scale, int64_t N, float* dA,
+                           float* dB, void* ws, size_t ws_bytes, pact_stream_t stream);
+
+/*
  * Fused RMSNorm -> NVFP4 (abstract: "reuses quantized RMSNorm outputs"; Table 7
  * "RMSNorm": BF16 input, FP32 normalisation, retains the NVFP4 output and the FP32
  * per-token statistic).  Per row:

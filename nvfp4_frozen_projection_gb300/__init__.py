@@ -20,7 +20,7 @@ __all__ = [
     "NVFP4", "PactError", "load_library", "library_path",
     "pact_quant_nvfp4", "pact_pack_weight_fwd", "pact_pack_weight_bwd",
     "pact_lora_linear_fwd", "pact_lora_linear_fwd_noalloc", "pact_lora_linear_dgrad",
-    "pact_rmsnorm_quant",
+    "pact_lora_adapter_grad", "pact_rmsnorm_quant",
     "pact_silu_mul_quant", "pact_silu_mul_bwd", "pact_rmsnorm_bwd", "pact_test_pexp",
     "pact_test_wait_timeout", "pact_check_status", "pact_device_supported", "pact_launch_count", "pact_profile_next_gemm",
 ]
@@ -62,6 +62,8 @@ _SIGNATURES = {
     "pact_lora_linear_fwd_noalloc": (_int, [_SP, _SP, _vp, _vp, _int, _f32, _vp, _vp, _vp, _vp]),
     "pact_lora_linear_dgrad_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
     "pact_lora_linear_dgrad": (_int, [_SP, _vp, _SP, _vp, _vp, _int, _f32, _int, _vp, _vp, _sz, _vp]),
+    "pact_lora_adapter_grad_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
+    "pact_lora_adapter_grad": (_int, [_SP, _vp, _vp, _vp, _int, _f32, _i64, _vp, _vp, _vp, _sz, _vp]),
     "pact_rmsnorm_quant_workspace_size": (_sz, [_i64, _i64]),
     "pact_rmsnorm_quant": (_int, [_vp, _vp, _i64, _i64, _f32, _SP, _vp, _vp, _sz, _vp]),
     "pact_silu_mul_quant_workspace_size": (_sz, [_i64, _i64]),
@@ -267,6 +269,31 @@ def pact_lora_linear_dgrad(dyq: NVFP4, dy: torch.Tensor, w_bwd: NVFP4, A: torch.
                                       _ptr(B), r, float(scale), int(bool(accumulate)), _ptr(dx),
                                       _ptr(ws), ws.numel(), _stream()))
     return dx
+
+
+def pact_lora_adapter_grad(xq: NVFP4, dy: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                           scale: float, dA: torch.Tensor | None = None,
+                           dB: torch.Tensor | None = None):
+    """dA = scale Xhat^T (dY B^T) FP32 [K, r] and dB = scale (Xhat A)^T dY FP32 [r, N]."""
+    lib = load_library()
+    _need_cuda(dy, torch.bfloat16, "dy")
+    _need_cuda(A, torch.bfloat16, "A")
+    _need_cuda(B, torch.bfloat16, "B")
+    M, K = xq.rows, xq.cols
+    N = dy.shape[1]
+    r = A.shape[1]
+    if dA is None:
+        dA = torch.empty((K, r), dtype=torch.float32, device=dy.device)
+    if dB is None:
+        dB = torch.empty((r, N), dtype=torch.float32, device=dy.device)
+    _need_cuda(dA, torch.float32, "dA")
+    _need_cuda(dB, torch.float32, "dB")
+    ws = _workspace(lib.pact_lora_adapter_grad_workspace_size(M, N, K, r), dy.device)
+    sx = xq.struct()
+    _check(lib.pact_lora_adapter_grad(ctypes.byref(sx), _ptr(dy), _ptr(A), _ptr(B), r,
+                                      float(scale), N, _ptr(dA), _ptr(dB), _ptr(ws), ws.numel(),
+                                      _stream()))
+    return dA, dB
 
 
 def pact_rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-5,

@@ -388,6 +388,50 @@ int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact
                   s);
 }
 
+// ---------------------------------------------------------------- adapter gradients
+size_t pact_lora_adapter_grad_workspace_size(int64_t M, int64_t N, int64_t K, int r) {
+  if (M < 1 || N < 1 || K < 1 || r < 1 || r > 64) return 0;
+  const int rp = rp_for(r);
+  int64_t rps;
+  const int64_t part_n = lora_ts_splits(M, N, &rps) * N, part_k = lora_ts_splits(M, K, &rps) * K;
+  return align256((size_t)rp * K * 2) + align256((size_t)N * rp * 2) +
+         2 * align256((size_t)M * 2 * rp * 2) +
+         align256((size_t)(part_n > part_k ? part_n : part_k) * rp * 4);
+}
+
+int pact_lora_adapter_grad(const pact_nvfp4* xq, const uint16_t* dy, const uint16_t* A,
+                           const uint16_t* B, int r, float scale, int64_t N, float* dA, float* dB,
+                           void* ws, size_t ws_bytes, pact_stream_t stream) {
+  DeviceInfo* d;
+  int rc = device_info(&d);
+  if (rc) return rc;
+  if (!xq) return fail(PACT_ERR_INVALID_ARG, "xq is required");
+  const int64_t M = xq->rows, K = xq->cols;
+  if ((rc = check_gemm_dims(M, N, K, r))) return rc;
+  if ((rc = check_nvfp4(xq, "xq", M, K, 16))) return rc;
+  if (!dy || !A || !B || !dA || !dB)
+    return fail(PACT_ERR_INVALID_ARG, "dy, A, B, dA and dB are required");
+  if (!aligned(dy, 16) || !aligned(B, 8) || !aligned(A, 2) || !aligned(dA, 4) || !aligned(dB, 4))
+    return fail(PACT_ERR_ALIGN, "dy must be 16-byte aligned, B 8-byte aligned");
+  if (!ws || ws_bytes < pact_lora_adapter_grad_workspace_size(M, N, K, r) || !aligned(ws, 256))
+    return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
+  const int rp = rp_for(r);
+  char* p = (char*)ws;
+  uint16_t* at = (uint16_t*)p;
+  p += align256((size_t)rp * K * 2);
+  uint16_t* bt = (uint16_t*)p;
+  p += align256((size_t)N * rp * 2);
+  uint16_t* t = (uint16_t*)p;
+  p += align256((size_t)M * 2 * rp * 2);
+  uint16_t* u = (uint16_t*)p;
+  p += align256((size_t)M * 2 * rp * 2);
+  float* part = (float*)p;
+  cudaError_t e = launch_lora_adapter_grad((const uint8_t*)xq->codes, (const uint8_t*)xq->sf, xq->g,
+                                           M, K, dy, N, A, B, r, rp, scale, dA, dB, at, bt, t, u,
+                                           part, d->sms, (cudaStream_t)stream);
+  return e == cudaSuccess ? PACT_OK : cuda_fail(e, "adapter gradient launch");
+}
+
 // ---------------------------------------------------------------- fused nonlinear ops
 size_t pact_rmsnorm_quant_workspace_size(int64_t, int64_t) { return 256; }
 

@@ -77,6 +77,17 @@ cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const f
                                    int r, int rp, float scale, int64_t K, uint16_t* u_out,
                                    uint16_t* ap_out, cudaStream_t stream);
 
+// LoRA adapter gradients dA [K, r] and dB [r, N] (FP32, overwritten).  Workspace:
+// at_ws [rp, K] and bt_ws [N, rp] (adapter layouts), t_ws and u_ws [M, 2 rp] BF16,
+// part [splits][max(N, K)][rp] FP32 with splits from lora_ts_splits.
+int64_t lora_ts_splits(int64_t M, int64_t C, int64_t* rows_per_split);
+cudaError_t launch_lora_adapter_grad(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
+                                     int64_t M, int64_t K, const uint16_t* dy, int64_t N,
+                                     const uint16_t* A, const uint16_t* B, int r, int rp,
+                                     float scale, float* dA, float* dB, uint16_t* at_ws,
+                                     uint16_t* bt_ws, uint16_t* t_ws, uint16_t* u_ws, float* part,
+                                     int num_sms, cudaStream_t stream);
+
 cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M,
                                  int64_t H, float eps, uint8_t* codes, uint8_t* sf, float* g,
                                  float* rstd, unsigned* ws_amax, int num_sms,

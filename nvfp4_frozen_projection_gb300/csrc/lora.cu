@@ -27,8 +27,11 @@
 // CTA owns 16 rows; its 8 warps split K in 64-wide chunks and reduce through
 // shared memory.  Inside a chunk, lane (g, c) holds block c (16 elements) of rows
 // g and g+8; the MMA's k index is permuted accordingly on both operands.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace pact {
 
@@ -157,7 +160,8 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_fwd(const uint8_t* __restr
                                                        const float* __restrict__ gx,
                                                        const float* __restrict__ gw, int64_t M,
                                                        int64_t K, const uint16_t* __restrict__ At,
-                                                       float scale, uint16_t* __restrict__ t_out) {
+                                                       float scale, int plain,
+                                                       uint16_t* __restrict__ t_out) {
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * G * RP];
   __shared__ uint32_t dec[256];
@@ -246,8 +250,9 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_fwd(const uint8_t* __restr
     }
     x0 = x1;
   }
-  const float ga = *gx, gb = *gw;
-  const bool normal = __fmul_rn(ga, gb) > 0.0f;
+  // plain: f = scale * g_x, i.e. v = scale * (Xhat A) for the adapter gradients
+  const float ga = *gx, gb = plain ? 0.0f : *gw;
+  const bool normal = !plain && __fmul_rn(ga, gb) > 0.0f;
   const float f = normal ? __fdiv_rn(scale, gb) : __fmul_rn(scale, ga);
   reduce_and_store<RP, G>(acc, red, m0, M, f, t_out);
 }
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dgrad(const uint16_t* __re
                                                          const float* __restrict__ gw,
                                                          int64_t M, int64_t N,
                                                          const uint16_t* __restrict__ B, int r,
-                                                         float scale,
+                                                         float scale, int plain,
                                                          uint16_t* __restrict__ u_out) {
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * G * RP];
@@ -319,8 +324,8 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dgrad(const uint16_t* __re
         x1[gi][h] = x2[gi][h];
       }
   }
-  const float ga = *gdy, gb = *gw;
-  const float s_main = __fmul_rn(ga, gb);
+  // plain: f = scale, i.e. v = scale * (dY B^T) for the adapter gradients
+  const float s_main = plain ? 0.0f : __fmul_rn(*gdy, *gw);
   const float f = s_main > 0.0f ? __fdiv_rn(scale, s_main) : scale;
   reduce_and_store<RP, G>(acc, red, m0, M, f, u_out);
 }
@@ -336,7 +341,7 @@ static cudaError_t fwd_rp(const uint8_t* xc, const uint8_t* xsf, const float* gx
                                                                     bt_out);
   note_launch();
   k_lora_down_fwd<RP, G><<<(int)((M + 16 * G - 1) / (16 * G)), 256, 0, stream>>>(
-      xc, xsf, gx, gw, M, K, at_ws, scale, t_out);
+      xc, xsf, gx, gw, M, K, at_ws, scale, 0, t_out);
   return cudaGetLastError();
 }
 
@@ -349,7 +354,7 @@ static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* g
   k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
   note_launch();
   k_lora_down_dgrad<RP, G><<<(int)((M + 16 * G - 1) / (16 * G)), 256, 0, stream>>>(
-      dy, gdy, gw, M, N, B, r, scale, u_out);
+      dy, gdy, gw, M, N, B, r, scale, 0, u_out);
   return cudaGetLastError();
 }
 
@@ -374,6 +379,215 @@ cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const f
   if (rp == 16) return dgrad_rp<16>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, stream);
   if (rp == 32) return dgrad_rp<32>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, stream);
   return dgrad_rp<64>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, stream);
+}
+
+// ============================================================== adapter gradients
+// dA = (alpha/r) Xhat^T (dY B^T) [K, r] and dB = (alpha/r) (Xhat A)^T dY [r, N]:
+// the down-projection kernels above produce T' = (alpha/r) Xhat A and
+// U' = (alpha/r) dY B^T as hi|lo BF16 pairs ("plain" mode), and one tall-skinny
+// kernel forms OUT[c, j] = sum_m L[m, c] R[m, j] for L = dY, R = T' (dB) and for
+// L = Xhat without its per-tensor scale, R = U' (dA, times g_x afterwards).
+
+// Four 8x8 BF16 matrices from shared memory, each transposed: lanes 8i .. 8i + 7
+// give the row addresses of matrix i.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// OUT partials for 128 columns of L and one split of its rows.  8 warps own 16
+// columns each.  Per round of 32 rows the CTA stages L [32, 128] (BF16; NVFP4 is
+// decoded exactly to BF16 on the way) and R [32, 2 RP] in shared memory, rows
+// padded by 16 bytes so that the 8 rows of an 8x8 matrix load fall in 8 bank
+// groups.  Transposing matrix loads give the m16n8k16 operands: L^T (16 columns x
+// 16 rows) as A and R (16 rows x 8 of its columns, the hi half then the lo half)
+// as B.  The split's sums go to part[split][C][RP] in FP32.
+template <int RP, bool FP4>
+__global__ void __launch_bounds__(256) k_lora_ts(const uint16_t* __restrict__ Lb,
+                                                 const uint8_t* __restrict__ Lc,
+                                                 const uint8_t* __restrict__ Lsf, int64_t M,
+                                                 int64_t C, const uint16_t* __restrict__ R,
+                                                 int64_t rows_per_split,
+                                                 float* __restrict__ part) {
+  constexpr int NT = RP / 8;
+  constexpr int LST = 128 * 2 + 16;     // L tile row stride, bytes
+  constexpr int RST = 2 * RP * 2 + 16;  // R tile row stride, bytes
+  constexpr int PPR = 4 * RP / 16;      // 16-byte pieces per R row
+  __shared__ __align__(16) uint8_t Ls[32 * LST];
+  __shared__ __align__(16) uint8_t Rs[32 * RST];
+  __shared__ uint32_t dec[256];
+  if (FP4) {
+    const float2 f = e2m1x2_to_f32x2(threadIdx.x);
+    dec[threadIdx.x] = pack_bf16x2(f.x, f.y);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t c_base = (int64_t)blockIdx.x * 128;
+  const int64_t m_begin = (int64_t)blockIdx.y * rows_per_split;
+  const int64_t m_end = min(M, m_begin + rows_per_split);
+  const int64_t c16p = pad_to(C >> 4, 4);
+  float acc[NT][4];
+#pragma unroll
+  for (int jn = 0; jn < NT; ++jn) acc[jn][0] = acc[jn][1] = acc[jn][2] = acc[jn][3] = 0.0f;
+  // this thread's piece of the L tile: row t / 8, 16 columns at (t % 8) * 16
+  const int lrow = threadIdx.x >> 3, lcol = (threadIdx.x & 7) * 16;
+  for (int64_t m0 = m_begin; m0 < m_end; m0 += 32) {
+    __syncthreads();  // the previous round's operands have been read
+    {
+      const int64_t m = m0 + lrow, c = c_base + lcol;
+      uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+      if (m < m_end && c < C) {
+        if constexpr (FP4) {
+          const uint2 q = *reinterpret_cast<const uint2*>(Lc + m * (C >> 1) + (c >> 1));
+          const __nv_bfloat162 s2 = __float2bfloat162_rn(e4m3_to_f32(Lsf[sf_offset(m, c >> 4, c16p)]));
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t byte = ((i < 4 ? q.x : q.y) >> (8 * (i & 3))) & 0xFFu;
+            __nv_bfloat162 t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[byte]), s2);
+            w[i] = *reinterpret_cast<uint32_t*>(&t);
+          }
+          v0 = make_uint4(w[0], w[1], w[2], w[3]);
+          v1 = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+          const uint4* src = reinterpret_cast<const uint4*>(Lb + m * C + c);
+          v0 = ldg_stream(src);
+          v1 = ldg_stream(src + 1);
+        }
+      }
+      uint4* dst = reinterpret_cast<uint4*>(Ls + lrow * LST + lcol * 2);
+      dst[0] = v0;
+      dst[1] = v1;
+    }
+    for (int t = threadIdx.x; t < 32 * PPR; t += 256) {
+      const int row = t / PPR, pc = t - row * PPR;
+      const int64_t m = m0 + row;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (m < m_end) v = *reinterpret_cast<const uint4*>(R + m * (2 * RP) + pc * 8);
+      *reinterpret_cast<uint4*>(Rs + row * RST + pc * 16) = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      uint32_t a[4];
+      {
+        // matrices: (rows 0-7, cols 0-7), (rows 0-7, cols 8-15), (rows 8-15, cols
+        // 0-7), (rows 8-15, cols 8-15) of this k-step and the warp's 16 columns
+        const int row = ks * 16 + ((lane >> 4) & 1) * 8 + (lane & 7);
+        const int col = warp * 16 + ((lane >> 3) & 1) * 8;
+        ldmatrix_x4_trans(a, smem_addr(Ls + row * LST + col * 2));
+      }
+#pragma unroll
+      for (int jn = 0; jn < NT; ++jn) {
+        // matrices: rows 0-7 and 8-15 of R columns 8 jn .. (hi), then the same of
+        // the lo half (columns RP + 8 jn ..)
+        uint32_t b[4];
+        const int row = ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int col = jn * 8 + ((lane >> 4) & 1) * RP;
+        ldmatrix_x4_trans(b, smem_addr(Rs + row * RST + col * 2));
+        mma_bf16_16816(acc[jn], a, b);
+        mma_bf16_16816(acc[jn], a, b + 2);
+      }
+    }
+  }
+  // acc[jn]: (column g, j = 8 jn + 2 (lane % 4) + {0, 1}) and (column g + 8, same j)
+  const int g = lane >> 2, cq = lane & 3;
+  float* out = part + (int64_t)blockIdx.y * C * RP;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int64_t c = c_base + warp * 16 + g + 8 * h;
+    if (c < C) {
+#pragma unroll
+      for (int jn = 0; jn < NT; ++jn)
+        *reinterpret_cast<float2*>(out + c * RP + jn * 8 + 2 * cq) =
+            make_float2(acc[jn][2 * h], acc[jn][2 * h + 1]);
+    }
+  }
+}
+
+// out = factor * sum over the splits (in split order) of part; layout 0 writes
+// out[c * r + j] ([C, r], dA), layout 1 out[j * C + c] ([r, C], dB).
+__global__ void __launch_bounds__(256) k_lora_ts_reduce(const float* __restrict__ part,
+                                                        int nsplit, int64_t C, int RP, int r,
+                                                        const float* __restrict__ factor,
+                                                        int layout, float* __restrict__ out) {
+  const float f = factor ? *factor : 1.0f;
+  const int64_t total = C * r;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    int64_t c, j;
+    if (layout == 0) {
+      c = e / r;
+      j = e - c * r;
+    } else {
+      j = e / C;
+      c = e - j * C;
+    }
+    float s = 0.0f;
+    for (int sp = 0; sp < nsplit; ++sp) s += part[((int64_t)sp * C + c) * RP + j];
+    out[e] = __fmul_rn(s, f);
+  }
+}
+
+// Row splits of the tall-skinny product: enough CTAs for two per SM of a 152-SM
+// GPU, at most 64 splits, each a multiple of 32 rows.
+int64_t lora_ts_splits(int64_t M, int64_t C, int64_t* rows_per_split) {
+  const int64_t ctiles = (C + 127) / 128;
+  int64_t ns = (304 + ctiles - 1) / ctiles;
+  ns = ns < 1 ? 1 : (ns > 64 ? 64 : ns);
+  int64_t rps = ((M + ns - 1) / ns + 31) / 32 * 32;
+  if (rps < 32) rps = 32;
+  *rows_per_split = rps;
+  return (M + rps - 1) / rps;
+}
+
+template <int RP>
+static cudaError_t adapter_grad_rp(const uint8_t* xc, const uint8_t* xsf, const float* gx,
+                                   int64_t M, int64_t K, const uint16_t* dy, int64_t N,
+                                   const uint16_t* A, const uint16_t* B, int r, float scale,
+                                   float* dA, float* dB, uint16_t* at_ws, uint16_t* bt_ws,
+                                   uint16_t* t_ws, uint16_t* u_ws, float* part, int num_sms,
+                                   cudaStream_t stream) {
+  constexpr int G = RP <= 32 ? 2 : 1;
+  const int mb = (int)((M + 16 * G - 1) / (16 * G));
+  note_launch();
+  k_lora_prep<RP><<<(int)((N + K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 1, at_ws, bt_ws);
+  note_launch();
+  k_lora_down_fwd<RP, G><<<mb, 256, 0, stream>>>(xc, xsf, gx, gx, M, K, at_ws, scale, 1, t_ws);
+  note_launch();
+  k_lora_down_dgrad<RP, G><<<mb, 256, 0, stream>>>(dy, gx, gx, M, N, B, r, scale, 1, u_ws);
+  int64_t rps;
+  int64_t ns = lora_ts_splits(M, N, &rps);
+  note_launch();
+  k_lora_ts<RP, false><<<dim3((unsigned)((N + 127) / 128), (unsigned)ns), 256, 0, stream>>>(
+      dy, nullptr, nullptr, M, N, t_ws, rps, part);
+  note_launch();
+  k_lora_ts_reduce<<<std::min<int64_t>((N * r + 255) / 256, num_sms * 8), 256, 0, stream>>>(
+      part, (int)ns, N, RP, r, nullptr, 1, dB);
+  ns = lora_ts_splits(M, K, &rps);
+  note_launch();
+  k_lora_ts<RP, true><<<dim3((unsigned)((K + 127) / 128), (unsigned)ns), 256, 0, stream>>>(
+      nullptr, xc, xsf, M, K, u_ws, rps, part);
+  note_launch();
+  k_lora_ts_reduce<<<std::min<int64_t>((K * r + 255) / 256, num_sms * 8), 256, 0, stream>>>(
+      part, (int)ns, K, RP, r, gx, 0, dA);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lora_adapter_grad(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
+                                     int64_t M, int64_t K, const uint16_t* dy, int64_t N,
+                                     const uint16_t* A, const uint16_t* B, int r, int rp,
+                                     float scale, float* dA, float* dB, uint16_t* at_ws,
+                                     uint16_t* bt_ws, uint16_t* t_ws, uint16_t* u_ws, float* part,
+                                     int num_sms, cudaStream_t stream) {
+  if (rp == 16)
+    return adapter_grad_rp<16>(x_codes, x_sf, gx, M, K, dy, N, A, B, r, scale, dA, dB, at_ws,
+                               bt_ws, t_ws, u_ws, part, num_sms, stream);
+  if (rp == 32)
+    return adapter_grad_rp<32>(x_codes, x_sf, gx, M, K, dy, N, A, B, r, scale, dA, dB, at_ws,
+                               bt_ws, t_ws, u_ws, part, num_sms, stream);
+  return adapter_grad_rp<64>(x_codes, x_sf, gx, M, K, dy, N, A, B, r, scale, dA, dB, at_ws,
+                             bt_ws, t_ws, u_ws, part, num_sms, stream);
 }
 
 }  // namespace pact

@@ -27,7 +27,7 @@ def lib():
 def test_header_declares_the_hot_path():
     names = set(_declared())
     for n in ("pact_quant_nvfp4", "pact_pack_weight_fwd", "pact_pack_weight_bwd",
-              "pact_lora_linear_fwd", "pact_lora_linear_dgrad", "pact_rmsnorm_quant",
+              "pact_lora_linear_fwd", "pact_lora_linear_dgrad", "pact_lora_adapter_grad", "pact_rmsnorm_quant",
               "pact_silu_mul_quant", "pact_silu_mul_bwd", "pact_rmsnorm_bwd",
               "pact_check_status"):
         assert n in names
