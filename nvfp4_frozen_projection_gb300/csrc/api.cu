@@ -393,7 +393,8 @@ size_t pact_lora_adapter_grad_workspace_size(int64_t M, int64_t N, int64_t K, in
   if (M < 1 || N < 1 || K < 1 || r < 1 || r > 64) return 0;
   const int rp = rp_for(r);
   int64_t rps;
-  const int64_t part_n = lora_ts_splits(M, N, &rps) * N, part_k = lora_ts_splits(M, K, &rps) * K;
+  const int64_t part_n = lora_ts_splits(M, N, rp, false, &rps) * N;
+  const int64_t part_k = lora_ts_splits(M, K, rp, true, &rps) * K;
   return align256((size_t)rp * K * 2) + align256((size_t)N * rp * 2) +
          2 * align256((size_t)M * 2 * rp * 2) +
          align256((size_t)(part_n > part_k ? part_n : part_k) * rp * 4);

@@ -206,6 +206,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// An E4M3 byte -> FP16 (exact: E4M3 values are FP16 normals), in both halves.
+__device__ __forceinline__ __half2 e4m3_dup_h2(uint32_t b) {
+  uint32_t h2;
+  const uint16_t in = (uint16_t)((b & 0xFFu) * 0x0101u);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return *reinterpret_cast<__half2*>(&h2);
+}
+
+// Two E2M1 codes (the low byte of `byte`, first element in the low nibble) times
+// a block scale -> BF16x2, exactly: the codes convert exactly to FP16, the product
+// of an E2M1 value and an E4M3 scale has at most 6 significant bits and lies in
+// [2^-10, 2688] (or is zero), so the FP16 multiply, the widening to FP32 and the
+// narrowing to BF16 are all exact.  Register-only (no lookup table).
+__device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, __half2 s) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h2)
+      : "r"(byte));
+  const float2 f = __half22float2(__hmul2(*reinterpret_cast<__half2*>(&h2), s));
+  return pack_bf16x2(f.x, f.y);
+}
+
 // max |bf16| over 8 packed values, as FP32 bits (non-negative, so unsigned order).
 __device__ __forceinline__ uint32_t absmax_bf16x8_bits(const uint4& v) {
   uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),

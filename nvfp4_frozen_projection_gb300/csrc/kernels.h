@@ -79,8 +79,9 @@ cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const f
 
 // LoRA adapter gradients dA [K, r] and dB [r, N] (FP32, overwritten).  Workspace:
 // at_ws [rp, K] and bt_ws [N, rp] (adapter layouts), t_ws and u_ws [M, 2 rp] BF16,
-// part [splits][max(N, K)][rp] FP32 with splits from lora_ts_splits.
-int64_t lora_ts_splits(int64_t M, int64_t C, int64_t* rows_per_split);
+// part [splits][max(N, K) rp] FP32 with splits = max over the two products of
+// lora_ts_splits(M, N, rp, false) and lora_ts_splits(M, K, rp, true).
+int64_t lora_ts_splits(int64_t M, int64_t C, int rp, bool fp4, int64_t* rows_per_split);
 cudaError_t launch_lora_adapter_grad(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
                                      int64_t M, int64_t K, const uint16_t* dy, int64_t N,
                                      const uint16_t* A, const uint16_t* B, int r, int rp,

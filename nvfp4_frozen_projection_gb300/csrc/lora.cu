@@ -43,18 +43,6 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, cons
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Two E2M1 codes (one byte) times an E4M3 scale -> BF16x2, exact.
-__device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, __half2 sc) {
-  uint32_t h2;
-  uint16_t in = (uint16_t)(byte & 0xFFu);
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(h2)
-      : "h"(in));
-  __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h2), sc);
-  float2 f = __half22float2(v);
-  return pack_bf16x2(f.x, f.y);
-}
-
 // Sums the 8 warps' partial products (fixed order) and stores f * T as a BF16
 // pair per element: out[m, j] = hi = bf16(v), out[m, RP + j] = lo = bf16(v - hi),
 // so that the fused GEMM's BF16 LoRA product sees v to about 16 significant bits.
@@ -152,8 +140,8 @@ __global__ void __launch_bounds__(256) k_lora_prep(const uint16_t* __restrict__ 
 
 // T' = f * (X~ A): x_codes [M, K/2], x_sf (128x4 atoms), At [RP, K].  A chunk is
 // 128 codes of a row: lane c holds blocks 2c and 2c + 1 (32 codes, 16 bytes).  E2M1
-// pairs are decoded through a 256-entry byte -> BF16x2 table in shared memory and
-// scaled by their block's E4M3 scale with one exact BF16x2 multiply.
+// pairs are converted in registers and scaled by their block's E4M3 scale exactly
+// (e2m1x2_scaled_bf16x2).
 template <int RP, int G>
 __global__ void __launch_bounds__(256, 2) k_lora_down_fwd(const uint8_t* __restrict__ xc,
                                                        const uint8_t* __restrict__ xsf,
@@ -164,12 +152,6 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_fwd(const uint8_t* __restr
                                                        uint16_t* __restrict__ t_out) {
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * G * RP];
-  __shared__ uint32_t dec[256];
-  {
-    const float2 f = e2m1x2_to_f32x2(threadIdx.x);
-    dec[threadIdx.x] = pack_bf16x2(f.x, f.y);
-  }
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int64_t m0 = (int64_t)blockIdx.x * (16 * G);
@@ -209,13 +191,13 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_fwd(const uint8_t* __restr
   for (int ch = warp; ch < nch; ch += 8) {
     if (ch + 8 < nch) load(ch + 8, x1);
     const bool live = !(half_tail && ch == nch - 1 && c >= 2);
-    __nv_bfloat162 scl[G][2][2];
+    __half2 scl[G][2][2];
 #pragma unroll
     for (int gi = 0; gi < G; ++gi)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        scl[gi][h][0] = __float2bfloat162_rn(e4m3_to_f32(x0.sc[gi][h] & 0xFFu));
-        scl[gi][h][1] = __float2bfloat162_rn(e4m3_to_f32(x0.sc[gi][h] >> 8));
+        scl[gi][h][0] = e4m3_dup_h2(x0.sc[gi][h] & 0xFFu);
+        scl[gi][h][1] = e4m3_dup_h2(x0.sc[gi][h] >> 8);
       }
     const int64_t kb = (int64_t)ch * 128 + 32 * c;
 #pragma unroll
@@ -237,12 +219,8 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_fwd(const uint8_t* __restr
           const uint32_t word = (s < 4 ? (s < 2 ? x0.q[gi][h].x : x0.q[gi][h].y)
                                        : (s < 6 ? x0.q[gi][h].z : x0.q[gi][h].w)) >>
                                 (16 * (s & 1));
-          __nv_bfloat162 t;
-          t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[word & 0xFFu]), scl[gi][h][s >> 2]);
-          a[h] = *reinterpret_cast<uint32_t*>(&t);  // elements 4s, 4s+1
-          t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[(word >> 8) & 0xFFu]),
-                      scl[gi][h][s >> 2]);
-          a[2 + h] = *reinterpret_cast<uint32_t*>(&t);  // elements 4s+2, 4s+3
+          a[h] = e2m1x2_scaled_bf16x2(word, scl[gi][h][s >> 2]);            // elements 4s, 4s+1
+          a[2 + h] = e2m1x2_scaled_bf16x2(word >> 8, scl[gi][h][s >> 2]);   // elements 4s+2, 4s+3
         }
 #pragma unroll
         for (int jn = 0; jn < NT; ++jn) mma_bf16_16816(acc[gi][jn], a, bfr[jn]);
@@ -396,86 +374,152 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, uint32_t addr) {
                : "r"(addr));
 }
 
-// OUT partials for 128 columns of L and one split of its rows.  8 warps own 16
-// columns each.  Per round of 32 rows the CTA stages L [32, 128] (BF16; NVFP4 is
-// decoded exactly to BF16 on the way) and R [32, 2 RP] in shared memory, rows
-// padded by 16 bytes so that the 8 rows of an 8x8 matrix load fall in 8 bank
-// groups.  Transposing matrix loads give the m16n8k16 operands: L^T (16 columns x
-// 16 rows) as A and R (16 rows x 8 of its columns, the hi half then the lo half)
-// as B.  The split's sums go to part[split][C][RP] in FP32.
+// cp.async copies into shared memory; src_bytes = 0 writes zeros instead of reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Shared-memory plan of the tall-skinny kernel.  A stage holds ROWS rows of L (the
+// 128 columns of the CTA: BF16, or NVFP4 codes plus their 8 block scales) and of R
+// (2 RP BF16 columns).  Rows are padded by 16 bytes so that the 8 row addresses of
+// a matrix load fall in distinct bank groups.  NVFP4 stages are decoded into one
+// BF16 tile before the MMAs read them.
 template <int RP, bool FP4>
-__global__ void __launch_bounds__(256) k_lora_ts(const uint16_t* __restrict__ Lb,
-                                                 const uint8_t* __restrict__ Lc,
-                                                 const uint8_t* __restrict__ Lsf, int64_t M,
-                                                 int64_t C, const uint16_t* __restrict__ R,
-                                                 int64_t rows_per_split,
-                                                 float* __restrict__ part) {
+struct TsPlan {
+  static constexpr int ROWS = FP4 ? 64 : 32;
+  static constexpr int LST = FP4 ? 64 + 16 : 256 + 16;  // staged L row, bytes
+  static constexpr int DST = 256 + 16;                   // decoded BF16 row (NVFP4)
+  static constexpr int SFB = FP4 ? 8 : 0;                // block scales per row
+  static constexpr int RST = 4 * RP + 16;                // staged R row, bytes
+  static constexpr int S_OFF = ROWS * LST;
+  static constexpr int R_OFF = S_OFF + ROWS * SFB;
+  static constexpr int STAGE = R_OFF + ROWS * RST;
+  static constexpr int STAGES = FP4 ? (RP == 64 ? 4 : 6) : 4;
+  static constexpr int DEC_OFF = STAGE * STAGES;
+  static constexpr int SMEM = DEC_OFF + (FP4 ? ROWS * DST : 0);
+};
+
+// OUT partials for 128 columns of L and one split of its rows: OUT[c, j] = sum over
+// the split's rows m of L[m, c] R[m, j].  8 warps own 16 columns each.  Every
+// thread copies its share of each stage with cp.async (STAGES - 1 stages in flight
+// ahead of the one being multiplied; rows past the split read as zeros).
+// Transposing matrix loads give the m16n8k16 operands: L^T (16 columns x 16 rows)
+// as A and R (16 rows x 8 of its columns, the hi half then the lo half) as B.  The
+// split's FP32 sums go to part[split][C][RP] (tr = 0) or part[split][RP][C] (tr = 1),
+// the layout whose reduction reads contiguous memory for the final output order.
+template <int RP, bool FP4>
+__global__ void __launch_bounds__(256, 2) k_lora_ts(const uint16_t* __restrict__ Lb,
+                                                    const uint8_t* __restrict__ Lc,
+                                                    const uint8_t* __restrict__ Lsf, int64_t M,
+                                                    int64_t C, const uint16_t* __restrict__ R,
+                                                    int64_t rows_per_split, int tr,
+                                                    float* __restrict__ part) {
+  using P = TsPlan<RP, FP4>;
   constexpr int NT = RP / 8;
-  constexpr int LST = 128 * 2 + 16;     // L tile row stride, bytes
-  constexpr int RST = 2 * RP * 2 + 16;  // R tile row stride, bytes
-  constexpr int PPR = 4 * RP / 16;      // 16-byte pieces per R row
-  __shared__ __align__(16) uint8_t Ls[32 * LST];
-  __shared__ __align__(16) uint8_t Rs[32 * RST];
-  __shared__ uint32_t dec[256];
-  if (FP4) {
-    const float2 f = e2m1x2_to_f32x2(threadIdx.x);
-    dec[threadIdx.x] = pack_bf16x2(f.x, f.y);
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int PPR = RP / 4;  // 16-byte pieces per R row
+  extern __shared__ __align__(128) uint8_t sm[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t c_base = (int64_t)blockIdx.x * 128;
   const int64_t m_begin = (int64_t)blockIdx.y * rows_per_split;
   const int64_t m_end = min(M, m_begin + rows_per_split);
+  const int nr = (int)((m_end - m_begin + P::ROWS - 1) / P::ROWS);
   const int64_t c16p = pad_to(C >> 4, 4);
+  const uint32_t sbase = smem_addr(sm);
+
+  auto issue = [&](int i) {
+    const uint32_t st = sbase + (uint32_t)((i % P::STAGES) * P::STAGE);
+    const int64_t m0 = m_begin + (int64_t)i * P::ROWS;
+    if constexpr (FP4) {
+      {  // codes: row tid / 4, 16 bytes (32 columns) at piece tid % 4
+        const int row = tid >> 2, pc = tid & 3;
+        const int64_t m = m0 + row, c = c_base + pc * 32;
+        const bool ok = m < m_end && c < C;
+        cp_async16(st + row * P::LST + pc * 16, ok ? Lc + m * (C >> 1) + (c >> 1) : Lc, ok ? 16 : 0);
+      }
+      if (tid < 2 * P::ROWS) {  // scales: row tid / 2, blocks 4h .. 4h + 3 of the tile
+        const int row = tid >> 1, h = tid & 1;
+        const int64_t m = m0 + row;
+        const bool ok = m < m_end && c_base + 64 * h < C;
+        cp_async4(st + P::S_OFF + row * 8 + 4 * h,
+                  ok ? Lsf + sf_offset(m, (c_base >> 4) + 4 * h, c16p) : Lsf, ok ? 4 : 0);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < P::ROWS * 16 / 256; ++k) {  // row p / 16, 8 columns at p % 16
+        const int p = tid + 256 * k, row = p >> 4, pc = p & 15;
+        const int64_t m = m0 + row, c = c_base + pc * 8;
+        const bool ok = m < m_end && c < C;
+        cp_async16(st + row * P::LST + pc * 16, ok ? Lb + m * C + c : Lb, ok ? 16 : 0);
+      }
+    }
+    for (int p = tid; p < P::ROWS * PPR; p += 256) {
+      const int row = p / PPR, pc = p - row * PPR;
+      const int64_t m = m0 + row;
+      const bool ok = m < m_end;
+      cp_async16(st + P::R_OFF + row * P::RST + pc * 16, ok ? R + m * (2 * RP) + pc * 8 : R,
+                 ok ? 16 : 0);
+    }
+  };
+
   float acc[NT][4];
 #pragma unroll
   for (int jn = 0; jn < NT; ++jn) acc[jn][0] = acc[jn][1] = acc[jn][2] = acc[jn][3] = 0.0f;
-  // this thread's piece of the L tile: row t / 8, 16 columns at (t % 8) * 16
-  const int lrow = threadIdx.x >> 3, lcol = (threadIdx.x & 7) * 16;
-  for (int64_t m0 = m_begin; m0 < m_end; m0 += 32) {
-    __syncthreads();  // the previous round's operands have been read
-    {
-      const int64_t m = m0 + lrow, c = c_base + lcol;
-      uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-      if (m < m_end && c < C) {
-        if constexpr (FP4) {
-          const uint2 q = *reinterpret_cast<const uint2*>(Lc + m * (C >> 1) + (c >> 1));
-          const __nv_bfloat162 s2 = __float2bfloat162_rn(e4m3_to_f32(Lsf[sf_offset(m, c >> 4, c16p)]));
-          uint32_t w[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t byte = ((i < 4 ? q.x : q.y) >> (8 * (i & 3))) & 0xFFu;
-            __nv_bfloat162 t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dec[byte]), s2);
-            w[i] = *reinterpret_cast<uint32_t*>(&t);
-          }
-          v0 = make_uint4(w[0], w[1], w[2], w[3]);
-          v1 = make_uint4(w[4], w[5], w[6], w[7]);
-        } else {
-          const uint4* src = reinterpret_cast<const uint4*>(Lb + m * C + c);
-          v0 = ldg_stream(src);
-          v1 = ldg_stream(src + 1);
-        }
-      }
-      uint4* dst = reinterpret_cast<uint4*>(Ls + lrow * LST + lcol * 2);
-      dst[0] = v0;
-      dst[1] = v1;
-    }
-    for (int t = threadIdx.x; t < 32 * PPR; t += 256) {
-      const int row = t / PPR, pc = t - row * PPR;
-      const int64_t m = m0 + row;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (m < m_end) v = *reinterpret_cast<const uint4*>(R + m * (2 * RP) + pc * 8);
-      *reinterpret_cast<uint4*>(Rs + row * RST + pc * 16) = v;
-    }
+  for (int s = 0; s < P::STAGES - 1; ++s) {
+    if (s < nr) issue(s);
+    cp_async_commit();
+  }
+  for (int i = 0; i < nr; ++i) {
+    cp_async_wait<P::STAGES - 2>();
+    // stage i has landed for every thread; every thread is done with stage i - 1
+    // (and with the decoded tile), so both can be refilled
     __syncthreads();
+    if (i + P::STAGES - 1 < nr) issue(i + P::STAGES - 1);
+    cp_async_commit();
+    const uint8_t* st = sm + (i % P::STAGES) * P::STAGE;
+    const uint8_t* Ls = st;
+    if constexpr (FP4) {
+      // decode: row tid / 4, the 32 columns of piece tid % 4 (blocks 2 pc, 2 pc + 1),
+      // exactly: E2M1 x E4M3 products fit in BF16
+      const int row = tid >> 2, pc = tid & 3;
+      const uint4 q = *reinterpret_cast<const uint4*>(st + row * P::LST + pc * 16);
+      const uint32_t sw = *reinterpret_cast<const uint16_t*>(st + P::S_OFF + row * 8 + 2 * pc);
+      const __half2 s0 = e4m3_dup_h2(sw & 0xFFu), s1 = e4m3_dup_h2(sw >> 8);
+      uint32_t w[16];
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
+      for (int b = 0; b < 16; ++b) {
+        const uint32_t word = b < 4 ? q.x : (b < 8 ? q.y : (b < 12 ? q.z : q.w));
+        w[b] = e2m1x2_scaled_bf16x2(word >> (8 * (b & 3)), b < 8 ? s0 : s1);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(sm + P::DEC_OFF + row * P::DST + pc * 64);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+      dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+      __syncthreads();
+      Ls = sm + P::DEC_OFF;
+    }
+    constexpr int LS = FP4 ? P::DST : P::LST;
+    const uint8_t* Rs = st + P::R_OFF;
+#pragma unroll
+    for (int ks = 0; ks < P::ROWS / 16; ++ks) {
       uint32_t a[4];
       {
         // matrices: (rows 0-7, cols 0-7), (rows 0-7, cols 8-15), (rows 8-15, cols
         // 0-7), (rows 8-15, cols 8-15) of this k-step and the warp's 16 columns
         const int row = ks * 16 + ((lane >> 4) & 1) * 8 + (lane & 7);
         const int col = warp * 16 + ((lane >> 3) & 1) * 8;
-        ldmatrix_x4_trans(a, smem_addr(Ls + row * LST + col * 2));
+        ldmatrix_x4_trans(a, smem_addr(Ls + row * LS + col * 2));
       }
 #pragma unroll
       for (int jn = 0; jn < NT; ++jn) {
@@ -484,12 +528,13 @@ __global__ void __launch_bounds__(256) k_lora_ts(const uint16_t* __restrict__ Lb
         uint32_t b[4];
         const int row = ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
         const int col = jn * 8 + ((lane >> 4) & 1) * RP;
-        ldmatrix_x4_trans(b, smem_addr(Rs + row * RST + col * 2));
+        ldmatrix_x4_trans(b, smem_addr(Rs + row * P::RST + col * 2));
         mma_bf16_16816(acc[jn], a, b);
         mma_bf16_16816(acc[jn], a, b + 2);
       }
     }
   }
+  cp_async_wait<0>();  // only empty groups can remain; keep the invariant explicit
   // acc[jn]: (column g, j = 8 jn + 2 (lane % 4) + {0, 1}) and (column g + 8, same j)
   const int g = lane >> 2, cq = lane & 3;
   float* out = part + (int64_t)blockIdx.y * C * RP;
@@ -498,15 +543,22 @@ __global__ void __launch_bounds__(256) k_lora_ts(const uint16_t* __restrict__ Lb
     const int64_t c = c_base + warp * 16 + g + 8 * h;
     if (c < C) {
 #pragma unroll
-      for (int jn = 0; jn < NT; ++jn)
-        *reinterpret_cast<float2*>(out + c * RP + jn * 8 + 2 * cq) =
-            make_float2(acc[jn][2 * h], acc[jn][2 * h + 1]);
+      for (int jn = 0; jn < NT; ++jn) {
+        const int j = jn * 8 + 2 * cq;
+        if (tr) {
+          out[(int64_t)j * C + c] = acc[jn][2 * h];
+          out[(int64_t)(j + 1) * C + c] = acc[jn][2 * h + 1];
+        } else {
+          *reinterpret_cast<float2*>(out + c * RP + j) = make_float2(acc[jn][2 * h], acc[jn][2 * h + 1]);
+        }
+      }
     }
   }
 }
 
-// out = factor * sum over the splits (in split order) of part; layout 0 writes
-// out[c * r + j] ([C, r], dA), layout 1 out[j * C + c] ([r, C], dB).
+// out = factor * sum over the splits (in split order) of part; layout 0 reads
+// part[split][C][RP] and writes out[c * r + j] ([C, r], dA), layout 1 reads
+// part[split][RP][C] and writes out[j * C + c] ([r, C], dB).
 __global__ void __launch_bounds__(256) k_lora_ts_reduce(const float* __restrict__ part,
                                                         int nsplit, int64_t C, int RP, int r,
                                                         const float* __restrict__ factor,
@@ -515,30 +567,72 @@ __global__ void __launch_bounds__(256) k_lora_ts_reduce(const float* __restrict_
   const int64_t total = C * r;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
-    int64_t c, j;
+    int64_t idx, stride;
     if (layout == 0) {
-      c = e / r;
-      j = e - c * r;
+      const int64_t c = e / r, j = e - c * r;
+      idx = c * RP + j;
     } else {
-      j = e / C;
-      c = e - j * C;
+      const int64_t j = e / C, c = e - j * C;
+      idx = j * C + c;
     }
+    stride = C * RP;
     float s = 0.0f;
-    for (int sp = 0; sp < nsplit; ++sp) s += part[((int64_t)sp * C + c) * RP + j];
+    for (int sp = 0; sp < nsplit; ++sp) s += part[(int64_t)sp * stride + idx];
     out[e] = __fmul_rn(s, f);
   }
 }
 
-// Row splits of the tall-skinny product: enough CTAs for two per SM of a 152-SM
-// GPU, at most 64 splits, each a multiple of 32 rows.
-int64_t lora_ts_splits(int64_t M, int64_t C, int64_t* rows_per_split) {
+// Row splits of the tall-skinny product.  A fixed model of a 152-SM GPU running two
+// CTAs per SM (304 slots) picks the split count: waves of CTAs times the rows each
+// streams (plus its partial-sum write), plus the reduction's reads, in units of one
+// 128-column row of L.  The plan depends on the shape only, so results are the same
+// on every device.
+int64_t lora_ts_splits(int64_t M, int64_t C, int rp, bool fp4, int64_t* rows_per_split) {
+  const int64_t gran = fp4 ? 64 : 32, slots = 304;
+  const double row_bytes = fp4 ? 128 * 0.5625 : 128 * 2.0;
+  const double part_rows = 128.0 * rp * 4 / row_bytes;  // one CTA's partial write
   const int64_t ctiles = (C + 127) / 128;
-  int64_t ns = (304 + ctiles - 1) / ctiles;
-  ns = ns < 1 ? 1 : (ns > 64 ? 64 : ns);
-  int64_t rps = ((M + ns - 1) / ns + 31) / 32 * 32;
-  if (rps < 32) rps = 32;
-  *rows_per_split = rps;
-  return (M + rps - 1) / rps;
+  double best = 1e300;
+  int64_t best_ns = 1, best_rps = pad_to(M, gran);
+  for (int64_t want = 1; want <= 64; ++want) {
+    const int64_t rps = pad_to((M + want - 1) / want, gran);
+    const int64_t ns = (M + rps - 1) / rps;
+    const int64_t units = ns * ctiles;
+    const double cost = (double)((units + slots - 1) / slots) * ((double)rps + part_rows) +
+                        (double)units * part_rows / slots;
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_ns = ns;
+      best_rps = rps;
+    }
+  }
+  *rows_per_split = best_rps;
+  return best_ns;
+}
+
+template <int RP, bool FP4>
+static cudaError_t launch_ts(const uint16_t* Lb, const uint8_t* Lc, const uint8_t* Lsf, int64_t M,
+                             int64_t C, const uint16_t* R, int tr, float* part, int64_t* nsplit,
+                             cudaStream_t stream) {
+  using P = TsPlan<RP, FP4>;
+  static bool attr_set[64] = {};  // per instantiation and device, before its first launch
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(k_lora_ts<RP, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             P::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int64_t rps;
+  const int64_t ns = lora_ts_splits(M, C, RP, FP4, &rps);
+  *nsplit = ns;
+  note_launch();
+  k_lora_ts<RP, FP4><<<dim3((unsigned)((C + 127) / 128), (unsigned)ns), 256, P::SMEM, stream>>>(
+      Lb, Lc, Lsf, M, C, R, rps, tr, part);
+  return cudaSuccess;
 }
 
 template <int RP>
@@ -556,18 +650,14 @@ static cudaError_t adapter_grad_rp(const uint8_t* xc, const uint8_t* xsf, const 
   k_lora_down_fwd<RP, G><<<mb, 256, 0, stream>>>(xc, xsf, gx, gx, M, K, at_ws, scale, 1, t_ws);
   note_launch();
   k_lora_down_dgrad<RP, G><<<mb, 256, 0, stream>>>(dy, gx, gx, M, N, B, r, scale, 1, u_ws);
-  int64_t rps;
-  int64_t ns = lora_ts_splits(M, N, &rps);
-  note_launch();
-  k_lora_ts<RP, false><<<dim3((unsigned)((N + 127) / 128), (unsigned)ns), 256, 0, stream>>>(
-      dy, nullptr, nullptr, M, N, t_ws, rps, part);
+  int64_t ns;
+  cudaError_t e = launch_ts<RP, false>(dy, nullptr, nullptr, M, N, t_ws, 1, part, &ns, stream);
+  if (e != cudaSuccess) return e;
   note_launch();
   k_lora_ts_reduce<<<std::min<int64_t>((N * r + 255) / 256, num_sms * 8), 256, 0, stream>>>(
       part, (int)ns, N, RP, r, nullptr, 1, dB);
-  ns = lora_ts_splits(M, K, &rps);
-  note_launch();
-  k_lora_ts<RP, true><<<dim3((unsigned)((K + 127) / 128), (unsigned)ns), 256, 0, stream>>>(
-      nullptr, xc, xsf, M, K, u_ws, rps, part);
+  e = launch_ts<RP, true>(nullptr, xc, xsf, M, K, u_ws, 0, part, &ns, stream);
+  if (e != cudaSuccess) return e;
   note_launch();
   k_lora_ts_reduce<<<std::min<int64_t>((K * r + 255) / 256, num_sms * 8), 256, 0, stream>>>(
       part, (int)ns, K, RP, r, gx, 0, dA);
