@@ -236,6 +236,29 @@ def time_gemm_kernels(stack, inputs, reps):
     return out
 
 
+def time_adapter_grads(stack, inputs, reps):
+    """pact_lora_adapter_grad for each projection of the layer step, on the tensors a
+    training step retains (CUDA events around each call)."""
+    x, attn, dy, dq, dk, dv = inputs
+    stack.forward(x, attn)
+    stack.backward(dy, dq, dk, dv)
+    p, m = stack.p, stack.m
+    pairs = {"q": (stack.xq1, dq), "k": (stack.xq1, dk), "v": (stack.xq1, dv),
+             "o": (stack.attnq, stack.dh1), "gate_up": (stack.xq2, stack.dgu),
+             "down": (stack.hq, dy)}
+    out, total = {}, 0.0
+    for name, (xq, g) in pairs.items():
+        proj = p[name]
+        dA = torch.empty(proj.d_in, proj.A.shape[1], device=g.device, dtype=torch.float32)
+        dB = torch.empty(proj.A.shape[1], proj.d_out, device=g.device, dtype=torch.float32)
+        ms = time_call(lambda: proj.adapter_grad(xq, g, dA=dA, dB=dB), reps)
+        one_pass = m * proj.d_in * (0.5 + 1 / 16) + m * proj.d_out * 2
+        out[name] = {"ms": round(ms, 5), "one_pass_gbs": round(one_pass / (ms * 1e-3) / 1e9, 1)}
+        total += ms
+    out["total_ms"] = round(total, 5)
+    return out
+
+
 def time_bf16_comparator(m, shapes, reps):
     """The same GEMM shapes as plain BF16 matmuls through torch (cuBLAS): the BF16
     column of the pages' Table 1, for context.  shapes: name -> (N, K)."""
@@ -425,6 +448,7 @@ def main():
                      reps=10)
     s_bytes = m * stack.inter * (4 + 3 * (0.5 + 1 / 16))
     pk.pact_check_status()
+    adapter = time_adapter_grads(stack, inputs, reps=10)
     bf16 = time_bf16_comparator(m, GEMM_SHAPES, reps=10)
 
     line = {
@@ -456,6 +480,10 @@ def main():
             "silu_mul_quant 8192x2x8192": {"ms": s_ms, "gbs": s_bytes / (s_ms * 1e-3) / 1e9},
             "hbm_peak_gbs": P["hbm_gbs"]},
         "quant_gbs": q_bytes / (q_ms * 1e-3) / 1e9,
+        # the LoRA adapter gradients dA, dB of the seven projections (outside the
+        # fwd+dgrad step that the metric times): per call, and bandwidth against one
+        # read of the NVFP4 input and of the BF16 output gradient
+        "adapter_grad": adapter,
         # context: the same GEMM shapes as cuBLAS BF16 matmuls (no LoRA, no epilogue
         # work), and the NVFP4 kernel's speedup over them
         "bf16_comparator": {k: {"ms": round(v["ms"], 5), "tflops": round(v["tflops"], 1),

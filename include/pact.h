@@ -253,11 +253,13 @@ int pact_silu_mul_bwd(const pact_nvfp4* gate_q, const pact_nvfp4* up_q, const ui
  * dx = rstd*(dn - n*c)  [+ dres]  (dres: residual-stream gradient, BF16 addition).
  *   yq NVFP4 [M, H] (the forward output);  gamma BF16 [H];  rstd FP32 [M];
  *   dy BF16 [M, H];  dres_opt BF16 [M, H] or NULL (may alias dx);  dx BF16 [M, H].
+ *   out_amax_opt: if non-null (4-byte aligned, device) receives max |dx| over the
+ *   BF16 outputs, so that a following pact_quant_nvfp4 of dx is single-pass.
  * Rules: M >= 1, H % 64 == 0, H <= 16384.
  */
 int pact_rmsnorm_bwd(const pact_nvfp4* yq, const uint16_t* gamma, const float* rstd,
                      const uint16_t* dy, const uint16_t* dres_opt, uint16_t* dx,
-                     pact_stream_t stream);
+                     float* out_amax_opt, pact_stream_t stream);
 
 /*
  * The FP32 exp recipe used by pact_silu_mul_quant, exposed so that it can be

@@ -69,7 +69,7 @@ _SIGNATURES = {
     "pact_silu_mul_quant_workspace_size": (_sz, [_i64, _i64]),
     "pact_silu_mul_quant": (_int, [_vp, _i64, _i64, _vp, _SP, _SP, _SP, _vp, _sz, _vp]),
     "pact_silu_mul_bwd": (_int, [_SP, _SP, _vp, _vp, _vp, _vp]),
-    "pact_rmsnorm_bwd": (_int, [_SP, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "pact_rmsnorm_bwd": (_int, [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "pact_test_pexp": (_int, [_vp, _vp, _i64, _vp]),
     "pact_test_wait_timeout": (_int, [ctypes.c_uint32, _vp]),
     "pact_check_status": (_int, [_vp]),
@@ -346,15 +346,19 @@ def pact_silu_mul_bwd(gate_q: NVFP4, up_q: NVFP4, dh: torch.Tensor,
 
 def pact_rmsnorm_bwd(yq: NVFP4, gamma: torch.Tensor, rstd: torch.Tensor, dy: torch.Tensor,
                      dres: torch.Tensor | None = None,
-                     dx: torch.Tensor | None = None) -> torch.Tensor:
-    """RMSNorm backward from the retained NVFP4 output and rstd [+ dres]."""
+                     dx: torch.Tensor | None = None,
+                     out_amax: torch.Tensor | None = None) -> torch.Tensor:
+    """RMSNorm backward from the retained NVFP4 output and rstd [+ dres].  out_amax
+    (FP32 [1], optional) receives max |dx| for a single-pass quantisation of dx."""
     lib = load_library()
     _need_cuda(dy, torch.bfloat16, "dy")
     if dx is None:
         dx = torch.empty_like(dy)
+    if out_amax is not None:
+        _need_cuda(out_amax, torch.float32, "out_amax")
     s = yq.struct()
     _check(lib.pact_rmsnorm_bwd(ctypes.byref(s), _ptr(gamma), _ptr(rstd), _ptr(dy), _ptr(dres),
-                                _ptr(dx), _stream()))
+                                _ptr(dx), _ptr(out_amax), _stream()))
     return dx
 
 

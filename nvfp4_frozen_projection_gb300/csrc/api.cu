@@ -505,7 +505,7 @@ int pact_silu_mul_bwd(const pact_nvfp4* gate_q, const pact_nvfp4* up_q, const ui
 
 int pact_rmsnorm_bwd(const pact_nvfp4* yq, const uint16_t* gamma, const float* rstd,
                      const uint16_t* dy, const uint16_t* dres_opt, uint16_t* dx,
-                     pact_stream_t stream) {
+                     float* out_amax_opt, pact_stream_t stream) {
   DeviceInfo* d;
   int rc = device_info(&d);
   if (rc) return rc;
@@ -516,11 +516,11 @@ int pact_rmsnorm_bwd(const pact_nvfp4* yq, const uint16_t* gamma, const float* r
     return fail(PACT_ERR_SHAPE, "need M >= 1, H %% 64 == 0, H <= 16384");
   if ((rc = check_nvfp4(yq, "yq", M, H, 16))) return rc;
   if (!aligned(gamma, 16) || !aligned(dy, 16) || !aligned(dx, 16) ||
-      (dres_opt && !aligned(dres_opt, 16)))
+      (dres_opt && !aligned(dres_opt, 16)) || (out_amax_opt && !aligned(out_amax_opt, 4)))
     return fail(PACT_ERR_ALIGN, "gamma, dy, dres and dx must be 16-byte aligned");
   cudaError_t e = launch_rmsnorm_bwd((const uint8_t*)yq->codes, (const uint8_t*)yq->sf, yq->g,
-                                     gamma, rstd, dy, dres_opt, M, H, dx, d->sms,
-                                     (cudaStream_t)stream);
+                                     gamma, rstd, dy, dres_opt, M, H, dx,
+                                     (unsigned*)out_amax_opt, d->sms, (cudaStream_t)stream);
   return e == cudaSuccess ? PACT_OK : cuda_fail(e, "rmsnorm bwd launch");
 }
 

@@ -104,7 +104,7 @@ cudaError_t launch_silu_mul_bwd(const uint8_t* gc, const uint8_t* gsf, const flo
 cudaError_t launch_rmsnorm_bwd(const uint8_t* yc, const uint8_t* ysf, const float* yg,
                                const uint16_t* gamma, const float* rstd, const uint16_t* dy,
                                const uint16_t* dres, int64_t M, int64_t H, uint16_t* dx,
-                               int num_sms, cudaStream_t stream);
+                               unsigned* out_amax, int num_sms, cudaStream_t stream);
 cudaError_t launch_pexp(const float* x, float* y, int64_t n, cudaStream_t stream);
 
 }  // namespace pact

@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
     const uint8_t* __restrict__ yc, const uint8_t* __restrict__ ysf, const float* __restrict__ yg,
     const uint16_t* __restrict__ gamma, const float* __restrict__ rstd,
     const uint16_t* __restrict__ dy, const uint16_t* dres, int64_t M, int64_t H,
-    uint16_t* dx) {
+    uint16_t* dx, unsigned* __restrict__ out_amax) {
   // The row's codes, scales and dy stay in registers between the reduction and the
   // output pass.  sum(dn * n) = sum(dy * gamma * yhat / gamma) = sum(dy * yhat), so
   // the reduction needs no division; the output pass divides by gamma with the
@@ -496,6 +496,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
   const int lane = threadIdx.x & 31;
   const int nb = (int)(H >> 4);
   const float g = *yg;
+  uint32_t amax = 0;  // max |dx| over this thread's outputs, as FP32 bits of the BF16 values
   for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < M;
        row += (int64_t)gridDim.x * 8) {
     uint2 cw[BPL];
@@ -555,6 +556,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
             if (dres) v[k] += r[i + k];
           }
           o[i / 2] = pack_bf16x2(v[0], v[1]);
+          amax = max(amax, max((o[i / 2] & 0x7FFFu) << 16, (o[i / 2] >> 16 & 0x7FFFu) << 16));
         }
         uint4* op = reinterpret_cast<uint4*>(dx + row * H + b * 16);
         op[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -562,6 +564,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
       }
     }
   }
+  if (out_amax) block_max_atomic(amax, out_amax);
 }
 
 __global__ void k_pexp(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
@@ -654,12 +657,16 @@ cudaError_t launch_silu_mul_bwd(const uint8_t* gc, const uint8_t* gsf, const flo
 cudaError_t launch_rmsnorm_bwd(const uint8_t* yc, const uint8_t* ysf, const float* yg,
                                const uint16_t* gamma, const float* rstd, const uint16_t* dy,
                                const uint16_t* dres, int64_t M, int64_t H, uint16_t* dx,
-                               int num_sms, cudaStream_t stream) {
+                               unsigned* out_amax, int num_sms, cudaStream_t stream) {
+  if (out_amax) {
+    cudaError_t e = cudaMemsetAsync(out_amax, 0, sizeof(unsigned), stream);
+    if (e != cudaSuccess) return e;
+  }
   return dispatch_bpl(H, [&](auto bpl) {
     constexpr int BPL = decltype(bpl)::value;
     note_launch();
     k_rmsnorm_bwd<BPL><<<blocks_for(M, 8, num_sms * 8), 256, 0, stream>>>(
-        yc, ysf, yg, gamma, rstd, dy, dres, M, H, dx);
+        yc, ysf, yg, gamma, rstd, dy, dres, M, H, dx, out_amax);
     return cudaGetLastError();
   });
 }

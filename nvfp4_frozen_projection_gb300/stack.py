@@ -17,7 +17,8 @@ import numpy as np
 import torch
 
 from . import (NVFP4, pact_lora_linear_dgrad, pact_lora_linear_fwd, pact_pack_weight_bwd,
-               pact_pack_weight_fwd, pact_quant_nvfp4, pact_rmsnorm_bwd, pact_rmsnorm_quant,
+               pact_lora_adapter_grad, pact_pack_weight_fwd, pact_quant_nvfp4, pact_rmsnorm_bwd,
+               pact_rmsnorm_quant,
                pact_silu_mul_bwd, pact_silu_mul_quant)
 
 
@@ -38,6 +39,9 @@ class LoraLinear:
     def dgrad(self, dyq: NVFP4, dy: torch.Tensor, dx: torch.Tensor, accumulate=False):
         return pact_lora_linear_dgrad(dyq, dy, self.w_bwd, self.A, self.B, self.scale, dx=dx,
                                       accumulate=accumulate)
+
+    def adapter_grad(self, xq: NVFP4, dy: torch.Tensor, dA=None, dB=None):
+        return pact_lora_adapter_grad(xq, dy, self.A, self.B, self.scale, dA=dA, dB=dB)
 
     def gemm_flops(self, m: int) -> float:
         return 2.0 * m * self.d_in * self.d_out
@@ -76,6 +80,7 @@ class DecoderProjectionStack:
         self.dh = torch.empty(m, inter, **bf)
         self.dgu = torch.empty(m, 2 * inter, **bf)
         self.dgu_amax = torch.empty(1, dtype=torch.float32, device=dev)
+        self.dh1_amax = torch.empty(1, dtype=torch.float32, device=dev)
         self.dguq = NVFP4.empty(m, 2 * inter, dev)
         self.dxn2 = torch.empty(m, hidden, **bf)
         self.dh1 = torch.empty(m, hidden, **bf)
@@ -102,6 +107,16 @@ class DecoderProjectionStack:
         p["down"].forward(self.hq, self.out, residual=self.h1)
         return self.out
 
+    def adapter_grads(self, dy, dq, dk, dv) -> dict:
+        """dA, dB of all seven adapters from the tensors the forward and backward
+        retained (call after backward): each projection's NVFP4 input and the BF16
+        gradient of its output."""
+        p = self.p
+        pairs = {"q": (self.xq1, dq), "k": (self.xq1, dk), "v": (self.xq1, dv),
+                 "o": (self.attnq, self.dh1), "gate_up": (self.xq2, self.dgu),
+                 "down": (self.hq, dy)}
+        return {name: p[name].adapter_grad(xq, g) for name, (xq, g) in pairs.items()}
+
     def backward(self, dy, dq, dk, dv) -> torch.Tensor:
         """dy: gradient of the layer output; dq/dk/dv: gradients flowing back from
         the (out of scope) attention core into the q/k/v outputs."""
@@ -111,8 +126,9 @@ class DecoderProjectionStack:
         pact_silu_mul_bwd(self.gq, self.uq, self.dh, dgateup=self.dgu, out_amax=self.dgu_amax)
         pact_quant_nvfp4(self.dgu, amax=self.dgu_amax, out=self.dguq)
         p["gate_up"].dgrad(self.dguq, self.dgu, self.dxn2)
-        pact_rmsnorm_bwd(self.xq2, self.gamma2, self.rstd2, self.dxn2, dres=dy, dx=self.dh1)
-        pact_quant_nvfp4(self.dh1, out=self.dh1q)
+        pact_rmsnorm_bwd(self.xq2, self.gamma2, self.rstd2, self.dxn2, dres=dy, dx=self.dh1,
+                         out_amax=self.dh1_amax)
+        pact_quant_nvfp4(self.dh1, amax=self.dh1_amax, out=self.dh1q)
         p["o"].dgrad(self.dh1q, self.dh1, self.dattn)  # into the attention core
         pact_quant_nvfp4(dq, out=self.dqq)
         pact_quant_nvfp4(dk, out=self.dkq)

@@ -137,8 +137,13 @@ def test_rmsnorm_bwd(M, H, with_res):
     dy = wl.bf16_round(wl.normal(rng, (M, H), 1e-2))
     dres = wl.bf16_round(wl.normal(rng, (M, H), 1e-2)) if with_res else None
     yq, rstd = pact_rmsnorm_quant(bf16(x), bf16(gamma))
-    dx = pact_rmsnorm_bwd(yq, bf16(gamma), rstd, bf16(dy), None if dres is None else bf16(dres))
+    amax = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    dx = pact_rmsnorm_bwd(yq, bf16(gamma), rstd, bf16(dy), None if dres is None else bf16(dres),
+                          out_amax=amax)
     pact_check_status()
     ref_q, ref_rstd = orc.rmsnorm_quant(x, gamma)
     ref = orc.rmsnorm_bwd(ref_q, gamma, ref_rstd, dy, dres)
-    assert_close(host(dx), ref, "rmsnorm bwd")
+    got = host(dx)
+    assert_close(got, ref, "rmsnorm bwd")
+    # producer-epilogue amax: exactly the max |.| of the BF16 gradient written
+    assert float(amax.item()) == float(np.abs(got).max())
