@@ -8,6 +8,8 @@ Cases (M = tokens; the other sizes are the Llama-3B layer's):
   quant               NVFP4 quantisation of a BF16 [M, 3072] tensor
   silu                SiLU-multiply -> NVFP4 of a BF16 [M, 2 x 8192] tensor
   lora-down-fwd       the q projection's forward (down-projection + GEMM)
+  adapter-grad-q      dA, dB of the q projection (3072 -> 3072, r = 16)
+  adapter-grad-gate-up  dA, dB of the fused gate|up projection (3072 -> 2 x 8192, r = 32)
 
 The default M (4096) keeps every case's inputs above the 129 MB L2 and its device
 memory under 1 GB, which is the size a full ncu capture wants.  Each run exits 0
@@ -19,9 +21,9 @@ import argparse
 
 import torch
 
-from . import (pact_check_status, pact_lora_linear_dgrad, pact_lora_linear_fwd,
-               pact_pack_weight_bwd, pact_pack_weight_fwd, pact_quant_nvfp4,
-               pact_silu_mul_quant)
+from . import (pact_check_status, pact_lora_adapter_grad, pact_lora_linear_dgrad,
+               pact_lora_linear_fwd, pact_pack_weight_bwd, pact_pack_weight_fwd,
+               pact_quant_nvfp4, pact_silu_mul_quant)
 
 HIDDEN, INTER = 3072, 8192
 
@@ -55,6 +57,16 @@ def run(case: str, m: int, reps: int) -> None:
         y = torch.empty(m, n_out, dtype=torch.bfloat16, device=dev)
         for _ in range(reps):
             pact_lora_linear_fwd(xq, wf, A, B, 2.0, y=y)
+    elif case in ("adapter-grad-q", "adapter-grad-gate-up"):
+        n_out, r = (HIDDEN, 16) if case == "adapter-grad-q" else (2 * INTER, 32)
+        _, A, B = _lora(HIDDEN, n_out, r, dev, gen)
+        x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
+        xq = pact_quant_nvfp4(x)
+        dy = (torch.randn(m, n_out, device=dev, generator=gen) * 0.01).bfloat16()
+        dA = torch.empty(HIDDEN, r, dtype=torch.float32, device=dev)
+        dB = torch.empty(r, n_out, dtype=torch.float32, device=dev)
+        for _ in range(reps):
+            pact_lora_adapter_grad(xq, dy, A, B, 2.0, dA=dA, dB=dB)
     elif case == "quant":
         x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
         q = pact_quant_nvfp4(x)
