@@ -13,9 +13,12 @@ namespace pact {
 
 // ---------------------------------------------------------------- pass 1: amax
 // max |x| over BF16 [M, K] (row stride ldx elements), folded into *amax_bits.
-__global__ void __launch_bounds__(256) k_amax_bf16(const uint16_t* __restrict__ x, int64_t M,
-                                                   int64_t K, int64_t ldx,
-                                                   unsigned* __restrict__ amax_bits) {
+// Eight 16-byte loads in flight per thread and four CTAs per SM (64 registers):
+// 128 KB of reads in flight per SM, what HBM needs at the latency it has under
+// full load.
+__global__ void __launch_bounds__(256, 4) k_amax_bf16(const uint16_t* __restrict__ x, int64_t M,
+                                                      int64_t K, int64_t ldx,
+                                                      unsigned* __restrict__ amax_bits) {
   const int64_t vpr = K >> 3;  // 16-byte vectors per row
   const int64_t total = M * vpr;
   uint32_t m = 0;
@@ -23,11 +26,12 @@ __global__ void __launch_bounds__(256) k_amax_bf16(const uint16_t* __restrict__ 
   int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (ldx == K) {
     const uint4* p = reinterpret_cast<const uint4*>(x);
-    for (; v + 3 * stride < total; v += 4 * stride) {
-      uint4 a = ldg_stream(p + v), b = ldg_stream(p + v + stride);
-      uint4 c = ldg_stream(p + v + 2 * stride), d = ldg_stream(p + v + 3 * stride);
-      m = max(m, max(max(absmax_bf16x8_bits(a), absmax_bf16x8_bits(b)),
-                     max(absmax_bf16x8_bits(c), absmax_bf16x8_bits(d))));
+    for (; v + 7 * stride < total; v += 8 * stride) {
+      uint4 a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = ldg_stream(p + v + u * stride);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m = max(m, absmax_bf16x8_bits(a[u]));
     }
     for (; v < total; v += stride) m = max(m, absmax_bf16x8_bits(ldg_stream(p + v)));
   } else {
@@ -58,7 +62,7 @@ __global__ void __launch_bounds__(256) k_amax_f32(const float* __restrict__ w, i
 // One thread encodes 64 consecutive elements (4 blocks) of one row: 128 bytes in,
 // 32 code bytes and one 4-byte scale word out.  Threads past row M (up to
 // pad128(M)) write zero scale words so the padded scale array is fully defined.
-__global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__ x, int64_t M,
+__global__ void __launch_bounds__(256, 4) k_quant_bf16(const uint16_t* __restrict__ x, int64_t M,
                                                     int64_t K, int64_t ldx, int64_t Mpad,
                                                     FastDiv chunks_div,
                                                     const float* __restrict__ amax_opt,
@@ -172,7 +176,7 @@ cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
     cudaError_t e = cudaMemsetAsync(ws_amax, 0, sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
     note_launch();
-    k_amax_bf16<<<grid_for(M * K / 8, 256, num_sms * 8), 256, 0, stream>>>(x, M, K, ldx,
+    k_amax_bf16<<<grid_for(M * K / 8, 256, num_sms * 4), 256, 0, stream>>>(x, M, K, ldx,
                                                                             ws_amax);
   }
   const int64_t Mpad = pad_to(M, 128);
