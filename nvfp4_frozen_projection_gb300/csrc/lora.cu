@@ -200,16 +200,24 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_fwd(const uint8_t* __restr
         scl[gi][h][1] = e4m3_dup_h2(x0.sc[gi][h] >> 8);
       }
     const int64_t kb = (int64_t)ch * 128 + 32 * c;
+    // the chunk's At fragments (lane (g, c): row 8 jn + g, columns kb .. kb + 32),
+    // all requested before the first MMA so the chunk pays one L2 round trip
+    uint4 bq[NT][4];
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn) {
+      // At rows >= r are zero; a dead lane of a half chunk multiplies zeros
+      const uint4* src = reinterpret_cast<const uint4*>(At + (int64_t)(jn * 8 + g) * K + kb);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) bq[jn][i] = live ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       uint32_t bfr[NT][2];
 #pragma unroll
       for (int jn = 0; jn < NT; ++jn) {
-        // At rows >= r are zero; a dead lane of a half chunk multiplies zeros
-        uint2 bb = make_uint2(0u, 0u);
-        if (live) bb = __ldg(reinterpret_cast<const uint2*>(At + (int64_t)(jn * 8 + g) * K + kb + 4 * s));
-        bfr[jn][0] = bb.x;
-        bfr[jn][1] = bb.y;
+        const uint4 v = bq[jn][s >> 1];
+        bfr[jn][0] = (s & 1) ? v.z : v.x;
+        bfr[jn][1] = (s & 1) ? v.w : v.y;
       }
 #pragma unroll
       for (int gi = 0; gi < G; ++gi) {
@@ -269,22 +277,39 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dgrad(const uint16_t* __re
                            : make_uint4(0u, 0u, 0u, 0u);
       }
   };
+  // the chunk's B fragments: lane (g, c) needs B[8 jn + g, n0 .. n0 + 8) (two 8-byte
+  // halves, one per MMA step); they are loaded one chunk ahead with the dY rows, so
+  // no L2 round trip sits between a chunk's arrival and its MMAs
+  auto load_b = [&](int ch, uint4 (&b)[NT]) {
+    const int64_t n0 = (int64_t)ch * 32 + 8 * c;
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn) {
+      const int col = jn * 8 + g;
+      b[jn] = make_uint4(0u, 0u, 0u, 0u);
+      if (col < r) {  // two 8-byte loads: B is only required to be 8-byte aligned
+        const uint2* src = reinterpret_cast<const uint2*>(B + (int64_t)col * N + n0);
+        const uint2 lo = __ldg(src), hi = __ldg(src + 1);
+        b[jn] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      }
+    }
+  };
   uint4 x0[G][2], x1[G][2], x2[G][2];
-  if (warp < nch) load(warp, x0);
+  uint4 b0[NT], b1[NT];
+  if (warp < nch) {
+    load(warp, x0);
+    load_b(warp, b0);
+  }
   if (warp + 8 < nch) load(warp + 8, x1);
   for (int ch = warp; ch < nch; ch += 8) {
     if (ch + 16 < nch) load(ch + 16, x2);
-    const int64_t n0 = (int64_t)ch * 32 + 8 * c;
+    if (ch + 8 < nch) load_b(ch + 8, b1);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       uint32_t bfr[NT][2];
 #pragma unroll
       for (int jn = 0; jn < NT; ++jn) {
-        const int col = jn * 8 + g;
-        uint2 bb = make_uint2(0u, 0u);
-        if (col < r) bb = __ldg(reinterpret_cast<const uint2*>(B + (int64_t)col * N + n0 + 4 * s));
-        bfr[jn][0] = bb.x;
-        bfr[jn][1] = bb.y;
+        bfr[jn][0] = s ? b0[jn].z : b0[jn].x;
+        bfr[jn][1] = s ? b0[jn].w : b0[jn].y;
       }
 #pragma unroll
       for (int gi = 0; gi < G; ++gi) {
@@ -301,6 +326,8 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dgrad(const uint16_t* __re
         x0[gi][h] = x1[gi][h];
         x1[gi][h] = x2[gi][h];
       }
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn) b0[jn] = b1[jn];
   }
   // plain: f = scale, i.e. v = scale * (dY B^T) for the adapter gradients
   const float s_main = plain ? 0.0f : __fmul_rn(*gdy, *gw);
