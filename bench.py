@@ -413,23 +413,77 @@ def main():
     value = job_throughput(flops, world, ms) / 1e12
     tokens_per_s = job_throughput(stack.m, world, ms)
 
-    # ---------------- end to end: pinned host inputs in, result (dx) out, per step
-    host_out = torch.empty_like(stack.dx, device="cpu").pin_memory()
+    # ---------------- end to end: pinned host inputs in, result (dx) out, every step.
+    # As a training loop would run it: two sets of device buffers (a second stack
+    # sharing the packed weights, each with its own captured step), the next step's
+    # inputs uploaded on one copy stream while this step computes, and each step's
+    # result read back on another while the next one computes.
+    from nvfp4_frozen_projection_gb300.stack import DecoderProjectionStack
+    stack2 = DecoderProjectionStack(stack.m, stack.p, stack.gamma1, stack.gamma2, stack.eps)
+    inputs2 = [torch.empty_like(t) for t in inputs]
+    sets = [(stack, inputs), (stack2, inputs2)]
+    runs = []
+    for st, ins in sets:
+        def step_on(st=st, ins=ins):
+            st.forward(ins[0], ins[1])
+            st.backward(ins[2], ins[3], ins[4], ins[5])
+        if graph is not None and st is stack:
+            runs.append(run)
+            continue
+        for t_dev, h in zip(ins, host_in):
+            t_dev.copy_(h)
+        step_on()
+        torch.cuda.synchronize()
+        if graph is not None:
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2):
+                step_on()
+            runs.append(g2.replay)
+        else:
+            runs.append(step_on)
+    host_out = [torch.empty_like(stack.dx, device="cpu").pin_memory() for _ in range(2)]
+    compute = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def upload(b, after=None):
+        with torch.cuda.stream(up):
+            if after is not None:
+                up.wait_event(after)  # the step that last read buffer b has finished
+            for h, t_dev in zip(host_in, sets[b][1]):
+                t_dev.copy_(h, non_blocking=True)
+            ev_in[b].record(up)
+
     barrier()
     torch.cuda.synchronize()
     e_begin, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_begin.record()
-    for _ in range(args.steps):
-        for h, dvc in zip(host_in, inputs):
-            dvc.copy_(h, non_blocking=True)
-        run()
-        host_out.copy_(stack.dx, non_blocking=True)
-    e_end.record()
+    e_begin.record(compute)
+    up.wait_stream(compute)
+    down.wait_stream(compute)
+    upload(0)
+    for i in range(args.steps):
+        b = i % 2
+        if i + 1 < args.steps:
+            upload(1 - b, ev_done[1 - b] if i >= 1 else None)
+        compute.wait_event(ev_in[b])
+        if i >= 2:
+            compute.wait_event(ev_out[b])  # step i-2's result has left this buffer
+        runs[b]()
+        ev_done[b].record(compute)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[b])
+            host_out[b].copy_(sets[b][0].dx, non_blocking=True)
+            ev_out[b].record(down)
+    compute.wait_stream(up)
+    compute.wait_stream(down)
+    e_end.record(compute)
     torch.cuda.synchronize()
     barrier()
     ms_e2e = max_over_ranks(e_begin.elapsed_time(e_end) / args.steps, dev)
     h2d = sum(h.numel() * h.element_size() for h in host_in)
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
 
     # ---------------- per-kernel live timing (GEMM kernels alone; quantiser)
     kern = time_gemm_kernels(stack, inputs, reps=max(5, args.steps // 2))
