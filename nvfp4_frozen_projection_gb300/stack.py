@@ -49,11 +49,14 @@ class LoraLinear:
 
 class DecoderProjectionStack:
     """The seven LoRA projections of a Llama decoder layer with both RMSNorms, the
-    SiLU-multiply and the two residual adds; forward and input-gradient pass."""
+    SiLU-multiply and the two residual adds; forward and input-gradient pass.
+    Same-shaped projections that read the same input run as one fused GEMM: kv
+    (k | v) and gate_up (gate | up), each with its adapters side by side and B
+    block-diagonal."""
 
     def __init__(self, m: int, proj: dict, gamma1, gamma2, eps: float = 1e-5):
         self.m = m
-        self.p = proj  # q, k, v, o, gate_up, down -> LoraLinear
+        self.p = proj  # q, kv, o, gate_up, down -> LoraLinear
         self.gamma1, self.gamma2, self.eps = gamma1, gamma2, float(eps)
         hidden = proj["q"].d_in
         inter = proj["down"].d_in
@@ -64,8 +67,7 @@ class DecoderProjectionStack:
         self.xq1 = NVFP4.empty(m, hidden, dev)
         self.rstd1 = torch.empty(m, dtype=torch.float32, device=dev)
         self.q = torch.empty(m, proj["q"].d_out, **bf)
-        self.k = torch.empty(m, proj["k"].d_out, **bf)
-        self.v = torch.empty(m, proj["v"].d_out, **bf)
+        self.kv = torch.empty(m, proj["kv"].d_out, **bf)  # k | v
         self.attnq = NVFP4.empty(m, hidden, dev)
         self.h1 = torch.empty(m, hidden, **bf)
         self.xq2 = NVFP4.empty(m, hidden, dev)
@@ -87,8 +89,7 @@ class DecoderProjectionStack:
         self.dh1q = NVFP4.empty(m, hidden, dev)
         self.dattn = torch.empty(m, hidden, **bf)
         self.dqq = NVFP4.empty(m, proj["q"].d_out, dev)
-        self.dkq = NVFP4.empty(m, proj["k"].d_out, dev)
-        self.dvq = NVFP4.empty(m, proj["v"].d_out, dev)
+        self.dkvq = NVFP4.empty(m, proj["kv"].d_out, dev)
         self.dxn1 = torch.empty(m, hidden, **bf)
         self.dx = torch.empty(m, hidden, **bf)
 
@@ -96,8 +97,7 @@ class DecoderProjectionStack:
         p = self.p
         pact_rmsnorm_quant(x, self.gamma1, self.eps, out=self.xq1, rstd=self.rstd1)
         p["q"].forward(self.xq1, self.q)
-        p["k"].forward(self.xq1, self.k)
-        p["v"].forward(self.xq1, self.v)
+        p["kv"].forward(self.xq1, self.kv)
         # attention core (out of scope): its output is the given tensor attn
         pact_quant_nvfp4(attn, out=self.attnq)
         p["o"].forward(self.attnq, self.h1, residual=x)
@@ -107,19 +107,19 @@ class DecoderProjectionStack:
         p["down"].forward(self.hq, self.out, residual=self.h1)
         return self.out
 
-    def adapter_grads(self, dy, dq, dk, dv) -> dict:
+    def adapter_grads(self, dy, dq, dkv) -> dict:
         """dA, dB of all seven adapters from the tensors the forward and backward
         retained (call after backward): each projection's NVFP4 input and the BF16
-        gradient of its output."""
+        gradient of its output.  For the fused projections the adapters' gradients
+        are the diagonal blocks of dB (and the matching columns of dA)."""
         p = self.p
-        pairs = {"q": (self.xq1, dq), "k": (self.xq1, dk), "v": (self.xq1, dv),
-                 "o": (self.attnq, self.dh1), "gate_up": (self.xq2, self.dgu),
-                 "down": (self.hq, dy)}
+        pairs = {"q": (self.xq1, dq), "kv": (self.xq1, dkv), "o": (self.attnq, self.dh1),
+                 "gate_up": (self.xq2, self.dgu), "down": (self.hq, dy)}
         return {name: p[name].adapter_grad(xq, g) for name, (xq, g) in pairs.items()}
 
-    def backward(self, dy, dq, dk, dv) -> torch.Tensor:
-        """dy: gradient of the layer output; dq/dk/dv: gradients flowing back from
-        the (out of scope) attention core into the q/k/v outputs."""
+    def backward(self, dy, dq, dkv) -> torch.Tensor:
+        """dy: gradient of the layer output; dq and dkv (dk | dv): the gradients
+        flowing back from the (out of scope) attention core into the q/k/v outputs."""
         p = self.p
         pact_quant_nvfp4(dy, out=self.dyq)
         p["down"].dgrad(self.dyq, dy, self.dh)
@@ -131,24 +131,22 @@ class DecoderProjectionStack:
         pact_quant_nvfp4(self.dh1, amax=self.dh1_amax, out=self.dh1q)
         p["o"].dgrad(self.dh1q, self.dh1, self.dattn)  # into the attention core
         pact_quant_nvfp4(dq, out=self.dqq)
-        pact_quant_nvfp4(dk, out=self.dkq)
-        pact_quant_nvfp4(dv, out=self.dvq)
+        pact_quant_nvfp4(dkv, out=self.dkvq)
         p["q"].dgrad(self.dqq, dq, self.dxn1)
-        p["k"].dgrad(self.dkq, dk, self.dxn1, accumulate=True)
-        p["v"].dgrad(self.dvq, dv, self.dxn1, accumulate=True)
+        p["kv"].dgrad(self.dkvq, dkv, self.dxn1, accumulate=True)
         pact_rmsnorm_bwd(self.xq1, self.gamma1, self.rstd1, self.dxn1, dres=self.dh1, dx=self.dx)
         return self.dx
 
     @classmethod
     def from_workload(cls, d: dict, device) -> "DecoderProjectionStack":
         """Build the stack from host arrays: d holds x (for M), gamma1, gamma2, eps and
-        projections q, k, v, o, gate_up, down with FP32 W [d_out, d_in], adapters A
+        projections q, kv, o, gate_up, down with FP32 W [d_out, d_in], adapters A
         [d_in, r], B [r, d_out] (BF16 values) and alpha, r.  Weights are packed here."""
         def t32(a):
             return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
 
         proj = {}
-        for k in ("q", "k", "v", "o", "gate_up", "down"):
+        for k in ("q", "kv", "o", "gate_up", "down"):
             p = d[k]
             proj[k] = LoraLinear(t32(p.W), t32(p.A).bfloat16(), t32(p.B).bfloat16(),
                                  float(p.alpha) / float(p.r))

@@ -83,19 +83,29 @@ def make_proj(rng, name, d_in, d_out, r, alpha, w_std, b_std=0.1) -> Proj:
     return p
 
 
-def fuse_gate_up(gate: Proj, up: Proj) -> Proj:
-    """gate and up as one [2I, H] GEMM: W stacked, A side by side, B block-diagonal.
-    The LoRA scale alpha/r of the separate adapters is kept."""
-    assert gate.r == up.r and gate.alpha == up.alpha
-    r = gate.r
-    p = Proj("gate_up", gate.d_in, gate.d_out + up.d_out, 2 * r, gate.alpha * 2)
-    p.W = np.concatenate([gate.W, up.W], axis=0)
-    p.A = np.concatenate([gate.A, up.A], axis=1)
-    B = np.zeros((2 * r, p.d_out), np.float32)
-    B[:r, :gate.d_out] = gate.B
-    B[r:, gate.d_out:] = up.B
+def fuse_outputs(name: str, parts: list) -> Proj:
+    """Projections of one input as one GEMM: W stacked along the outputs (one frozen
+    weight, so one per-tensor scale), A side by side, B block-diagonal.  Each part's
+    LoRA scale alpha/r is kept, so every output column gets exactly its own
+    adapter's term."""
+    r, alpha = parts[0].r, parts[0].alpha
+    assert all(q.r == r and q.alpha == alpha and q.d_in == parts[0].d_in for q in parts)
+    n = len(parts)
+    p = Proj(name, parts[0].d_in, sum(q.d_out for q in parts), n * r, alpha * n)
+    p.W = np.concatenate([q.W for q in parts], axis=0)
+    p.A = np.concatenate([q.A for q in parts], axis=1)
+    B = np.zeros((n * r, p.d_out), np.float32)
+    c = 0
+    for i, q in enumerate(parts):
+        B[i * r:(i + 1) * r, c:c + q.d_out] = q.B
+        c += q.d_out
     p.B = B
     return p
+
+
+def fuse_gate_up(gate: Proj, up: Proj) -> Proj:
+    """gate and up as one [2I, H] GEMM (see fuse_outputs)."""
+    return fuse_outputs("gate_up", [gate, up])
 
 
 WORKLOAD_NAMES = {1: "tiny", 2: "q-3b", 3: "mlp-3b", 4: "attn-1b", 5: "layer-3b"}
@@ -148,7 +158,8 @@ def attn1b(m: int = 26624, hidden: int = 2048, kv: int = 512):
 def layer3b(m: int = 8192, hidden: int = 3072, kv: int = 1024, inter: int = 8192):
     """Workload 5: Llama-3B decoder-layer projection stack.  The attention core is
     replaced by a seeded N(0,1) BF16 tensor; the gradients flowing into q/k/v from
-    the (out of scope) attention backward are seeded N(0, 1e-2^2) tensors."""
+    the (out of scope) attention backward are seeded N(0, 1e-2^2) tensors.  The
+    stack runs k/v as the fused projection kv and gate/up as gate_up."""
     rng = rng_for(5)
     x = bf16_round(student_t_unit_rms(rng, (m, hidden)))
     gamma1 = bf16_round(1.0 + normal(rng, (hidden,), 0.1))
@@ -165,9 +176,12 @@ def layer3b(m: int = 8192, hidden: int = 3072, kv: int = 1024, inter: int = 8192
     dq = bf16_round(normal(rng, (m, hidden), 1e-2))
     dk = bf16_round(normal(rng, (m, kv), 1e-2))
     dv = bf16_round(normal(rng, (m, kv), 1e-2))
-    return dict(x=x, gamma1=gamma1, gamma2=gamma2, q=q, k=k, v=v, o=o,
-                gate_up=fuse_gate_up(gate, up), down=down, attn=attn,
-                dy=dy, dq=dq, dk=dk, dv=dv, eps=np.float32(1e-5))
+    # k and v read the same input and have the same shape: one fused projection (as
+    # gate|up), whose incoming gradient is the attention core's dk | dv side by side
+    return dict(x=x, gamma1=gamma1, gamma2=gamma2, q=q, k=k, v=v, kv=fuse_outputs("kv", [k, v]),
+                o=o, gate_up=fuse_gate_up(gate, up), down=down, attn=attn,
+                dy=dy, dq=dq, dk=dk, dv=dv, dkv=np.concatenate([dk, dv], axis=1),
+                eps=np.float32(1e-5))
 
 
 def gemm_flops_per_step(which: int, m: int | None = None) -> float:
