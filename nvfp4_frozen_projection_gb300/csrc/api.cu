@@ -299,6 +299,7 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   p.ga = a->g;
   p.gb = b->g;
   p.addend = addend;
+  p.addend32 = addend && aligned(addend, 32);
   p.out = out;
   p.out_amax = (unsigned*)out_amax;
   p.status = d->status;

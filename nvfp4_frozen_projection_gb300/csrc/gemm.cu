@@ -473,14 +473,29 @@ __global__ void __launch_bounds__(448, 1)
       for (int ch = 0; ch < NCH; ++ch) {
         const int n = n0 + c0 + 32 * ch;
         if (p.addend && row_ok && n < p.N) {
-          const uint4* ad = reinterpret_cast<const uint4*>(p.addend + (size_t)m * p.N + n);
+          const uint16_t* ap = p.addend + (size_t)m * p.N + n;
+          if (p.addend32) {
+            // a lane reads its own row: 32-byte loads fill whole sectors, so each
+            // load instruction costs half the L1 transactions of 16-byte ones (the
+            // MIO queue these share with the scale-staging warps' shared loads)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 a4 = ad[k];
-            out[ch][4 * k] = a4.x;
-            out[ch][4 * k + 1] = a4.y;
-            out[ch][4 * k + 2] = a4.z;
-            out[ch][4 * k + 3] = a4.w;
+            for (int k = 0; k < 2; ++k) {
+              uint32_t* o8 = &out[ch][8 * k];
+              asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                           : "=r"(o8[0]), "=r"(o8[1]), "=r"(o8[2]), "=r"(o8[3]), "=r"(o8[4]),
+                             "=r"(o8[5]), "=r"(o8[6]), "=r"(o8[7])
+                           : "l"(ap + 16 * k));
+            }
+          } else {
+            const uint4* ad = reinterpret_cast<const uint4*>(ap);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint4 a4 = ad[k];
+              out[ch][4 * k] = a4.x;
+              out[ch][4 * k + 1] = a4.y;
+              out[ch][4 * k + 2] = a4.z;
+              out[ch][4 * k + 3] = a4.w;
+            }
           }
         } else {
 #pragma unroll

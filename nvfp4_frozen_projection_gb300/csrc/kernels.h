@@ -36,6 +36,7 @@ struct GemmParams {
   int num_m, num_n;        // tile grid
   int lora_steps;          // K=16 BF16 MMAs of the LoRA product per tile (0 = none)
   int band_mc;             // tile order: bands of band_mc M-units, each swept over all N
+  int addend32;            // addend 32-byte aligned: fetched with 32-byte loads
 };
 
 struct GemmLaunch {

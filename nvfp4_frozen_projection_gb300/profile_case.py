@@ -8,6 +8,7 @@ Cases (M = tokens; the other sizes are the Llama-3B layer's):
   quant               NVFP4 quantisation of a BF16 [M, 3072] tensor
   silu                SiLU-multiply -> NVFP4 of a BF16 [M, 2 x 8192] tensor
   lora-down-fwd       the q projection's forward (down-projection + GEMM)
+  gemm-o-fwd          the o projection's forward: the same GEMM plus the residual add
   adapter-grad-q      dA, dB of the q projection (3072 -> 3072, r = 16)
   adapter-grad-gate-up  dA, dB of the fused gate|up projection (3072 -> 2 x 8192, r = 32)
 
@@ -47,16 +48,17 @@ def run(case: str, m: int, reps: int) -> None:
         dx = torch.empty(m, HIDDEN, dtype=torch.bfloat16, device=dev)
         for _ in range(reps):
             pact_lora_linear_dgrad(dyq, dy, wb, A, B, 2.0, dx=dx)
-    elif case in ("gemm-gate-up-fwd", "lora-down-fwd"):
+    elif case in ("gemm-gate-up-fwd", "lora-down-fwd", "gemm-o-fwd"):
         n_out = 2 * INTER if case == "gemm-gate-up-fwd" else HIDDEN
         r = 32 if case == "gemm-gate-up-fwd" else 16
         W, A, B = _lora(HIDDEN, n_out, r, dev, gen)
         wf = pact_pack_weight_fwd(W)
         x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
         xq = pact_quant_nvfp4(x)
+        res = x if case == "gemm-o-fwd" else None
         y = torch.empty(m, n_out, dtype=torch.bfloat16, device=dev)
         for _ in range(reps):
-            pact_lora_linear_fwd(xq, wf, A, B, 2.0, y=y)
+            pact_lora_linear_fwd(xq, wf, A, B, 2.0, residual=res, y=y)
     elif case in ("adapter-grad-q", "adapter-grad-gate-up"):
         n_out, r = (HIDDEN, 16) if case == "adapter-grad-q" else (2 * INTER, 32)
         _, A, B = _lora(HIDDEN, n_out, r, dev, gen)
