@@ -381,12 +381,14 @@ int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact
   const int rp = rp_for(r);
   uint16_t* u = (uint16_t*)ws;
   uint16_t* ap = (uint16_t*)((char*)ws + align256((size_t)M * 2 * rp * 2));
+  // A [K, r] with r == rp is already the zero-padded [K, rp] operand the GEMM reads
+  const bool a_direct = r == rp && aligned(A, 16);
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_lora_down_dgrad(dy, dyq->g, w_bwd->g, M, N, A, B, r, rp, scale, K, u, ap,
-                                         s);
+  cudaError_t e = launch_lora_down_dgrad(dy, dyq->g, w_bwd->g, M, N, A, B, r, rp, scale, K, u,
+                                         a_direct ? nullptr : ap, s);
   if (e != cudaSuccess) return cuda_fail(e, "lora down launch");
-  return run_gemm(d, dyq, w_bwd, M, K, N, u, ap, 2 * rp, accumulate ? dx : nullptr, dx, nullptr,
-                  s);
+  return run_gemm(d, dyq, w_bwd, M, K, N, u, a_direct ? A : ap, 2 * rp, accumulate ? dx : nullptr,
+                  dx, nullptr, s);
 }
 
 // ---------------------------------------------------------------- adapter gradients

@@ -78,6 +78,7 @@ cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const f
                                    int r, int rp, float scale, int64_t K, uint16_t* u_out,
                                    uint16_t* ap_out, cudaStream_t stream);
 
+// (launch_lora_down_dgrad: ap_out null skips the padded copy of A, for r == rp.)
 // LoRA adapter gradients dA [K, r] and dB [r, N] (FP32, overwritten).  Workspace:
 // at_ws [rp, K] and bt_ws [N, rp] (adapter layouts), t_ws and u_ws [M, 2 rp] BF16,
 // part [splits][max(N, K) rp] FP32 with splits = max over the two products of

@@ -355,8 +355,10 @@ static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* g
                             int64_t N, const uint16_t* A, const uint16_t* B, int r, float scale,
                             int64_t K, uint16_t* u_out, uint16_t* ap_out, cudaStream_t stream) {
   constexpr int G = RP <= 32 ? 2 : 1;
-  note_launch();
-  k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
+  if (ap_out) {  // null: A is already [K, RP] (r == RP) and serves as the GEMM operand
+    note_launch();
+    k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
+  }
   note_launch();
   k_lora_down_dgrad<RP, G><<<(int)((M + 16 * G - 1) / (16 * G)), 256, 0, stream>>>(
       dy, gdy, gw, M, N, B, r, scale, 0, u_out);
