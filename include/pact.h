@@ -178,6 +178,26 @@ int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact
                            pact_stream_t stream);
 
 /*
+ * LoRA linear input gradient with the quantisation of dY fused in: the same result
+ * as pact_quant_nvfp4(dy, M, N, N, dy_amax_opt, dyq_out, ...) followed by
+ * pact_lora_linear_dgrad(dyq_out, dy, w_bwd, ...) (the same bytes in dyq_out, the
+ * same dx), with one pass over dY fewer: one kernel encodes dY to NVFP4 and forms
+ * the LoRA down-projection dY B^T from the same loads.
+ *   dy BF16 [M, N], contiguous rows;  dy_amax_opt: optional device FP32 max |dy|
+ *   (e.g. a producer's out_amax; without it an amax pass runs first);
+ *   dyq_out NVFP4 [M, N], caller-owned, written (codes, every scale byte of the
+ *   padded atoms, g) and left for reuse;  the other arguments as for
+ *   pact_lora_linear_dgrad.
+ * Rules as for pact_lora_linear_dgrad, plus pad128(M) * N / 64 < 2^31.
+ * ws: pact_lora_linear_dgrad_q_workspace_size() bytes, 256-byte aligned.
+ */
+size_t pact_lora_linear_dgrad_q_workspace_size(int64_t M, int64_t N, int64_t K, int r);
+int pact_lora_linear_dgrad_q(const uint16_t* dy, const float* dy_amax_opt,
+                             const pact_nvfp4* w_bwd, const uint16_t* A, const uint16_t* B, int r,
+                             float scale, int accumulate, pact_nvfp4* dyq_out, uint16_t* dx,
+                             void* ws, size_t ws_bytes, pact_stream_t stream);
+
+/*
  * LoRA adapter gradients (Table 7: LoRA branch "BF16 adapter gradients"; Figure 1,
  * the trainable A, B beside the frozen NVFP4 projection).  With Xhat the dequantised
  * NVFP4 input that the forward multiplied (the tensor retained for backward):

@@ -20,7 +20,7 @@ __all__ = [
     "NVFP4", "PactError", "load_library", "library_path",
     "pact_quant_nvfp4", "pact_pack_weight_fwd", "pact_pack_weight_bwd",
     "pact_lora_linear_fwd", "pact_lora_linear_fwd_noalloc", "pact_lora_linear_dgrad",
-    "pact_lora_adapter_grad", "pact_rmsnorm_quant",
+    "pact_lora_linear_dgrad_q", "pact_lora_adapter_grad", "pact_rmsnorm_quant",
     "pact_silu_mul_quant", "pact_silu_mul_bwd", "pact_rmsnorm_bwd", "pact_test_pexp",
     "pact_test_wait_timeout", "pact_check_status", "pact_device_supported", "pact_launch_count", "pact_profile_next_gemm",
 ]
@@ -62,6 +62,9 @@ _SIGNATURES = {
     "pact_lora_linear_fwd_noalloc": (_int, [_SP, _SP, _vp, _vp, _int, _f32, _vp, _vp, _vp, _vp]),
     "pact_lora_linear_dgrad_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
     "pact_lora_linear_dgrad": (_int, [_SP, _vp, _SP, _vp, _vp, _int, _f32, _int, _vp, _vp, _sz, _vp]),
+    "pact_lora_linear_dgrad_q_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
+    "pact_lora_linear_dgrad_q": (_int, [_vp, _vp, _SP, _vp, _vp, _int, _f32, _int, _SP, _vp, _vp,
+                                        _sz, _vp]),
     "pact_lora_adapter_grad_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
     "pact_lora_adapter_grad": (_int, [_SP, _vp, _vp, _vp, _int, _f32, _i64, _vp, _vp, _vp, _sz, _vp]),
     "pact_rmsnorm_quant_workspace_size": (_sz, [_i64, _i64]),
@@ -269,6 +272,36 @@ def pact_lora_linear_dgrad(dyq: NVFP4, dy: torch.Tensor, w_bwd: NVFP4, A: torch.
                                       _ptr(B), r, float(scale), int(bool(accumulate)), _ptr(dx),
                                       _ptr(ws), ws.numel(), _stream()))
     return dx
+
+
+def pact_lora_linear_dgrad_q(dy: torch.Tensor, w_bwd: NVFP4, A: torch.Tensor, B: torch.Tensor,
+                             scale: float, amax: torch.Tensor | None = None,
+                             dyq: NVFP4 | None = None, dx: torch.Tensor | None = None,
+                             accumulate: bool = False):
+    """Quantise dY into dyq and run the LoRA-linear input gradient in one call:
+    the same results as pact_quant_nvfp4 + pact_lora_linear_dgrad.  Returns (dx, dyq)."""
+    lib = load_library()
+    _need_cuda(dy, torch.bfloat16, "dy")
+    _need_cuda(A, torch.bfloat16, "A")
+    _need_cuda(B, torch.bfloat16, "B")
+    M, N = dy.shape
+    K = w_bwd.rows
+    r = A.shape[1]
+    if amax is not None:
+        _need_cuda(amax, torch.float32, "amax")
+    if dyq is None:
+        dyq = NVFP4.empty(M, N, dy.device)
+    if dx is None:
+        if accumulate:
+            raise ValueError("accumulate needs dx")
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
+    _need_cuda(dx, torch.bfloat16, "dx")
+    ws = _workspace(lib.pact_lora_linear_dgrad_q_workspace_size(M, N, K, r), dy.device)
+    sq, sw = dyq.struct(), w_bwd.struct()
+    _check(lib.pact_lora_linear_dgrad_q(_ptr(dy), _ptr(amax), ctypes.byref(sw), _ptr(A), _ptr(B),
+                                        r, float(scale), int(bool(accumulate)), ctypes.byref(sq),
+                                        _ptr(dx), _ptr(ws), ws.numel(), _stream()))
+    return dx, dyq
 
 
 def pact_lora_adapter_grad(xq: NVFP4, dy: torch.Tensor, A: torch.Tensor, B: torch.Tensor,

@@ -391,6 +391,48 @@ int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact
                   dx, nullptr, s);
 }
 
+// ---------------------------------------------------------------- dgrad with dY quantisation
+size_t pact_lora_linear_dgrad_q_workspace_size(int64_t M, int64_t N, int64_t K, int r) {
+  const size_t w = pact_lora_linear_dgrad_workspace_size(M, N, K, r);
+  return w ? w + 256 : 0;
+}
+
+int pact_lora_linear_dgrad_q(const uint16_t* dy, const float* dy_amax_opt,
+                             const pact_nvfp4* w_bwd, const uint16_t* A, const uint16_t* B, int r,
+                             float scale, int accumulate, pact_nvfp4* dyq_out, uint16_t* dx,
+                             void* ws, size_t ws_bytes, pact_stream_t stream) {
+  DeviceInfo* d;
+  int rc = device_info(&d);
+  if (rc) return rc;
+  if (!dyq_out || !w_bwd) return fail(PACT_ERR_INVALID_ARG, "dyq_out and w_bwd are required");
+  const int64_t M = dyq_out->rows, N = dyq_out->cols, K = w_bwd->rows;
+  if ((rc = check_gemm_dims(M, N, K, r))) return rc;
+  if (pad_to(M, 128) * (N / 64) >= (int64_t)1 << 31)
+    return fail(PACT_ERR_SHAPE, "tensor too large: pad128(M) * N / 64 must be < 2^31");
+  if ((rc = check_nvfp4(dyq_out, "dyq_out", M, N, 128)) ||
+      (rc = check_nvfp4(w_bwd, "w_bwd", K, N, 128)))
+    return rc;
+  if (!dy || !A || !B || !dx) return fail(PACT_ERR_INVALID_ARG, "dy, A, B and dx are required");
+  if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(B, 8) || !aligned(A, 2) ||
+      (dy_amax_opt && !aligned(dy_amax_opt, 4)))
+    return fail(PACT_ERR_ALIGN, "dx and dy must be 16-byte aligned, B 8-byte aligned");
+  if (!ws || ws_bytes < pact_lora_linear_dgrad_q_workspace_size(M, N, K, r) || !aligned(ws, 256))
+    return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
+  const int rp = rp_for(r);
+  uint16_t* u = (uint16_t*)ws;
+  uint16_t* ap = (uint16_t*)((char*)ws + align256((size_t)M * 2 * rp * 2));
+  unsigned* amax_ws = (unsigned*)((char*)ws + pact_lora_linear_dgrad_workspace_size(M, N, K, r));
+  const bool a_direct = r == rp && aligned(A, 16);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_quant_lora_down(dy, M, N, dy_amax_opt, amax_ws, w_bwd->g, A, B, r, rp,
+                                         scale, K, (uint8_t*)dyq_out->codes,
+                                         (uint8_t*)dyq_out->sf, dyq_out->g, u,
+                                         a_direct ? nullptr : ap, d->sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "quant + lora down launch");
+  return run_gemm(d, dyq_out, w_bwd, M, K, N, u, a_direct ? A : ap, 2 * rp,
+                  accumulate ? dx : nullptr, dx, nullptr, s);
+}
+
 // ---------------------------------------------------------------- adapter gradients
 size_t pact_lora_adapter_grad_workspace_size(int64_t M, int64_t N, int64_t K, int r) {
   if (M < 1 || N < 1 || K < 1 || r < 1 || r > 64) return 0;

@@ -57,6 +57,9 @@ cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, int cm, cuda
 cudaError_t status_word_ptr(unsigned** ptr);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 
+// amax pass alone (contiguous rows): max |x| as FP32 bits into *ws_amax.
+cudaError_t launch_amax_bf16(const uint16_t* x, int64_t M, int64_t K, unsigned* ws_amax,
+                             int num_sms, cudaStream_t stream);
 cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
                               const float* amax_opt, uint8_t* codes, uint8_t* sf, float* g,
                               unsigned* ws_amax, int num_sms, cudaStream_t stream);
@@ -79,6 +82,14 @@ cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const f
                                    uint16_t* ap_out, cudaStream_t stream);
 
 // (launch_lora_down_dgrad: ap_out null skips the padded copy of A, for r == rp.)
+// The same down-projection fused with the NVFP4 quantisation of dY (bit-identical
+// to launch_quant_bf16 and launch_lora_down_dgrad): codes/sf/g of dYq and u_out in
+// one pass over dY.  amax_opt (device) or ws_amax (filled here by an amax pass).
+cudaError_t launch_quant_lora_down(const uint16_t* dy, int64_t M, int64_t N, const float* amax_opt,
+                                   unsigned* ws_amax, const float* gw, const uint16_t* A,
+                                   const uint16_t* B, int r, int rp, float scale, int64_t K,
+                                   uint8_t* codes, uint8_t* sf, float* g, uint16_t* u_out,
+                                   uint16_t* ap_out, int num_sms, cudaStream_t stream);
 // LoRA adapter gradients dA [K, r] and dB [r, N] (FP32, overwritten).  Workspace:
 // at_ws [rp, K] and bt_ws [N, rp] (adapter layouts), t_ws and u_ws [M, 2 rp] BF16,
 // part [splits][max(N, K) rp] FP32 with splits = max over the two products of

@@ -243,24 +243,49 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_fwd(const uint8_t* __restr
   reduce_and_store<RP, G>(acc, red, m0, M, f, t_out);
 }
 
+// The NVFP4 quantisation of dY that k_quant_lora_down performs on the way: the
+// per-tensor amax (given, or from an amax pass) and the code/scale/g outputs.
+struct DyQuant {
+  const float* amax_opt;
+  const unsigned* amax_bits;
+  uint8_t* codes;  // [M, N/2]
+  uint8_t* sf;     // 128x4 atoms, rows padded to 128
+  float* g_out;
+};
+
 // U' = f * (dY B^T): dy [M, N] BF16, B [r, N] row-major.  A chunk is 32 elements
 // of a row: lane c holds elements [8c, 8c + 8) (16 bytes).  N is long here (up to
 // 2 x the intermediate size), so two chunks are in flight ahead of the one being
 // multiplied.
-template <int RP, int G>
+// With QUANT the same pass also quantises dY to NVFP4, byte for byte as the
+// quantiser does (the same block-scale table and element encode): a block of 16 is
+// lanes c and c ^ 1 of a row, so its amax takes one shuffle.  The grid then covers
+// the rows up to the 128-row padding of the scale atoms, whose scales encode zero.
+template <int RP, int G, bool QUANT>
 __global__ void __launch_bounds__(256, 2) k_lora_down_dgrad(const uint16_t* __restrict__ dy,
                                                          const float* __restrict__ gdy,
                                                          const float* __restrict__ gw,
                                                          int64_t M, int64_t N,
                                                          const uint16_t* __restrict__ B, int r,
                                                          float scale, int plain,
-                                                         uint16_t* __restrict__ u_out) {
+                                                         uint16_t* __restrict__ u_out,
+                                                         DyQuant qz) {
   constexpr int NT = RP / 8;
   __shared__ float red[8 * 16 * G * RP];
+  __shared__ ScaleTable tab[1];  // used with QUANT only
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int64_t m0 = (int64_t)blockIdx.x * (16 * G);
   const int nch = (int)(N >> 5);
+  TensorScale tsq = {0.0f, 0.0f};
+  if constexpr (QUANT) {
+    const float amax = qz.amax_opt ? *qz.amax_opt : __uint_as_float(*qz.amax_bits);
+    tsq = tensor_scale(amax);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *qz.g_out = tsq.g;
+    scale_table_init(&tab[0], tsq);
+    __syncthreads();
+  }
+  const int64_t c16p = N >> 4;  // N % 64 == 0: no column padding of the scale atoms
   float acc[G][NT][4];
 #pragma unroll
   for (int gi = 0; gi < G; ++gi)
@@ -319,6 +344,25 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dgrad(const uint16_t* __re
         for (int jn = 0; jn < NT; ++jn) mma_bf16_16816(acc[gi][jn], a, bfr[jn]);
       }
     }
+    if constexpr (QUANT) {
+      // rows g (+ 8) of each group; this lane's 8 elements are columns
+      // 32 ch + 8c .. + 8 of block 2 ch + c / 2
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t row = m0 + 16 * gi + g + 8 * h;
+          uint32_t am = absmax_bf16x8_bits(x0[gi][h]);
+          am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+          float f[8], t, rcp;
+          bf16x8_to_f32(x0[gi][h], f);
+          const uint32_t sc = block_scale_tab(__uint_as_float(am), tsq, &tab[0], &t, &rcp);
+          const uint32_t w = encode8(f, t, rcp);
+          if (row < M)
+            *reinterpret_cast<uint32_t*>(qz.codes + row * (N >> 1) + (int64_t)ch * 16 + 4 * c) = w;
+          if ((c & 1) == 0) qz.sf[sf_offset(row, (int64_t)ch * 2 + (c >> 1), c16p)] = (uint8_t)sc;
+        }
+    }
 #pragma unroll
     for (int gi = 0; gi < G; ++gi)
 #pragma unroll
@@ -330,7 +374,7 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dgrad(const uint16_t* __re
     for (int jn = 0; jn < NT; ++jn) b0[jn] = b1[jn];
   }
   // plain: f = scale, i.e. v = scale * (dY B^T) for the adapter gradients
-  const float s_main = plain ? 0.0f : __fmul_rn(*gdy, *gw);
+  const float s_main = plain ? 0.0f : __fmul_rn(QUANT ? tsq.g : *gdy, *gw);
   const float f = s_main > 0.0f ? __fdiv_rn(scale, s_main) : scale;
   reduce_and_store<RP, G>(acc, red, m0, M, f, u_out);
 }
@@ -360,8 +404,8 @@ static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* g
     k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
   }
   note_launch();
-  k_lora_down_dgrad<RP, G><<<(int)((M + 16 * G - 1) / (16 * G)), 256, 0, stream>>>(
-      dy, gdy, gw, M, N, B, r, scale, 0, u_out);
+  k_lora_down_dgrad<RP, G, false><<<(int)((M + 16 * G - 1) / (16 * G)), 256, 0, stream>>>(
+      dy, gdy, gw, M, N, B, r, scale, 0, u_out, DyQuant{});
   return cudaGetLastError();
 }
 
@@ -386,6 +430,38 @@ cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const f
   if (rp == 16) return dgrad_rp<16>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, stream);
   if (rp == 32) return dgrad_rp<32>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, stream);
   return dgrad_rp<64>(dy, gdy, gw, M, N, A, B, r, scale, K, u_out, ap_out, stream);
+}
+
+template <int RP>
+static cudaError_t quant_dgrad_rp(const uint16_t* dy, int64_t M, int64_t N, DyQuant qz,
+                                  const float* gw, const uint16_t* A, const uint16_t* B, int r,
+                                  float scale, int64_t K, uint16_t* u_out, uint16_t* ap_out,
+                                  cudaStream_t stream) {
+  constexpr int G = RP <= 32 ? 2 : 1;
+  if (ap_out) {
+    note_launch();
+    k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
+  }
+  const int64_t Mpad = pad_to(M, 128);
+  note_launch();
+  k_lora_down_dgrad<RP, G, true><<<(int)(Mpad / (16 * G)), 256, 0, stream>>>(
+      dy, nullptr, gw, M, N, B, r, scale, 0, u_out, qz);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_lora_down(const uint16_t* dy, int64_t M, int64_t N, const float* amax_opt,
+                                   unsigned* ws_amax, const float* gw, const uint16_t* A,
+                                   const uint16_t* B, int r, int rp, float scale, int64_t K,
+                                   uint8_t* codes, uint8_t* sf, float* g, uint16_t* u_out,
+                                   uint16_t* ap_out, int num_sms, cudaStream_t stream) {
+  if (!amax_opt) {
+    cudaError_t e = launch_amax_bf16(dy, M, N, ws_amax, num_sms, stream);
+    if (e != cudaSuccess) return e;
+  }
+  const DyQuant qz{amax_opt, ws_amax, codes, sf, g};
+  if (rp == 16) return quant_dgrad_rp<16>(dy, M, N, qz, gw, A, B, r, scale, K, u_out, ap_out, stream);
+  if (rp == 32) return quant_dgrad_rp<32>(dy, M, N, qz, gw, A, B, r, scale, K, u_out, ap_out, stream);
+  return quant_dgrad_rp<64>(dy, M, N, qz, gw, A, B, r, scale, K, u_out, ap_out, stream);
 }
 
 // ============================================================== adapter gradients
@@ -678,7 +754,8 @@ static cudaError_t adapter_grad_rp(const uint8_t* xc, const uint8_t* xsf, const 
   note_launch();
   k_lora_down_fwd<RP, G><<<mb, 256, 0, stream>>>(xc, xsf, gx, gx, M, K, at_ws, scale, 1, t_ws);
   note_launch();
-  k_lora_down_dgrad<RP, G><<<mb, 256, 0, stream>>>(dy, gx, gx, M, N, B, r, scale, 1, u_ws);
+  k_lora_down_dgrad<RP, G, false><<<mb, 256, 0, stream>>>(dy, gx, gx, M, N, B, r, scale, 1, u_ws,
+                                                          DyQuant{});
   int64_t ns;
   cudaError_t e = launch_ts<RP, false>(dy, nullptr, nullptr, M, N, t_ws, 1, part, &ns, stream);
   if (e != cudaSuccess) return e;

@@ -169,6 +169,15 @@ static int grid_for(int64_t work, int threads, int max_blocks) {
   return (int)b;
 }
 
+cudaError_t launch_amax_bf16(const uint16_t* x, int64_t M, int64_t K, unsigned* ws_amax,
+                             int num_sms, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(ws_amax, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  note_launch();
+  k_amax_bf16<<<grid_for(M * K / 8, 256, num_sms * 4), 256, 0, stream>>>(x, M, K, K, ws_amax);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
                               const float* amax_opt, uint8_t* codes, uint8_t* sf, float* g,
                               unsigned* ws_amax, int num_sms, cudaStream_t stream) {

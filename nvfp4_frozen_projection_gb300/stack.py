@@ -16,7 +16,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (NVFP4, pact_lora_linear_dgrad, pact_lora_linear_fwd, pact_pack_weight_bwd,
+from . import (NVFP4, pact_lora_linear_dgrad, pact_lora_linear_dgrad_q, pact_lora_linear_fwd,
+               pact_pack_weight_bwd,
                pact_lora_adapter_grad, pact_pack_weight_fwd, pact_quant_nvfp4, pact_rmsnorm_bwd,
                pact_rmsnorm_quant,
                pact_silu_mul_bwd, pact_silu_mul_quant)
@@ -39,6 +40,12 @@ class LoraLinear:
     def dgrad(self, dyq: NVFP4, dy: torch.Tensor, dx: torch.Tensor, accumulate=False):
         return pact_lora_linear_dgrad(dyq, dy, self.w_bwd, self.A, self.B, self.scale, dx=dx,
                                       accumulate=accumulate)
+
+    def dgrad_q(self, dy: torch.Tensor, dyq: NVFP4, dx: torch.Tensor, amax=None,
+                accumulate=False):
+        """Quantise dy into dyq and run the input gradient, in one pass over dy."""
+        return pact_lora_linear_dgrad_q(dy, self.w_bwd, self.A, self.B, self.scale, amax=amax,
+                                        dyq=dyq, dx=dx, accumulate=accumulate)
 
     def adapter_grad(self, xq: NVFP4, dy: torch.Tensor, dA=None, dB=None):
         return pact_lora_adapter_grad(xq, dy, self.A, self.B, self.scale, dA=dA, dB=dB)
@@ -121,19 +128,16 @@ class DecoderProjectionStack:
         """dy: gradient of the layer output; dq and dkv (dk | dv): the gradients
         flowing back from the (out of scope) attention core into the q/k/v outputs."""
         p = self.p
-        pact_quant_nvfp4(dy, out=self.dyq)
-        p["down"].dgrad(self.dyq, dy, self.dh)
+        # every input gradient quantises its dY in the same pass that forms the
+        # LoRA down-projection (pact_lora_linear_dgrad_q)
+        p["down"].dgrad_q(dy, self.dyq, self.dh)
         pact_silu_mul_bwd(self.gq, self.uq, self.dh, dgateup=self.dgu, out_amax=self.dgu_amax)
-        pact_quant_nvfp4(self.dgu, amax=self.dgu_amax, out=self.dguq)
-        p["gate_up"].dgrad(self.dguq, self.dgu, self.dxn2)
+        p["gate_up"].dgrad_q(self.dgu, self.dguq, self.dxn2, amax=self.dgu_amax)
         pact_rmsnorm_bwd(self.xq2, self.gamma2, self.rstd2, self.dxn2, dres=dy, dx=self.dh1,
                          out_amax=self.dh1_amax)
-        pact_quant_nvfp4(self.dh1, amax=self.dh1_amax, out=self.dh1q)
-        p["o"].dgrad(self.dh1q, self.dh1, self.dattn)  # into the attention core
-        pact_quant_nvfp4(dq, out=self.dqq)
-        pact_quant_nvfp4(dkv, out=self.dkvq)
-        p["q"].dgrad(self.dqq, dq, self.dxn1)
-        p["kv"].dgrad(self.dkvq, dkv, self.dxn1, accumulate=True)
+        p["o"].dgrad_q(self.dh1, self.dh1q, self.dattn, amax=self.dh1_amax)  # into attention
+        p["q"].dgrad_q(dq, self.dqq, self.dxn1)
+        p["kv"].dgrad_q(dkv, self.dkvq, self.dxn1, accumulate=True)
         pact_rmsnorm_bwd(self.xq1, self.gamma1, self.rstd1, self.dxn1, dres=self.dh1, dx=self.dx)
         return self.dx
 
