@@ -61,8 +61,11 @@ class DecoderProjectionStack:
     (k | v) and gate_up (gate | up), each with its adapters side by side and B
     block-diagonal."""
 
-    def __init__(self, m: int, proj: dict, gamma1, gamma2, eps: float = 1e-5):
+    def __init__(self, m: int, proj: dict, gamma1, gamma2, eps: float = 1e-5,
+                 concurrent: bool = True):
         self.m = m
+        self.concurrent = concurrent
+        self._side_stream = None
         self.p = proj  # q, kv, o, gate_up, down -> LoraLinear
         self.gamma1, self.gamma2, self.eps = gamma1, gamma2, float(eps)
         hidden = proj["q"].d_in
@@ -100,14 +103,33 @@ class DecoderProjectionStack:
         self.dxn1 = torch.empty(m, hidden, **bf)
         self.dx = torch.empty(m, hidden, **bf)
 
+    def _side(self):
+        """A second stream for work independent of the main chain: its kernels fill
+        the SMs that a persistent GEMM's last tiles leave idle.  Forked from and
+        joined back into the current stream, so graph capture records both."""
+        if self.concurrent is False:
+            return None
+        if self._side_stream is None:
+            self._side_stream = torch.cuda.Stream(device=self.gamma1.device)
+        return self._side_stream
+
     def forward(self, x: torch.Tensor, attn: torch.Tensor) -> torch.Tensor:
         p = self.p
+        main, side = torch.cuda.current_stream(), self._side()
+        if side is not None:
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                # attention core (out of scope): its output is the given tensor attn
+                pact_quant_nvfp4(attn, out=self.attnq)
+                p["o"].forward(self.attnq, self.h1, residual=x)
         pact_rmsnorm_quant(x, self.gamma1, self.eps, out=self.xq1, rstd=self.rstd1)
         p["q"].forward(self.xq1, self.q)
         p["kv"].forward(self.xq1, self.kv)
-        # attention core (out of scope): its output is the given tensor attn
-        pact_quant_nvfp4(attn, out=self.attnq)
-        p["o"].forward(self.attnq, self.h1, residual=x)
+        if side is None:
+            pact_quant_nvfp4(attn, out=self.attnq)
+            p["o"].forward(self.attnq, self.h1, residual=x)
+        else:
+            main.wait_stream(side)
         pact_rmsnorm_quant(self.h1, self.gamma2, self.eps, out=self.xq2, rstd=self.rstd2)
         p["gate_up"].forward(self.xq2, self.gu)
         pact_silu_mul_quant(self.gu, outs=(self.hq, self.gq, self.uq))
@@ -128,16 +150,27 @@ class DecoderProjectionStack:
         """dy: gradient of the layer output; dq and dkv (dk | dv): the gradients
         flowing back from the (out of scope) attention core into the q/k/v outputs."""
         p = self.p
+        main, side = torch.cuda.current_stream(), self._side()
         # every input gradient quantises its dY in the same pass that forms the
-        # LoRA down-projection (pact_lora_linear_dgrad_q)
+        # LoRA down-projection (pact_lora_linear_dgrad_q).  The q and k|v input
+        # gradients need only the attention core's gradients: they run beside the
+        # down -> SiLU -> gate|up -> RMSNorm -> o chain.
+        if side is not None:
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                p["q"].dgrad_q(dq, self.dqq, self.dxn1)
+                p["kv"].dgrad_q(dkv, self.dkvq, self.dxn1, accumulate=True)
         p["down"].dgrad_q(dy, self.dyq, self.dh)
         pact_silu_mul_bwd(self.gq, self.uq, self.dh, dgateup=self.dgu, out_amax=self.dgu_amax)
         p["gate_up"].dgrad_q(self.dgu, self.dguq, self.dxn2, amax=self.dgu_amax)
         pact_rmsnorm_bwd(self.xq2, self.gamma2, self.rstd2, self.dxn2, dres=dy, dx=self.dh1,
                          out_amax=self.dh1_amax)
         p["o"].dgrad_q(self.dh1, self.dh1q, self.dattn, amax=self.dh1_amax)  # into attention
-        p["q"].dgrad_q(dq, self.dqq, self.dxn1)
-        p["kv"].dgrad_q(dkv, self.dkvq, self.dxn1, accumulate=True)
+        if side is None:
+            p["q"].dgrad_q(dq, self.dqq, self.dxn1)
+            p["kv"].dgrad_q(dkv, self.dkvq, self.dxn1, accumulate=True)
+        else:
+            main.wait_stream(side)
         pact_rmsnorm_bwd(self.xq1, self.gamma1, self.rstd1, self.dxn1, dres=self.dh1, dx=self.dx)
         return self.dx
 
