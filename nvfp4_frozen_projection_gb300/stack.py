@@ -65,7 +65,7 @@ class DecoderProjectionStack:
                  concurrent: bool = True):
         self.m = m
         self.concurrent = concurrent
-        self._side_stream = None
+        self._side_streams = []
         self.p = proj  # q, kv, o, gate_up, down -> LoraLinear
         self.gamma1, self.gamma2, self.eps = gamma1, gamma2, float(eps)
         hidden = proj["q"].d_in
@@ -103,15 +103,15 @@ class DecoderProjectionStack:
         self.dxn1 = torch.empty(m, hidden, **bf)
         self.dx = torch.empty(m, hidden, **bf)
 
-    def _side(self):
-        """A second stream for work independent of the main chain: its kernels fill
+    def _side(self, i: int = 0):
+        """Side stream i for work independent of the main chain: its kernels fill
         the SMs that a persistent GEMM's last tiles leave idle.  Forked from and
-        joined back into the current stream, so graph capture records both."""
+        joined back into the current stream, so graph capture records every branch."""
         if self.concurrent is False:
             return None
-        if self._side_stream is None:
-            self._side_stream = torch.cuda.Stream(device=self.gamma1.device)
-        return self._side_stream
+        while len(self._side_streams) <= i:
+            self._side_streams.append(torch.cuda.Stream(device=self.gamma1.device))
+        return self._side_streams[i]
 
     def forward(self, x: torch.Tensor, attn: torch.Tensor) -> torch.Tensor:
         p = self.p
@@ -123,8 +123,16 @@ class DecoderProjectionStack:
                 pact_quant_nvfp4(attn, out=self.attnq)
                 p["o"].forward(self.attnq, self.h1, residual=x)
         pact_rmsnorm_quant(x, self.gamma1, self.eps, out=self.xq1, rstd=self.rstd1)
+        side2 = self._side(1)
+        if side2 is not None:  # q and k|v both read xq1 only: run them side by side
+            side2.wait_stream(main)
+            with torch.cuda.stream(side2):
+                p["kv"].forward(self.xq1, self.kv)
         p["q"].forward(self.xq1, self.q)
-        p["kv"].forward(self.xq1, self.kv)
+        if side2 is None:
+            p["kv"].forward(self.xq1, self.kv)
+        else:
+            main.wait_stream(side2)
         if side is None:
             pact_quant_nvfp4(attn, out=self.attnq)
             p["o"].forward(self.attnq, self.h1, residual=x)
