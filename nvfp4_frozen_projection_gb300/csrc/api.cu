@@ -285,7 +285,8 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   if ((rc = make_map(&L.tmLA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, la, rpe, M, abox, 128,
                      lsw(abox))))
     return rc;
-  if ((rc = make_map(&L.tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lb, rp, Nout, bbox, bn,
+  const uint32_t lb_rows = gemm_uses_pair(M, Nout, rpe) ? (uint32_t)bn / 2 : (uint32_t)bn;
+  if ((rc = make_map(&L.tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lb, rp, Nout, bbox, lb_rows,
                      lsw(bbox))))
     return rc;
   // output: 32 x 32 BF16 blocks written by TMA stores from the epilogue's 64-byte

@@ -54,14 +54,18 @@ constexpr int kStageK = 256;
 // Shared memory: [ring: STAGES x (A | B | SFA | SFB)] [LA] [LB] [epilogue staging]
 // [barriers].  A stage's scale factors travel with its A/B tiles (loaded after
 // them, on the same barrier): issuing them apart or ahead measured slower.
-template <int BN, int BK, int STAGES, int RPE>
+// PAIR: the tile is computed by a CTA pair with .cta_group::2 MMAs (M = 256 over the
+// pair): each CTA holds its 128 A rows and half of the B tile (and of the LoRA
+// up-projection rows); the scale factors of all BN B rows are staged in both.
+template <int BN, int BK, int STAGES, int RPE, bool PAIR = false>
 struct GemmCfg {
   static constexpr int BM = 128;
   static constexpr int ROWB = BK / 2;   // bytes of one tile row per stage
   static constexpr int KSUB = BK / 64;  // K=64 MMAs per stage
   static constexpr int NRB = BN / 128;  // 128-row scale atoms of the B tile
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows in this CTA's shared memory
   static constexpr int A_BYTES = BM * ROWB;
-  static constexpr int B_BYTES = BN * ROWB;
+  static constexpr int B_BYTES = B_ROWS * ROWB;
   static constexpr int SFA_BYTES = KSUB * 512;
   static constexpr int SFB_BYTES = NRB * KSUB * 512;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
@@ -74,7 +78,7 @@ struct GemmCfg {
   static constexpr int NLA = RPE * 2 / LA_CH;
   static constexpr int NLB = RP * 2 / LB_CH;
   static constexpr int LA_CHUNK = BM * LA_CH;
-  static constexpr int LB_CHUNK = BN * LB_CH;
+  static constexpr int LB_CHUNK = B_ROWS * LB_CH;
   static constexpr int LA_OFF = STAGES * STAGE_BYTES;
   static constexpr int LA_BYTES = NLA * LA_CHUNK;
   static constexpr int LB_OFF = LA_OFF + LA_BYTES;
@@ -107,8 +111,8 @@ struct GemmCfg {
   static constexpr int SFA_TCOLS = 4 * KSUB;        // TMEM columns of a stage's A scales
   static constexpr int SFB_TCOLS = 4 * KSUB * NRB;  // ... and B scales
   // barriers (8 bytes each): full[S], empty[S], sf_full[S] (the stage's scales are
-  // in TMEM), then lora_full, lora_empty, acc_full, acc_empty, final
-  static constexpr int NBARS = 3 * STAGES + 5;
+  // in TMEM), then lora_full, lora_empty, acc_full, acc_empty, final, lora_peer
+  static constexpr int NBARS = 3 * STAGES + 6;
   static_assert((SFA_TCOLS == 8 || SFA_TCOLS == 16) &&
                     (SFB_TCOLS == 8 || SFB_TCOLS == 16 || SFB_TCOLS == 32),
                 "SF staging shapes");
@@ -123,15 +127,15 @@ struct GemmCfg {
   static_assert(NBARS * 8 <= 504, "barrier area");
 };
 
-// Instruction descriptors (M = 128, K-major A and B, dense).
-__host__ __device__ constexpr uint32_t idesc_nvf4(int n) {
+// Instruction descriptors (M = 128, or 256 for a CTA pair; K-major A and B, dense).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int n, int m = 128) {
   // atype = btype = E2M1 (1), scale type UE4M3 (bit 23 = 0)
-  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+__host__ __device__ constexpr uint32_t idesc_bf16(int n, int m = 128) {
   // D = F32 (bits 4-5 = 1), A = B = BF16 (1)
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(128 >> 4) << 24);
+         ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void raise_error(volatile uint32_t* abort_flag, unsigned* status,
@@ -144,13 +148,19 @@ __device__ __forceinline__ void raise_error(volatile uint32_t* abort_flag, unsig
 // compute the tiles (m, n) and (m + 1, n) in lock step: each loads half of the
 // shared B tile and multicasts it to both, so every B byte leaves L2 once per pair,
 // and a stage is refilled only after both CTAs' MMAs released it.
-template <int BN, int BK, int STAGES, int RPE, int CM>
+// PAIR (CM = 2): the two CTAs of a cluster compute the tiles (m, n) and (m + 1, n)
+// as one M = 256 pair MMA issued by the even CTA ("leader"): each CTA loads its A
+// tile and half of the B tile (no multicast), stages its scale factors into its own
+// TMEM and reports to the leader's barriers (sf_full, acc_empty, lora_peer); the
+// leader's commits reach both CTAs.
+template <int BN, int BK, int STAGES, int RPE, int CM, bool PAIR = false>
 __global__ void __launch_bounds__(448, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmLA,
                  const __grid_constant__ CUtensorMap tmLB,
                  const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  using C = GemmCfg<BN, BK, STAGES, RPE>;
+  static_assert(!PAIR || CM == 2, "a pair is a cluster of two");
+  using C = GemmCfg<BN, BK, STAGES, RPE, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -163,6 +173,7 @@ __global__ void __launch_bounds__(448, 1)
   const uint32_t acc_full = lora_full + 16;
   const uint32_t acc_empty = lora_full + 24;
   const uint32_t final_bar = lora_full + 32;
+  const uint32_t lora_peer = lora_full + 40;  // PAIR: the peer's LoRA operands landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 504);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 508);
 
@@ -203,14 +214,17 @@ __global__ void __launch_bounds__(448, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, CM);
-      mbar_init(sf_full0 + 8 * s, 128);
+      // PAIR: one multicast commit from the leader; else one from each CTA
+      mbar_init(empty0 + 8 * s, PAIR ? 1 : CM);
+      // PAIR: one arrival per scale-staging warp of both CTAs (at the leader)
+      mbar_init(sf_full0 + 8 * s, PAIR ? 8 : 128);
     }
     mbar_init(lora_full, 1);
     mbar_init(lora_empty, 1);
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, C::EPI_THREADS);
+    mbar_init(acc_empty, PAIR ? 16 : C::EPI_THREADS);  // PAIR: one per epilogue warp, both CTAs
     mbar_init(final_bar, 1);
+    mbar_init(lora_peer, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -224,8 +238,13 @@ __global__ void __launch_bounds__(448, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_addr(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -257,7 +276,8 @@ __global__ void __launch_bounds__(448, 1)
             tma_load_2d(base + C::LA_OFF + c * C::LA_CHUNK, &tmLA, 64 * c, m0, lora_full);
 #pragma unroll
           for (int c = 0; c < C::NLB; ++c)
-            tma_load_2d(base + C::LB_OFF + c * C::LB_CHUNK, &tmLB, 64 * c, n0, lora_full);
+            tma_load_2d(base + C::LB_OFF + c * C::LB_CHUNK, &tmLB, 64 * c,
+                        PAIR ? n0 + (int)crank * C::B_ROWS : n0, lora_full);
           lpend = 1u;
           lpend_par = lphase;
           lphase ^= 1u;
@@ -279,7 +299,9 @@ __global__ void __launch_bounds__(448, 1)
           const uint32_t sb = base + stage * C::STAGE_BYTES;
           mbar_expect_tx(fb, C::A_BYTES + C::B_BYTES + (uint32_t)(ksub * 512 * (1 + nrb)));
           tma_load_2d(sb, &tmA, ks * C::ROWB, m0, fb);
-          if constexpr (CM > 1)
+          if constexpr (PAIR)
+            tma_load_2d(sb + C::A_BYTES, &tmB, ks * C::ROWB, nb, fb);
+          else if constexpr (CM > 1)
             tma_load_2d_mc(sb + C::A_BYTES + crank * (C::B_BYTES / CM), &tmB, ks * C::ROWB, nb,
                            fb, (uint16_t)((1u << CM) - 1u));
           else
@@ -317,21 +339,48 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (PAIR && crank != 0) {
+      // the peer: tell the leader when this CTA's LoRA operands have landed
+      if (lane == 0 && p.lora_steps) {
+        uint32_t lphase = 0;
+        for (int u = unit0; u < nunits; u += nclusters) {
+          if (!mbar_wait(lora_full, lphase, kWaitLimitNs, abort_flag)) {
+            raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_MMA);
+            break;
+          }
+          mbar_arrive_cta(lora_peer, 0);
+          lphase ^= 1u;
+        }
+      }
+    } else if (lane == 0) {
       uint32_t lphase = 0, aphase = 0, phase = 0;
       int stage = 0;
       bool ok = true;
-      const uint32_t idesc = idesc_nvf4(BN);
-      const uint32_t idesc_l = idesc_bf16(BN);
+      constexpr int MM = PAIR ? 256 : 128;
+      const uint32_t idesc = idesc_nvf4(BN, MM);
+      const uint32_t idesc_l = idesc_bf16(BN, MM);
+      auto wait_x = [&](uint32_t bar, uint32_t par) {  // barriers the peer also arrives on
+        return PAIR ? mbar_wait_cluster(bar, par, kWaitLimitNs, abort_flag)
+                    : mbar_wait(bar, par, kWaitLimitNs, abort_flag);
+      };
+      auto commit_all = [&](uint32_t bar) {  // reaches both CTAs of a cluster
+        if constexpr (PAIR)
+          mma_commit_pair(bar, (uint16_t)3u);
+        else if constexpr (CM > 1)
+          mma_commit_mc(bar, (uint16_t)((1u << CM) - 1u));
+        else
+          mma_commit(bar);
+      };
       for (int u = unit0; u < nunits && ok; u += nclusters) {
-        if (!mbar_wait(acc_empty, aphase ^ 1u, kWaitLimitNs, abort_flag)) {
+        if (!wait_x(acc_empty, aphase ^ 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t accum = 0;
         if (p.lora_steps) {
-          if (!mbar_wait(lora_full, lphase, kWaitLimitNs, abort_flag)) {
+          if (!mbar_wait(lora_full, lphase, kWaitLimitNs, abort_flag) ||
+              (PAIR && !wait_x(lora_peer, lphase))) {
             ok = false;
             break;
           }
@@ -346,15 +395,22 @@ __global__ void __launch_bounds__(448, 1)
             const uint64_t db = smem_desc(base + C::LB_OFF + (jb / C::LB_STEPS) * C::LB_CHUNK +
                                               32u * (uint32_t)(jb % C::LB_STEPS),
                                           16, C::LB_SBO, C::LB_SWZ);
-            mma_bf16(tmem, da, db, idesc_l, accum);
+            if constexpr (PAIR)
+              mma_bf16_pair(tmem, da, db, idesc_l, accum);
+            else
+              mma_bf16(tmem, da, db, idesc_l, accum);
             accum = 1;
           }
-          mma_commit(lora_empty);
+          if constexpr (PAIR)
+            commit_all(lora_empty);
+          else
+            mma_commit(lora_empty);
           lphase ^= 1u;
         }
         for (int ks = 0; ks < nks; ++ks) {
-          // the stage's A/B tiles are in shared memory and its scales in TMEM
-          if (!mbar_wait(sf_full0 + 8 * stage, phase, kWaitLimitNs, abort_flag)) {
+          // the stage's A/B tiles are in shared memory and its scales in TMEM (for a
+          // pair: in both CTAs)
+          if (!wait_x(sf_full0 + 8 * stage, phase)) {
             ok = false;
             break;
           }
@@ -365,25 +421,33 @@ __global__ void __launch_bounds__(448, 1)
           for (int j = 0; j < ksub; ++j) {
             const uint64_t da = smem_desc(sb + 32 * j, 16, C::AB_SBO, C::AB_SWZ);
             const uint64_t db = smem_desc(sb + C::A_BYTES + 32 * j, 16, C::AB_SBO, C::AB_SWZ);
-            mma_nvf4(tmem, da, db, idesc, tsf + 4 * j, tsf + 4 * C::KSUB + j * C::NRB * 4, accum);
+            if constexpr (PAIR)
+              mma_nvf4_pair(tmem, da, db, idesc, tsf + 4 * j, tsf + 4 * C::KSUB + j * C::NRB * 4,
+                            accum);
+            else
+              mma_nvf4(tmem, da, db, idesc, tsf + 4 * j, tsf + 4 * C::KSUB + j * C::NRB * 4,
+                       accum);
             accum = 1;
           }
-          if constexpr (CM > 1)
-            mma_commit_mc(empty0 + 8 * stage, (uint16_t)((1u << CM) - 1u));
-          else
-            mma_commit(empty0 + 8 * stage);
+          commit_all(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(acc_full);
+        if constexpr (PAIR)
+          commit_all(acc_full);
+        else
+          mma_commit(acc_full);
         aphase ^= 1u;
       }
       if (!ok) raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_MMA);
       // every MMA issued by this thread has completed once final_bar flips
-      mma_commit(final_bar);
+      if constexpr (PAIR)
+        mma_commit_pair(final_bar, (uint16_t)1u);
+      else
+        mma_commit(final_bar);
       mbar_wait(final_bar, 0, kWaitLimitNs, nullptr);
     }
   } else if (warp >= C::SF_WARP0 && warp < C::SF_WARP0 + 4) {
@@ -433,7 +497,13 @@ __global__ void __launch_bounds__(448, 1)
       tmem_st<C::SFB_TCOLS>(tsf + C::SFA_TCOLS, vb);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(sf_full0 + 8 * stage);
+      if constexpr (PAIR) {
+        // one arrival per warp, at the leader (which issues the pair MMAs)
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cta_relaxed(sf_full0 + 8 * stage, 0u);
+      } else {
+        mbar_arrive(sf_full0 + 8 * stage);
+      }
       if (++stage == STAGES) {
         stage = 0;
         phase ^= 1u;
@@ -502,7 +572,8 @@ __global__ void __launch_bounds__(448, 1)
           for (int i = 0; i < 16; ++i) out[ch][i] = 0u;
         }
       }
-      if (!mbar_wait(acc_full, aphase, kWaitLimitNs, abort_flag)) {
+      if (!(PAIR ? mbar_wait_cluster(acc_full, aphase, kWaitLimitNs, abort_flag)
+                 : mbar_wait(acc_full, aphase, kWaitLimitNs, abort_flag))) {
         raise_error(abort_flag, p.status, PACT_DEV_TIMEOUT | PACT_DEV_ROLE_EPI);
         break;
       }
@@ -524,7 +595,12 @@ __global__ void __launch_bounds__(448, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(acc_empty);
+      if constexpr (PAIR) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cta_relaxed(acc_empty, 0u);  // at the leader
+      } else {
+        mbar_arrive(acc_empty);
+      }
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) {
         const int n = n0 + c0 + 32 * ch;
@@ -570,15 +646,18 @@ __global__ void __launch_bounds__(448, 1)
   if constexpr (CM > 1) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
 // ---------------------------------------------------------------- host side
-template <int BN, int BK, int STAGES, int RPE, int CM>
+template <int BN, int BK, int STAGES, int RPE, int CM, bool PAIR = false>
 static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
-  using C = GemmCfg<BN, BK, STAGES, RPE>;
-  auto kern = k_gemm_nvfp4<BN, BK, STAGES, RPE, CM>;
+  using C = GemmCfg<BN, BK, STAGES, RPE, PAIR>;
+  auto kern = k_gemm_nvfp4<BN, BK, STAGES, RPE, CM, PAIR>;
   // per device: shared-memory attribute set, and how many clusters fit at once
   static int max_clusters[64] = {};
   int dev = 0;
@@ -634,13 +713,20 @@ int gemm_cluster_m(int64_t M) { return (PACT_GEMM_CM > 1 && M > 128) ? 2 : 1; }
 
 int gemm_stage_row_bytes() { return kStageK / 2; }
 
+bool gemm_pair_enabled() { return true; }
+
+bool gemm_uses_pair(int64_t M, int64_t N, int rpe) {
+  return gemm_pair_enabled() && gemm_cluster_m(M) == 2 && gemm_block_n(N, rpe) == 256;
+}
+
 // Ring depth: as many stages as shared memory holds next to the LoRA operands and
 // one staging buffer per epilogue warp, within the TMEM left for scale factors, at
 // most 10.
-template <int BN, int BK, int RPE>
+template <int BN, int BK, int RPE, bool PAIR = false>
 constexpr int ring_stages() {
-  constexpr int stage = 128 * BK / 2 + BN * BK / 2 + (BK / 64) * 512 * (1 + BN / 128);
-  constexpr int fixed = 128 * RPE * 2 + BN * (RPE / 2) * 2 + 8 * 2048 + 1536;
+  constexpr int brows = PAIR ? BN / 2 : BN;  // B rows held by one CTA
+  constexpr int stage = 128 * BK / 2 + brows * BK / 2 + (BK / 64) * 512 * (1 + BN / 128);
+  constexpr int fixed = 128 * RPE * 2 + brows * (RPE / 2) * 2 + 8 * 2048 + 1536;
   constexpr int by_smem = (232448 - fixed) / stage;
   constexpr int by_tmem = 256 / (4 * (BK / 64) * (1 + BN / 128));
   constexpr int s = by_smem < by_tmem ? by_smem : by_tmem;
@@ -652,9 +738,18 @@ static cudaError_t launch_one(const GemmLaunch& L, cudaStream_t stream) {
   return launch_cfg<BN, kStageK, ring_stages<BN, kStageK, RPE>(), RPE, CM>(L, stream);
 }
 
+template <int BN, int RPE>
+static cudaError_t launch_pair(const GemmLaunch& L, cudaStream_t stream) {
+  return launch_cfg<BN, kStageK, ring_stages<BN, kStageK, RPE, true>(), RPE, 2, true>(L, stream);
+}
+
 template <int CM>
 static cudaError_t launch_cm(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream) {
   if (bn == 256) {
+    if (CM == 2 && gemm_pair_enabled()) {
+      if (rpe == 32) return launch_pair<256, 32>(L, stream);
+      return launch_pair<256, 64>(L, stream);
+    }
     if (rpe == 32) return launch_one<256, 32, CM>(L, stream);
     return launch_one<256, 64, CM>(L, stream);
   }

@@ -53,6 +53,10 @@ int gemm_cluster_m(int64_t M);
 // Bytes of K per A/B tile row in one ring stage (the TMA box width; 64 -> 64B
 // swizzle, 128 -> 128B swizzle).
 int gemm_stage_row_bytes();
+// Whether tiles are computed by CTA pairs (.cta_group::2): each CTA then holds half
+// of the B and LoRA up-projection rows of a tile (their tensor-map boxes are bn/2).
+bool gemm_pair_enabled();
+bool gemm_uses_pair(int64_t M, int64_t N, int rpe);
 cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, int cm, cudaStream_t stream);
 cudaError_t status_word_ptr(unsigned** ptr);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
