@@ -9,6 +9,8 @@ Cases (M = tokens; the other sizes are the Llama-3B layer's):
   silu                SiLU-multiply -> NVFP4 of a BF16 [M, 2 x 8192] tensor
   lora-down-fwd       the q projection's forward (down-projection + GEMM)
   gemm-o-fwd          the o projection's forward: the same GEMM plus the residual add
+  dgrad-q-gate-up     the fused gate|up input gradient (dY quantised inside the LoRA
+                      down-projection, then the GEMM): pact_lora_linear_dgrad_q
   adapter-grad-q      dA, dB of the q projection (3072 -> 3072, r = 16)
   adapter-grad-gate-up  dA, dB of the fused gate|up projection (3072 -> 2 x 8192, r = 32)
 
@@ -23,6 +25,7 @@ import argparse
 import torch
 
 from . import (pact_check_status, pact_lora_adapter_grad, pact_lora_linear_dgrad,
+               pact_lora_linear_dgrad_q,
                pact_lora_linear_fwd, pact_pack_weight_bwd, pact_pack_weight_fwd,
                pact_quant_nvfp4, pact_silu_mul_quant)
 
@@ -48,6 +51,15 @@ def run(case: str, m: int, reps: int) -> None:
         dx = torch.empty(m, HIDDEN, dtype=torch.bfloat16, device=dev)
         for _ in range(reps):
             pact_lora_linear_dgrad(dyq, dy, wb, A, B, 2.0, dx=dx)
+    elif case == "dgrad-q-gate-up":
+        W, A, B = _lora(HIDDEN, 2 * INTER, 32, dev, gen)
+        wb = pact_pack_weight_bwd(W)
+        dy = (torch.randn(m, 2 * INTER, device=dev, generator=gen) * 0.01).bfloat16()
+        amax = dy.float().abs().max().reshape(1)
+        dx = torch.empty(m, HIDDEN, dtype=torch.bfloat16, device=dev)
+        dyq = None
+        for _ in range(reps):
+            dx, dyq = pact_lora_linear_dgrad_q(dy, wb, A, B, 2.0, amax=amax, dyq=dyq, dx=dx)
     elif case in ("gemm-gate-up-fwd", "lora-down-fwd", "gemm-o-fwd"):
         n_out = 2 * INTER if case == "gemm-gate-up-fwd" else HIDDEN
         r = 32 if case == "gemm-gate-up-fwd" else 16
