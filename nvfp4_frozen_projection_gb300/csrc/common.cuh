@@ -95,10 +95,35 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
 __device__ __forceinline__ uint32_t encode8(const float* x, float t, float rcp) {
   uint32_t w = 0;
   if (t > 0.0f && rcp <= 3.4028234663852886e38f) {
-    // x * rcp keeps the sign of x (rcp > 0) and the convert keeps it on zeros
-#pragma unroll
-    for (int i = 0; i < 8; i += 2)
-      w |= e2m1x2_mag(__fmul_rn(x[i], rcp), __fmul_rn(x[i + 1], rcp)) << (4 * i);
+    // x * rcp keeps the sign of x (rcp > 0) and the convert keeps it on zeros.  The
+    // products are formed two at a time (mul.rn.f32x2 rounds each lane as mul.rn.f32
+    // does) and the four code bytes are packed by one vector move.
+    asm("{\n\t"
+        ".reg .b64 rr, p0, p1, p2, p3;\n\t"
+        ".reg .f32 q0, q1, q2, q3, q4, q5, q6, q7;\n\t"
+        ".reg .b8 c0, c1, c2, c3;\n\t"
+        "mov.b64 rr, {%9, %9};\n\t"
+        "mov.b64 p0, {%1, %2};\n\t"
+        "mov.b64 p1, {%3, %4};\n\t"
+        "mov.b64 p2, {%5, %6};\n\t"
+        "mov.b64 p3, {%7, %8};\n\t"
+        "mul.rn.f32x2 p0, p0, rr;\n\t"
+        "mul.rn.f32x2 p1, p1, rr;\n\t"
+        "mul.rn.f32x2 p2, p2, rr;\n\t"
+        "mul.rn.f32x2 p3, p3, rr;\n\t"
+        "mov.b64 {q0, q1}, p0;\n\t"
+        "mov.b64 {q2, q3}, p1;\n\t"
+        "mov.b64 {q4, q5}, p2;\n\t"
+        "mov.b64 {q6, q7}, p3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c0, q1, q0;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c1, q3, q2;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c2, q5, q4;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c3, q7, q6;\n\t"
+        "mov.b32 %0, {c0, c1, c2, c3};\n\t"
+        "}"
+        : "=r"(w)
+        : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+          "f"(x[7]), "f"(rcp));
     return w;
   }
 #pragma unroll
