@@ -289,6 +289,17 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   if ((rc = make_map(&L.tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lb, rp, Nout, bbox, lb_rows,
                      lsw(bbox))))
     return rc;
+  // scale factors: each 128-row block is one row of k16p / 4 atoms (512 bytes each),
+  // read as 8-byte elements; a stage takes 4 atoms (2 KB) of one A block and of the
+  // bn / 128 B blocks of its tile (zero fill past K and past the last block)
+  const uint64_t sf_row = (uint64_t)pad_to(Kr / 16, 4) * 16;  // 8-byte elements per block row
+  if ((rc = make_map(&L.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, a->sf, sf_row,
+                     (uint64_t)pad_to(M, 128) / 128, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE)))
+    return rc;
+  if ((rc = make_map(&L.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, b->sf, sf_row,
+                     (uint64_t)pad_to(Nout, 128) / 128, 256, (uint32_t)bn / 128,
+                     CU_TENSOR_MAP_SWIZZLE_NONE)))
+    return rc;
   // output: 32 x 32 BF16 blocks written by TMA stores from the epilogue's 64-byte
   // swizzled staging buffers
   if ((rc = make_map(&L.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, Nout, M, 32, 32,

@@ -22,7 +22,8 @@
 // along M (when M spans more than one tile) and share each B tile by multicast.
 //   warp 0      TMA producer: A/B tiles (128-byte rows, 128B swizzle; one 16 KB
 //               A box and half of the B tile per CTA, multicast to the pair) and
-//               the scale-factor atoms (plain bulk copies) into a STAGES-deep
+//               the scale-factor atoms (tiled copies: one box of 4 atoms per
+//               row block; plain bulk copies measured ~8 % slower) into a STAGES-deep
 //               shared-memory ring; the LoRA operands once per tile.
 //   warp 1      TMEM allocator and MMA issuer (one thread): MMAs only;
 //               tcgen05.commit frees ring slots (in both CTAs of the pair) and
@@ -158,7 +159,9 @@ __global__ void __launch_bounds__(448, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmLA,
                  const __grid_constant__ CUtensorMap tmLB,
-                 const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+                 const __grid_constant__ CUtensorMap tmOut,
+                 const __grid_constant__ CUtensorMap tmSFA,
+                 const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
   static_assert(!PAIR || CM == 2, "a pair is a cluster of two");
   using C = GemmCfg<BN, BK, STAGES, RPE, PAIR>;
   extern __shared__ uint8_t smem_raw[];
@@ -179,7 +182,6 @@ __global__ void __launch_bounds__(448, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nks = (p.K + BK - 1) / BK;
-  const int rb_total = (p.N + 127) / 128;
   // work units: CM vertically adjacent tiles (an M-unit) sharing one B tile.  The
   // units are ordered in bands of band_mc M-units: a band is swept over every
   // N-tile, M-units fastest, before the next band starts.  With one band (the
@@ -232,6 +234,8 @@ __global__ void __launch_bounds__(448, 1)
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
     prefetch_tensormap(&tmOut);
+    prefetch_tensormap(&tmSFA);
+    prefetch_tensormap(&tmSFB);
     if (p.lora_steps) {
       prefetch_tensormap(&tmLA);
       prefetch_tensormap(&tmLB);
@@ -283,21 +287,18 @@ __global__ void __launch_bounds__(448, 1)
           lphase ^= 1u;
         }
         // a CTA whose m-tile lies past M (odd tile count) computes on zero-filled A
-        // and stores nothing; its scale reads stay inside the last row atom
-        const uint8_t* sfa_t = p.sfa + (size_t)min(mt, p.num_m - 1) * (p.k16p / 4) * 512;
-        const uint8_t* sfb_t = p.sfb + (size_t)(n0 / 128) * (p.k16p / 4) * 512;
-        const size_t sfb_rb = (size_t)(p.k16p / 4) * 512;  // one 128-row block of B scales
-        const int nrb = min(C::NRB, rb_total - n0 / 128);
+        // and stores nothing; its scale reads stay inside the last row block
+        const int sfa_row = min(mt, p.num_m - 1);
         const int nb = n0 + (int)crank * (BN / CM);
         for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs, abort_flag)) {
             ok = false;
             break;
           }
-          const int ksub = min(C::KSUB, (p.K - ks * BK) / 64);
           const uint32_t fb = full0 + 8 * stage;
           const uint32_t sb = base + stage * C::STAGE_BYTES;
-          mbar_expect_tx(fb, C::A_BYTES + C::B_BYTES + (uint32_t)(ksub * 512 * (1 + nrb)));
+          // tiled copies always deliver whole boxes (zero fill past K and past N)
+          mbar_expect_tx(fb, C::STAGE_BYTES);
           tma_load_2d(sb, &tmA, ks * C::ROWB, m0, fb);
           if constexpr (PAIR)
             tma_load_2d(sb + C::A_BYTES, &tmB, ks * C::ROWB, nb, fb);
@@ -306,11 +307,11 @@ __global__ void __launch_bounds__(448, 1)
                            fb, (uint16_t)((1u << CM) - 1u));
           else
             tma_load_2d(sb + C::A_BYTES, &tmB, ks * C::ROWB, n0, fb);
-          const size_t koff = (size_t)ks * C::KSUB * 512;
-          bulk_load(sb + C::A_BYTES + C::B_BYTES, sfa_t + koff, (uint32_t)(ksub * 512), fb);
-          for (int rb = 0; rb < nrb; ++rb)
-            bulk_load(sb + C::A_BYTES + C::B_BYTES + C::SFA_BYTES + rb * C::KSUB * 512,
-                      sfb_t + rb * sfb_rb + koff, (uint32_t)(ksub * 512), fb);
+          // the stage's scale atoms: 4 of the A row block, 4 of each B row block
+          // (x in 8-byte elements: 64 per atom)
+          tma_load_2d(sb + C::A_BYTES + C::B_BYTES, &tmSFA, ks * C::KSUB * 64, sfa_row, fb);
+          tma_load_2d(sb + C::A_BYTES + C::B_BYTES + C::SFA_BYTES, &tmSFB, ks * C::KSUB * 64,
+                      n0 / 128, fb);
           pend |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -701,7 +702,8 @@ static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
     p.band_mc = b < 1 ? 1 : (b > num_mc ? num_mc : b);
   }
   note_launch();
-  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmLA, L.tmLB, L.tmOut, p);
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmLA, L.tmLB, L.tmOut, L.tmSFA, L.tmSFB,
+                            p);
 }
 
 int gemm_block_n(int64_t N, int rpe) { return (N % 256 == 0 && rpe <= 64) ? 256 : 128; }

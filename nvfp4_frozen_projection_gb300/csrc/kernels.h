@@ -41,6 +41,7 @@ struct GemmParams {
 
 struct GemmLaunch {
   CUtensorMap tmA, tmB, tmLA, tmLB, tmOut;
+  CUtensorMap tmSFA, tmSFB;  // scale-factor atoms: rows = 128-row blocks, 8-byte elements
   GemmParams p;
   int num_sms;
 };
