@@ -364,6 +364,18 @@ __global__ void __launch_bounds__(448, 1)
         return PAIR ? mbar_wait_cluster(bar, par, kWaitLimitNs, abort_flag)
                     : mbar_wait(bar, par, kWaitLimitNs, abort_flag);
       };
+      // descriptors of stage 0 (a stage's are these plus its offset in 16-byte units:
+      // every operand address stays inside the 14-bit start-address field)
+      const uint64_t da0 = smem_desc(base, 16, C::AB_SBO, C::AB_SWZ);
+      const uint64_t db0 = smem_desc(base + C::A_BYTES, 16, C::AB_SBO, C::AB_SWZ);
+      const uint32_t tsf0 = tmem + C::SF_BASE;
+      const int nks_full = p.K / BK;
+      auto issue_nvf4 = [&](uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb, uint32_t acc) {
+        if constexpr (PAIR)
+          mma_nvf4_pair(tmem, a, b, idesc, sfa, sfb, acc);
+        else
+          mma_nvf4(tmem, a, b, idesc, sfa, sfb, acc);
+      };
       auto commit_all = [&](uint32_t bar) {  // reaches both CTAs of a cluster
         if constexpr (PAIR)
           mma_commit_pair(bar, (uint16_t)3u);
@@ -416,20 +428,24 @@ __global__ void __launch_bounds__(448, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sb = base + stage * C::STAGE_BYTES;
-          const uint32_t tsf = tmem + C::SF_BASE + stage * C::SF_COLS;
-          const int ksub = min(C::KSUB, (p.K - ks * BK) / 64);
-          for (int j = 0; j < ksub; ++j) {
-            const uint64_t da = smem_desc(sb + 32 * j, 16, C::AB_SBO, C::AB_SWZ);
-            const uint64_t db = smem_desc(sb + C::A_BYTES + 32 * j, 16, C::AB_SBO, C::AB_SWZ);
-            if constexpr (PAIR)
-              mma_nvf4_pair(tmem, da, db, idesc, tsf + 4 * j, tsf + 4 * C::KSUB + j * C::NRB * 4,
-                            accum);
-            else
-              mma_nvf4(tmem, da, db, idesc, tsf + 4 * j, tsf + 4 * C::KSUB + j * C::NRB * 4,
-                       accum);
-            accum = 1;
+          // this thread's instruction latency between MMAs is what the tensor pipe
+          // sees, so a whole stage is issued unrolled from precomputed descriptors
+          // (the runtime-count loop measured 15-18 % slower per stage)
+          const uint64_t soff = (uint64_t)(stage * (C::STAGE_BYTES >> 4));
+          const uint64_t da = da0 + soff, db = db0 + soff;
+          const uint32_t tsf = tsf0 + (uint32_t)(stage * C::SF_COLS);
+          if (ks < nks_full) {
+#pragma unroll
+            for (int j = 0; j < C::KSUB; ++j)
+              issue_nvf4(da + 2u * j, db + 2u * j, tsf + 4 * j, tsf + 4 * C::KSUB + j * C::NRB * 4,
+                         j == 0 ? accum : 1u);
+          } else {  // K tail: ksub < KSUB 64-wide steps
+            const int ksub = (p.K - ks * BK) / 64;
+            for (int j = 0; j < ksub; ++j)
+              issue_nvf4(da + 2u * j, db + 2u * j, tsf + 4 * j, tsf + 4 * C::KSUB + j * C::NRB * 4,
+                         j == 0 ? accum : 1u);
           }
+          accum = 1;
           commit_all(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
