@@ -45,7 +45,7 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
 # DRAM bytes (read + write) of one full-size launch of the GEMM kernel, from a
 # one-pass ncu capture of profile_case at M = 8192 (profiles/gemm_nvfp4_gate_up.md);
 # they describe the kernel as of that capture.
-GEMM_TRAFFIC_BYTES = {"gate_up.dgrad": 184.79e6, "gate_up.fwd": 263.97e6}
+GEMM_TRAFFIC_BYTES = {"gate_up.fwd": 263.73e6}
 # (N, K) of each distinct frozen-projection GEMM of the layer-3b step (out = M x N)
 GEMM_SHAPES = {"q.fwd": (3072, 3072), "kv.fwd": (2048, 3072), "o.fwd": (3072, 3072),
                "gate_up.fwd": (16384, 3072), "down.fwd": (3072, 8192),
