@@ -48,6 +48,32 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, cons
 // so that the fused GEMM's BF16 LoRA product sees v to about 16 significant bits.
 // acc[g][jn][*] is the m16n8 accumulator of row group g (rows 16g + lane/4 and
 // 16g + lane/4 + 8) and columns 8 jn + 2 (lane % 4) + {0, 1}.
+// Four 8x8 BF16 matrices from shared memory, each transposed: lanes 8i .. 8i + 7
+// give the row addresses of matrix i.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// cp.async copies into shared memory; src_bytes = 0 writes zeros instead of reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 template <int RP, int G>
 __device__ __forceinline__ void reduce_and_store(float (*acc)[RP / 8][4], float* red, int64_t m0,
                                                  int64_t M, float f, uint16_t* out) {
@@ -253,130 +279,214 @@ struct DyQuant {
   float* g_out;
 };
 
-// U' = f * (dY B^T): dy [M, N] BF16, B [r, N] row-major.  A chunk is 32 elements
-// of a row: lane c holds elements [8c, 8c + 8) (16 bytes).  N is long here (up to
-// 2 x the intermediate size), so two chunks are in flight ahead of the one being
-// multiplied.
-// With QUANT the same pass also quantises dY to NVFP4, byte for byte as the
-// quantiser does (the same block-scale table and element encode): a block of 16 is
-// lanes c and c ^ 1 of a row, so its amax takes one shuffle.  The grid then covers
-// the rows up to the 128-row padding of the scale atoms, whose scales encode zero.
-template <int RP, int G, bool QUANT>
-__global__ void __launch_bounds__(256, 2) k_lora_down_dgrad(const uint16_t* __restrict__ dy,
+// U' = f * (dY B^T), dy [M, N] BF16, B [r, N] row-major, for 128-row blocks of dY
+// whose column range is split over a cluster of NS CTAs (NS a power of two <= 8,
+// along grid x).  Warp w multiplies rows 16w .. 16w + 15 of the block; the eight
+// warps step through the same 64-column chunks, so each chunk of B (RP rows, zero
+// past r) is copied into shared memory once per CTA (a 4-slot cp.async ring) and
+// read by all of them.  Lane (g, c) holds 16 consecutive elements of rows g and
+// g + 8, [16c, 16c + 16) of the chunk: in K step s of the m16n8k16 MMA its k slots
+// 2c, 2c + 1 / 2c + 8, 2c + 9 carry columns 16c + 4s + 0, 1 / 2, 3, and the B
+// fragment is read at the same columns (a k permutation both operands share).
+// The CTAs' partial sums meet in distributed shared memory at the end: CTA j of
+// the cluster adds the NS partials of rows [128 j / NS, 128 (j + 1) / NS) in rank
+// order, so the result does not depend on scheduling.
+// With QUANT the same pass quantises dY to NVFP4, byte for byte as the quantiser
+// does (the same block-scale table and element encode): a lane's 16 elements of a
+// row are exactly one NVFP4 block.  The grid covers the rows up to the 128-row
+// padding of the scale atoms, whose scales encode zero.
+constexpr int kDyRing = 4;      // chunk slots (3 chunks in flight)
+constexpr int kDyBRow = 136;    // bytes per B row in shared memory: 128 + 8 makes the
+                                // fragment reads of a half-warp hit 32 distinct banks
+constexpr int kDyXRow = 144;    // bytes per dY row: 128 + 16, conflict-free 16-byte reads
+constexpr int kDyXSlot = 128 * kDyXRow;
+
+template <int RP>
+constexpr int dy_smem_bytes() {
+  return kDyRing * (RP * kDyBRow + kDyXSlot);  // >= 128 RP 4 bytes of partial sums
+}
+
+template <int RP, bool QUANT>
+__global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restrict__ dy,
                                                          const float* __restrict__ gdy,
-                                                         const float* __restrict__ gw,
-                                                         int64_t M, int64_t N,
-                                                         const uint16_t* __restrict__ B, int r,
-                                                         float scale, int plain,
-                                                         uint16_t* __restrict__ u_out,
-                                                         DyQuant qz) {
+                                                         const float* __restrict__ gw, int64_t M,
+                                                         int64_t N, const uint16_t* __restrict__ B,
+                                                         int r, float scale, int plain,
+                                                         uint16_t* __restrict__ u_out, DyQuant qz) {
   constexpr int NT = RP / 8;
-  __shared__ float red[8 * 16 * G * RP];
+  constexpr int SLOT = RP * kDyBRow;
+  constexpr int XOFF = kDyRing * SLOT;  // the dY ring follows the B ring
+  extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ ScaleTable tab[1];  // used with QUANT only
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t m0 = (int64_t)blockIdx.x * (16 * G);
-  const int nch = (int)(N >> 5);
+  const int ns = (int)gridDim.x, split = (int)blockIdx.x;  // split == rank in the cluster
+  const int64_t mb0 = (int64_t)blockIdx.y * 128;
+  const int nch = (int)(N >> 6);
+  const int ch0 = (int)((int64_t)nch * split / ns), ch1 = (int)((int64_t)nch * (split + 1) / ns);
   TensorScale tsq = {0.0f, 0.0f};
   if constexpr (QUANT) {
     const float amax = qz.amax_opt ? *qz.amax_opt : __uint_as_float(*qz.amax_bits);
     tsq = tensor_scale(amax);
-    if (blockIdx.x == 0 && threadIdx.x == 0) *qz.g_out = tsq.g;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *qz.g_out = tsq.g;
     scale_table_init(&tab[0], tsq);
-    __syncthreads();
   }
-  const int64_t c16p = N >> 4;  // N % 64 == 0: no column padding of the scale atoms
-  float acc[G][NT][4];
+  // rows r .. RP - 1 of every B slot stay zero (the copies never touch them)
+  for (int i = threadIdx.x; i < kDyRing * (RP - r) * (kDyBRow / 4); i += blockDim.x) {
+    const int slot = i / ((RP - r) * (kDyBRow / 4)), rem = i - slot * ((RP - r) * (kDyBRow / 4));
+    reinterpret_cast<uint32_t*>(dsm + slot * SLOT + r * kDyBRow)[rem] = 0u;
+  }
+  const uint32_t sbase = smem_addr(dsm);
+  // one chunk: the B columns (RP rows, 8-byte pieces) and the block's 128 dY rows
+  // (16-byte pieces, zeros past M), one cp.async group
+  auto load_chunk = [&](int ch, int slot) {
+    for (int pc = threadIdx.x; pc < r * 16; pc += blockDim.x) {
+      const int row = pc >> 4, q8 = pc & 15;
+      cp_async8(sbase + slot * SLOT + row * kDyBRow + q8 * 8,
+                B + (int64_t)row * N + (int64_t)ch * 64 + q8 * 4);
+    }
 #pragma unroll
-  for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-    for (int jn = 0; jn < NT; ++jn) acc[gi][jn][0] = acc[gi][jn][1] = acc[gi][jn][2] = acc[gi][jn][3] = 0.0f;
-
-  auto load = [&](int ch, uint4 (&x)[G][2]) {
-#pragma unroll
-    for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t row = m0 + 16 * gi + g + 8 * h;
-        x[gi][h] = row < M ? ldg_stream(reinterpret_cast<const uint4*>(dy + row * N + (int64_t)ch * 32 + 8 * c))
-                           : make_uint4(0u, 0u, 0u, 0u);
-      }
-  };
-  // the chunk's B fragments: lane (g, c) needs B[8 jn + g, n0 .. n0 + 8) (two 8-byte
-  // halves, one per MMA step); they are loaded one chunk ahead with the dY rows, so
-  // no L2 round trip sits between a chunk's arrival and its MMAs
-  auto load_b = [&](int ch, uint4 (&b)[NT]) {
-    const int64_t n0 = (int64_t)ch * 32 + 8 * c;
-#pragma unroll
-    for (int jn = 0; jn < NT; ++jn) {
-      const int col = jn * 8 + g;
-      b[jn] = make_uint4(0u, 0u, 0u, 0u);
-      if (col < r) {  // two 8-byte loads: B is only required to be 8-byte aligned
-        const uint2* src = reinterpret_cast<const uint2*>(B + (int64_t)col * N + n0);
-        const uint2 lo = __ldg(src), hi = __ldg(src + 1);
-        b[jn] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-      }
+    for (int i = 0; i < 4; ++i) {
+      const int pc = (int)threadIdx.x + 256 * i, row = pc >> 3, q16 = pc & 7;
+      const int64_t m = mb0 + row;
+      const bool ok = m < M;
+      cp_async16(sbase + XOFF + slot * kDyXSlot + row * kDyXRow + q16 * 16,
+                 ok ? dy + m * N + (int64_t)ch * 64 + q16 * 8 : dy, ok ? 16u : 0u);
     }
   };
-  uint4 x0[G][2], x1[G][2], x2[G][2];
-  uint4 b0[NT], b1[NT];
-  if (warp < nch) {
-    load(warp, x0);
-    load_b(warp, b0);
-  }
-  if (warp + 8 < nch) load(warp + 8, x1);
-  for (int ch = warp; ch < nch; ch += 8) {
-    if (ch + 16 < nch) load(ch + 16, x2);
-    if (ch + 8 < nch) load_b(ch + 8, b1);
+  const int64_t row0 = mb0 + warp * 16 + g;
+  const bool ok0 = row0 < M, ok1 = row0 + 8 < M;
+  float acc[NT][4];
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      uint32_t bfr[NT][2];
+  for (int jn = 0; jn < NT; ++jn) acc[jn][0] = acc[jn][1] = acc[jn][2] = acc[jn][3] = 0.0f;
+  // scale-byte offsets of the two rows' blocks in chunk 0 (block 4 ch + c of a row
+  // sits at ch * 512 + c past them)
+  const int64_t c16p = N >> 4;  // N % 64 == 0: no column padding of the scale atoms
+  auto sf_row = [&](int64_t row) {
+    return ((row >> 7) * (c16p >> 2)) * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4 + c;
+  };
+  const int64_t sfo0 = sf_row(row0), sfo1 = sf_row(row0 + 8);
+
+#pragma unroll
+  for (int i = 0; i < kDyRing - 1; ++i) {
+    if (ch0 + i < ch1) load_chunk(ch0 + i, i);
+    cp_async_commit();
+  }
+  for (int cc = ch0; cc < ch1; ++cc) {
+    const int k = cc - ch0, slot = k % kDyRing;
+    cp_async_wait<kDyRing - 2>();  // this thread's copies of chunk cc have landed
+    __syncthreads();                 // everyone's have; chunk cc - 1 is done with
+    if (cc + kDyRing - 1 < ch1) load_chunk(cc + kDyRing - 1, (k + kDyRing - 1) % kDyRing);
+    cp_async_commit();
+    uint4 xc[2][2];
+    const uint8_t* xs = dsm + XOFF + slot * kDyXSlot + (warp * 16 + g) * kDyXRow + 32 * c;
+    xc[0][0] = *reinterpret_cast<const uint4*>(xs);
+    xc[0][1] = *reinterpret_cast<const uint4*>(xs + 16);
+    xc[1][0] = *reinterpret_cast<const uint4*>(xs + 8 * kDyXRow);
+    xc[1][1] = *reinterpret_cast<const uint4*>(xs + 8 * kDyXRow + 16);
+    const uint8_t* bs = dsm + slot * SLOT + (g * kDyBRow + 32 * c);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const uint4& lo0 = xc[0][s >> 1];
+      const uint4& lo1 = xc[1][s >> 1];
+      const uint32_t a[4] = {(s & 1) ? lo0.z : lo0.x, (s & 1) ? lo1.z : lo1.x,
+                             (s & 1) ? lo0.w : lo0.y, (s & 1) ? lo1.w : lo1.y};
 #pragma unroll
       for (int jn = 0; jn < NT; ++jn) {
-        bfr[jn][0] = s ? b0[jn].z : b0[jn].x;
-        bfr[jn][1] = s ? b0[jn].w : b0[jn].y;
-      }
-#pragma unroll
-      for (int gi = 0; gi < G; ++gi) {
-        const uint32_t a[4] = {s ? x0[gi][0].z : x0[gi][0].x, s ? x0[gi][1].z : x0[gi][1].x,
-                               s ? x0[gi][0].w : x0[gi][0].y, s ? x0[gi][1].w : x0[gi][1].y};
-#pragma unroll
-        for (int jn = 0; jn < NT; ++jn) mma_bf16_16816(acc[gi][jn], a, bfr[jn]);
+        const uint2 bb = *reinterpret_cast<const uint2*>(bs + jn * 8 * kDyBRow + 8 * s);
+        const uint32_t bfr[2] = {bb.x, bb.y};
+        mma_bf16_16816(acc[jn], a, bfr);
       }
     }
     if constexpr (QUANT) {
-      // rows g (+ 8) of each group; this lane's 8 elements are columns
-      // 32 ch + 8c .. + 8 of block 2 ch + c / 2
-#pragma unroll
-      for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t row = m0 + 16 * gi + g + 8 * h;
-          uint32_t am = absmax_bf16x8_bits(x0[gi][h]);
-          am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-          float f[8], t, rcp;
-          bf16x8_to_f32(x0[gi][h], f);
-          const uint32_t sc = block_scale_tab(__uint_as_float(am), tsq, &tab[0], &t, &rcp);
-          const uint32_t w = encode8(f, t, rcp);
-          if (row < M)
-            *reinterpret_cast<uint32_t*>(qz.codes + row * (N >> 1) + (int64_t)ch * 16 + 4 * c) = w;
-          if ((c & 1) == 0) qz.sf[sf_offset(row, (int64_t)ch * 2 + (c >> 1), c16p)] = (uint8_t)sc;
-        }
-    }
-#pragma unroll
-    for (int gi = 0; gi < G; ++gi)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        x0[gi][h] = x1[gi][h];
-        x1[gi][h] = x2[gi][h];
+        const uint32_t am = max(absmax_bf16x8_bits(xc[h][0]), absmax_bf16x8_bits(xc[h][1]));
+        float t, rcp, f8[8];
+        const uint32_t sc = block_scale_tab(__uint_as_float(am), tsq, &tab[0], &t, &rcp);
+        bf16x8_to_f32(xc[h][0], f8);
+        const uint32_t w0 = encode8(f8, t, rcp);
+        bf16x8_to_f32(xc[h][1], f8);
+        const uint32_t w1 = encode8(f8, t, rcp);
+        const int64_t row = row0 + 8 * h;
+        if (h ? ok1 : ok0)
+          *reinterpret_cast<uint2*>(qz.codes + row * (N >> 1) + (int64_t)cc * 32 + 8 * c) =
+              make_uint2(w0, w1);
+        qz.sf[(h ? sfo1 : sfo0) + (int64_t)cc * 512] = (uint8_t)sc;
       }
-#pragma unroll
-    for (int jn = 0; jn < NT; ++jn) b0[jn] = b1[jn];
+    }
   }
+  cp_async_wait<0>();  // only empty groups can remain
+  __syncthreads();     // the ring is free: it now holds this CTA's partial sums
+  float* part = reinterpret_cast<float*>(dsm);  // [128 rows][RP]
+#pragma unroll
+  for (int jn = 0; jn < NT; ++jn) {
+    float* p0 = part + (warp * 16 + g) * RP + jn * 8 + 2 * c;
+    *reinterpret_cast<float2*>(p0) = make_float2(acc[jn][0], acc[jn][1]);
+    *reinterpret_cast<float2*>(p0 + 8 * RP) = make_float2(acc[jn][2], acc[jn][3]);
+  }
+  cluster_sync();  // every CTA's partials are in its shared memory
   // plain: f = scale, i.e. v = scale * (dY B^T) for the adapter gradients
   const float s_main = plain ? 0.0f : __fmul_rn(QUANT ? tsq.g : *gdy, *gw);
   const float f = s_main > 0.0f ? __fdiv_rn(scale, s_main) : scale;
-  reduce_and_store<RP, G>(acc, red, m0, M, f, u_out);
+  const int rows = 128 / ns;
+  for (int e = threadIdx.x; e < rows * RP; e += blockDim.x) {
+    const int rl = split * rows + e / RP, col = e % RP;
+    const uint32_t local = smem_addr(part + rl * RP + col);
+    float sum = 0.0f;
+    for (int j = 0; j < ns; ++j) sum += ld_shared_cluster_f32(local, (uint32_t)j);
+    const int64_t m = mb0 + rl;
+    if (m < M) {
+      const float v = sum * f;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      u_out[m * (2 * RP) + col] = *reinterpret_cast<const uint16_t*>(&hi);
+      u_out[m * (2 * RP) + RP + col] = *reinterpret_cast<const uint16_t*>(&lo);
+    }
+  }
+  cluster_sync();  // no CTA leaves while a peer may still read its partials
+}
+
+// CTAs per cluster for a dY of N columns: the largest power of two <= 8 that leaves
+// every CTA at least 12 of the 64-column chunks (a CTA's start-up and cluster
+// reduction are worth a few chunks), or 1.
+static int dy_splits(int64_t N) {
+  const int64_t nch = N >> 6;
+  int ns = 1;
+  while (ns < 8 && 2 * ns * 12 <= nch) ns *= 2;
+  return ns;
+}
+
+template <int RP, bool QUANT>
+static cudaError_t launch_down_dy(const uint16_t* dy, const float* gdy, const float* gw,
+                                  int64_t M, int64_t N, const uint16_t* B, int r, float scale,
+                                  int plain, uint16_t* u_out, DyQuant qz, cudaStream_t stream) {
+  const int ns = dy_splits(N);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ns;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(ns, (unsigned)(pad_to(M, 128) / 128));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = dy_smem_bytes<RP>();
+  static bool attr_set[64] = {};  // per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(k_lora_down_dy<RP, QUANT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               dy_smem_bytes<RP>());
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, k_lora_down_dy<RP, QUANT>, dy, gdy, gw, M, N, B, r, scale,
+                            plain, u_out, qz);
 }
 
 template <int RP>
@@ -398,15 +508,13 @@ template <int RP>
 static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* gw, int64_t M,
                             int64_t N, const uint16_t* A, const uint16_t* B, int r, float scale,
                             int64_t K, uint16_t* u_out, uint16_t* ap_out, cudaStream_t stream) {
-  constexpr int G = RP <= 32 ? 2 : 1;
   if (ap_out) {  // null: A is already [K, RP] (r == RP) and serves as the GEMM operand
     note_launch();
     k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
   }
-  note_launch();
-  k_lora_down_dgrad<RP, G, false><<<(int)((M + 16 * G - 1) / (16 * G)), 256, 0, stream>>>(
-      dy, gdy, gw, M, N, B, r, scale, 0, u_out, DyQuant{});
-  return cudaGetLastError();
+  const cudaError_t e = launch_down_dy<RP, false>(dy, gdy, gw, M, N, B, r, scale, 0, u_out,
+                                                  DyQuant{}, stream);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_lora_down_fwd(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
@@ -437,16 +545,13 @@ static cudaError_t quant_dgrad_rp(const uint16_t* dy, int64_t M, int64_t N, DyQu
                                   const float* gw, const uint16_t* A, const uint16_t* B, int r,
                                   float scale, int64_t K, uint16_t* u_out, uint16_t* ap_out,
                                   cudaStream_t stream) {
-  constexpr int G = RP <= 32 ? 2 : 1;
   if (ap_out) {
     note_launch();
     k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
   }
-  const int64_t Mpad = pad_to(M, 128);
-  note_launch();
-  k_lora_down_dgrad<RP, G, true><<<(int)(Mpad / (16 * G)), 256, 0, stream>>>(
-      dy, nullptr, gw, M, N, B, r, scale, 0, u_out, qz);
-  return cudaGetLastError();
+  const cudaError_t e =
+      launch_down_dy<RP, true>(dy, nullptr, gw, M, N, B, r, scale, 0, u_out, qz, stream);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_quant_lora_down(const uint16_t* dy, int64_t M, int64_t N, const float* amax_opt,
@@ -470,29 +575,6 @@ cudaError_t launch_quant_lora_down(const uint16_t* dy, int64_t M, int64_t N, con
 // U' = (alpha/r) dY B^T as hi|lo BF16 pairs ("plain" mode), and one tall-skinny
 // kernel forms OUT[c, j] = sum_m L[m, c] R[m, j] for L = dY, R = T' (dB) and for
 // L = Xhat without its per-tensor scale, R = U' (dA, times g_x afterwards).
-
-// Four 8x8 BF16 matrices from shared memory, each transposed: lanes 8i .. 8i + 7
-// give the row addresses of matrix i.
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-// cp.async copies into shared memory; src_bytes = 0 writes zeros instead of reading.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // Shared-memory plan of the tall-skinny kernel.  A stage holds ROWS rows of L (the
 // 128 columns of the CTA: BF16, or NVFP4 codes plus their 8 block scales) and of R
@@ -753,11 +835,11 @@ static cudaError_t adapter_grad_rp(const uint8_t* xc, const uint8_t* xsf, const 
   k_lora_prep<RP><<<(int)((N + K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 1, at_ws, bt_ws);
   note_launch();
   k_lora_down_fwd<RP, G><<<mb, 256, 0, stream>>>(xc, xsf, gx, gx, M, K, at_ws, scale, 1, t_ws);
-  note_launch();
-  k_lora_down_dgrad<RP, G, false><<<mb, 256, 0, stream>>>(dy, gx, gx, M, N, B, r, scale, 1, u_ws,
-                                                          DyQuant{});
+  cudaError_t e =
+      launch_down_dy<RP, false>(dy, gx, gx, M, N, B, r, scale, 1, u_ws, DyQuant{}, stream);
+  if (e != cudaSuccess) return e;
   int64_t ns;
-  cudaError_t e = launch_ts<RP, false>(dy, nullptr, nullptr, M, N, t_ws, 1, part, &ns, stream);
+  e = launch_ts<RP, false>(dy, nullptr, nullptr, M, N, t_ws, 1, part, &ns, stream);
   if (e != cudaSuccess) return e;
   note_launch();
   k_lora_ts_reduce<<<std::min<int64_t>((N * r + 255) / 256, num_sms * 8), 256, 0, stream>>>(

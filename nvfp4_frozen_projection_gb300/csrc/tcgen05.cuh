@@ -61,6 +61,16 @@ __device__ __forceinline__ void mbar_arrive_cta_relaxed(uint32_t bar, uint32_t c
                : "memory");
 }
 
+// A 32-bit load from the shared memory of CTA `cta` of the cluster at this CTA-local
+// address (distributed shared memory).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t local, uint32_t cta) {
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local), "r"(cta));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
 // try_wait with acquire at cluster scope: for barriers that other CTAs arrive on.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
