@@ -171,9 +171,11 @@ __device__ __forceinline__ float silu_exact_at(const uint4& g0, const uint4& g1,
 __device__ __forceinline__ float silu_block_fast(const float* gf, const float* uf, float* hf) {
   float am = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    hf[i] = silu_mul_fast(gf[i], uf[i]);
-    am = fmaxf(am, fabsf(hf[i]));
+  for (int i = 0; i < 16; i += 2) {
+    const float2 h = silu_mul_fast2(make_float2(gf[i], gf[i + 1]), make_float2(uf[i], uf[i + 1]));
+    hf[i] = h.x;
+    hf[i + 1] = h.y;
+    am = fmaxf(am, fmaxf(fabsf(h.x), fabsf(h.y)));
   }
   return am;
 }
@@ -386,9 +388,12 @@ __global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restri
         redo = 0;
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-          const float x0 = __fmul_rn(hf[i], rcp), x1 = __fmul_rn(hf[i + 1], rcp);
-          const uint32_t cl = e2m1x2_mag(__fmul_rn(x0, lo_f), __fmul_rn(x1, lo_f));
-          const uint32_t ch = e2m1x2_mag(__fmul_rn(x0, hi_f), __fmul_rn(x1, hi_f));
+          // packed pairs: each lane rounds as the scalar multiply does
+          const float2 x = __fmul2_rn(make_float2(hf[i], hf[i + 1]), make_float2(rcp, rcp));
+          const float2 xl = __fmul2_rn(x, make_float2(lo_f, lo_f));
+          const float2 xh = __fmul2_rn(x, make_float2(hi_f, hi_f));
+          const uint32_t cl = e2m1x2_mag(xl.x, xl.y);
+          const uint32_t ch = e2m1x2_mag(xh.x, xh.y);
           const uint32_t d = cl ^ ch;
           redo |= ((d & 0x0Fu) ? 1u : 0u) << i;
           redo |= ((d & 0xF0u) ? 1u : 0u) << (i + 1);
