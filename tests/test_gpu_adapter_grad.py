@@ -115,7 +115,7 @@ def test_adapter_grad_tiny_workload():
 
 
 @pytest.mark.parametrize("M,N,K,r", [(1, 64, 64, 4), (333, 192, 448, 12), (1000, 2048, 512, 64),
-                                     (257, 384, 1536, 33)])
+                                     (257, 384, 1536, 33), (300, 1600, 256, 16)])
 def test_adapter_grad_odd_shapes(M, N, K, r):
     rng = np.random.default_rng(M + 7 * N + K + r)
     x = wl.bf16_round(rng.standard_normal((M, K)).astype(np.float32))

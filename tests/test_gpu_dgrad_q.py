@@ -4,8 +4,9 @@ and its LoRA down-projection formed in one pass, then the NVFP4 dgrad GEMM).
 It must reproduce the two-call path (pact_quant_nvfp4, then pact_lora_linear_dgrad)
 byte for byte: codes, every scale byte of the padded atoms, g and the BF16 dX; and
 its NVFP4 dY must equal the oracle's quantisation of the same tensor bit for bit.
-Shapes cover one row, rows off the 32-row CTA and the 128-row scale atom, every
-padded rank, a given amax and the accumulate mode."""
+Shapes cover one row, rows off the 128-row CTA and scale atom, every padded rank,
+column counts whose 64-column chunks split unevenly over the CTAs of a cluster, a
+given amax and the accumulate mode."""
 import numpy as np
 import pytest
 import torch
@@ -35,6 +36,7 @@ def _same_nvfp4(a: NVFP4, b: NVFP4, what):
     (130, 512, 256, 32, False, True),
     (97, 320, 1024, 64, True, False),
     (512, 3072, 1024, 16, False, False),
+    (300, 1600, 256, 16, False, True),  # 25 column chunks: an uneven 12 / 13 cluster split
 ])
 def test_dgrad_q_matches_two_calls(M, N, K, r, given_amax, acc):
     rng = np.random.default_rng(M * 5 + N + K + r)
