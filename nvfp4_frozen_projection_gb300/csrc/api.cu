@@ -264,7 +264,7 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
   const int bn = gemm_block_n(Nout, rpe);
-  const int cm = gemm_cluster_m(M);  // each CTA of a cluster loads bn / cm rows of B
+  const int cm = gemm_cluster_m(M, Nout, rpe);  // each CTA of a cluster loads bn / cm rows of B
   int rc;
   const uint32_t rowb = (uint32_t)gemm_stage_row_bytes();
   const CUtensorMapSwizzle absw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;

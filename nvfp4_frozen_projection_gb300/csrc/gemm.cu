@@ -18,10 +18,12 @@
 // chunks.  s = g_a * g_b (or 1 when either per-tensor scale is zero, in which
 // case the NVFP4 operand is all zero).
 //
-// Structure: one persistent CTA per SM, 14 warps; CTAs pair up in clusters of two
-// along M (when M spans more than one tile) and share each B tile by multicast.
+// Structure: one persistent CTA per SM, 14 warps.  Tiles 256 wide run on CTA
+// pairs (clusters of two along M, .cta_group::2 MMAs over 256 rows); tiles 128
+// wide run on single CTAs.  Every CTA loads its own operands: no TMA copy is
+// multicast.
 //   warp 0      TMA producer: A/B tiles (128-byte rows, 128B swizzle; one 16 KB
-//               A box and half of the B tile per CTA, multicast to the pair) and
+//               A box per CTA and, for a pair, half of the B tile each) and
 //               the scale-factor atoms (tiled copies: one box of 4 atoms per
 //               row block; plain bulk copies measured ~8 % slower) into a STAGES-deep
 //               shared-memory ring; the LoRA operands once per tile.
@@ -145,10 +147,7 @@ __device__ __forceinline__ void raise_error(volatile uint32_t* abort_flag, unsig
   atomicOr(status, code);
 }
 
-// CM = CTAs per cluster along M (1 or 2).  With CM = 2 the two CTAs of a cluster
-// compute the tiles (m, n) and (m + 1, n) in lock step: each loads half of the
-// shared B tile and multicasts it to both, so every B byte leaves L2 once per pair,
-// and a stage is refilled only after both CTAs' MMAs released it.
+// CM = CTAs per cluster along M: 1, or 2 for a pair.
 // PAIR (CM = 2): the two CTAs of a cluster compute the tiles (m, n) and (m + 1, n)
 // as one M = 256 pair MMA issued by the even CTA ("leader"): each CTA loads its A
 // tile and half of the B tile (no multicast), stages its scale factors into its own
@@ -162,7 +161,7 @@ __global__ void __launch_bounds__(448, 1)
                  const __grid_constant__ CUtensorMap tmOut,
                  const __grid_constant__ CUtensorMap tmSFA,
                  const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
-  static_assert(!PAIR || CM == 2, "a pair is a cluster of two");
+  static_assert(PAIR ? CM == 2 : CM == 1, "a pair is a cluster of two; other tiles one CTA");
   using C = GemmCfg<BN, BK, STAGES, RPE, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -216,8 +215,8 @@ __global__ void __launch_bounds__(448, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      // PAIR: one multicast commit from the leader; else one from each CTA
-      mbar_init(empty0 + 8 * s, PAIR ? 1 : CM);
+      // one commit: this CTA's own, or for a pair the leader's (reaching both)
+      mbar_init(empty0 + 8 * s, 1);
       // PAIR: one arrival per scale-staging warp of both CTAs (at the leader)
       mbar_init(sf_full0 + 8 * s, PAIR ? 8 : 128);
     }
@@ -289,7 +288,7 @@ __global__ void __launch_bounds__(448, 1)
         // a CTA whose m-tile lies past M (odd tile count) computes on zero-filled A
         // and stores nothing; its scale reads stay inside the last row block
         const int sfa_row = min(mt, p.num_m - 1);
-        const int nb = n0 + (int)crank * (BN / CM);
+        const int nb = n0 + (int)crank * C::B_ROWS;  // this CTA's B rows
         for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, kWaitLimitNs, abort_flag)) {
             ok = false;
@@ -300,13 +299,7 @@ __global__ void __launch_bounds__(448, 1)
           // tiled copies always deliver whole boxes (zero fill past K and past N)
           mbar_expect_tx(fb, C::STAGE_BYTES);
           tma_load_2d(sb, &tmA, ks * C::ROWB, m0, fb);
-          if constexpr (PAIR)
-            tma_load_2d(sb + C::A_BYTES, &tmB, ks * C::ROWB, nb, fb);
-          else if constexpr (CM > 1)
-            tma_load_2d_mc(sb + C::A_BYTES + crank * (C::B_BYTES / CM), &tmB, ks * C::ROWB, nb,
-                           fb, (uint16_t)((1u << CM) - 1u));
-          else
-            tma_load_2d(sb + C::A_BYTES, &tmB, ks * C::ROWB, n0, fb);
+          tma_load_2d(sb + C::A_BYTES, &tmB, ks * C::ROWB, nb, fb);
           // the stage's scale atoms: 4 of the A row block, 4 of each B row block
           // (x in 8-byte elements: 64 per atom)
           tma_load_2d(sb + C::A_BYTES + C::B_BYTES, &tmSFA, ks * C::KSUB * 64, sfa_row, fb);
@@ -379,8 +372,6 @@ __global__ void __launch_bounds__(448, 1)
       auto commit_all = [&](uint32_t bar) {  // reaches both CTAs of a cluster
         if constexpr (PAIR)
           mma_commit_pair(bar, (uint16_t)3u);
-        else if constexpr (CM > 1)
-          mma_commit_mc(bar, (uint16_t)((1u << CM) - 1u));
         else
           mma_commit(bar);
       };
@@ -724,18 +715,13 @@ static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
 
 int gemm_block_n(int64_t N, int rpe) { return (N % 256 == 0 && rpe <= 64) ? 256 : 128; }
 
-#ifndef PACT_GEMM_CM
-#define PACT_GEMM_CM 2
-#endif
-int gemm_cluster_m(int64_t M) { return (PACT_GEMM_CM > 1 && M > 128) ? 2 : 1; }
-
 int gemm_stage_row_bytes() { return kStageK / 2; }
 
-bool gemm_pair_enabled() { return true; }
-
 bool gemm_uses_pair(int64_t M, int64_t N, int rpe) {
-  return gemm_pair_enabled() && gemm_cluster_m(M) == 2 && gemm_block_n(N, rpe) == 256;
+  return M > 128 && gemm_block_n(N, rpe) == 256;
 }
+
+int gemm_cluster_m(int64_t M, int64_t N, int rpe) { return gemm_uses_pair(M, N, rpe) ? 2 : 1; }
 
 // Ring depth: as many stages as shared memory holds next to the LoRA operands and
 // one staging buffer per epilogue warp, within the TMEM left for scale factors, at
@@ -761,23 +747,18 @@ static cudaError_t launch_pair(const GemmLaunch& L, cudaStream_t stream) {
   return launch_cfg<BN, kStageK, ring_stages<BN, kStageK, RPE, true>(), RPE, 2, true>(L, stream);
 }
 
-template <int CM>
-static cudaError_t launch_cm(const GemmLaunch& L, int bn, int rpe, cudaStream_t stream) {
+cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, int cm, cudaStream_t stream) {
   if (bn == 256) {
-    if (CM == 2 && gemm_pair_enabled()) {
+    if (cm == 2) {
       if (rpe == 32) return launch_pair<256, 32>(L, stream);
       return launch_pair<256, 64>(L, stream);
     }
-    if (rpe == 32) return launch_one<256, 32, CM>(L, stream);
-    return launch_one<256, 64, CM>(L, stream);
+    if (rpe == 32) return launch_one<256, 32, 1>(L, stream);
+    return launch_one<256, 64, 1>(L, stream);
   }
-  if (rpe == 32) return launch_one<128, 32, CM>(L, stream);
-  if (rpe == 64) return launch_one<128, 64, CM>(L, stream);
-  return launch_one<128, 128, CM>(L, stream);
-}
-
-cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, int cm, cudaStream_t stream) {
-  return cm == 2 ? launch_cm<2>(L, bn, rpe, stream) : launch_cm<1>(L, bn, rpe, stream);
+  if (rpe == 32) return launch_one<128, 32, 1>(L, stream);
+  if (rpe == 64) return launch_one<128, 64, 1>(L, stream);
+  return launch_one<128, 128, 1>(L, stream);
 }
 
 // Test of the bounded-wait path: one thread waits on an mbarrier that nothing

@@ -49,14 +49,13 @@ struct GemmLaunch {
 // Tile width (128 or 256) for an output of N columns and a LoRA operand of rpe
 // columns, and the launcher.
 int gemm_block_n(int64_t N, int rpe);
-// CTAs per cluster along M (2: pairs share each B tile by multicast), for M rows.
-int gemm_cluster_m(int64_t M);
+// CTAs per cluster along M: 2 when the tile is computed by a CTA pair, else 1.
+int gemm_cluster_m(int64_t M, int64_t N, int rpe);
 // Bytes of K per A/B tile row in one ring stage (the TMA box width; 64 -> 64B
 // swizzle, 128 -> 128B swizzle).
 int gemm_stage_row_bytes();
 // Whether tiles are computed by CTA pairs (.cta_group::2): each CTA then holds half
 // of the B and LoRA up-projection rows of a tile (their tensor-map boxes are bn/2).
-bool gemm_pair_enabled();
 bool gemm_uses_pair(int64_t M, int64_t N, int rpe);
 cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, int cm, cudaStream_t stream);
 cudaError_t status_word_ptr(unsigned** ptr);
