@@ -87,55 +87,147 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
   return __half22float2(*reinterpret_cast<__half2*>(&h2));
 }
 
-// Encode 8 FP32 values that share the block decode step t (with rcp = 1/t) into
-// 8 E2M1 codes packed in a uint32 (element 0 in bits 0..3).  Signed-zero codes
-// when t == 0 or the element is zero.  With t > 0 and a finite rcp a zero element
-// already encodes as a zero magnitude; the masked path covers rcp = inf (a
-// subnormal t), where 0 * inf would otherwise be NaN.
-__device__ __forceinline__ uint32_t encode8(const float* x, float t, float rcp) {
-  uint32_t w = 0;
-  if (t > 0.0f && rcp <= 3.4028234663852886e38f) {
-    // x * rcp keeps the sign of x (rcp > 0) and the convert keeps it on zeros.  The
-    // products are formed two at a time (mul.rn.f32x2 rounds each lane as mul.rn.f32
-    // does) and the four code bytes are packed by one vector move.
-    asm("{\n\t"
-        ".reg .b64 rr, p0, p1, p2, p3;\n\t"
-        ".reg .f32 q0, q1, q2, q3, q4, q5, q6, q7;\n\t"
-        ".reg .b8 c0, c1, c2, c3;\n\t"
-        "mov.b64 rr, {%9, %9};\n\t"
-        "mov.b64 p0, {%1, %2};\n\t"
-        "mov.b64 p1, {%3, %4};\n\t"
-        "mov.b64 p2, {%5, %6};\n\t"
-        "mov.b64 p3, {%7, %8};\n\t"
-        "mul.rn.f32x2 p0, p0, rr;\n\t"
-        "mul.rn.f32x2 p1, p1, rr;\n\t"
-        "mul.rn.f32x2 p2, p2, rr;\n\t"
-        "mul.rn.f32x2 p3, p3, rr;\n\t"
-        "mov.b64 {q0, q1}, p0;\n\t"
-        "mov.b64 {q2, q3}, p1;\n\t"
-        "mov.b64 {q4, q5}, p2;\n\t"
-        "mov.b64 {q6, q7}, p3;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 c0, q1, q0;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 c1, q3, q2;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 c2, q5, q4;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 c3, q7, q6;\n\t"
-        "mov.b32 %0, {c0, c1, c2, c3};\n\t"
-        "}"
-        : "=r"(w)
-        : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
-          "f"(x[7]), "f"(rcp));
-    return w;
+// Element encode of a block with decode step t = RN(e4m3(s) g):
+//   q = e2m1_rne_satfinite(RN(x / t)),
+// the quotient being one IEEE division.  A division per element is slow on the
+// GPU, so the code is certified from two products instead.  Per block, rlo and rhi
+// bracket 1/t: with rcp = RN(1/t) (relative error at most 2^-24, and normal since
+// t < 2^126), rlo = RN(rcp (1 - 2^-21)) < 1/t < rhi = RN(rcp (1 + 2^-21)).  Then
+// |x| rlo <= |x / t| <= |x| rhi, and rounding to FP32 and then to E2M1 are both
+// monotonic, so when RN(x rlo) and RN(x rhi) give the same E2M1 code, RN(x / t)
+// gives it too (a zero x gives the signed zero either way).  Only where the bracket
+// straddles an E2M1 rounding threshold (about one element in 10^5, or every
+// element whose quotient is exactly a threshold) is the code decided exactly
+// without the products (e2m1_code_exact).
+struct BlockStep {
+  float t;    // decode step e4m3(s) * g
+  float rlo;  // < 1/t (0 when t == 0)
+  float rhi;  // > 1/t (0 when t == 0; infinite when 1/t overflows)
+};
+
+__device__ __forceinline__ BlockStep block_step(float t) {
+  BlockStep b;
+  b.t = t;
+  if (t == 0.0f) {
+    b.rlo = b.rhi = 0.0f;
+  } else {
+    const float r = __fdiv_rn(1.0f, t);
+    b.rlo = __fmul_rn(r, 1.0f - 0x1p-21f);
+    b.rhi = __fmul_rn(r, 1.0f + 0x1p-21f);
   }
+  return b;
+}
+
+// Whether the products may certify codes for this block (t > 0 and 1/t finite).
+__device__ __forceinline__ bool step_certifiable(const BlockStep& b) {
+  return b.t > 0.0f && b.rhi <= 3.4028234663852886e38f;
+}
+
+// Magnitude code (0..7) of e2m1_rne_satfinite(RN(a / t)) for a >= 0 and t > 0,
+// decided without dividing.  The E2M1 thresholds m (0.25, 0.75, 1.25, 1.75, 2.5,
+// 3.5, 5) are FP32 values with an even significand, so RN(q) == m exactly when q
+// lies in [m - hl, m + hh], hl and hh being half the FP32 spacing below and above
+// m (ties at both ends go to the even m).  RN(q) <= m is then q <= m + hh, and
+// RN(q) == m is q >= m - hl as well, where the E2M1 rounding ties to the even code.
+// Each test is the sign of A - e T in FP64 with one fused multiply-add: e has at
+// most 27 significant bits and T 24, so e T is exact, and a nonzero difference is
+// far above FP64's underflow, so the computed sign is the exact one.  On a tie
+// (RN(q) == m) the code is the even one of the two neighbours.
+__device__ __forceinline__ int e2m1_side(double A, double T, double mid, double hl, double hh) {
+  if (fma(-(mid + hh), T, A) > 0.0) return 1;   // RN(q) > mid
+  if (fma(-(mid - hl), T, A) >= 0.0) return 0;  // RN(q) == mid
+  return -1;                                     // RN(q) < mid
+}
+__device__ __forceinline__ uint32_t e2m1_mag_exact(float a, float t) {
+  const double A = (double)a, T = (double)t;
+  int s;
+  // thresholds in increasing order; the first one that RN(q) does not exceed decides
+  if ((s = e2m1_side(A, T, 0.25, 0x1p-27, 0x1p-26)) <= 0) return s < 0 ? 0u : 0u;
+  if ((s = e2m1_side(A, T, 0.75, 0x1p-25, 0x1p-25)) <= 0) return s < 0 ? 1u : 2u;
+  if ((s = e2m1_side(A, T, 1.25, 0x1p-24, 0x1p-24)) <= 0) return s < 0 ? 2u : 2u;
+  if ((s = e2m1_side(A, T, 1.75, 0x1p-24, 0x1p-24)) <= 0) return s < 0 ? 3u : 4u;
+  if ((s = e2m1_side(A, T, 2.5, 0x1p-23, 0x1p-23)) <= 0) return s < 0 ? 4u : 4u;
+  if ((s = e2m1_side(A, T, 3.5, 0x1p-23, 0x1p-23)) <= 0) return s < 0 ? 5u : 6u;
+  if ((s = e2m1_side(A, T, 5.0, 0x1p-22, 0x1p-22)) <= 0) return s < 0 ? 6u : 6u;
+  return 7u;
+}
+
+// The code of one element, e2m1(RN(x / t)), by the exact decision above: a signed
+// zero when t == 0 (a zero block or a zero tensor); the sign bit of a code is the
+// sign bit of x, also when the value rounds to zero.
+__device__ __forceinline__ uint32_t e2m1_code_exact(float x, float t) {
+  const uint32_t sg = sign_bit(x) << 3;
+  if (!(t > 0.0f)) return sg;
+  return sg | e2m1_mag_exact(fabsf(x), t);
+}
+
+// Element i (runtime, 0..7) of eight register values, by a chain of selects: an
+// indexed register array would move to local memory.
+__device__ __forceinline__ float pick8(const float* x, uint32_t i) {
+  float v = x[7];
 #pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    float a0 = fabsf(x[i]), a1 = fabsf(x[i + 1]);
-    uint32_t mag = (t == 0.0f) ? 0u : e2m1x2_mag(__fmul_rn(a0, rcp), __fmul_rn(a1, rcp));
-    if (a0 == 0.0f) mag &= 0xF0u;
-    if (a1 == 0.0f) mag &= 0x0Fu;
-    uint32_t b = mag | (sign_bit(x[i]) << 3) | (sign_bit(x[i + 1]) << 7);
-    w |= b << (4 * i);
+  for (int k = 6; k >= 0; --k) v = (i == (uint32_t)k) ? x[k] : v;
+  return v;
+}
+
+// Replace, in the packed codes w, every code whose nibble is set in `redo` by the
+// exactly decided code.  A loop over the marked elements (not unrolled): the rare
+// path stays short in the instruction stream.
+__device__ __forceinline__ uint32_t fix_codes_exact(uint32_t w, uint32_t redo, const float* x,
+                                                    float t) {
+#pragma unroll 1
+  for (uint32_t i = 0; i < 8; ++i) {
+    if ((redo >> (4 * i)) & 0xFu) {
+      const uint32_t c = e2m1_code_exact(pick8(x, i), t);
+      w = (w & ~(0xFu << (4 * i))) | (c << (4 * i));
+    }
   }
   return w;
+}
+
+// RN(x * f) for 8 values -> 8 E2M1 codes packed in a uint32 (element 0 in bits
+// 0..3).  The products are formed two at a time (mul.rn.f32x2 rounds each lane as
+// mul.rn.f32 does) and the four code bytes are packed by one vector move.
+__device__ __forceinline__ uint32_t e2m1x8_of_products(const float* x, float f) {
+  uint32_t w;
+  asm("{\n\t"
+      ".reg .b64 rr, p0, p1, p2, p3;\n\t"
+      ".reg .f32 q0, q1, q2, q3, q4, q5, q6, q7;\n\t"
+      ".reg .b8 c0, c1, c2, c3;\n\t"
+      "mov.b64 rr, {%9, %9};\n\t"
+      "mov.b64 p0, {%1, %2};\n\t"
+      "mov.b64 p1, {%3, %4};\n\t"
+      "mov.b64 p2, {%5, %6};\n\t"
+      "mov.b64 p3, {%7, %8};\n\t"
+      "mul.rn.f32x2 p0, p0, rr;\n\t"
+      "mul.rn.f32x2 p1, p1, rr;\n\t"
+      "mul.rn.f32x2 p2, p2, rr;\n\t"
+      "mul.rn.f32x2 p3, p3, rr;\n\t"
+      "mov.b64 {q0, q1}, p0;\n\t"
+      "mov.b64 {q2, q3}, p1;\n\t"
+      "mov.b64 {q4, q5}, p2;\n\t"
+      "mov.b64 {q6, q7}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, q1, q0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, q3, q2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, q5, q4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, q7, q6;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t"
+      "}"
+      : "=r"(w)
+      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+        "f"(x[7]), "f"(f));
+  return w;
+}
+
+// Encode 8 FP32 values of one block (element 0 in bits 0..3 of the result).
+__device__ __forceinline__ uint32_t encode8(const float* x, const BlockStep& b) {
+  uint32_t wl = 0, redo = 0xFFFFFFFFu;
+  if (step_certifiable(b)) {
+    wl = e2m1x8_of_products(x, b.rlo);
+    redo = wl ^ e2m1x8_of_products(x, b.rhi);
+  }
+  if (redo == 0u) return wl;
+  return fix_codes_exact(wl, redo, x, b.t);
 }
 
 // Dequantise one block of 16 codes (8 bytes) with decode step s = e4m3(scale) * g.
@@ -163,36 +255,36 @@ __device__ __forceinline__ TensorScale tensor_scale(float amax) {
   return s;
 }
 
-// Block scale byte and decode step for a block whose absolute maximum is amax_blk.
-__device__ __forceinline__ uint32_t block_scale(float amax_blk, TensorScale ts, float* t,
-                                                float* rcp) {
+// Block scale byte s = e4m3(RN(amax_blk / d)) and the block's decode step for a
+// block whose absolute maximum is amax_blk.
+__device__ __forceinline__ uint32_t block_scale(float amax_blk, TensorScale ts, BlockStep* st) {
   uint32_t s = (ts.g == 0.0f) ? 0u : e4m3_from_f32(__fdiv_rn(amax_blk, ts.d));
-  float tt = __fmul_rn(e4m3_to_f32(s), ts.g);
-  *t = tt;
-  *rcp = (tt == 0.0f) ? 0.0f : __fdiv_rn(1.0f, tt);
+  *st = block_step(__fmul_rn(e4m3_to_f32(s), ts.g));
   return s;
 }
 
-// Per-tensor table of a block's decode step t = RN(e4m3(s) g) and rcp = RN(1/t)
-// (0 for t = 0) for every scale byte an encoder can produce (0 .. 0x7E, 0x7F for a
-// NaN), kept in shared memory and filled once per CTA: it replaces the division
-// 1/t of block_scale.  The scale byte itself comes from q = amax * RN(1/d): q is
+// Per-tensor table of a block's decode step t = RN(e4m3(s) g) and its reciprocal
+// bracket (BlockStep) for every scale byte an encoder can produce (0 .. 0x7E, 0x7F
+// for a NaN), kept in shared memory and filled once per CTA: it replaces the
+// division 1/t of block_scale.  The scale byte itself comes from q = amax * RN(1/d): q is
 // within 2^-22.4 of RN(amax / d) (relative), so when q (1 - 2^-21) and q (1 + 2^-21)
 // round to the same E4M3 byte, so does RN(amax / d) (the rounding is monotonic);
 // otherwise the exact division decides.  E4M3 thresholds lie at 2^-10 and above,
 // so subnormal quotients never reach the check's margin.
 struct ScaleTable {
   float t[128];
-  float rcp[128];
+  float rlo[128];
+  float rhi[128];
   float rcp_d;  // RN(1/d), or 0 when the fast quotient may not be used
 };
 
 // Fill the table (all threads of the CTA; the caller synchronises afterwards).
 __device__ __forceinline__ void scale_table_init(ScaleTable* tab, TensorScale ts) {
   for (int i = threadIdx.x; i < 128; i += blockDim.x) {
-    const float t = __fmul_rn(e4m3_to_f32((uint32_t)i), ts.g);
-    tab->t[i] = t;
-    tab->rcp[i] = (t == 0.0f) ? 0.0f : __fdiv_rn(1.0f, t);
+    const BlockStep b = block_step(__fmul_rn(e4m3_to_f32((uint32_t)i), ts.g));
+    tab->t[i] = b.t;
+    tab->rlo[i] = b.rlo;
+    tab->rhi[i] = b.rhi;
   }
   if (threadIdx.x == 0) {
     const float r = ts.d > 0.0f ? __fdiv_rn(1.0f, ts.d) : 0.0f;
@@ -200,9 +292,18 @@ __device__ __forceinline__ void scale_table_init(ScaleTable* tab, TensorScale ts
   }
 }
 
-// block_scale() with the table: the same byte, t and rcp.
+// The decode step of scale byte s from the table.
+__device__ __forceinline__ BlockStep table_step(const ScaleTable* tab, uint32_t s) {
+  BlockStep b;
+  b.t = tab->t[s & 0x7Fu];
+  b.rlo = tab->rlo[s & 0x7Fu];
+  b.rhi = tab->rhi[s & 0x7Fu];
+  return b;
+}
+
+// block_scale() with the table: the same byte and decode step.
 __device__ __forceinline__ uint32_t block_scale_tab(float amax_blk, TensorScale ts,
-                                                    const ScaleTable* tab, float* t, float* rcp) {
+                                                    const ScaleTable* tab, BlockStep* st) {
   uint32_t s = 0;
   if (ts.g != 0.0f) {
     const float rd = tab->rcp_d;
@@ -211,8 +312,7 @@ __device__ __forceinline__ uint32_t block_scale_tab(float amax_blk, TensorScale 
     if (rd == 0.0f || s != e4m3_from_f32(__fmul_rn(q, 1.0f + 0x1p-21f)))
       s = e4m3_from_f32(__fdiv_rn(amax_blk, ts.d));
   }
-  *t = tab->t[s & 0x7Fu];
-  *rcp = tab->rcp[s & 0x7Fu];
+  *st = table_step(tab, s);
   return s;
 }
 

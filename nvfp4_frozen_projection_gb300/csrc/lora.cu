@@ -402,12 +402,13 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t am = max(absmax_bf16x8_bits(xc[h][0]), absmax_bf16x8_bits(xc[h][1]));
-        float t, rcp, f8[8];
-        const uint32_t sc = block_scale_tab(__uint_as_float(am), tsq, &tab[0], &t, &rcp);
+        float f8[8];
+        BlockStep st;
+        const uint32_t sc = block_scale_tab(__uint_as_float(am), tsq, &tab[0], &st);
         bf16x8_to_f32(xc[h][0], f8);
-        const uint32_t w0 = encode8(f8, t, rcp);
+        const uint32_t w0 = encode8(f8, st);
         bf16x8_to_f32(xc[h][1], f8);
-        const uint32_t w1 = encode8(f8, t, rcp);
+        const uint32_t w1 = encode8(f8, st);
         const int64_t row = row0 + 8 * h;
         if (h ? ok1 : ok0)
           *reinterpret_cast<uint2*>(qz.codes + row * (N >> 1) + (int64_t)cc * 32 + 8 * c) =

@@ -135,11 +135,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm_encode(
           f[i] = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
           am = max(am, __float_as_uint(f[i]) & 0x7FFFFFFFu);
         }
-        float t, rcp;
-        const uint32_t s = block_scale_tab(__uint_as_float(am), ts, &tab, &t, &rcp);
+        BlockStep st;
+        const uint32_t s = block_scale_tab(__uint_as_float(am), ts, &tab, &st);
         uint2 cw;
-        cw.x = encode8(f, t, rcp);
-        cw.y = encode8(f + 8, t, rcp);
+        cw.x = encode8(f, st);
+        cw.y = encode8(f + 8, st);
         *reinterpret_cast<uint2*>(codes + row * (H >> 1) + b * 8) = cw;
         sf[sf_offset(row, b, nb)] = (uint8_t)s;
       }
@@ -293,25 +293,19 @@ __global__ void __launch_bounds__(256, 3) k_silu_amax(const uint16_t* __restrict
 // Pass 2: one thread per block of 16 columns of one row; encodes h, gate and up.
 // Fast values give the exact encoding of h wherever both roundings are certain:
 // the block scale when e4m3 of the fast block maximum over d, widened by
-// (1 -/+ 2r), rounds to one code; an element's code when its scaled fast value
-// widened by (1 -/+ 2r) rounds to one E2M1 code (the exact scaled value lies in
-// between, and both roundings are monotonic).  Elements that fail the second test
-// are encoded from their exact values; a block that fails the first, or lies
-// outside the fast bound, is encoded from exact values throughout.
+// (1 -/+ 2r), rounds to one code; an element's code e2m1(RN(h / t)) when the fast
+// value times fl = RN(rlo (1 - 2r)) and times fh = RN(rhi (1 + 2r)) round to one
+// E2M1 code.  With |h - fast| <= 2^-20.5 |h| and rlo < 1/t < rhi, the rounded
+// products bound |h| / t from both sides (each adds at most two roundings of
+// 2^-24 to a widening of 2r = 2^-17), and both roundings to FP32 and to E2M1 are
+// monotonic.  Elements that fail the second test are encoded from their exact
+// values; a block that fails the first, or lies outside the fast bound, is encoded
+// from exact values throughout.
 struct SiluOut {
   uint8_t* codes[3];
   uint8_t* sf[3];
   float* g[3];
 };
-
-// The E2M1 code of x as encode8 makes it for a block with decode step t and
-// rcp = 1/t (0 when t == 0).
-__device__ __forceinline__ uint32_t e2m1_code_of(float x, float t, float rcp) {
-  if (t > 0.0f && rcp <= 3.4028234663852886e38f) return e2m1x2_mag(__fmul_rn(x, rcp), 0.0f) & 0xFu;
-  const float a = fabsf(x);
-  const uint32_t mag = (t == 0.0f || a == 0.0f) ? 0u : (e2m1x2_mag(__fmul_rn(a, rcp), 0.0f) & 0x7u);
-  return mag | (sign_bit(x) << 3);
-}
 
 __global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restrict__ gu,
                                                         int64_t M, int64_t Mpad, int64_t I,
@@ -373,15 +367,17 @@ __global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restri
                                      max(absmax_bf16x8_bits(u0), absmax_bf16x8_bits(u1)),
                                      bf16x8_has_tiny(g0) || bf16x8_has_tiny(g1), am_blk) &&
                   ts[0].g > 0.0f;
-      float t = 0.0f, rcp = 0.0f;
+      BlockStep st = {0.0f, 0.0f, 0.0f};
+      float fl = 0.0f, fh = 0.0f;
       fast = fast && rcp_d > 0.0f;
       if (fast) {
         const float q = __fmul_rn(am_blk, rcp_d);
         sh = e4m3_from_f32(__fmul_rn(q, lo_f));
         fast = sh == e4m3_from_f32(__fmul_rn(q, hi_f));
-        t = tab[0].t[sh & 0x7Fu];
-        rcp = tab[0].rcp[sh & 0x7Fu];
-        fast = fast && t > 0.0f && rcp <= 3.4028234663852886e38f;
+        st = table_step(&tab[0], sh);
+        fl = __fmul_rn(st.rlo, lo_f);
+        fh = __fmul_rn(st.rhi, hi_f);
+        fast = fast && st.t > 0.0f && fh <= 3.4028234663852886e38f;
       }
       uint32_t redo = 0xFFFFu;
       if (fast) {
@@ -389,9 +385,8 @@ __global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restri
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
           // packed pairs: each lane rounds as the scalar multiply does
-          const float2 x = __fmul2_rn(make_float2(hf[i], hf[i + 1]), make_float2(rcp, rcp));
-          const float2 xl = __fmul2_rn(x, make_float2(lo_f, lo_f));
-          const float2 xh = __fmul2_rn(x, make_float2(hi_f, hi_f));
+          const float2 xl = __fmul2_rn(make_float2(hf[i], hf[i + 1]), make_float2(fl, fl));
+          const float2 xh = __fmul2_rn(make_float2(hf[i], hf[i + 1]), make_float2(fh, fh));
           const uint32_t cl = e2m1x2_mag(xl.x, xl.y);
           const uint32_t ch = e2m1x2_mag(xh.x, xh.y);
           const uint32_t d = cl ^ ch;
@@ -405,12 +400,12 @@ __global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restri
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
           em = max(em, __float_as_uint(silu_exact_at(g0, g1, u0, u1, i)) & 0x7FFFFFFFu);
-        sh = block_scale_tab(__uint_as_float(em), ts[0], &tab[0], &t, &rcp);
+        sh = block_scale_tab(__uint_as_float(em), ts[0], &tab[0], &st);
       }
       while (redo) {
         const int i = __ffs(redo) - 1;
         redo &= redo - 1;
-        const uint32_t c = e2m1_code_of(silu_exact_at(g0, g1, u0, u1, i), t, rcp);
+        const uint32_t c = e2m1_code_exact(silu_exact_at(g0, g1, u0, u1, i), st.t);
         const int sh4 = 4 * (i & 7);
         w[i >> 3] = (w[i >> 3] & ~(0xFu << sh4)) | (c << sh4);
       }
@@ -420,15 +415,15 @@ __global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restri
     // ---- gate and up: their BF16 values are exact
 #pragma unroll
     for (int k = 1; k < 3; ++k) {
-      float v[16];
-      bf16x8_to_f32(k == 1 ? g0 : u0, v);
-      bf16x8_to_f32(k == 1 ? g1 : u1, v + 8);
       const uint32_t am = max(absmax_bf16x8_bits(k == 1 ? g0 : u0), absmax_bf16x8_bits(k == 1 ? g1 : u1));
-      float tk, rk;
-      const uint32_t s = block_scale_tab(__uint_as_float(am), ts[k], &tab[k], &tk, &rk);
+      BlockStep sk;
+      const uint32_t s = block_scale_tab(__uint_as_float(am), ts[k], &tab[k], &sk);
       uint2 ck;
-      ck.x = encode8(v, tk, rk);
-      ck.y = encode8(v + 8, tk, rk);
+      float v[8];  // one half of the block at a time keeps fewer values live
+      bf16x8_to_f32(k == 1 ? g0 : u0, v);
+      ck.x = encode8(v, sk);
+      bf16x8_to_f32(k == 1 ? g1 : u1, v);
+      ck.y = encode8(v, sk);
       *reinterpret_cast<uint2*>(out.codes[k] + row * (I >> 1) + b * 8) = ck;
       out.sf[k][so] = (uint8_t)s;
     }

@@ -96,10 +96,10 @@ __global__ void __launch_bounds__(256, 4) k_quant_bf16(const uint16_t* __restric
         bf16x8_to_f32(v[2 * b + 1], f + 8);
         float amax_blk = __uint_as_float(
             max(absmax_bf16x8_bits(v[2 * b]), absmax_bf16x8_bits(v[2 * b + 1])));
-        float t, rcp;
-        uint32_t s = block_scale_tab(amax_blk, ts, &tab, &t, &rcp);
-        w[2 * b] = encode8(f, t, rcp);
-        w[2 * b + 1] = encode8(f + 8, t, rcp);
+        BlockStep st;
+        uint32_t s = block_scale_tab(amax_blk, ts, &tab, &st);
+        w[2 * b] = encode8(f, st);
+        w[2 * b + 1] = encode8(f + 8, st);
         sfw |= s << (8 * b);
       }
       uint4* dst = reinterpret_cast<uint4*>(codes + (int64_t)r * (K >> 1) + ch * 32);
@@ -138,9 +138,9 @@ __global__ void __launch_bounds__(256) k_pack_weight(const float* __restrict__ W
 #pragma unroll
     for (int j = 0; j < 8; ++j) m = max(m, __float_as_uint(f[j]) & 0x7FFFFFFFu);
     m = __reduce_max_sync(0xFFFFFFFFu, m);
-    float t, rcp;
-    const uint32_t s = block_scale(__uint_as_float(m), ts, &t, &rcp);
-    const uint32_t w = encode8(f, t, rcp);
+    BlockStep st;
+    const uint32_t s = block_scale(__uint_as_float(m), ts, &st);
+    const uint32_t w = encode8(f, st);
     if (!backward) {
       const int64_t n = tn * 16 + i;
       *reinterpret_cast<uint32_t*>(codes + n * (K >> 1) + tk * 8 + 4 * h) = w;

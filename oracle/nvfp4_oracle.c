@@ -97,19 +97,19 @@ float orc_amax(const float* x, int64_t n) {
 float orc_global_scale(float amax) { return amax / 2688.0f; }
 
 /* Encode one block of 16 values that share the E4M3 scale s (already chosen).
- * t = e4m3(s) * g is the block's decode step; the FP32 order is fixed as one
- * reciprocal per block and one product per element:
- *   r = 1 / t;  q = e2m1(x * r).
- * If t is zero every code is a signed zero, and a zero element always gets the
- * signed-zero code. */
+ * t = e4m3(s) * g is the block's decode step (one FP32 product), and each element
+ * is divided by it, one IEEE division rounded to nearest:
+ *   q = e2m1(x / t),
+ * the element formula q = e2m1_rne_sat(x / (s g)) with its FP32 order written out.
+ * If t is zero (a zero block, a zero tensor, or an underflowed product) every code
+ * is a signed zero.  A quotient that overflows saturates to 6. */
 static void encode_block(const float* x, int64_t stride, float t, uint32_t* codes16) {
-  float r = (t == 0.0f) ? 0.0f : 1.0f / t;
   for (int i = 0; i < 16; ++i) {
     float v = x[(int64_t)i * stride];
-    if (t == 0.0f || v == 0.0f)
-      codes16[i] = signbit(v) ? 8u : 0u; /* also when 1/t overflowed: 0 * inf */
+    if (t == 0.0f)
+      codes16[i] = signbit(v) ? 8u : 0u;
     else
-      codes16[i] = orc_e2m1_encode(v * r);
+      codes16[i] = orc_e2m1_encode(v / t);
   }
 }
 

@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle as orc
+from exact_round import code_of_quotient
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -150,7 +151,9 @@ def test_global_max_block_encodes_448():
 
 def test_quant_is_nearest_representable():
     """Each scale is the E4M3 value nearest amax_blk/(6g) and each code the E2M1
-    value nearest x * (1/t) (brute force over all candidates)."""
+    value nearest the FP32 quotient RN(x / t), t = RN(e4m3(s) g): the quotient is
+    formed from exact rationals here, so an encoder that multiplied by a rounded
+    reciprocal instead would fail wherever the two round apart."""
     rng = np.random.default_rng(4)
     x = (rng.standard_normal((16, 128)) * np.exp(rng.uniform(-3, 3, (16, 1)))).astype(np.float32)
     x[3, 5:21] = 0.0  # a zero block
@@ -168,10 +171,49 @@ def test_quant_is_nearest_representable():
             s = q.scales[r, b]
             assert s in s_best
             t = np.float32(orc.e4m3_decode(s)) * g
-            rcp = np.float32(1.0) / t if t != 0 else np.float32(0)
             for i in range(16):
-                want = (8 if np.signbit(blk[i]) else 0) if t == 0 else _e2m1_brute(blk[i] * rcp)
-                assert codes[r, b * 16 + i] == want
+                assert codes[r, b * 16 + i] == code_of_quotient(blk[i], t)
+
+
+def _near_midpoint_blocks(rng, nblk: int):
+    """Blocks of 16 FP32 values, each block's first element fixing the decode step
+    t (so that the scale is 448 under g) and the other 15 within a few FP32 steps of
+    m t for an E2M1 threshold m: the quotients sit on and around the thresholds."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    g = np.float32(np.exp(rng.uniform(-6, 6)))
+    t = np.float32(448.0) * g
+    x = np.zeros((nblk, 16), np.float32)
+    x[:, 0] = np.float32(2688.0) * g * np.float32(0.999)  # block amax -> scale 448
+    for b in range(nblk):
+        for i in range(1, 16):
+            m = rng.choice(mids)
+            v = np.float32(np.float32(m) * t)
+            for _ in range(int(rng.integers(-3, 4))):
+                v = np.nextafter(v, np.float32(np.inf) if rng.random() < 0.5 else np.float32(0))
+            x[b, i] = -v if rng.random() < 0.3 else v
+    return x, g
+
+
+def test_quant_divides_near_thresholds():
+    """Quotients on and beside the E2M1 thresholds: the oracle's codes follow the
+    exactly rounded quotient x / t, and the same inputs include elements where the
+    product with the rounded reciprocal, x * RN(1/t), rounds to another code (so an
+    encoder of that order is told apart)."""
+    rng = np.random.default_rng(41)
+    apart = 0
+    for trial in range(40):
+        x, g = _near_midpoint_blocks(rng, 8)
+        q = orc.quantize(x.reshape(1, -1), g=g)
+        codes = orc.unpack_codes(q.codes).reshape(8, 16)
+        assert np.all(q.scales == 0x7E)
+        t = np.float32(448.0) * g
+        rcp = np.float32(1.0) / t
+        for b in range(8):
+            for i in range(16):
+                want = code_of_quotient(x[b, i], t)
+                assert codes[b, i] == want
+                apart += int(_e2m1_brute(np.float32(x[b, i] * rcp)) != want)
+    assert apart > 0
 
 
 def test_zero_tensor():
