@@ -47,10 +47,13 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
 # they describe the kernel as of that capture.
 GEMM_TRAFFIC_BYTES = {"gate_up.fwd": 263.73e6}
 # (N, K) of each distinct frozen-projection GEMM of the layer-3b step (out = M x N)
-GEMM_SHAPES = {"q.fwd": (3072, 3072), "kv.fwd": (2048, 3072), "o.fwd": (3072, 3072),
-               "gate_up.fwd": (16384, 3072), "down.fwd": (3072, 8192),
+GEMM_SHAPES = {"q.fwd": (3072, 3072), "k.fwd": (1024, 3072), "v.fwd": (1024, 3072),
+               "o.fwd": (3072, 3072), "gate_up.fwd": (16384, 3072), "down.fwd": (3072, 8192),
                "down.dgrad": (8192, 3072), "gate_up.dgrad": (3072, 16384),
-               "o.dgrad": (3072, 3072), "q.dgrad": (3072, 3072), "kv.dgrad": (3072, 2048)}
+               "o.dgrad": (3072, 3072), "q.dgrad": (3072, 3072), "k.dgrad": (3072, 1024),
+               "v.dgrad": (3072, 1024)}
+PROJS = ("q", "k", "v", "o", "gate_up", "down")
+INPUTS = ("x", "attn", "dy", "dq", "dk", "dv")
 
 
 def peaks():
@@ -124,7 +127,7 @@ def oracle_stack_sample(d, packs, rows: int):
     step) over the first `rows` tokens.  Returns the GEMM FLOPs of the sample."""
     from oracle import chain
     sub = dict(d)
-    for k in ("x", "attn", "dy", "dq", "dkv"):
+    for k in INPUTS:
         sub[k] = d[k][:rows]
     chain.decoder_layer(sub, packs)
     return wl.gemm_flops_per_step(5, m=rows)
@@ -132,7 +135,7 @@ def oracle_stack_sample(d, packs, rows: int):
 
 def oracle_packs(d):
     import oracle as orc
-    return {k: orc.pack_weight(d[k].W) for k in ("q", "kv", "o", "gate_up", "down")}
+    return {k: orc.pack_weight(d[k].W) for k in PROJS}
 
 
 def cpu_baseline(d, rows=128, target_s=10.0):
@@ -148,7 +151,7 @@ def cpu_baseline(d, rows=128, target_s=10.0):
         t = time.perf_counter() - t0
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
             "kind": "oracle",
-            "sample": f"first {rows} tokens of the layer-3b step (fwd+dgrad chain, 10 FP64 "
+            "sample": f"first {rows} tokens of the layer-3b step (fwd+dgrad chain, 12 FP64 "
                       f"GEMMs on exactly dequantised operands), {n} pass(es) in {t:.1f} s; "
                       "weight packs excluded (offline, as on the GPU)"}
 
@@ -199,12 +202,13 @@ def time_gemm_kernels(stack, inputs, reps):
     """Per-GEMM kernel time (CUDA events around the GEMM kernel alone, on the launch
     stream), averaged over reps eager calls."""
     import nvfp4_frozen_projection_gb300 as pk
-    x, attn, dy, dq, dkv = inputs
+    x, attn, dy, dq, dk, dv = inputs
     stack.forward(x, attn)
-    stack.backward(dy, dq, dkv)
+    stack.backward(dy, dq, dk, dv)
     calls = {
         "q.fwd": lambda: stack.p["q"].forward(stack.xq1, stack.q),
-        "kv.fwd": lambda: stack.p["kv"].forward(stack.xq1, stack.kv),
+        "k.fwd": lambda: stack.p["k"].forward(stack.xq1, stack.k),
+        "v.fwd": lambda: stack.p["v"].forward(stack.xq1, stack.v),
         "o.fwd": lambda: stack.p["o"].forward(stack.attnq, stack.h1, residual=x),
         "gate_up.fwd": lambda: stack.p["gate_up"].forward(stack.xq2, stack.gu),
         "down.fwd": lambda: stack.p["down"].forward(stack.hq, stack.out, residual=stack.h1),
@@ -212,7 +216,8 @@ def time_gemm_kernels(stack, inputs, reps):
         "gate_up.dgrad": lambda: stack.p["gate_up"].dgrad(stack.dguq, stack.dgu, stack.dxn2),
         "o.dgrad": lambda: stack.p["o"].dgrad(stack.dh1q, stack.dh1, stack.dattn),
         "q.dgrad": lambda: stack.p["q"].dgrad(stack.dqq, dq, stack.dxn1),
-        "kv.dgrad": lambda: stack.p["kv"].dgrad(stack.dkvq, dkv, stack.dxn1, accumulate=True),
+        "k.dgrad": lambda: stack.p["k"].dgrad(stack.dkq, dk, stack.dxn1, accumulate=True),
+        "v.dgrad": lambda: stack.p["v"].dgrad(stack.dvq, dv, stack.dxn1, accumulate=True),
     }
     m = stack.m
     flops = GEMM_SHAPES
@@ -240,11 +245,12 @@ def time_gemm_kernels(stack, inputs, reps):
 def time_adapter_grads(stack, inputs, reps):
     """pact_lora_adapter_grad for each projection of the layer step, on the tensors a
     training step retains (CUDA events around each call)."""
-    x, attn, dy, dq, dkv = inputs
+    x, attn, dy, dq, dk, dv = inputs
     stack.forward(x, attn)
-    stack.backward(dy, dq, dkv)
+    stack.backward(dy, dq, dk, dv)
     p, m = stack.p, stack.m
-    pairs = {"q": (stack.xq1, dq), "kv": (stack.xq1, dkv), "o": (stack.attnq, stack.dh1),
+    pairs = {"q": (stack.xq1, dq), "k": (stack.xq1, dk), "v": (stack.xq1, dv),
+             "o": (stack.attnq, stack.dh1),
              "gate_up": (stack.xq2, stack.dgu), "down": (stack.hq, dy)}
     out, total = {}, 0.0
     for name, (xq, g) in pairs.items():
@@ -352,15 +358,14 @@ def main():
 
     d = wl.layer3b()
     stack = build_stack(d, dev)
-    names = ("x", "attn", "dy", "dq", "dkv")
     host_in = [torch.from_numpy(np.ascontiguousarray(d[n], np.float32)).bfloat16().pin_memory()
-               for n in names]
+               for n in INPUTS]
     inputs = [h.to(dev) for h in host_in]
-    x, attn, dy, dq, dkv = inputs
+    x, attn, dy, dq, dk, dv = inputs
 
     def step():
         stack.forward(x, attn)
-        stack.backward(dy, dq, dkv)
+        stack.backward(dy, dq, dk, dv)
 
     for _ in range(args.warmup):
         step()
@@ -426,7 +431,7 @@ def main():
     for st, ins in sets:
         def step_on(st=st, ins=ins):
             st.forward(ins[0], ins[1])
-            st.backward(ins[2], ins[3], ins[4])
+            st.backward(*ins[2:])
         if graph is not None and st is stack:
             runs.append(run)
             continue
@@ -512,7 +517,7 @@ def main():
         "dtype": "nvfp4", "data": "synthetic",
         "config": {"workload": "layer-3b", "tokens_per_step": m, "hidden": hid,
                    "intermediate": stack.inter, "q_kv_o": [3072, 1024, 1024, 3072], "r": 16,
-                   "gemms_per_step": 10, "fused": "k|v and gate|up run as one GEMM each",
+                   "gemms_per_step": 12, "fused": "gate|up runs as one GEMM",
                    "gemm_flops_per_step": flops,
                    "l2": "no flush: one step moves several GB through HBM (L2 is 129 MB)",
                    "graph": graph is not None, "parallelism": f"replicas x{world}"},

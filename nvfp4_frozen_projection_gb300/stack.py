@@ -57,16 +57,16 @@ class LoraLinear:
 class DecoderProjectionStack:
     """The seven LoRA projections of a Llama decoder layer with both RMSNorms, the
     SiLU-multiply and the two residual adds; forward and input-gradient pass.
-    Same-shaped projections that read the same input run as one fused GEMM: kv
-    (k | v) and gate_up (gate | up), each with its adapters side by side and B
-    block-diagonal."""
+    q, k and v are separate projections, each with its own frozen weight and
+    per-tensor scales; gate and up run as one fused GEMM (gate_up), adapters side
+    by side and B block-diagonal."""
 
     def __init__(self, m: int, proj: dict, gamma1, gamma2, eps: float = 1e-5,
                  concurrent: bool = True):
         self.m = m
         self.concurrent = concurrent
         self._side_streams = []
-        self.p = proj  # q, kv, o, gate_up, down -> LoraLinear
+        self.p = proj  # q, k, v, o, gate_up, down -> LoraLinear
         self.gamma1, self.gamma2, self.eps = gamma1, gamma2, float(eps)
         hidden = proj["q"].d_in
         inter = proj["down"].d_in
@@ -77,7 +77,8 @@ class DecoderProjectionStack:
         self.xq1 = NVFP4.empty(m, hidden, dev)
         self.rstd1 = torch.empty(m, dtype=torch.float32, device=dev)
         self.q = torch.empty(m, proj["q"].d_out, **bf)
-        self.kv = torch.empty(m, proj["kv"].d_out, **bf)  # k | v
+        self.k = torch.empty(m, proj["k"].d_out, **bf)
+        self.v = torch.empty(m, proj["v"].d_out, **bf)
         self.attnq = NVFP4.empty(m, hidden, dev)
         self.h1 = torch.empty(m, hidden, **bf)
         self.xq2 = NVFP4.empty(m, hidden, dev)
@@ -99,7 +100,8 @@ class DecoderProjectionStack:
         self.dh1q = NVFP4.empty(m, hidden, dev)
         self.dattn = torch.empty(m, hidden, **bf)
         self.dqq = NVFP4.empty(m, proj["q"].d_out, dev)
-        self.dkvq = NVFP4.empty(m, proj["kv"].d_out, dev)
+        self.dkq = NVFP4.empty(m, proj["k"].d_out, dev)
+        self.dvq = NVFP4.empty(m, proj["v"].d_out, dev)
         self.dxn1 = torch.empty(m, hidden, **bf)
         self.dx = torch.empty(m, hidden, **bf)
 
@@ -124,13 +126,15 @@ class DecoderProjectionStack:
                 p["o"].forward(self.attnq, self.h1, residual=x)
         pact_rmsnorm_quant(x, self.gamma1, self.eps, out=self.xq1, rstd=self.rstd1)
         side2 = self._side(1)
-        if side2 is not None:  # q and k|v both read xq1 only: run them side by side
+        if side2 is not None:  # q, k and v all read xq1 only: run them side by side
             side2.wait_stream(main)
             with torch.cuda.stream(side2):
-                p["kv"].forward(self.xq1, self.kv)
+                p["k"].forward(self.xq1, self.k)
+                p["v"].forward(self.xq1, self.v)
         p["q"].forward(self.xq1, self.q)
         if side2 is None:
-            p["kv"].forward(self.xq1, self.kv)
+            p["k"].forward(self.xq1, self.k)
+            p["v"].forward(self.xq1, self.v)
         else:
             main.wait_stream(side2)
         if side is None:
@@ -144,30 +148,31 @@ class DecoderProjectionStack:
         p["down"].forward(self.hq, self.out, residual=self.h1)
         return self.out
 
-    def adapter_grads(self, dy, dq, dkv) -> dict:
+    def adapter_grads(self, dy, dq, dk, dv) -> dict:
         """dA, dB of all seven adapters from the tensors the forward and backward
         retained (call after backward): each projection's NVFP4 input and the BF16
         gradient of its output.  For the fused projections the adapters' gradients
         are the diagonal blocks of dB (and the matching columns of dA)."""
         p = self.p
-        pairs = {"q": (self.xq1, dq), "kv": (self.xq1, dkv), "o": (self.attnq, self.dh1),
+        pairs = {"q": (self.xq1, dq), "k": (self.xq1, dk), "v": (self.xq1, dv),
+                 "o": (self.attnq, self.dh1),
                  "gate_up": (self.xq2, self.dgu), "down": (self.hq, dy)}
         return {name: p[name].adapter_grad(xq, g) for name, (xq, g) in pairs.items()}
 
-    def backward(self, dy, dq, dkv) -> torch.Tensor:
-        """dy: gradient of the layer output; dq and dkv (dk | dv): the gradients
-        flowing back from the (out of scope) attention core into the q/k/v outputs."""
+    def backward(self, dy, dq, dk, dv) -> torch.Tensor:
+        """dy: gradient of the layer output; dq, dk, dv: the gradients flowing back
+        from the (out of scope) attention core into the q, k, v outputs."""
         p = self.p
         main, side = torch.cuda.current_stream(), self._side()
         # every input gradient quantises its dY in the same pass that forms the
-        # LoRA down-projection (pact_lora_linear_dgrad_q).  The q and k|v input
+        # LoRA down-projection (pact_lora_linear_dgrad_q).  The q, k and v input
         # gradients need only the attention core's gradients: they run beside the
-        # down -> SiLU -> gate|up -> RMSNorm -> o chain.
+        # down -> SiLU -> gate|up -> RMSNorm -> o chain, accumulating into one
+        # buffer in the order q, k, v.
         if side is not None:
             side.wait_stream(main)
             with torch.cuda.stream(side):
-                p["q"].dgrad_q(dq, self.dqq, self.dxn1)
-                p["kv"].dgrad_q(dkv, self.dkvq, self.dxn1, accumulate=True)
+                self._qkv_dgrad(dq, dk, dv)
         p["down"].dgrad_q(dy, self.dyq, self.dh)
         pact_silu_mul_bwd(self.gq, self.uq, self.dh, dgateup=self.dgu, out_amax=self.dgu_amax)
         p["gate_up"].dgrad_q(self.dgu, self.dguq, self.dxn2, amax=self.dgu_amax)
@@ -175,23 +180,28 @@ class DecoderProjectionStack:
                          out_amax=self.dh1_amax)
         p["o"].dgrad_q(self.dh1, self.dh1q, self.dattn, amax=self.dh1_amax)  # into attention
         if side is None:
-            p["q"].dgrad_q(dq, self.dqq, self.dxn1)
-            p["kv"].dgrad_q(dkv, self.dkvq, self.dxn1, accumulate=True)
+            self._qkv_dgrad(dq, dk, dv)
         else:
             main.wait_stream(side)
         pact_rmsnorm_bwd(self.xq1, self.gamma1, self.rstd1, self.dxn1, dres=self.dh1, dx=self.dx)
         return self.dx
 
+    def _qkv_dgrad(self, dq, dk, dv):
+        p = self.p
+        p["q"].dgrad_q(dq, self.dqq, self.dxn1)
+        p["k"].dgrad_q(dk, self.dkq, self.dxn1, accumulate=True)
+        p["v"].dgrad_q(dv, self.dvq, self.dxn1, accumulate=True)
+
     @classmethod
     def from_workload(cls, d: dict, device) -> "DecoderProjectionStack":
         """Build the stack from host arrays: d holds x (for M), gamma1, gamma2, eps and
-        projections q, kv, o, gate_up, down with FP32 W [d_out, d_in], adapters A
+        projections q, k, v, o, gate_up, down with FP32 W [d_out, d_in], adapters A
         [d_in, r], B [r, d_out] (BF16 values) and alpha, r.  Weights are packed here."""
         def t32(a):
             return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
 
         proj = {}
-        for k in ("q", "kv", "o", "gate_up", "down"):
+        for k in ("q", "k", "v", "o", "gate_up", "down"):
             p = d[k]
             proj[k] = LoraLinear(t32(p.W), t32(p.A).bfloat16(), t32(p.B).bfloat16(),
                                  float(p.alpha) / float(p.r))

@@ -158,8 +158,10 @@ def attn1b(m: int = 26624, hidden: int = 2048, kv: int = 512):
 def layer3b(m: int = 8192, hidden: int = 3072, kv: int = 1024, inter: int = 8192):
     """Workload 5: Llama-3B decoder-layer projection stack.  The attention core is
     replaced by a seeded N(0,1) BF16 tensor; the gradients flowing into q/k/v from
-    the (out of scope) attention backward are seeded N(0, 1e-2^2) tensors.  The
-    stack runs k/v as the fused projection kv and gate/up as gate_up."""
+    the (out of scope) attention backward are seeded N(0, 1e-2^2) tensors.  q, k
+    and v are separate projections (each its own frozen weight and per-tensor
+    scale, each incoming gradient its own tensor); gate and up run as the fused
+    projection gate_up."""
     rng = rng_for(5)
     x = bf16_round(student_t_unit_rms(rng, (m, hidden)))
     gamma1 = bf16_round(1.0 + normal(rng, (hidden,), 0.1))
@@ -176,12 +178,9 @@ def layer3b(m: int = 8192, hidden: int = 3072, kv: int = 1024, inter: int = 8192
     dq = bf16_round(normal(rng, (m, hidden), 1e-2))
     dk = bf16_round(normal(rng, (m, kv), 1e-2))
     dv = bf16_round(normal(rng, (m, kv), 1e-2))
-    # k and v read the same input and have the same shape: one fused projection (as
-    # gate|up), whose incoming gradient is the attention core's dk | dv side by side
-    return dict(x=x, gamma1=gamma1, gamma2=gamma2, q=q, k=k, v=v, kv=fuse_outputs("kv", [k, v]),
-                o=o, gate_up=fuse_gate_up(gate, up), down=down, attn=attn,
-                dy=dy, dq=dq, dk=dk, dv=dv, dkv=np.concatenate([dk, dv], axis=1),
-                eps=np.float32(1e-5))
+    return dict(x=x, gamma1=gamma1, gamma2=gamma2, q=q, k=k, v=v, o=o,
+                gate_up=fuse_gate_up(gate, up), down=down, attn=attn,
+                dy=dy, dq=dq, dk=dk, dv=dv, eps=np.float32(1e-5))
 
 
 def gemm_flops_per_step(which: int, m: int | None = None) -> float:

@@ -4,8 +4,8 @@ layer runs them.
 TEST INFRASTRUCTURE ONLY (same rule as the rest of this package).
 
 Source: "PACT: NVFP4 Data-Flow LoRA Fine-Tuning on Consumer GPUs", Figure 2 (the
-decoder data flow: RMSNorm -> NVFP4 feeds q/k/v (k and v here one fused
-projection, as gate/up), attention output feeds o, a
+decoder data flow: RMSNorm -> NVFP4 feeds the q, k and v projections (three
+frozen weights, each with its own per-tensor scale), attention output feeds o, a
 residual add, RMSNorm -> NVFP4 feeds the fused gate/up projection, SiLU-multiply
 -> NVFP4 feeds down, a second residual add) and Table 7 (which tensors are kept in
 NVFP4, which in BF16, and that gradients are BF16).
@@ -84,12 +84,12 @@ def mlp(x, gate_up, down, dy, packs=None) -> dict:
 
 def decoder_layer(d: dict, packs=None) -> dict:
     """Forward and input-gradient pass of the decoder-layer projection stack.
-    d holds x, attn, gamma1, gamma2, eps, the projections q, kv (k and v fused as
-    one: their weights stacked into one frozen weight, adapters side by side, B
-    block-diagonal), o, gate_up, down, and the incoming gradients dy (of the layer
-    output), dq and dkv (dk | dv, side by side) from the attention core.  Returns
-    every intermediate."""
-    names = ("q", "kv", "o", "gate_up", "down")
+    d holds x, attn, gamma1, gamma2, eps, the projections q, k, v, o, gate_up,
+    down, and the incoming gradients dy (of the layer output) and dq, dk, dv (from
+    the attention core into the q, k, v outputs).  The three input gradients of q,
+    k and v accumulate into one BF16 buffer in that order.  Returns every
+    intermediate."""
+    names = ("q", "k", "v", "o", "gate_up", "down")
     P = {k: d[k] for k in names}
     packs = packs or _packs(P)
 
@@ -105,8 +105,8 @@ def decoder_layer(d: dict, packs=None) -> dict:
 
     o = {}
     o["xq1"], o["rstd1"] = rmsnorm_quant(d["x"], d["gamma1"], d["eps"])
-    o["q"] = fwd("q", o["xq1"])
-    o["kv"] = fwd("kv", o["xq1"])
+    for n in ("q", "k", "v"):
+        o[n] = fwd(n, o["xq1"])
     o["attnq"] = quantize(d["attn"])
     o["h1"] = fwd("o", o["attnq"], residual=d["x"])
     o["xq2"], o["rstd2"] = rmsnorm_quant(o["h1"], d["gamma2"], d["eps"])
@@ -122,9 +122,10 @@ def decoder_layer(d: dict, packs=None) -> dict:
                                       dres=d["dy"]))
     o["dh1q"] = quantize(o["dh1"])
     o["dattn"] = dgrad("o", o["dh1q"], o["dh1"])
-    o["dqq"], o["dkvq"] = quantize(d["dq"]), quantize(d["dkv"])
+    o["dqq"], o["dkq"], o["dvq"] = (quantize(d[n]) for n in ("dq", "dk", "dv"))
     acc = dgrad("q", o["dqq"], d["dq"])
-    o["dxn1"] = dgrad("kv", o["dkvq"], d["dkv"], acc)
+    acc = dgrad("k", o["dkq"], d["dk"], acc)
+    o["dxn1"] = dgrad("v", o["dvq"], d["dv"], acc)
     o["dx"] = round_bf16(rmsnorm_bwd(o["xq1"], d["gamma1"], o["rstd1"], o["dxn1"],
                                      dres=o["dh1"]))
     return o

@@ -69,9 +69,9 @@ def layer():
     d = wl.layer3b(**LAYER)
     ref = chain.decoder_layer(d)
     st = DecoderProjectionStack.from_workload(d, "cuda")
-    ins = [_dev(d[n]) for n in ("x", "attn", "dy", "dq", "dkv")]
+    ins = [_dev(d[n]) for n in ("x", "attn", "dy", "dq", "dk", "dv")]
     st.forward(ins[0], ins[1])
-    st.backward(ins[2], ins[3], ins[4])
+    st.backward(*ins[2:])
     torch.cuda.synchronize()
     pk.pact_check_status()
     return d, ref, st
@@ -82,12 +82,12 @@ def test_layer_stages_with_identical_inputs(layer):
     assert_nvfp4_equal(st.xq1, ref["xq1"], "xq1")
     assert np.array_equal(host(st.rstd1).view(np.uint32), ref["rstd1"].view(np.uint32))
     assert_nvfp4_equal(st.attnq, ref["attnq"], "attnq")
-    for n in ("q", "kv", "h1"):
+    for n in ("q", "k", "v", "h1"):
         _close(getattr(st, n), ref[n], n)
     assert_nvfp4_equal(st.dyq, ref["dyq"], "dyq")
     _close(st.dh, ref["dh"], "dh")
-    # the fused k|v gradient is one seeded tensor: one quantisation
-    for n in ("dqq", "dkvq"):
+    # the attention core's gradients are seeded tensors: each one quantisation
+    for n in ("dqq", "dkq", "dvq"):
         assert_nvfp4_equal(getattr(st, n), ref[n], n)
 
 
@@ -95,8 +95,8 @@ def test_layer_downstream_stages(layer):
     d, ref, st = layer
     for n in ("xq2", "hq", "gq", "uq", "dguq", "dh1q"):
         _nvfp4_chain_close(getattr(st, n), ref[n], n)
-    # dxn1 too: the k|v dgrad adds onto a BF16 buffer that each side rounded on its
-    # own after the q dgrad
+    # dxn1 too: the k and v dgrads add onto a BF16 buffer that each side rounded on
+    # its own after the q dgrad
     for n in ("gu", "out", "dgu", "dxn2", "dh1", "dattn", "dxn1", "dx"):
         _chain_close(getattr(st, n), ref[n], n)
 

@@ -84,10 +84,7 @@ def _layer_errors(d):
     loss = ((out * _t(d["dy"])).sum() + (q * _t(d["dq"])).sum() + (k * _t(d["dk"])).sum()
             + (v * _t(d["dv"])).sum())
     dx, dattn = torch.autograd.grad(loss, (x, attn))
-    # the chain runs k and v as one fused projection: its output columns are k | v
-    nk = k.shape[1]
-    got = {"q": o["q"], "k": o["kv"][:, :nk], "v": o["kv"][:, nk:]}
-    got.update({n: o[n] for n in ("h1", "gu", "out")})
+    got = {n: o[n] for n in ("q", "k", "v", "h1", "gu", "out")}
     err = {n: _rel(got[n], ref.detach())
            for n, ref in (("q", q), ("k", k), ("v", v), ("h1", h1), ("gu", gu), ("out", out))}
     err["dattn"] = _rel(o["dattn"], dattn)
@@ -140,7 +137,7 @@ PLANTED = {
     "dgrad frozen GEMM dropped": ("lora_linear_dgrad", lambda q, dy, w, A, B, al, dx_prev=None:
                                   _DGRAD(orc.quantize(np.zeros((q.rows, q.cols), np.float32)),
                                          dy, w, A, B, al, dx_prev)),
-    "q and k|v gradients not accumulated": ("lora_linear_dgrad",
+    "q, k and v gradients not accumulated": ("lora_linear_dgrad",
                                             lambda q, dy, w, A, B, al, dx_prev=None:
                                             _DGRAD(q, dy, w, A, B, al)),
     "RMSNorm residual gradient dropped": ("rmsnorm_bwd", lambda yq, g, r, dy, dres=None:
@@ -206,6 +203,7 @@ def test_decoder_layer_residual_paths_are_exact():
     assert np.array_equal(o["dx"], want)
     # and without the q/k/v gradients dx is dy itself
     d["dq"] = np.zeros_like(d["dq"])
-    d["dkv"] = np.zeros_like(d["dkv"])
+    d["dk"] = np.zeros_like(d["dk"])
+    d["dv"] = np.zeros_like(d["dv"])
     o = chain.decoder_layer(d)
     assert np.array_equal(o["dx"], d["dy"])
