@@ -82,12 +82,13 @@ size_t pact_nvfp4_sf_bytes(int64_t rows, int64_t cols);
  * are NVFP4, so X and dY are quantised before the frozen-projection GEMMs).
  *   amax_t = max |x|;  g = amax_t / (6*448);  per block of 16 along a row:
  *   s = e4m3_rne_satfinite(amax_blk / (6*g));  t = e4m3(s)*g;
- *   q = e2m1_rne_satfinite(x * (1/t))  (one reciprocal per block; signed zero
- *   codes when t == 0).
+ *   q = e2m1_rne_satfinite(x / t)  (one IEEE division per element, rounded to
+ *   nearest; signed zero codes when t == 0).
  * x: BF16 [M, K], row stride ldx elements (ldx >= K, ldx % 8 == 0), 16-byte aligned.
  * amax_opt: optional device pointer to a precomputed amax_t (skips the first pass).
  * out: codes/sf/g preallocated for [M, K]; out->rows == M, out->cols == K.
- * Rules: M >= 1, K % 64 == 0.  ws: pact_quant_nvfp4_workspace_size() bytes.
+ * Rules: M >= 1, K % 64 == 0, pad128(M) * K / 16 < 2^31.
+ * ws: pact_quant_nvfp4_workspace_size() bytes.
  */
 size_t pact_quant_nvfp4_workspace_size(int64_t M, int64_t K);
 int pact_quant_nvfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
@@ -231,7 +232,8 @@ int pact_lora_adapter_grad(const pact_nvfp4* xq, const uint16_t* dy, const uint1
  *   rstd = 1 / sqrt(ss/H + eps);  y_j = (x_j * rstd) * gamma_j   (FP32);
  * then y (FP32, never rounded to BF16) is quantised like pact_quant_nvfp4.
  *   x BF16 [M, H];  gamma BF16 [H];  yq NVFP4 [M, H] out;  rstd FP32 [M] out.
- * Rules: M >= 1, H % 64 == 0, H <= 16384.  ws: pact_rmsnorm_quant_workspace_size().
+ * Rules: M >= 1, H % 64 == 0, H <= 16384, pad128(M) * H / 16 < 2^31.
+ * ws: pact_rmsnorm_quant_workspace_size().
  */
 size_t pact_rmsnorm_quant_workspace_size(int64_t M, int64_t H);
 int pact_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M, int64_t H,

@@ -192,8 +192,8 @@ int pact_quant_nvfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const
   if (rc) return rc;
   if (!x) return fail(PACT_ERR_INVALID_ARG, "x is null");
   if (M < 1 || K < 64 || K % 64) return fail(PACT_ERR_SHAPE, "need M >= 1 and K %% 64 == 0");
-  if (pad_to(M, 128) * (K / 64) >= (int64_t)1 << 31)
-    return fail(PACT_ERR_SHAPE, "tensor too large: pad128(M) * K / 64 must be < 2^31");
+  if (pad_to(M, 128) * (K / 16) >= (int64_t)1 << 31)
+    return fail(PACT_ERR_SHAPE, "tensor too large: pad128(M) * K / 16 must be < 2^31");
   if (ldx < K || ldx % 8) return fail(PACT_ERR_SHAPE, "need ldx >= K and ldx %% 8 == 0");
   if (!aligned(x, 16)) return fail(PACT_ERR_ALIGN, "x must be 16-byte aligned");
   if ((rc = check_nvfp4(out, "out", M, K, 16))) return rc;
@@ -502,13 +502,16 @@ int pact_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M, int6
   if (!x || !gamma || !rstd) return fail(PACT_ERR_INVALID_ARG, "x, gamma and rstd are required");
   if (M < 1 || H < 64 || H % 64 || H > 16384)
     return fail(PACT_ERR_SHAPE, "need M >= 1, H %% 64 == 0, H <= 16384");
+  if (pad_to(M, 128) * (H / 16) >= (int64_t)1 << 31)
+    return fail(PACT_ERR_SHAPE, "tensor too large: pad128(M) * H / 16 must be < 2^31");
   if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(rstd, 4))
     return fail(PACT_ERR_ALIGN, "x and gamma must be 16-byte aligned");
   if ((rc = check_nvfp4(yq, "yq", M, H, 16))) return rc;
   if (!ws || ws_bytes < 256 || !aligned(ws, 256))
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
   cudaError_t e = launch_rmsnorm_quant(x, gamma, M, H, eps, (uint8_t*)yq->codes, (uint8_t*)yq->sf,
-                                       yq->g, rstd, (unsigned*)ws, d->sms, (cudaStream_t)stream);
+                                       yq->g, rstd, (unsigned*)ws, d->status, d->sms,
+                                       (cudaStream_t)stream);
   return e == cudaSuccess ? PACT_OK : cuda_fail(e, "rmsnorm launch");
 }
 

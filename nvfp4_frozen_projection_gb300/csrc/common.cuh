@@ -91,64 +91,80 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
 //   q = e2m1_rne_satfinite(RN(x / t)),
 // the quotient being one IEEE division.  A division per element is slow on the
 // GPU, so the code is certified from two products instead.  Per block, rlo and rhi
-// bracket 1/t: with rcp = RN(1/t) (relative error at most 2^-24, and normal since
-// t < 2^126), rlo = RN(rcp (1 - 2^-21)) < 1/t < rhi = RN(rcp (1 + 2^-21)).  Then
-// |x| rlo <= |x / t| <= |x| rhi, and rounding to FP32 and then to E2M1 are both
-// monotonic, so when RN(x rlo) and RN(x rhi) give the same E2M1 code, RN(x / t)
-// gives it too (a zero x gives the signed zero either way).  Only where the bracket
-// straddles an E2M1 rounding threshold (about one element in 10^5, or every
-// element whose quotient is exactly a threshold) is the code decided exactly
-// without the products (e2m1_code_exact).
+// bracket 1/t: both are a hardware reciprocal estimate of t widened by 2^-19, and
+// rlo t < 1 < rhi t is then verified exactly (the sign of a fused multiply-add),
+// so the bracket holds whatever the estimate's error.  Then |x| rlo <= |x / t| <=
+// |x| rhi, and rounding to FP32 and then to E2M1 are both monotonic, so when
+// RN(x rlo) and RN(x rhi) give the same E2M1 code, RN(x / t) gives it too (a zero x
+// gives the signed zero either way).  Only where the bracket straddles an E2M1
+// rounding threshold is the code decided exactly without the products.  With BF16
+// inputs that is about one element in 10^3: a BF16 value, an E4M3 scale and
+// g = RN(amax / 2688) from a BF16 amax often put a quotient on a threshold up to
+// the roundings of g and t, which is exactly where the division matters.  Blocks
+// with t below 2^-96 (only in tensors whose amax is below about 2^-76) take the
+// exact path throughout.
 struct BlockStep {
   float t;    // decode step e4m3(s) * g
-  float rlo;  // < 1/t (0 when t == 0)
-  float rhi;  // > 1/t (0 when t == 0; infinite when 1/t overflows)
+  float rlo;  // < 1/t, or 0 when the products may not be used
+  float rhi;  // > 1/t, or 0 likewise
 };
+
+__device__ __forceinline__ float rcp_estimate(float x) {
+  float y;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ BlockStep block_step(float t) {
   BlockStep b;
   b.t = t;
-  if (t == 0.0f) {
-    b.rlo = b.rhi = 0.0f;
-  } else {
-    const float r = __fdiv_rn(1.0f, t);
-    b.rlo = __fmul_rn(r, 1.0f - 0x1p-21f);
-    b.rhi = __fmul_rn(r, 1.0f + 0x1p-21f);
+  b.rlo = b.rhi = 0.0f;
+  if (t >= 0x1p-96f && t <= 0x1p+125f) {
+    const float r = rcp_estimate(t);
+    const float lo = __fmul_rn(r, 1.0f - 0x1p-19f), hi = __fmul_rn(r, 1.0f + 0x1p-19f);
+    if (__fmaf_rn(lo, t, -1.0f) < 0.0f && __fmaf_rn(hi, t, -1.0f) > 0.0f) {
+      b.rlo = lo;
+      b.rhi = hi;
+    }
   }
   return b;
 }
 
-// Whether the products may certify codes for this block (t > 0 and 1/t finite).
-__device__ __forceinline__ bool step_certifiable(const BlockStep& b) {
-  return b.t > 0.0f && b.rhi <= 3.4028234663852886e38f;
-}
+// Whether the products may certify codes for this block.
+__device__ __forceinline__ bool step_certifiable(const BlockStep& b) { return b.rlo > 0.0f; }
 
 // Magnitude code (0..7) of e2m1_rne_satfinite(RN(a / t)) for a >= 0 and t > 0,
 // decided without dividing.  The E2M1 thresholds m (0.25, 0.75, 1.25, 1.75, 2.5,
 // 3.5, 5) are FP32 values with an even significand, so RN(q) == m exactly when q
 // lies in [m - hl, m + hh], hl and hh being half the FP32 spacing below and above
-// m (ties at both ends go to the even m).  RN(q) <= m is then q <= m + hh, and
-// RN(q) == m is q >= m - hl as well, where the E2M1 rounding ties to the even code.
-// Each test is the sign of A - e T in FP64 with one fused multiply-add: e has at
-// most 27 significant bits and T 24, so e T is exact, and a nonzero difference is
-// far above FP64's underflow, so the computed sign is the exact one.  On a tie
-// (RN(q) == m) the code is the even one of the two neighbours.
-__device__ __forceinline__ int e2m1_side(double A, double T, double mid, double hl, double hh) {
-  if (fma(-(mid + hh), T, A) > 0.0) return 1;   // RN(q) > mid
-  if (fma(-(mid - hl), T, A) >= 0.0) return 0;  // RN(q) == mid
-  return -1;                                     // RN(q) < mid
+// m (ties at both ends go to the even m).  So RN(q) > m is a - (m + hh) t > 0, and
+// RN(q) == m is a - (m - hl) t >= 0 as well, where the E2M1 rounding ties to the
+// even code.  With D = RN(a - m t) from one fused multiply-add these are D > hh t
+// and D >= -hl t: near the threshold (|a - m t| <= 2^-17 m t) a - m t is a
+// multiple of at least a 2^-27 of a with at most ten significant bits, so D is
+// exact; far from it |D| exceeds both hh t and hl t (at most 2^-23 m t), whose
+// products are exact for t >= 2^-96.  A smaller t (and a, whose quotient is what
+// matters) is first scaled by 2^64, exactly: t < 2^-96 forces g < 2^-87 and so
+// a < 2^-75, far from overflow.
+__device__ __forceinline__ bool e2m1_above(float a, float t, float mid, float hh) {
+  return __fmaf_rn(-mid, t, a) > __fmul_rn(hh, t);
+}
+__device__ __forceinline__ bool e2m1_at(float a, float t, float mid, float hl) {
+  return __fmaf_rn(-mid, t, a) >= -__fmul_rn(hl, t);
 }
 __device__ __forceinline__ uint32_t e2m1_mag_exact(float a, float t) {
-  const double A = (double)a, T = (double)t;
-  int s;
+  if (t < 0x1p-96f) {
+    a = __fmul_rn(a, 0x1p+64f);
+    t = __fmul_rn(t, 0x1p+64f);
+  }
   // thresholds in increasing order; the first one that RN(q) does not exceed decides
-  if ((s = e2m1_side(A, T, 0.25, 0x1p-27, 0x1p-26)) <= 0) return s < 0 ? 0u : 0u;
-  if ((s = e2m1_side(A, T, 0.75, 0x1p-25, 0x1p-25)) <= 0) return s < 0 ? 1u : 2u;
-  if ((s = e2m1_side(A, T, 1.25, 0x1p-24, 0x1p-24)) <= 0) return s < 0 ? 2u : 2u;
-  if ((s = e2m1_side(A, T, 1.75, 0x1p-24, 0x1p-24)) <= 0) return s < 0 ? 3u : 4u;
-  if ((s = e2m1_side(A, T, 2.5, 0x1p-23, 0x1p-23)) <= 0) return s < 0 ? 4u : 4u;
-  if ((s = e2m1_side(A, T, 3.5, 0x1p-23, 0x1p-23)) <= 0) return s < 0 ? 5u : 6u;
-  if ((s = e2m1_side(A, T, 5.0, 0x1p-22, 0x1p-22)) <= 0) return s < 0 ? 6u : 6u;
+  if (!e2m1_above(a, t, 0.25f, 0x1p-26f)) return 0u;  // a tie at 0.25 goes to 0 too
+  if (!e2m1_above(a, t, 0.75f, 0x1p-25f)) return e2m1_at(a, t, 0.75f, 0x1p-25f) ? 2u : 1u;
+  if (!e2m1_above(a, t, 1.25f, 0x1p-24f)) return 2u;  // a tie at 1.25 goes to 2
+  if (!e2m1_above(a, t, 1.75f, 0x1p-24f)) return e2m1_at(a, t, 1.75f, 0x1p-24f) ? 4u : 3u;
+  if (!e2m1_above(a, t, 2.5f, 0x1p-23f)) return 4u;   // a tie at 2.5 goes to 4
+  if (!e2m1_above(a, t, 3.5f, 0x1p-23f)) return e2m1_at(a, t, 3.5f, 0x1p-23f) ? 6u : 5u;
+  if (!e2m1_above(a, t, 5.0f, 0x1p-22f)) return 6u;   // a tie at 5 goes to 6
   return 7u;
 }
 
@@ -170,17 +186,50 @@ __device__ __forceinline__ float pick8(const float* x, uint32_t i) {
   return v;
 }
 
-// Replace, in the packed codes w, every code whose nibble is set in `redo` by the
-// exactly decided code.  A loop over the marked elements (not unrolled): the rare
-// path stays short in the instruction stream.
-__device__ __forceinline__ uint32_t fix_codes_exact(uint32_t w, uint32_t redo, const float* x,
-                                                    float t) {
+// Every code of a block whose products may not be used (t below 2^-96, or a failed
+// bracket check): each code decided by e2m1_code_exact, in a loop that is not
+// unrolled (the path is for tensors of tiny magnitude only).
+__device__ __forceinline__ uint32_t codes8_exact(const float* x, float t) {
+  uint32_t w = 0;
 #pragma unroll 1
-  for (uint32_t i = 0; i < 8; ++i) {
-    if ((redo >> (4 * i)) & 0xFu) {
-      const uint32_t c = e2m1_code_exact(pick8(x, i), t);
-      w = (w & ~(0xFu << (4 * i))) | (c << (4 * i));
-    }
+  for (uint32_t i = 0; i < 8; ++i) w |= e2m1_code_exact(pick8(x, i), t) << (4 * i);
+  return w;
+}
+
+// Codes of a block with t == 0 (a zero block or a zero tensor): signed zeros.
+__device__ __forceinline__ uint32_t codes8_signed_zero(const float* x) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w |= (sign_bit(x[i]) << 3) << (4 * i);
+  return w;
+}
+
+// Fix the codes where the bracket straddles a threshold.  For such an element the
+// lower product gave magnitude code c and the upper c + 1, so the only threshold in
+// question is m = (e2m1(c) + e2m1(c + 1)) / 2 (exact; from the hardware decode),
+// and |x / t| is within 2^-18 m of it: the exact test of e2m1_mag_exact for that one
+// threshold decides (hh = half the FP32 spacing above m, hl the same below, which is
+// half of hh for m = 0.25, the one power of two among the thresholds).  The loop
+// visits only the straddling elements (usually one): in a warp its cost is the
+// largest count over the lanes, not the sum.
+__device__ __forceinline__ uint32_t fix_straddles(uint32_t wl, uint32_t redo, const float* x,
+                                                  float t) {
+  uint32_t w = wl;
+  // one bit per straddling element: bit 4i of redo | its neighbours folded down
+  uint32_t bits = (redo | (redo >> 1) | (redo >> 2) | (redo >> 3)) & 0x11111111u;
+#pragma unroll 1
+  while (bits) {
+    const uint32_t sh = (uint32_t)__ffs(bits) - 1u;  // 4 i
+    bits &= bits - 1u;
+    const float xi = pick8(x, sh >> 2);
+    const uint32_t c = (wl >> sh) & 7u;
+    const float2 d = e2m1x2_to_f32x2(c | ((c + 1u) << 4));
+    const float m = __fmul_rn(__fadd_rn(d.x, d.y), 0.5f);
+    const float hh = __int_as_float((__float_as_int(m) & 0x7F800000) - (24 << 23));
+    const float hl = c == 0u ? __fmul_rn(hh, 0.5f) : hh;
+    const float D = __fmaf_rn(-m, t, fabsf(xi));
+    const uint32_t mag = D > __fmul_rn(hh, t) ? c + 1u : (D >= -__fmul_rn(hl, t) ? c + (c & 1u) : c);
+    w = (w & ~(0xFu << sh)) | (((sign_bit(xi) << 3) | mag) << sh);
   }
   return w;
 }
@@ -221,13 +270,11 @@ __device__ __forceinline__ uint32_t e2m1x8_of_products(const float* x, float f) 
 
 // Encode 8 FP32 values of one block (element 0 in bits 0..3 of the result).
 __device__ __forceinline__ uint32_t encode8(const float* x, const BlockStep& b) {
-  uint32_t wl = 0, redo = 0xFFFFFFFFu;
-  if (step_certifiable(b)) {
-    wl = e2m1x8_of_products(x, b.rlo);
-    redo = wl ^ e2m1x8_of_products(x, b.rhi);
-  }
+  if (!step_certifiable(b)) return b.t == 0.0f ? codes8_signed_zero(x) : codes8_exact(x, b.t);
+  const uint32_t wl = e2m1x8_of_products(x, b.rlo);
+  const uint32_t redo = wl ^ e2m1x8_of_products(x, b.rhi);
   if (redo == 0u) return wl;
-  return fix_codes_exact(wl, redo, x, b.t);
+  return fix_straddles(wl, redo, x, b.t);
 }
 
 // Dequantise one block of 16 codes (8 bytes) with decode step s = e4m3(scale) * g.
@@ -243,76 +290,50 @@ __device__ __forceinline__ void dequant16_f32(uint2 cw, float s, float* out) {
     }
 }
 
-// Per-tensor scale and its block-scale divisor.
+// Per-tensor scale, its block-scale divisor and that divisor's reciprocal.
 struct TensorScale {
-  float g;  // amax / 2688
-  float d;  // 6 * g
+  float g;      // amax / 2688
+  float d;      // 6 * g
+  float rcp_d;  // RN(1 / d), or 0 when the fast block-scale quotient may not be used
 };
 __device__ __forceinline__ TensorScale tensor_scale(float amax) {
   TensorScale s;
   s.g = __fdiv_rn(amax, 2688.0f);
   s.d = __fmul_rn(6.0f, s.g);
+  const float r = s.d > 0.0f ? __fdiv_rn(1.0f, s.d) : 0.0f;
+  s.rcp_d = (r > 0.0f && r <= 3.4028234663852886e38f) ? r : 0.0f;
   return s;
 }
 
-// Block scale byte s = e4m3(RN(amax_blk / d)) and the block's decode step for a
-// block whose absolute maximum is amax_blk.
-__device__ __forceinline__ uint32_t block_scale(float amax_blk, TensorScale ts, BlockStep* st) {
-  uint32_t s = (ts.g == 0.0f) ? 0u : e4m3_from_f32(__fdiv_rn(amax_blk, ts.d));
-  *st = block_step(__fmul_rn(e4m3_to_f32(s), ts.g));
+// The decode step of scale byte s under the per-tensor scale g.
+__device__ __forceinline__ BlockStep scale_step(uint32_t s, const TensorScale& ts) {
+  return block_step(__fmul_rn(e4m3_to_f32(s), ts.g));
+}
+
+// Block scale byte s = e4m3(RN(amax_blk / d)) and the block's decode step, with the
+// division itself (the offline weight pack).
+__device__ __forceinline__ uint32_t block_scale(float amax_blk, const TensorScale& ts,
+                                                BlockStep* st) {
+  const uint32_t s = (ts.g == 0.0f) ? 0u : e4m3_from_f32(__fdiv_rn(amax_blk, ts.d));
+  *st = scale_step(s, ts);
   return s;
 }
 
-// Per-tensor table of a block's decode step t = RN(e4m3(s) g) and its reciprocal
-// bracket (BlockStep) for every scale byte an encoder can produce (0 .. 0x7E, 0x7F
-// for a NaN), kept in shared memory and filled once per CTA: it replaces the
-// division 1/t of block_scale.  The scale byte itself comes from q = amax * RN(1/d): q is
-// within 2^-22.4 of RN(amax / d) (relative), so when q (1 - 2^-21) and q (1 + 2^-21)
-// round to the same E4M3 byte, so does RN(amax / d) (the rounding is monotonic);
-// otherwise the exact division decides.  E4M3 thresholds lie at 2^-10 and above,
-// so subnormal quotients never reach the check's margin.
-struct ScaleTable {
-  float t[128];
-  float rlo[128];
-  float rhi[128];
-  float rcp_d;  // RN(1/d), or 0 when the fast quotient may not be used
-};
-
-// Fill the table (all threads of the CTA; the caller synchronises afterwards).
-__device__ __forceinline__ void scale_table_init(ScaleTable* tab, TensorScale ts) {
-  for (int i = threadIdx.x; i < 128; i += blockDim.x) {
-    const BlockStep b = block_step(__fmul_rn(e4m3_to_f32((uint32_t)i), ts.g));
-    tab->t[i] = b.t;
-    tab->rlo[i] = b.rlo;
-    tab->rhi[i] = b.rhi;
-  }
-  if (threadIdx.x == 0) {
-    const float r = ts.d > 0.0f ? __fdiv_rn(1.0f, ts.d) : 0.0f;
-    tab->rcp_d = (r > 0.0f && r <= 3.4028234663852886e38f) ? r : 0.0f;
-  }
-}
-
-// The decode step of scale byte s from the table.
-__device__ __forceinline__ BlockStep table_step(const ScaleTable* tab, uint32_t s) {
-  BlockStep b;
-  b.t = tab->t[s & 0x7Fu];
-  b.rlo = tab->rlo[s & 0x7Fu];
-  b.rhi = tab->rhi[s & 0x7Fu];
-  return b;
-}
-
-// block_scale() with the table: the same byte and decode step.
-__device__ __forceinline__ uint32_t block_scale_tab(float amax_blk, TensorScale ts,
-                                                    const ScaleTable* tab, BlockStep* st) {
+// The same byte without a division per block: q = amax_blk * RN(1/d) is within
+// 2^-22.4 of RN(amax_blk / d) (relative), so when q (1 - 2^-21) and q (1 + 2^-21)
+// round to the same E4M3 byte, so does RN(amax_blk / d) (the rounding is
+// monotonic); otherwise the division decides.  E4M3 thresholds lie at 2^-10 and
+// above, so subnormal quotients never reach the check's margin.
+__device__ __forceinline__ uint32_t block_scale_fast(float amax_blk, const TensorScale& ts,
+                                                     BlockStep* st) {
   uint32_t s = 0;
   if (ts.g != 0.0f) {
-    const float rd = tab->rcp_d;
-    const float q = __fmul_rn(amax_blk, rd);
+    const float q = __fmul_rn(amax_blk, ts.rcp_d);
     s = e4m3_from_f32(__fmul_rn(q, 1.0f - 0x1p-21f));
-    if (rd == 0.0f || s != e4m3_from_f32(__fmul_rn(q, 1.0f + 0x1p-21f)))
+    if (ts.rcp_d == 0.0f || s != e4m3_from_f32(__fmul_rn(q, 1.0f + 0x1p-21f)))
       s = e4m3_from_f32(__fdiv_rn(amax_blk, ts.d));
   }
-  *st = table_step(tab, s);
+  *st = scale_step(s, ts);
   return s;
 }
 

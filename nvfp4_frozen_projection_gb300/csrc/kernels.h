@@ -108,7 +108,7 @@ cudaError_t launch_lora_adapter_grad(const uint8_t* x_codes, const uint8_t* x_sf
 
 cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M,
                                  int64_t H, float eps, uint8_t* codes, uint8_t* sf, float* g,
-                                 float* rstd, unsigned* ws_amax, int num_sms,
+                                 float* rstd, unsigned* ws_amax, unsigned* status, int num_sms,
                                  cudaStream_t stream);
 cudaError_t launch_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I,
                                   const float* amax3_opt, uint8_t* const codes[3],

@@ -317,19 +317,17 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
   constexpr int SLOT = RP * kDyBRow;
   constexpr int XOFF = kDyRing * SLOT;  // the dY ring follows the B ring
   extern __shared__ __align__(16) uint8_t dsm[];
-  __shared__ ScaleTable tab[1];  // used with QUANT only
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int ns = (int)gridDim.x, split = (int)blockIdx.x;  // split == rank in the cluster
   const int64_t mb0 = (int64_t)blockIdx.y * 128;
   const int nch = (int)(N >> 6);
   const int ch0 = (int)((int64_t)nch * split / ns), ch1 = (int)((int64_t)nch * (split + 1) / ns);
-  TensorScale tsq = {0.0f, 0.0f};
+  TensorScale tsq = {0.0f, 0.0f, 0.0f};
   if constexpr (QUANT) {
     const float amax = qz.amax_opt ? *qz.amax_opt : __uint_as_float(*qz.amax_bits);
     tsq = tensor_scale(amax);
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *qz.g_out = tsq.g;
-    scale_table_init(&tab[0], tsq);
   }
   // rows r .. RP - 1 of every B slot stay zero (the copies never touch them)
   for (int i = threadIdx.x; i < kDyRing * (RP - r) * (kDyBRow / 4); i += blockDim.x) {
@@ -404,7 +402,7 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
         const uint32_t am = max(absmax_bf16x8_bits(xc[h][0]), absmax_bf16x8_bits(xc[h][1]));
         float f8[8];
         BlockStep st;
-        const uint32_t sc = block_scale_tab(__uint_as_float(am), tsq, &tab[0], &st);
+        const uint32_t sc = block_scale_fast(__uint_as_float(am), tsq, &st);
         bf16x8_to_f32(xc[h][0], f8);
         const uint32_t w0 = encode8(f8, st);
         bf16x8_to_f32(xc[h][1], f8);

@@ -14,136 +14,231 @@
 // Quantising a tensor needs its global amax first, so each fused quantiser runs
 // two passes: pass 1 computes the statistic/activation and its amax, pass 2
 // recomputes the FP32 values (re-reading the input, mostly from L2) and encodes.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace pact {
 
 // ============================================================== RMSNorm forward
-// One warp per row.  Lane l owns blocks l, l+32, ... (BPL of them); the sum of
-// squares runs block by block, element by element, then a butterfly over the
-// lanes (offsets 16, 8, 4, 2, 1).  The same order is the oracle's.
-template <int BPL>
-__device__ __forceinline__ float row_rstd(const uint4 (*xv)[2], int nb, int lane, float H,
-                                          float eps) {
-  float acc = 0.0f;
-#pragma unroll
-  for (int j = 0; j < BPL; ++j) {
-    if (lane + 32 * j < nb) {
-      float f[16];
-      bf16x8_to_f32(xv[j][0], f);
-      bf16x8_to_f32(xv[j][1], f + 8);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) acc = __fadd_rn(acc, __fmul_rn(f[i], f[i]));
-    }
-  }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1)
-    acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, off));
-  const float ms = __fdiv_rn(acc, H);
-  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+// Both passes stream whole rows through a per-warp ring of shared-memory slots,
+// filled by bulk asynchronous copies (one per row, issued by lane 0 and completed
+// on the slot's mbarrier), so every warp keeps several rows in flight while it
+// works on one, with few registers.  gamma is staged once per CTA.  Lane l owns
+// blocks l, l+32, ... (BPL of them) of a row.
+constexpr uint64_t kRowWaitNs = 2000000000ull;  // 2 s per ring wait
+
+struct RowRing {
+  uint32_t data;   // shared address of this warp's slot 0
+  uint32_t bars;   // shared address of this warp's barrier 0
+  uint32_t bytes;  // bytes of one row (one slot)
+  int ns;          // slots
+};
+
+// Lane 0 issues the copy of row `row` (bytes at src) into slot k.
+__device__ __forceinline__ void ring_issue(const RowRing& rr, int k, const void* src) {
+  mbar_expect_tx(rr.bars + 8u * k, rr.bytes);
+  bulk_load(rr.data + (uint32_t)k * rr.bytes, src, rr.bytes, rr.bars + 8u * k);
 }
 
+// Dynamic shared memory of a row-ring kernel: [gamma (padded to 128)] [warps x ns
+// slots] [warps x ns barriers].  Warps per CTA and ring depth are chosen so the
+// whole fits in 200 KB.
+struct RingShape {
+  int warps, ns;
+  size_t smem;
+};
+static RingShape ring_shape(int64_t H, int copies_per_row, bool with_gamma) {
+  const size_t row = (size_t)H * 2 * copies_per_row;
+  const size_t fixed = with_gamma ? (size_t)((H * 2 + 127) / 128 * 128) : 0;
+  const size_t avail = 200 * 1024 - fixed;
+  RingShape r;
+  r.warps = (int)std::min<size_t>(8, std::max<size_t>(1, avail / (2 * row)));
+  r.ns = (int)std::min<size_t>(4, std::max<size_t>(2, avail / (r.warps * row)));
+  r.smem = fixed + (size_t)r.warps * r.ns * row + (size_t)r.warps * r.ns * 8 + 128;
+  return r;
+}
+
+__device__ __forceinline__ void stage_gamma(uint8_t* sm, const uint16_t* gamma, int64_t H) {
+  for (int i = threadIdx.x; i < (int)(H >> 3); i += blockDim.x)
+    reinterpret_cast<uint4*>(sm)[i] = reinterpret_cast<const uint4*>(gamma)[i];
+}
+
+// Set up this warp's ring (barriers by lane 0) and return it.  The caller syncs the
+// CTA before the first copy.
+__device__ __forceinline__ RowRing ring_setup(uint8_t* sm, uint32_t base_off, int64_t H,
+                                              int copies, int ns) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  RowRing rr;
+  rr.bytes = (uint32_t)(H * 2 * copies);
+  rr.ns = ns;
+  rr.data = smem_addr(sm) + base_off + (uint32_t)(warp * ns) * rr.bytes;
+  rr.bars = smem_addr(sm) + base_off + (uint32_t)(nw * ns) * rr.bytes + 8u * (uint32_t)(warp * ns);
+  if ((threadIdx.x & 31) == 0) {
+    for (int k = 0; k < ns; ++k) mbar_init(rr.bars + 8u * k, 1);
+    fence_mbar_init();
+  }
+  return rr;
+}
+
+// Before a CTA leaves after a timeout: let this warp's copies still in flight land
+// (bounded), so no copy writes shared memory that another CTA may own next.
+__device__ __forceinline__ void ring_drain(const RowRing& rr, uint32_t pending, uint32_t phases) {
+  for (int k = 0; k < rr.ns; ++k)
+    if (pending & (1u << k)) mbar_wait(rr.bars + 8u * k, (phases >> k) & 1u, 10000000ull, nullptr);
+}
+
+// Pass 1: per row, rstd in the fixed order (sum of squares block by block, element
+// by element, per lane; then a butterfly over offsets 16, 8, 4, 2, 1; the oracle's
+// order) and max |y| of y = RN(RN(x rstd) gamma), folded into *amax_bits.
 template <int BPL>
 __global__ void __launch_bounds__(256) k_rmsnorm_stat(const uint16_t* __restrict__ x,
                                                       const uint16_t* __restrict__ gamma,
-                                                      int64_t M, int64_t H, float eps,
+                                                      int64_t M, int64_t H, float eps, int ns,
                                                       float* __restrict__ rstd,
-                                                      unsigned* __restrict__ amax_bits) {
+                                                      unsigned* __restrict__ amax_bits,
+                                                      unsigned* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t sm[];
   const int lane = threadIdx.x & 31;
   const int nb = (int)(H >> 4);
+  const uint32_t goff = (uint32_t)((H * 2 + 127) / 128 * 128);
+  stage_gamma(sm, gamma, H);
+  const RowRing rr = ring_setup(sm, goff, H, 1, ns);
+  __syncthreads();
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t step = (int64_t)gridDim.x * (blockDim.x >> 5);
+  uint32_t pending = 0, phases = 0;
+  if (lane == 0)
+    for (int k = 0; k < ns; ++k) {
+      const int64_t r = wid + k * step;
+      if (r < M) {
+        ring_issue(rr, k, x + r * H);
+        pending |= 1u << k;
+      }
+    }
   uint32_t amax = 0;
-  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < M;
-       row += (int64_t)gridDim.x * 8) {
-    uint4 xv[BPL][2];
-    const uint16_t* xr = x + row * H;
+  int k = 0;
+  uint32_t par = 0;
+  for (int64_t row = wid; row < M; row += step) {
+    // every lane observes the copy's completion; the decision to give up is the warp's
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(rr.bars + 8u * k, par, kRowWaitNs, nullptr))) {
+      if (lane == 0) {
+        atomicOr(status, PACT_DEV_TIMEOUT);
+        ring_drain(rr, pending, phases);
+      }
+      break;
+    }
+    const uint8_t* slot = sm + (rr.data - smem_addr(sm)) + (uint32_t)k * rr.bytes;
+    float acc = 0.0f;
 #pragma unroll
     for (int j = 0; j < BPL; ++j) {
       const int b = lane + 32 * j;
       if (b < nb) {
-        const uint4* p = reinterpret_cast<const uint4*>(xr + b * 16);
-        xv[j][0] = __ldg(p);
-        xv[j][1] = __ldg(p + 1);
+        float f[16];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(slot + 32 * b), f);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(slot + 32 * b + 16), f + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc = __fadd_rn(acc, __fmul_rn(f[i], f[i]));
       }
     }
-    const float rs = row_rstd<BPL>(xv, nb, lane, (float)H, eps);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+      acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, off));
+    const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, (float)H), eps)));
     if (lane == 0) rstd[row] = rs;
 #pragma unroll
     for (int j = 0; j < BPL; ++j) {
       const int b = lane + 32 * j;
       if (b < nb) {
         float f[16], gm[16];
-        bf16x8_to_f32(xv[j][0], f);
-        bf16x8_to_f32(xv[j][1], f + 8);
-        const uint4* gp = reinterpret_cast<const uint4*>(gamma + b * 16);
-        bf16x8_to_f32(__ldg(gp), gm);
-        bf16x8_to_f32(__ldg(gp + 1), gm + 8);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(slot + 32 * b), f);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(slot + 32 * b + 16), f + 8);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + 32 * b), gm);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + 32 * b + 16), gm + 8);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float y = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
-          amax = max(amax, __float_as_uint(y) & 0x7FFFFFFFu);
-        }
+        for (int i = 0; i < 16; ++i)
+          amax = max(amax, __float_as_uint(__fmul_rn(__fmul_rn(f[i], rs), gm[i])) & 0x7FFFFFFFu);
       }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      pending &= ~(1u << k);
+      const int64_t nr = row + (int64_t)ns * step;
+      if (nr < M) {
+        fence_proxy_async_smem();  // the slot's reads are done before the copy refills it
+        ring_issue(rr, k, x + nr * H);
+        pending |= 1u << k;
+        phases ^= 1u << k;
+      }
+    }
+    if (++k == ns) {
+      k = 0;
+      par ^= 1u;
     }
   }
   block_max_atomic(amax, amax_bits);
 }
 
-// Pass 2: y recomputed from x and the stored rstd, then encoded.  Rows are walked
-// in reverse so the tail of the tensor, last touched by pass 1, is read from L2
-// first.  Rows past M up to pad128(M) get zero scale bytes.
-template <int BPL>
+// Pass 2: y recomputed from x (read again, mostly from L2) and the stored rstd, then
+// encoded.  Streaming layout of the activation quantiser: lane = one block of 16
+// elements, warp = 32 consecutive blocks of the row-major [pad128(M), H/16] block
+// grid, the next block's loads in flight while the current one is encoded; gamma
+// and rstd come through L1.  Rows past M up to pad128(M) get zero scale bytes.
 __global__ void __launch_bounds__(256) k_rmsnorm_encode(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
-    const float* __restrict__ rstd, int64_t M, int64_t Mpad, int64_t H,
+    const float* __restrict__ rstd, int64_t M, int64_t Mpad, int64_t H, FastDiv bpr_div,
     const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ sf, float* __restrict__ g_out) {
-  const int lane = threadIdx.x & 31;
-  const int nb = (int)(H >> 4);
   const TensorScale ts = tensor_scale(__uint_as_float(*amax_bits));
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
-  __shared__ ScaleTable tab;
-  scale_table_init(&tab, ts);
-  __syncthreads();
-  for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < Mpad;
-       w += (int64_t)gridDim.x * 8) {
-    const int64_t row = Mpad - 1 - w;
-    if (row >= M) {
-#pragma unroll
-      for (int j = 0; j < BPL; ++j) {
-        const int b = lane + 32 * j;
-        if (b < nb) sf[sf_offset(row, b, nb)] = 0;
-      }
-      continue;
-    }
-    const float rs = rstd[row];
-    const uint16_t* xr = x + row * H;
-#pragma unroll
-    for (int j = 0; j < BPL; ++j) {
-      const int b = lane + 32 * j;
-      if (b < nb) {
-        const uint4* p = reinterpret_cast<const uint4*>(xr + b * 16);
-        const uint4* gp = reinterpret_cast<const uint4*>(gamma + b * 16);
-        float f[16], gm[16];
-        bf16x8_to_f32(__ldg(p), f);
-        bf16x8_to_f32(__ldg(p + 1), f + 8);
-        bf16x8_to_f32(__ldg(gp), gm);
-        bf16x8_to_f32(__ldg(gp + 1), gm + 8);
-        uint32_t am = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          f[i] = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
-          am = max(am, __float_as_uint(f[i]) & 0x7FFFFFFFu);
-        }
-        BlockStep st;
-        const uint32_t s = block_scale_tab(__uint_as_float(am), ts, &tab, &st);
-        uint2 cw;
-        cw.x = encode8(f, st);
-        cw.y = encode8(f + 8, st);
-        *reinterpret_cast<uint2*>(codes + row * (H >> 1) + b * 8) = cw;
-        sf[sf_offset(row, b, nb)] = (uint8_t)s;
+  const uint32_t bpr = (uint32_t)(H >> 4);
+  const uint32_t total = (uint32_t)Mpad * bpr;  // < 2^31 (checked by the caller)
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  uint32_t blk = blockIdx.x * blockDim.x + threadIdx.x;
+  uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
+  auto fetch = [&](uint32_t b) {
+    if (b < total) {
+      const uint32_t r = bpr_div.div(b);
+      if (r < M) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * H + (b - r * bpr) * 16);
+        n0 = __ldg(src);
+        n1 = __ldg(src + 1);
       }
     }
+  };
+  fetch(blk);
+  for (; blk - lane < total; blk += stride) {  // warp-uniform trip count
+    const uint4 v0 = n0, v1 = n1;
+    fetch(blk + stride);
+    const bool live = blk < total;
+    const uint32_t r = bpr_div.div(blk), cb = blk - r * bpr;
+    uint32_t sb = 0;
+    if (live && r < M) {
+      const float rs = __ldg(rstd + r);
+      const uint4* gp = reinterpret_cast<const uint4*>(gamma + cb * 16);
+      float f[16], gm[16];
+      bf16x8_to_f32(v0, f);
+      bf16x8_to_f32(v1, f + 8);
+      bf16x8_to_f32(__ldg(gp), gm);
+      bf16x8_to_f32(__ldg(gp + 1), gm + 8);
+      uint32_t am = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        f[i] = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
+        am = max(am, __float_as_uint(f[i]) & 0x7FFFFFFFu);
+      }
+      BlockStep st;
+      sb = block_scale_fast(__uint_as_float(am), ts, &st);
+      *reinterpret_cast<uint2*>(codes + (int64_t)r * (H >> 1) + cb * 8) =
+          make_uint2(encode8(f, st), encode8(f + 8, st));
+    }
+    // scale bytes of blocks cb .. cb+3 (same row) into one word
+    uint32_t w = sb | (__shfl_down_sync(0xFFFFFFFFu, sb, 1) << 8);
+    w |= __shfl_down_sync(0xFFFFFFFFu, w, 2) << 16;
+    if (live && (cb & 3u) == 0u) *reinterpret_cast<uint32_t*>(sf + sf_offset(r, cb, bpr)) = w;
   }
 }
 
@@ -307,23 +402,20 @@ struct SiluOut {
   float* g[3];
 };
 
-__global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restrict__ gu,
+__global__ void __launch_bounds__(256, 2) k_silu_encode(const uint16_t* __restrict__ gu,
                                                         int64_t M, int64_t Mpad, int64_t I,
                                                         FastDiv bpr_div,
                                                         const float* __restrict__ amax3_opt,
                                                         const unsigned* __restrict__ amax3,
                                                         SiluOut out) {
   TensorScale ts[3];
-  __shared__ ScaleTable tab[3];
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
     ts[k] = tensor_scale(amax3_opt ? amax3_opt[k] : __uint_as_float(amax3[k]));
     if (blockIdx.x == 0 && threadIdx.x == 0) *out.g[k] = ts[k].g;
-    scale_table_init(&tab[k], ts[k]);
   }
-  __syncthreads();
   const float lo_f = 1.0f - 2.0f * kSiluRel, hi_f = 1.0f + 2.0f * kSiluRel;
-  const float rcp_d = tab[0].rcp_d;
+  const float rcp_d = ts[0].rcp_d;
   const uint32_t bpr = (uint32_t)(I >> 4);
   const uint32_t total = (uint32_t)Mpad * bpr;
   const uint32_t stride = gridDim.x * blockDim.x;
@@ -374,10 +466,10 @@ __global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restri
         const float q = __fmul_rn(am_blk, rcp_d);
         sh = e4m3_from_f32(__fmul_rn(q, lo_f));
         fast = sh == e4m3_from_f32(__fmul_rn(q, hi_f));
-        st = table_step(&tab[0], sh);
+        st = scale_step(sh, ts[0]);
         fl = __fmul_rn(st.rlo, lo_f);
         fh = __fmul_rn(st.rhi, hi_f);
-        fast = fast && st.t > 0.0f && fh <= 3.4028234663852886e38f;
+        fast = fast && step_certifiable(st) && fh <= 3.4028234663852886e38f;
       }
       uint32_t redo = 0xFFFFu;
       if (fast) {
@@ -400,7 +492,7 @@ __global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restri
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
           em = max(em, __float_as_uint(silu_exact_at(g0, g1, u0, u1, i)) & 0x7FFFFFFFu);
-        sh = block_scale_tab(__uint_as_float(em), ts[0], &tab[0], &st);
+        sh = block_scale_fast(__uint_as_float(em), ts[0], &st);
       }
       while (redo) {
         const int i = __ffs(redo) - 1;
@@ -417,7 +509,7 @@ __global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restri
     for (int k = 1; k < 3; ++k) {
       const uint32_t am = max(absmax_bf16x8_bits(k == 1 ? g0 : u0), absmax_bf16x8_bits(k == 1 ? g1 : u1));
       BlockStep sk;
-      const uint32_t s = block_scale_tab(__uint_as_float(am), ts[k], &tab[k], &sk);
+      const uint32_t s = block_scale_fast(__uint_as_float(am), ts[k], &sk);
       uint2 ck;
       float v[8];  // one half of the block at a time keeps fewer values live
       bf16x8_to_f32(k == 1 ? g0 : u0, v);
@@ -599,21 +691,28 @@ static cudaError_t dispatch_bpl(int64_t H, F&& f) {
 
 cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M,
                                  int64_t H, float eps, uint8_t* codes, uint8_t* sf, float* g,
-                                 float* rstd, unsigned* ws_amax, int num_sms,
+                                 float* rstd, unsigned* ws_amax, unsigned* status, int num_sms,
                                  cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(ws_amax, 0, sizeof(unsigned), stream);
   if (e != cudaSuccess) return e;
   const int64_t Mpad = pad_to(M, 128);
-  return dispatch_bpl(H, [&](auto bpl) {
+  const RingShape rs = ring_shape(H, 1, true);
+  e = dispatch_bpl(H, [&](auto bpl) {
     constexpr int BPL = decltype(bpl)::value;
+    auto ks = k_rmsnorm_stat<BPL>;
+    cudaError_t err = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)rs.smem);
+    if (err != cudaSuccess) return err;
     note_launch();
-    k_rmsnorm_stat<BPL><<<blocks_for(M, 8, num_sms * 8), 256, 0, stream>>>(x, gamma, M, H, eps,
-                                                                            rstd, ws_amax);
-    note_launch();
-    k_rmsnorm_encode<BPL><<<blocks_for(Mpad, 8, num_sms * 8), 256, 0, stream>>>(
-        x, gamma, rstd, M, Mpad, H, ws_amax, codes, sf, g);
+    ks<<<blocks_for(M, rs.warps, num_sms), 32 * rs.warps, rs.smem, stream>>>(
+        x, gamma, M, H, eps, rs.ns, rstd, ws_amax, status);
     return cudaGetLastError();
   });
+  if (e != cudaSuccess) return e;
+  note_launch();
+  k_rmsnorm_encode<<<blocks_for(Mpad * (H / 16), 256, num_sms * 8), 256, 0, stream>>>(
+      x, gamma, rstd, M, Mpad, H, FastDiv::make((uint32_t)(H / 16)), ws_amax, codes, sf, g);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_silu_mul_quant(const uint16_t* gateup, int64_t M, int64_t I,

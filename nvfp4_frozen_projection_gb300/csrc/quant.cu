@@ -59,12 +59,30 @@ __global__ void __launch_bounds__(256) k_amax_f32(const float* __restrict__ w, i
 }
 
 // ---------------------------------------------------------------- pass 2: encode
-// One thread encodes 64 consecutive elements (4 blocks) of one row: 128 bytes in,
-// 32 code bytes and one 4-byte scale word out.  Threads past row M (up to
-// pad128(M)) write zero scale words so the padded scale array is fully defined.
-__global__ void __launch_bounds__(256, 4) k_quant_bf16(const uint16_t* __restrict__ x, int64_t M,
+// Lane = one block of 16 elements, warp = 32 consecutive blocks (a contiguous 1 KB
+// of a contiguous tensor), blocks numbered row-major over [pad128(M), K/16].  Each
+// lane holds the next block's 32 bytes in flight while it encodes the current one.
+// A block's 8 code bytes leave as one 8-byte store (256 contiguous bytes per warp);
+// the scale bytes of four consecutive blocks (one 4-byte word of the 128x4 atom
+// layout, never split across rows since K/16 is a multiple of 4) are gathered by
+// two shuffles and stored by the first lane of the four.  Blocks of rows past M (up
+// to pad128(M)) get zero scale bytes so the padded scale array is fully defined.
+__device__ __forceinline__ void quant_fetch(const uint16_t* x, int64_t ldx, uint32_t blk,
+                                            uint32_t total, uint32_t M, const FastDiv& bpr_div,
+                                            uint32_t bpr, uint4& v0, uint4& v1) {
+  if (blk < total) {
+    const uint32_t r = bpr_div.div(blk);
+    if (r < M) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * ldx + (blk - r * bpr) * 16);
+      v0 = ldg_stream(src);
+      v1 = ldg_stream(src + 1);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__ x, int64_t M,
                                                     int64_t K, int64_t ldx, int64_t Mpad,
-                                                    FastDiv chunks_div,
+                                                    FastDiv bpr_div,
                                                     const float* __restrict__ amax_opt,
                                                     const unsigned* __restrict__ amax_bits,
                                                     uint8_t* __restrict__ codes,
@@ -73,40 +91,35 @@ __global__ void __launch_bounds__(256, 4) k_quant_bf16(const uint16_t* __restric
   const float amax = amax_opt ? *amax_opt : __uint_as_float(*amax_bits);
   const TensorScale ts = tensor_scale(amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
-  __shared__ ScaleTable tab;
-  scale_table_init(&tab, ts);
-  __syncthreads();
-  const uint32_t chunks = (uint32_t)(K >> 6);
-  const uint32_t total = (uint32_t)Mpad * chunks;  // < 2^31 (checked by the caller)
-  const int64_t c16p = K >> 4;
-  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += gridDim.x * blockDim.x) {
-    const uint32_t r = chunks_div.div(it), ch = it - r * chunks;
-    uint32_t sfw = 0;
-    if (r < M) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * ldx + ch * 64);
-      uint4 v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i);
-      uint32_t w[8];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        float f[16];
-        bf16x8_to_f32(v[2 * b], f);
-        bf16x8_to_f32(v[2 * b + 1], f + 8);
-        float amax_blk = __uint_as_float(
-            max(absmax_bf16x8_bits(v[2 * b]), absmax_bf16x8_bits(v[2 * b + 1])));
-        BlockStep st;
-        uint32_t s = block_scale_tab(amax_blk, ts, &tab, &st);
-        w[2 * b] = encode8(f, st);
-        w[2 * b + 1] = encode8(f + 8, st);
-        sfw |= s << (8 * b);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(codes + (int64_t)r * (K >> 1) + ch * 32);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  const uint32_t bpr = (uint32_t)(K >> 4);           // blocks per row
+  const uint32_t total = (uint32_t)Mpad * bpr;        // < 2^31 (checked by the caller)
+  const uint32_t lane = threadIdx.x & 31u;
+  // warps take 32-block strips in turn, so each warp iteration covers 1 KB
+  const uint32_t stride = gridDim.x * blockDim.x;
+  uint32_t blk = blockIdx.x * blockDim.x + threadIdx.x;
+  uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
+  quant_fetch(x, ldx, blk, total, (uint32_t)M, bpr_div, bpr, n0, n1);
+  for (; blk - lane < total; blk += stride) {  // warp-uniform trip count
+    const uint4 v0 = n0, v1 = n1;
+    quant_fetch(x, ldx, blk + stride, total, (uint32_t)M, bpr_div, bpr, n0, n1);
+    const bool live = blk < total;
+    const uint32_t r = bpr_div.div(blk), cb = blk - r * bpr;
+    uint32_t sb = 0;
+    if (live && r < M) {
+      float f[16];
+      bf16x8_to_f32(v0, f);
+      bf16x8_to_f32(v1, f + 8);
+      BlockStep st;
+      sb = block_scale_fast(__uint_as_float(max(absmax_bf16x8_bits(v0), absmax_bf16x8_bits(v1))),
+                            ts, &st);
+      const uint2 cw = make_uint2(encode8(f, st), encode8(f + 8, st));
+      *reinterpret_cast<uint2*>(codes + (int64_t)r * (K >> 1) + cb * 8) = cw;
     }
-    *reinterpret_cast<uint32_t*>(sf + sf_offset(r, ch * 4, c16p)) = sfw;
+    // scale bytes of blocks cb .. cb+3 (same row) into one word
+    uint32_t w = sb | (__shfl_down_sync(0xFFFFFFFFu, sb, 1) << 8);
+    w |= __shfl_down_sync(0xFFFFFFFFu, w, 2) << 16;
+    if (live && (cb & 3u) == 0u)
+      *reinterpret_cast<uint32_t*>(sf + sf_offset(r, cb, bpr)) = w;
   }
 }
 
@@ -190,8 +203,8 @@ cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
   }
   const int64_t Mpad = pad_to(M, 128);
   note_launch();
-  k_quant_bf16<<<grid_for(Mpad * (K / 64), 256, num_sms * 16), 256, 0, stream>>>(
-      x, M, K, ldx, Mpad, FastDiv::make((uint32_t)(K / 64)), amax_opt, ws_amax, codes, sf, g);
+  k_quant_bf16<<<grid_for(Mpad * (K / 16), 256, num_sms * 8), 256, 0, stream>>>(
+      x, M, K, ldx, Mpad, FastDiv::make((uint32_t)(K / 16)), amax_opt, ws_amax, codes, sf, g);
   return cudaGetLastError();
 }
 

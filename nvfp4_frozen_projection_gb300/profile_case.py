@@ -13,6 +13,10 @@ Cases (M = tokens; the other sizes are the Llama-3B layer's):
                       down-projection, then the GEMM): pact_lora_linear_dgrad_q
   adapter-grad-q      dA, dB of the q projection (3072 -> 3072, r = 16)
   adapter-grad-gate-up  dA, dB of the fused gate|up projection (3072 -> 2 x 8192, r = 32)
+  rmsnorm             RMSNorm -> NVFP4 of a BF16 [M, 3072] tensor (statistic and encode)
+  rmsnorm-bwd         RMSNorm backward of a [M, 3072] NVFP4 output, with a residual gradient
+  silu-bwd            SiLU-multiply backward from [M, 8192] NVFP4 gate/up copies
+  pack-weight         forward and backward NVFP4 packs of the gate|up weight [2 x 8192, 3072]
 
 The default M (4096) keeps every case's inputs above the 129 MB L2 and its device
 memory under 1 GB, which is the size a full ncu capture wants.  Each run exits 0
@@ -27,7 +31,8 @@ import torch
 from . import (pact_check_status, pact_lora_adapter_grad, pact_lora_linear_dgrad,
                pact_lora_linear_dgrad_q,
                pact_lora_linear_fwd, pact_pack_weight_bwd, pact_pack_weight_fwd,
-               pact_quant_nvfp4, pact_silu_mul_quant)
+               pact_quant_nvfp4, pact_rmsnorm_bwd, pact_rmsnorm_quant, pact_silu_mul_bwd,
+               pact_silu_mul_quant)
 
 HIDDEN, INTER = 3072, 8192
 
@@ -91,6 +96,36 @@ def run(case: str, m: int, reps: int) -> None:
         outs = pact_silu_mul_quant(gu)
         for _ in range(reps):
             pact_silu_mul_quant(gu, outs=outs)
+    elif case == "rmsnorm":
+        x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
+        gamma = (1.0 + 0.1 * torch.randn(HIDDEN, device=dev, generator=gen)).bfloat16()
+        yq, rstd = pact_rmsnorm_quant(x, gamma)
+        for _ in range(reps):
+            pact_rmsnorm_quant(x, gamma, out=yq, rstd=rstd)
+    elif case == "rmsnorm-bwd":
+        x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
+        gamma = (1.0 + 0.1 * torch.randn(HIDDEN, device=dev, generator=gen)).bfloat16()
+        yq, rstd = pact_rmsnorm_quant(x, gamma)
+        dy = (torch.randn(m, HIDDEN, device=dev, generator=gen) * 0.01).bfloat16()
+        dres = (torch.randn(m, HIDDEN, device=dev, generator=gen) * 0.01).bfloat16()
+        dx = torch.empty_like(dy)
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+        for _ in range(reps):
+            pact_rmsnorm_bwd(yq, gamma, rstd, dy, dres=dres, dx=dx, out_amax=amax)
+    elif case == "silu-bwd":
+        gu = torch.randn(m, 2 * INTER, device=dev, generator=gen).bfloat16()
+        _, gq, uq = pact_silu_mul_quant(gu)
+        dh = (torch.randn(m, INTER, device=dev, generator=gen) * 0.01).bfloat16()
+        dgu = torch.empty_like(gu)
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+        for _ in range(reps):
+            pact_silu_mul_bwd(gq, uq, dh, dgateup=dgu, out_amax=amax)
+    elif case == "pack-weight":
+        W = torch.randn(2 * INTER, HIDDEN, device=dev, generator=gen) * 0.02
+        wf, wb = pact_pack_weight_fwd(W), pact_pack_weight_bwd(W)
+        for _ in range(reps):
+            pact_pack_weight_fwd(W, out=wf)
+            pact_pack_weight_bwd(W, out=wb)
     else:
         raise SystemExit(f"unknown case {case!r}")
     torch.cuda.synchronize()
