@@ -144,11 +144,15 @@ int pact_lora_linear_fwd(const pact_nvfp4* xq, const pact_nvfp4* w_fwd, const ui
  * Same arguments, rules and result as pact_lora_linear_fwd, without ws/ws_bytes.
  * The scratch lives in a fixed array of PACT_NOALLOC_SCRATCH_BYTES (16 MiB) that
  * is part of the library image; every GPU that loads libpact holds it until the
- * process exits.  A call needing more scratch than that
- * (pact_lora_linear_fwd_workspace_size(M, N, K, r) > 16 MiB) returns
- * PACT_ERR_SHAPE without launching anything.
+ * process exits.  A call needs pact_lora_linear_fwd_workspace_size(M, N, K, r) =
+ * align256(4 M rp) + align256(2 N rp) + align256(2 K rp) bytes of it (rp = r padded
+ * to 16, 32 or 64; align256 rounds up to a multiple of 256); one needing more than
+ * 16 MiB returns PACT_ERR_SHAPE without launching anything.
  * - The first call on each device looks up the array's device address (with that
- *   device current); make that first call before any stream capture.
+ *   device current) and keeps it for the rest of the process; make that first call
+ *   before any stream capture.  The kept address assumes the device's context lives
+ *   as long as the process: after cudaDeviceReset() on a device, do not call this
+ *   entry point on that device again.
  * - Every call shares the one array, so calls that overlap on the GPU (different
  *   streams, or different host threads) race and corrupt each other's results.
  *   Serialise them, e.g. issue them all on one stream.

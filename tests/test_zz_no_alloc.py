@@ -49,7 +49,8 @@ def test_noalloc_rejects_oversized_calls():
     lib = pk.load_library()
     cap = int(lib.pact_lora_linear_fwd_noalloc_max_scratch())
     assert cap == 16 << 20
-    M, N, K, r = 262144, 64, 64, 16   # (M + N) * 64 bytes of scratch > 16 MiB
+    # scratch: align256(4 M rp) + align256(2 N rp) + align256(2 K rp), rp = 16: > 16 MiB
+    M, N, K, r = 262144, 64, 64, 16
     assert lib.pact_lora_linear_fwd_workspace_size(M, N, K, r) > cap
     xq = pk.NVFP4.empty(1, 64)        # small real buffers; the shape fields claim more
     wf = pk.NVFP4.empty(N, K)
