@@ -9,9 +9,14 @@ activation/gradient quantisation, the fused SiLU-multiply -> NVFP4, the 14 NVFP4
 GEMMs with fused LoRA branches, and the RMSNorm and SiLU-multiply backward
 kernels.  The attention core and its backward are replaced by seeded tensors.
 
-metric = NVFP4 frozen-projection GEMM FLOPs (2*M*N*K over the 14 GEMMs) divided by
-the wall time of the whole step (all kernels), in TFLOP/s.  Also reported:
-layer tokens/s, the quantiser's GB/s, and each GEMM kernel's own TFLOP/s.
+metric = NVFP4 frozen-projection GEMM FLOPs (2*M*N*K over the 12 GEMMs) divided by
+the device time of the whole step (all kernels), in TFLOP/s.  Also reported: layer
+tokens/s; the per-step median and an L2-flushed figure; each GEMM kernel's own
+TFLOP/s; the memory-bound calls' GB/s (warm and L2-flushed); a sub-line for each
+other workload (q-3b, mlp-3b, attn-1b: fwd + input-gradient passes); model tokens/s
+projected from the layer stacks (layer-3b x 28, a 1B-shaped stack x 16); the LoRA
+adapter gradients; the BF16 comparator; the oracle on the host cores; and the
+end-to-end figure through pinned host buffers.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch one process per GPU with torch.distributed.run; the path has no
@@ -42,10 +47,7 @@ from nvfp4_frozen_projection_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "NVFP4 LoRA-linear fwd+dgrad TFLOPS (% FP4 peak); quant GB/s; layer tokens/s"
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
-# DRAM bytes (read + write) of one full-size launch of the GEMM kernel, from a
-# one-pass ncu capture of profile_case at M = 8192 (profiles/gemm_nvfp4_gate_up.md);
-# they describe the kernel as of that capture.
-GEMM_TRAFFIC_BYTES = {"gate_up.fwd": 263.73e6}
+L2_FLUSH_BYTES = 256 << 20  # written between flushed repetitions (L2 is 129 MB)
 # (N, K) of each distinct frozen-projection GEMM of the layer-3b step (out = M x N)
 GEMM_SHAPES = {"q.fwd": (3072, 3072), "k.fwd": (1024, 3072), "v.fwd": (1024, 3072),
                "o.fwd": (3072, 3072), "gate_up.fwd": (16384, 3072), "down.fwd": (3072, 8192),
@@ -200,7 +202,7 @@ def build_stack(d, dev):
 
 def time_gemm_kernels(stack, inputs, reps):
     """Per-GEMM kernel time (CUDA events around the GEMM kernel alone, on the launch
-    stream), averaged over reps eager calls."""
+    stream), the median over reps eager calls."""
     import nvfp4_frozen_projection_gb300 as pk
     x, attn, dy, dq, dk, dv = inputs
     stack.forward(x, attn)
@@ -235,7 +237,7 @@ def time_gemm_kernels(stack, inputs, reps):
             pk.pact_profile_next_gemm(b, e)
             fn()
         torch.cuda.synchronize()
-        ms = statistics.mean(b.elapsed_time(e) for b, e in evs)
+        ms = statistics.median(b.elapsed_time(e) for b, e in evs)
         n_, k_ = flops[name]
         f = 2.0 * m * n_ * k_
         out[name] = {"ms": ms, "tflops": f / (ms * 1e-3) / 1e12, "flops": f}
@@ -289,6 +291,185 @@ def time_bf16_comparator(m, shapes, reps):
     return out
 
 
+def graph_of(fn):
+    """fn captured in a CUDA graph (after one eager run that sizes its buffers)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+_FLUSH = None
+
+
+def l2_flush():
+    """Write a buffer twice the size of L2, evicting whatever it held."""
+    global _FLUSH
+    if _FLUSH is None:
+        _FLUSH = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    _FLUSH.zero_()
+
+
+def time_replays(run, reps, flush=False):
+    """Median over reps runs of run(), each bracketed by CUDA events on the current
+    stream; with flush, L2 is flushed before each run, outside the events."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    run()
+    if flush:
+        l2_flush()
+    torch.cuda.synchronize()
+    _gpu_head_start()
+    for b, e in evs:
+        if flush:
+            l2_flush()
+        b.record()
+        run()
+        e.record()
+    torch.cuda.synchronize()
+    return statistics.median(b.elapsed_time(e) for b, e in evs)
+
+
+def _t32(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+
+
+def _lin(p, dev):
+    from nvfp4_frozen_projection_gb300.stack import LoraLinear
+    return LoraLinear(_t32(p.W, dev), _t32(p.A, dev).bfloat16(), _t32(p.B, dev).bfloat16(),
+                      p.scale)
+
+
+def _pass_line(name, tokens, gemm_flops, run, reps, extra=None):
+    """One workload pass captured in a graph: median time warm and L2-flushed, GEMM
+    TFLOP/s and tokens/s from the warm median."""
+    g = graph_of(run)
+    ms = time_replays(g.replay, reps)
+    msf = time_replays(g.replay, reps, flush=True)
+    line = {"tokens": tokens, "ms_median": round(ms, 5), "ms_median_l2_flushed": round(msf, 5),
+            "gemm_tflops": round(gemm_flops / (ms * 1e-3) / 1e12, 1),
+            "gemm_tflops_l2_flushed": round(gemm_flops / (msf * 1e-3) / 1e12, 1),
+            "tokens_per_s": round(tokens / (ms * 1e-3), 1)}
+    line.update(extra or {})
+    del g
+    return line
+
+
+def config_lines(dev, reps):
+    """Fwd + input-gradient passes of the other workloads, each its own sub-line:
+    q-3b (one LoRA linear: X and dY quantised, forward, input gradient), mlp-3b
+    (gate|up, SiLU-multiply, down and their input gradients), attn-1b (RMSNorm ->
+    q/k/v forwards, their three input gradients accumulated, RMSNorm backward)."""
+    import nvfp4_frozen_projection_gb300 as pk
+    from nvfp4_frozen_projection_gb300 import NVFP4
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    out = {}
+    # q-3b
+    d = wl.q3b()
+    lin = _lin(d["proj"], dev)
+    m, k = d["x"].shape
+    x, dy = _t32(d["x"], dev).bfloat16(), _t32(d["dy"], dev).bfloat16()
+    xq, dyq = NVFP4.empty(m, k, dev), NVFP4.empty(m, lin.d_out, dev)
+    y, dx = torch.empty(m, lin.d_out, **bf), torch.empty(m, k, **bf)
+
+    def q_pass():
+        pk.pact_quant_nvfp4(x, out=xq)
+        lin.forward(xq, y)
+        lin.dgrad_q(dy, dyq, dx)
+    out["q-3b"] = _pass_line("q-3b", m, 2 * lin.gemm_flops(m), q_pass, reps)
+    del lin, x, dy, xq, dyq, y, dx
+    # mlp-3b
+    d = wl.mlp3b()
+    gu_l, dn_l = _lin(d["gate_up"], dev), _lin(d["down"], dev)
+    m, h = d["x"].shape
+    inter = dn_l.d_in
+    x, dy = _t32(d["x"], dev).bfloat16(), _t32(d["dy"], dev).bfloat16()
+    xq = NVFP4.empty(m, h, dev)
+    gu = torch.empty(m, 2 * inter, **bf)
+    hq, gq, uq = (NVFP4.empty(m, inter, dev) for _ in range(3))
+    y = torch.empty(m, h, **bf)
+    dyq, dh = NVFP4.empty(m, h, dev), torch.empty(m, inter, **bf)
+    dgu, dguq = torch.empty(m, 2 * inter, **bf), NVFP4.empty(m, 2 * inter, dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    dx = torch.empty(m, h, **bf)
+
+    def mlp_pass():
+        pk.pact_quant_nvfp4(x, out=xq)
+        gu_l.forward(xq, gu)
+        pk.pact_silu_mul_quant(gu, outs=(hq, gq, uq))
+        dn_l.forward(hq, y)
+        dn_l.dgrad_q(dy, dyq, dh)
+        pk.pact_silu_mul_bwd(gq, uq, dh, dgateup=dgu, out_amax=amax)
+        gu_l.dgrad_q(dgu, dguq, dx, amax=amax)
+    out["mlp-3b"] = _pass_line("mlp-3b", m, 2 * (gu_l.gemm_flops(m) + dn_l.gemm_flops(m)),
+                               mlp_pass, reps)
+    del gu_l, dn_l, x, dy, xq, gu, hq, gq, uq, y, dyq, dh, dgu, dguq, dx
+    # attn-1b
+    d = wl.attn1b()
+    lins = [_lin(p, dev) for p in d["projs"]]
+    m, h = d["x"].shape
+    x = _t32(d["x"], dev).bfloat16()
+    gamma = _t32(d["gamma"], dev).bfloat16()
+    dys = [_t32(a, dev).bfloat16() for a in d["dys"]]
+    xq, rstd = NVFP4.empty(m, h, dev), torch.empty(m, dtype=torch.float32, device=dev)
+    ys = [torch.empty(m, l.d_out, **bf) for l in lins]
+    dyqs = [NVFP4.empty(m, l.d_out, dev) for l in lins]
+    dn, dxx = torch.empty(m, h, **bf), torch.empty(m, h, **bf)
+    eps = float(d["eps"])
+
+    def attn_pass():
+        pk.pact_rmsnorm_quant(x, gamma, eps, out=xq, rstd=rstd)
+        for l, yy in zip(lins, ys):
+            l.forward(xq, yy)
+        for i, (l, dy_, dyq_) in enumerate(zip(lins, dys, dyqs)):
+            l.dgrad_q(dy_, dyq_, dn, accumulate=i > 0)
+        pk.pact_rmsnorm_bwd(xq, gamma, rstd, dn, dx=dxx)
+    out["attn-1b"] = _pass_line("attn-1b", m, 2 * sum(l.gemm_flops(m) for l in lins), attn_pass,
+                                reps)
+    del lins, x, dys, xq, ys, dyqs, dn, dxx
+    torch.cuda.empty_cache()
+    return out
+
+
+def layer_1b_projection(dev, reps, m=26 * 1024):
+    """The decoder-layer projection stack at Llama-1B shapes (hidden 2048, 32 q heads
+    / 8 kv heads of 64, intermediate 8192, r = 16), batch 26 x 1024, with weights and
+    inputs drawn on the device (normal draws of the workload scales; the values do not
+    change the work).  Returns the step's median time."""
+    from nvfp4_frozen_projection_gb300.stack import DecoderProjectionStack, LoraLinear
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1016)
+    hid, kv, inter, r = 2048, 512, 8192, 16
+
+    def lin(d_in, d_out, rr=r):
+        W = torch.randn(d_out, d_in, device=dev, generator=gen) * 0.02
+        A = (torch.randn(d_in, rr, device=dev, generator=gen) / d_in ** 0.5).bfloat16()
+        B = (torch.randn(rr, d_out, device=dev, generator=gen) * 0.1).bfloat16()
+        return LoraLinear(W, A, B, 2.0)
+    proj = {"q": lin(hid, hid), "k": lin(hid, kv), "v": lin(hid, kv), "o": lin(hid, hid),
+            "gate_up": lin(hid, 2 * inter, 2 * r), "down": lin(inter, hid)}
+    g1 = (1 + 0.1 * torch.randn(hid, device=dev, generator=gen)).bfloat16()
+    g2 = (1 + 0.1 * torch.randn(hid, device=dev, generator=gen)).bfloat16()
+    st = DecoderProjectionStack(m, proj, g1, g2, 1e-5)
+    x = torch.randn(m, hid, device=dev, generator=gen).bfloat16()
+    attn = torch.randn(m, hid, device=dev, generator=gen).bfloat16()
+    dy, dq = ((torch.randn(m, hid, device=dev, generator=gen) * 0.01).bfloat16() for _ in range(2))
+    dk, dv = ((torch.randn(m, kv, device=dev, generator=gen) * 0.01).bfloat16() for _ in range(2))
+
+    def step():
+        st.forward(x, attn)
+        st.backward(dy, dq, dk, dv)
+    g = graph_of(step)
+    ms = time_replays(g.replay, reps)
+    flops = st.gemm_flops()
+    del g, st, proj
+    torch.cuda.empty_cache()
+    return ms, flops
+
+
 def _gpu_head_start():
     """Keep the GPU busy for a few ms so the host enqueues every rep before the GPU
     reaches it: the events then time GPU execution, not host launch latency."""
@@ -296,17 +477,8 @@ def _gpu_head_start():
 
 
 def time_call(fn, reps):
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(reps)]
-    fn()
-    torch.cuda.synchronize()
-    _gpu_head_start()
-    for b, e in evs:
-        b.record()
-        fn()
-        e.record()
-    torch.cuda.synchronize()
-    return statistics.mean(b.elapsed_time(e) for b, e in evs)
+    """Median of reps eager calls (CUDA events around each)."""
+    return time_replays(fn, reps)
 
 
 # ------------------------------------------------------------------ multi-rank
@@ -330,7 +502,7 @@ def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-graph", action="store_true", help="replay the step eagerly")
@@ -398,19 +570,38 @@ def main():
             import torch.distributed as dist
             dist.barrier()
 
-    # ---------------- timed region: K steps, inputs resident in HBM
+    # ---------------- timed region: K steps, inputs resident in HBM.  The clock
+    # sampler runs through a one-second soak of the same replays just before the
+    # timed region and through the region itself, so it sees the GPU under this load
+    # however short K steps are.  Each step is also bracketed by its own events for
+    # the per-step median.
     barrier()
     torch.cuda.synchronize()
+    step_evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 1.0:
+            for _ in range(20):
+                run()
+            torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
         t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t_begin.record()
-        for _ in range(args.steps):
+        for i in range(args.steps):
+            step_evs[i].record()
             run()
+        step_evs[args.steps].record()
         t_end.record()
         torch.cuda.synchronize()
     barrier()
     ms = t_begin.elapsed_time(t_end) / args.steps
+    ms_median = statistics.median(step_evs[i].elapsed_time(step_evs[i + 1])
+                                  for i in range(args.steps))
     clocks = clk.summary()
+    clocks["window"] = "1 s of the same step replays just before the timed region, then the region"
+    # the same step with L2 flushed before each replay (outside its events)
+    ms_flushed = time_replays(run, max(10, min(args.steps, 50)), flush=True)
     pk.pact_check_status()
     ms = max_over_ranks(ms, dev)
 
@@ -498,17 +689,38 @@ def main():
     dominant = max(step_share, key=step_share.get)
     dk_ = kern[dominant]
     m, hid = stack.m, stack.hidden
-    q_ms = time_call(lambda: pk.pact_quant_nvfp4(dy, out=stack.dyq), reps=10)
-    q_bytes = m * hid * (2 + 0.5 + 1 / 16)
-    r_ms = time_call(lambda: pk.pact_rmsnorm_quant(x, stack.gamma1, stack.eps, out=stack.xq1,
-                                                   rstd=stack.rstd1), reps=10)
-    r_bytes = m * hid * (2 + 0.5 + 1 / 16) + 4 * m
-    s_ms = time_call(lambda: pk.pact_silu_mul_quant(stack.gu, outs=(stack.hq, stack.gq, stack.uq)),
-                     reps=10)
-    s_bytes = m * stack.inter * (4 + 3 * (0.5 + 1 / 16))
+    # memory-bound calls alone: algorithmic bytes (inputs read once, outputs written
+    # once) over the median call time, warm and with L2 flushed before each call
+    mem_calls = {
+        "quant_nvfp4 8192x3072": (lambda: pk.pact_quant_nvfp4(dy, out=stack.dyq),
+                                  m * hid * (2 + 0.5 + 1 / 16)),
+        "rmsnorm_quant 8192x3072": (lambda: pk.pact_rmsnorm_quant(
+            x, stack.gamma1, stack.eps, out=stack.xq1, rstd=stack.rstd1),
+            m * hid * (2 + 0.5 + 1 / 16) + 4 * m),
+        "silu_mul_quant 8192x2x8192": (lambda: pk.pact_silu_mul_quant(
+            stack.gu, outs=(stack.hq, stack.gq, stack.uq)), m * stack.inter * (4 + 3 * (0.5 + 1 / 16))),
+        "silu_mul_bwd 8192x8192": (lambda: pk.pact_silu_mul_bwd(
+            stack.gq, stack.uq, stack.dh, dgateup=stack.dgu, out_amax=stack.dgu_amax),
+            m * stack.inter * (2 * (0.5 + 1 / 16) + 2 + 4)),
+        "rmsnorm_bwd 8192x3072 (+dres)": (lambda: pk.pact_rmsnorm_bwd(
+            stack.xq2, stack.gamma2, stack.rstd2, stack.dxn2, dres=dy, dx=stack.dh1,
+            out_amax=stack.dh1_amax), m * hid * ((0.5 + 1 / 16) + 2 + 2 + 2) + 4 * m),
+    }
+    memory_kernels = {}
+    for name, (fn, nbytes) in mem_calls.items():
+        a = time_replays(fn, 20)
+        b = time_replays(fn, 20, flush=True)
+        memory_kernels[name] = {"ms": round(a, 5), "gbs": round(nbytes / (a * 1e-3) / 1e9, 1),
+                                "ms_l2_flushed": round(b, 5),
+                                "gbs_l2_flushed": round(nbytes / (b * 1e-3) / 1e9, 1)}
+    memory_kernels["hbm_peak_gbs"] = P["hbm_gbs"]
+    q_ms, q_bytes = memory_kernels["quant_nvfp4 8192x3072"]["ms"], mem_calls["quant_nvfp4 8192x3072"][1]
     pk.pact_check_status()
     adapter = time_adapter_grads(stack, inputs, reps=10)
     bf16 = time_bf16_comparator(m, GEMM_SHAPES, reps=10)
+    configs = config_lines(dev, reps=20)
+    ms_1b, flops_1b = layer_1b_projection(dev, reps=10)
+    pk.pact_check_status()
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -519,8 +731,11 @@ def main():
                    "intermediate": stack.inter, "q_kv_o": [3072, 1024, 1024, 3072], "r": 16,
                    "gemms_per_step": 12, "fused": "gate|up runs as one GEMM",
                    "gemm_flops_per_step": flops,
-                   "l2": "no flush: one step moves several GB through HBM (L2 is 129 MB)",
+                   "l2": "no flush between timed steps: one step moves several GB through HBM "
+                         "(L2 is 129 MB); ms_per_step_l2_flushed flushes before every step",
                    "graph": graph is not None, "parallelism": f"replicas x{world}"},
+        "ms_per_step_median": ms_median,
+        "ms_per_step_l2_flushed": ms_flushed,
         "clocks": clocks,
         "e2e": {"value": job_throughput(flops, world, ms_e2e) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
@@ -530,15 +745,22 @@ def main():
         "roofline": {"bound": "tensor", "kernel": f"k_gemm_nvfp4 ({dominant})",
                      "achieved": dk_["tflops"], "peak": fp4_peak, "unit": "TFLOP/s",
                      "frac": dk_["tflops"] / fp4_peak,
-                     "traffic": GEMM_TRAFFIC_BYTES.get(dominant),
+                     "traffic": None,
                      "peak_source": f"{src} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
         "gemm_kernels": {k: {"ms": round(v["ms"], 5), "tflops": round(v["tflops"], 1)}
                          for k, v in kern.items()},
-        "memory_kernels": {
-            "quant_nvfp4 8192x3072": {"ms": q_ms, "gbs": q_bytes / (q_ms * 1e-3) / 1e9},
-            "rmsnorm_quant 8192x3072": {"ms": r_ms, "gbs": r_bytes / (r_ms * 1e-3) / 1e9},
-            "silu_mul_quant 8192x2x8192": {"ms": s_ms, "gbs": s_bytes / (s_ms * 1e-3) / 1e9},
-            "hbm_peak_gbs": P["hbm_gbs"]},
+        "memory_kernels": memory_kernels,
+        # the other workloads' fwd + input-gradient passes (graph replays; medians)
+        "configs": configs,
+        # model tokens/s projected from one layer's projection stack (attention core,
+        # embeddings, LM head and optimizer excluded): layer-3b x 28 layers, and a
+        # Llama-1B-shaped stack at 26 x 1024 tokens x 16 layers
+        "projected_model_tokens_per_s": {
+            "llama-3b (28 layers, layer-3b step)": round(m / (28 * ms_median * 1e-3), 1),
+            "llama-1b (16 layers, 1B-shaped stack, 26624 tokens)": round(
+                26 * 1024 / (16 * ms_1b * 1e-3), 1),
+            "layer-1b step ms": round(ms_1b, 5),
+            "layer-1b gemm_tflops": round(flops_1b / (ms_1b * 1e-3) / 1e12, 1)},
         "quant_gbs": q_bytes / (q_ms * 1e-3) / 1e9,
         # the LoRA adapter gradients dA, dB of the seven projections (outside the
         # fwd+dgrad step that the metric times): per call, and bandwidth against one
