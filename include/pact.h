@@ -113,6 +113,19 @@ int pact_pack_weight_bwd(const float* W, int64_t N, int64_t K, pact_nvfp4* out_b
                          void* ws, size_t ws_bytes, pact_stream_t stream);
 
 /*
+ * Forward pack of a fused gate|up weight W [2I, K] (rows [0, I) gate, [I, 2I) up;
+ * Table 7 "SiLU-multiply" and the fused gate/up projection) for
+ * pact_lora_linear_fwd_gate_up: the same codes, tile scales and g as
+ * pact_pack_weight_fwd, with the rows reordered in groups of 32, a gate group then
+ * the matching up group (packed row 64 j + i is gate row 32 j + i, packed row
+ * 64 j + 32 + i is up row 32 j + i), so that a GEMM tile holds matching gate and up
+ * columns.  The backward layout is unchanged (pact_pack_weight_bwd).
+ * Rules as for pact_pack_weight_fwd; N = 2I, N % 64 == 0.
+ */
+int pact_pack_weight_fwd_gate_up(const float* W, int64_t N, int64_t K, pact_nvfp4* out_fwd,
+                                 void* ws, size_t ws_bytes, pact_stream_t stream);
+
+/*
  * LoRA linear forward (Table 7 rows "Frozen projections" and "LoRA branch";
  * Figure 3):
  *   Y = g_x g_w (Xq Wq^T) + scale * (Xhat A) B   [+ residual]
@@ -176,6 +189,26 @@ int pact_lora_linear_fwd_noalloc(const pact_nvfp4* xq, const pact_nvfp4* w_fwd,
  *   dx     BF16 [M, K] output
  * Rules as for the forward.  ws: pact_lora_linear_dgrad_workspace_size() bytes.
  */
+/*
+ * The fused gate|up projection's forward with the statistics of its output that the
+ * SiLU-multiply quantisation needs (Table 7 "SiLU-multiply": NVFP4 h and separate
+ * NVFP4 gate/up copies, each with its own per-tensor scale), produced by the GEMM
+ * epilogue so that pact_silu_mul_quant runs as one pass:
+ *   y = [gate | up] as pact_lora_linear_fwd computes it, bit for bit, in the logical
+ *       column order (gate columns [0, I), up columns [I, 2I));
+ *   amax3[0] = max |h|, h = silu(gate) * up by the SiLU-multiply's exact FP32
+ *   recipe on the BF16 values of y; amax3[1] = max |gate|, amax3[2] = max |up|;
+ *   the layout pact_silu_mul_quant takes as amax3_opt.
+ *   w_fwd_gu: pact_pack_weight_fwd_gate_up's layout;  A [K, r], B [r, 2I]: the fused
+ *   adapters in the logical order (B block-diagonal for separate gate and up
+ *   adapters);  amax3: device FP32 [3], 4-byte aligned, overwritten.
+ * Rules and workspace as for pact_lora_linear_fwd (no residual); N = 2I, N % 64 == 0.
+ */
+int pact_lora_linear_fwd_gate_up(const pact_nvfp4* xq, const pact_nvfp4* w_fwd_gu,
+                                 const uint16_t* A, const uint16_t* B, int r, float scale,
+                                 uint16_t* y, float* amax3, void* ws, size_t ws_bytes,
+                                 pact_stream_t stream);
+
 size_t pact_lora_linear_dgrad_workspace_size(int64_t M, int64_t N, int64_t K, int r);
 int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact_nvfp4* w_bwd,
                            const uint16_t* A, const uint16_t* B, int r, float scale,

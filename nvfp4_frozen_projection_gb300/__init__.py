@@ -56,8 +56,11 @@ _SIGNATURES = {
     "pact_pack_weight_workspace_size": (_sz, [_i64, _i64]),
     "pact_pack_weight_fwd": (_int, [_vp, _i64, _i64, _SP, _vp, _sz, _vp]),
     "pact_pack_weight_bwd": (_int, [_vp, _i64, _i64, _SP, _vp, _sz, _vp]),
+    "pact_pack_weight_fwd_gate_up": (_int, [_vp, _i64, _i64, _SP, _vp, _sz, _vp]),
     "pact_lora_linear_fwd_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
     "pact_lora_linear_fwd": (_int, [_SP, _SP, _vp, _vp, _int, _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "pact_lora_linear_fwd_gate_up": (_int, [_SP, _SP, _vp, _vp, _int, _f32, _vp, _vp, _vp, _sz,
+                                            _vp]),
     "pact_lora_linear_fwd_noalloc_max_scratch": (_sz, []),
     "pact_lora_linear_fwd_noalloc": (_int, [_SP, _SP, _vp, _vp, _int, _f32, _vp, _vp, _vp, _vp]),
     "pact_lora_linear_dgrad_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
@@ -188,14 +191,15 @@ def pact_quant_nvfp4(x: torch.Tensor, amax: torch.Tensor | None = None,
     return out
 
 
-def _pack(W: torch.Tensor, backward: bool, out: NVFP4 | None) -> NVFP4:
+def _pack(W: torch.Tensor, backward: bool, out: NVFP4 | None, gate_up: bool = False) -> NVFP4:
     lib = load_library()
     _need_cuda(W, torch.float32, "W")
     N, K = W.shape
     out = out or (NVFP4.empty(K, N, W.device) if backward else NVFP4.empty(N, K, W.device))
     ws = _workspace(lib.pact_pack_weight_workspace_size(N, K), W.device)
     s = out.struct()
-    fn = lib.pact_pack_weight_bwd if backward else lib.pact_pack_weight_fwd
+    fn = (lib.pact_pack_weight_bwd if backward else
+          (lib.pact_pack_weight_fwd_gate_up if gate_up else lib.pact_pack_weight_fwd))
     _check(fn(_ptr(W), N, K, ctypes.byref(s), _ptr(ws), ws.numel(), _stream()))
     return out
 
@@ -208,6 +212,36 @@ def pact_pack_weight_fwd(W: torch.Tensor, out: NVFP4 | None = None) -> NVFP4:
 def pact_pack_weight_bwd(W: torch.Tensor, out: NVFP4 | None = None) -> NVFP4:
     """Pack the frozen FP32 weight W [N, K] into the backward NVFP4 layout [K, N]."""
     return _pack(W, True, out)
+
+
+def pact_pack_weight_fwd_gate_up(W: torch.Tensor, out: NVFP4 | None = None) -> NVFP4:
+    """Forward pack of a fused gate|up weight [2I, K] in the interleaved row order that
+    pact_lora_linear_fwd_gate_up reads."""
+    return _pack(W, False, out, gate_up=True)
+
+
+def pact_lora_linear_fwd_gate_up(xq: NVFP4, w_fwd_gu: NVFP4, A: torch.Tensor, B: torch.Tensor,
+                                 scale: float, y: torch.Tensor | None = None,
+                                 amax3: torch.Tensor | None = None):
+    """The fused gate|up forward (y [M, 2I] as pact_lora_linear_fwd) and amax3 =
+    (max |silu(gate) up|, max |gate|, max |up|) of it.  Returns (y, amax3)."""
+    lib = load_library()
+    _need_cuda(A, torch.bfloat16, "A")
+    _need_cuda(B, torch.bfloat16, "B")
+    M, K, N = xq.rows, xq.cols, w_fwd_gu.rows
+    r = A.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if amax3 is None:
+        amax3 = torch.empty(3, dtype=torch.float32, device=A.device)
+    _need_cuda(y, torch.bfloat16, "y")
+    _need_cuda(amax3, torch.float32, "amax3")
+    ws = _workspace(lib.pact_lora_linear_fwd_workspace_size(M, N, K, r), A.device)
+    sx, sw = xq.struct(), w_fwd_gu.struct()
+    _check(lib.pact_lora_linear_fwd_gate_up(ctypes.byref(sx), ctypes.byref(sw), _ptr(A), _ptr(B), r,
+                                            float(scale), _ptr(y), _ptr(amax3), _ptr(ws),
+                                            ws.numel(), _stream()))
+    return y, amax3
 
 
 def pact_lora_linear_fwd(xq: NVFP4, w_fwd: NVFP4, A: torch.Tensor, B: torch.Tensor,

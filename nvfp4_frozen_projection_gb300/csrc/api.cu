@@ -209,7 +209,7 @@ int pact_quant_nvfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const
 size_t pact_pack_weight_workspace_size(int64_t, int64_t) { return 256; }
 
 static int pack_common(const float* W, int64_t N, int64_t K, pact_nvfp4* out, void* ws,
-                       size_t ws_bytes, pact_stream_t stream, int backward) {
+                       size_t ws_bytes, pact_stream_t stream, int backward, int64_t gu_half) {
   DeviceInfo* d;
   int rc = device_info(&d);
   if (rc) return rc;
@@ -222,19 +222,26 @@ static int pack_common(const float* W, int64_t N, int64_t K, pact_nvfp4* out, vo
     return rc;
   if (!ws || ws_bytes < 256 || !aligned(ws, 256))
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
-  cudaError_t e = launch_pack_weight(W, N, K, backward, (uint8_t*)out->codes, (uint8_t*)out->sf,
-                                     out->g, (unsigned*)ws, d->sms, (cudaStream_t)stream);
+  cudaError_t e = launch_pack_weight(W, N, K, backward, gu_half, (uint8_t*)out->codes,
+                                     (uint8_t*)out->sf, out->g, (unsigned*)ws, d->sms,
+                                     (cudaStream_t)stream);
   return e == cudaSuccess ? PACT_OK : cuda_fail(e, "pack launch");
 }
 
 int pact_pack_weight_fwd(const float* W, int64_t N, int64_t K, pact_nvfp4* out_fwd, void* ws,
                          size_t ws_bytes, pact_stream_t stream) {
-  return pack_common(W, N, K, out_fwd, ws, ws_bytes, stream, 0);
+  return pack_common(W, N, K, out_fwd, ws, ws_bytes, stream, 0, 0);
+}
+
+int pact_pack_weight_fwd_gate_up(const float* W, int64_t N, int64_t K, pact_nvfp4* out_fwd,
+                                 void* ws, size_t ws_bytes, pact_stream_t stream) {
+  if (N % 64) return fail(PACT_ERR_SHAPE, "need N %% 64 == 0 (gate and up each a multiple of 32)");
+  return pack_common(W, N, K, out_fwd, ws, ws_bytes, stream, 0, N / 2);
 }
 
 int pact_pack_weight_bwd(const float* W, int64_t N, int64_t K, pact_nvfp4* out_bwd, void* ws,
                          size_t ws_bytes, pact_stream_t stream) {
-  return pack_common(W, N, K, out_bwd, ws, ws_bytes, stream, 1);
+  return pack_common(W, N, K, out_bwd, ws, ws_bytes, stream, 1, 0);
 }
 
 // ---------------------------------------------------------------- LoRA linear
@@ -259,8 +266,8 @@ size_t pact_lora_linear_dgrad_workspace_size(int64_t M, int64_t, int64_t K, int 
 // lb [Nout, rpe] (both BF16, in the workspace).
 static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int64_t M,
                     int64_t Nout, int64_t Kr, const uint16_t* la, const uint16_t* lb, int rpe,
-                    const uint16_t* addend, uint16_t* out, float* out_amax,
-                    cudaStream_t stream) {
+                    const uint16_t* addend, uint16_t* out, float* out_amax, cudaStream_t stream,
+                    int64_t gu_half = 0, float* amax3 = nullptr) {
   GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
   const int bn = gemm_block_n(Nout, rpe);
@@ -322,9 +329,15 @@ static int run_gemm(DeviceInfo* d, const pact_nvfp4* a, const pact_nvfp4* b, int
   p.num_m = (int)((M + 127) / 128);
   p.num_n = (int)((Nout + bn - 1) / bn);
   p.lora_steps = rpe / 16;
+  p.gu_half = (int)gu_half;
+  p.amax3 = (unsigned*)amax3;
   L.num_sms = d->sms;
   if (out_amax) {
     cudaError_t e = cudaMemsetAsync(out_amax, 0, sizeof(float), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "amax reset");
+  }
+  if (amax3) {
+    cudaError_t e = cudaMemsetAsync(amax3, 0, 3 * sizeof(float), stream);
     if (e != cudaSuccess) return cuda_fail(e, "amax reset");
   }
   cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
@@ -344,10 +357,10 @@ static int check_gemm_dims(int64_t M, int64_t N, int64_t K, int r) {
   return PACT_OK;
 }
 
-int pact_lora_linear_fwd(const pact_nvfp4* xq, const pact_nvfp4* w_fwd, const uint16_t* A,
+static int lora_fwd_impl(const pact_nvfp4* xq, const pact_nvfp4* w_fwd, const uint16_t* A,
                          const uint16_t* B, int r, float scale, const uint16_t* residual_opt,
                          uint16_t* y, float* out_amax_opt, void* ws, size_t ws_bytes,
-                         pact_stream_t stream) {
+                         pact_stream_t stream, int gate_up, float* amax3) {
   DeviceInfo* d;
   int rc = device_info(&d);
   if (rc) return rc;
@@ -363,14 +376,35 @@ int pact_lora_linear_fwd(const pact_nvfp4* xq, const pact_nvfp4* w_fwd, const ui
   if (!ws || ws_bytes < pact_lora_linear_fwd_workspace_size(M, N, K, r) || !aligned(ws, 256))
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
   const int rp = rp_for(r);
+  const int64_t gu_half = gate_up ? N / 2 : 0;
+  if (gate_up && (N % 64 || !amax3 || !aligned(amax3, 4)))
+    return fail(PACT_ERR_INVALID_ARG, "gate|up forward: need N %% 64 == 0 and a 4-byte aligned amax3");
   uint16_t* t = (uint16_t*)ws;
   uint16_t* bt = (uint16_t*)((char*)ws + align256((size_t)M * 2 * rp * 2));
   uint16_t* at = (uint16_t*)((char*)bt + align256((size_t)N * rp * 2));
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = launch_lora_down_fwd((const uint8_t*)xq->codes, (const uint8_t*)xq->sf, xq->g,
-                                       w_fwd->g, M, K, A, B, r, rp, scale, N, t, bt, at, s);
+                                       w_fwd->g, M, K, A, B, r, rp, scale, N, gu_half, t, bt, at,
+                                       s);
   if (e != cudaSuccess) return cuda_fail(e, "lora down launch");
-  return run_gemm(d, xq, w_fwd, M, N, K, t, bt, 2 * rp, residual_opt, y, out_amax_opt, s);
+  return run_gemm(d, xq, w_fwd, M, N, K, t, bt, 2 * rp, residual_opt, y, out_amax_opt, s, gu_half,
+                  amax3);
+}
+
+int pact_lora_linear_fwd(const pact_nvfp4* xq, const pact_nvfp4* w_fwd, const uint16_t* A,
+                         const uint16_t* B, int r, float scale, const uint16_t* residual_opt,
+                         uint16_t* y, float* out_amax_opt, void* ws, size_t ws_bytes,
+                         pact_stream_t stream) {
+  return lora_fwd_impl(xq, w_fwd, A, B, r, scale, residual_opt, y, out_amax_opt, ws, ws_bytes,
+                       stream, 0, nullptr);
+}
+
+int pact_lora_linear_fwd_gate_up(const pact_nvfp4* xq, const pact_nvfp4* w_fwd_gu,
+                                 const uint16_t* A, const uint16_t* B, int r, float scale,
+                                 uint16_t* y, float* amax3, void* ws, size_t ws_bytes,
+                                 pact_stream_t stream) {
+  return lora_fwd_impl(xq, w_fwd_gu, A, B, r, scale, nullptr, y, nullptr, ws, ws_bytes, stream, 1,
+                       amax3);
 }
 
 int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact_nvfp4* w_bwd,

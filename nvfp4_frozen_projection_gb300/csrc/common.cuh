@@ -49,6 +49,19 @@ __host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int6
          (c & 3);
 }
 
+// Fused gate|up projection, interleaved forward layout: the output columns (the
+// rows of the forward weight) are reordered in groups of 32, a group of gate
+// columns then the matching group of up columns, so that one 32-column slice of an
+// accumulator tile holds gate values and the next slice the up values of the same
+// columns.  half = I, the width of each of gate and up.
+__host__ __device__ __forceinline__ int64_t gu_logical(int64_t n, int64_t half) {
+  const int64_t grp = n >> 6, j = n & 63;
+  return j < 32 ? 32 * grp + j : half + 32 * grp + (j - 32);
+}
+__host__ __device__ __forceinline__ int64_t gu_interleaved(int64_t l, int64_t half) {
+  return l < half ? 64 * (l >> 5) + (l & 31) : 64 * ((l - half) >> 5) + 32 + ((l - half) & 31);
+}
+
 // ------------------------------------------------------------------ codecs
 // E4M3 (satfinite, RN) of a non-negative FP32 value -> byte.
 __device__ __forceinline__ uint32_t e4m3_from_f32(float v) {

@@ -141,6 +141,135 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n, int m = 128) {
          ((uint32_t)(m >> 4) << 24);
 }
 
+// Word i (runtime, 0..15) of sixteen register values, by a chain of selects.
+__device__ __forceinline__ uint32_t pick16(const uint32_t* w, int i) {
+  uint32_t v = w[15];
+#pragma unroll
+  for (int k = 14; k >= 0; --k) v = (i == k) ? w[k] : v;
+  return v;
+}
+
+// silu_mul, kept out of the epilogue's instruction stream (it runs for a few elements
+// per warp only).
+static __device__ __noinline__ float silu_mul_out_of_line(float g, float u) {
+  return silu_mul(g, u);
+}
+
+// max(|a|, |b|) of two BF16 pairs, lane by lane (the sign bits are the xor of the
+// inputs' and are masked by the caller; a NaN loses to the other operand).
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Element e (0..31) of a 32-column BF16 slice held as 16 packed pairs.
+__device__ __forceinline__ float slice_elem(const uint32_t (&w)[16], int e) {
+  const uint32_t v = pick16(w, e >> 1);
+  return __uint_as_float((e & 1) ? (v & 0xFFFF0000u) : (v << 16));
+}
+
+// Statistics of the fused gate|up output for the SiLU-multiply quantisation, over
+// one lane's row of the tile: the epilogue holds its BF16 results in 32-column
+// slices, and in the interleaved order slice 2j is gate and slice 2j + 1 the up of
+// the same columns.  ag, au: max |gate|, max |up| (FP32 bits of BF16 values, exact).
+// xh: the exact max |h| of this lane's elements so far, h = silu_mul(gate, up) by the
+// exact FP32 recipe; xw: the warp's, a lower bound of the tensor's.  The recipe's
+// s = RN(g / RN(1 + e)) satisfies |s| <= max(g, 0) + 0.28: for g >= 0, RN(1 + e) >= 1
+// gives |s| <= g; for g < 0, |g| / (1 + e^-g) <= 0.2785 and the recipe's roundings
+// move it by a few units in the last place.  So |h| = |RN(s u)| <=
+// RN(RN(max(g, 0) + 0.3) |u|) (rounding is monotonic), and over a slice <=
+// RN((max |g| + 0.3) max |u|): a slice where that is below xw holds nothing above it
+// (three instructions per slice).  Otherwise the slice's largest per-element bound,
+// formed with BF16 roundings (a packed max, add and multiply per two elements),
+// decides; only if that reaches xw are the elements whose own FP32 bound reaches xw
+// evaluated exactly.  While xw < 2^-100 (the warp's first slices, or tiny values)
+// the packed stage is skipped and the lane seeds its threshold with the exact value
+// of its element of largest bound.
+__device__ __forceinline__ float gu_bound(float g, float u) {
+  return __fmul_rn(__fadd_rn(fmaxf(g, 0.0f), 0.3f), fabsf(u));
+}
+
+__device__ __forceinline__ void gate_up_slice(const uint32_t (&gs)[16], const uint32_t (&us)[16],
+                                              float xw, float& xh, uint32_t& ag, uint32_t& au) {
+  uint32_t gm = 0, um = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    gm = bf16x2_max_abs(gm, gs[i]);
+    um = bf16x2_max_abs(um, us[i]);
+  }
+  gm &= 0x7FFF7FFFu;
+  um &= 0x7FFF7FFFu;
+  const uint32_t gmb = max(gm & 0xFFFFu, gm >> 16) << 16;
+  const uint32_t umb = max(um & 0xFFFFu, um >> 16) << 16;
+  ag = max(ag, gmb);
+  au = max(au, umb);
+  const bool all = !(xw >= 0x1p-100f);
+  if (!all) {
+    if (__fmul_rn(__fadd_rn(__uint_as_float(gmb), 0.3f), __uint_as_float(umb)) < xw) return;
+    // the per-element bound with BF16 roundings: v = RN(max(g, 0) + 0.3) >= |s| exactly
+    // (g is a BF16 value) and RN_bf16(v |u|) (1 + 2^-8) >= RN(v |u|) >= |h|
+    const __nv_bfloat162 zero2 = __float2bfloat162_rn(0.0f), c2 = __float2bfloat162_rn(0.3f);
+    uint32_t bm = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t g2 = gs[i], u2 = us[i] & 0x7FFF7FFFu;
+      const __nv_bfloat162 v =
+          __hadd2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&g2), zero2), c2);
+      __nv_bfloat162 bnd = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&u2));
+      bm = __vmaxu2(bm, *reinterpret_cast<uint32_t*>(&bnd) & 0x7FFF7FFFu);
+    }
+    const float bmax = __uint_as_float(max(bm & 0xFFFFu, bm >> 16) << 16);
+    if (__fmul_rn(bmax, 1.0f + 0x1p-6f) < xw) return;
+  }
+  float thr = xw;
+  if (all) {
+    float best = -1.0f;
+    int be = 0;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const uint32_t gv = gs[e >> 1], uv = us[e >> 1];
+      const float bnd = gu_bound(__uint_as_float((e & 1) ? (gv & 0xFFFF0000u) : (gv << 16)),
+                                 __uint_as_float((e & 1) ? (uv & 0xFFFF0000u) : (uv << 16)));
+      if (bnd > best) {
+        best = bnd;
+        be = e;
+      }
+    }
+    xh = fmaxf(xh, fabsf(silu_mul_out_of_line(slice_elem(gs, be), slice_elem(us, be))));
+    thr = fmaxf(xw, xh);
+  }
+  uint32_t cand = 0;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const uint32_t gv = gs[e >> 1], uv = us[e >> 1];
+    const float bnd = gu_bound(__uint_as_float((e & 1) ? (gv & 0xFFFF0000u) : (gv << 16)),
+                               __uint_as_float((e & 1) ? (uv & 0xFFFF0000u) : (uv << 16)));
+    cand |= (bnd < thr ? 0u : 1u) << e;
+  }
+#pragma unroll 1
+  while (cand) {
+    const int e = __ffs(cand) - 1;
+    cand &= cand - 1;
+    // a NaN is ignored, as the amax of the oracle ignores it
+    xh = fmaxf(xh, fabsf(silu_mul_out_of_line(slice_elem(gs, e), slice_elem(us, e))));
+  }
+}
+
+// Called by every lane of the warp (live: the lane's row lies inside M); the warp's
+// threshold xw is refreshed after each slice pair.
+template <int NCH>
+__device__ __forceinline__ void gate_up_stats(const uint32_t (&out)[NCH][16], int nbase, int N,
+                                              bool live, float& xw, float& xh, uint32_t& ag,
+                                              uint32_t& au) {
+#pragma unroll
+  for (int ch = 0; ch + 1 < NCH; ch += 2) {
+    if (nbase + 32 * ch >= N) break;  // the whole slice pair lies past N (uniform)
+    if (live) gate_up_slice(out[ch], out[ch + 1], xw, xh, ag, au);
+    xw = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(xh)));
+  }
+}
+
 __device__ __forceinline__ void raise_error(volatile uint32_t* abort_flag, unsigned* status,
                                             unsigned code) {
   *abort_flag = 1u;
@@ -153,7 +282,10 @@ __device__ __forceinline__ void raise_error(volatile uint32_t* abort_flag, unsig
 // tile and half of the B tile (no multicast), stages its scale factors into its own
 // TMEM and reports to the leader's barriers (sf_full, acc_empty, lora_peer); the
 // leader's commits reach both CTAs.
-template <int BN, int BK, int STAGES, int RPE, int CM, bool PAIR = false>
+// GU: the fused gate|up forward (interleaved columns stored back in the logical
+// order, amax3 statistics); instantiated only for that call, so the other GEMMs carry
+// none of its code.
+template <int BN, int BK, int STAGES, int RPE, int CM, bool PAIR = false, bool GU = false>
 __global__ void __launch_bounds__(448, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmLA,
@@ -538,6 +670,8 @@ __global__ void __launch_bounds__(448, 1)
     uint32_t amax = 0;
     uint32_t aphase = 0;
     uint32_t nstore = 0;
+    float gu_xh = 0.0f, gu_xw = 0.0f;  // gate|up statistics (amax3): lane's and warp's
+    uint32_t gu_ag = 0, gu_au = 0;
     for (int u = unit0; u < nunits; u += nclusters) {
       const int m0 = tile_mt(u) * C::BM;
       const int n0 = tile_n0(u);
@@ -634,17 +768,29 @@ __global__ void __launch_bounds__(448, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmOut, buf, n, m0 + q * 32);
+          // the interleaved gate|up order goes back to the logical columns here
+          tma_store_2d(&tmOut, buf, GU ? (int)gu_logical(n, p.gu_half) : n, m0 + q * 32);
           bulk_commit();
         }
         ++nstore;
       }
+      if constexpr (GU) gate_up_stats<NCH>(out, n0 + c0, p.N, row_ok, gu_xw, gu_xh, gu_ag, gu_au);
       aphase ^= 1u;
     }
     if (lane == 0) bulk_wait_all();
     if (p.out_amax) {
       amax = __reduce_max_sync(0xFFFFFFFFu, amax);
       if (lane == 0 && amax) atomicMax(p.out_amax, amax);
+    }
+    if constexpr (GU) {  // order: h, gate, up
+      const uint32_t hx = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(gu_xh));
+      const uint32_t gx = __reduce_max_sync(0xFFFFFFFFu, gu_ag);
+      const uint32_t ux = __reduce_max_sync(0xFFFFFFFFu, gu_au);
+      if (lane == 0) {
+        if (hx) atomicMax(p.amax3, hx);
+        if (gx) atomicMax(p.amax3 + 1, gx);
+        if (ux) atomicMax(p.amax3 + 2, ux);
+      }
     }
   }
 
@@ -662,10 +808,10 @@ __global__ void __launch_bounds__(448, 1)
 }
 
 // ---------------------------------------------------------------- host side
-template <int BN, int BK, int STAGES, int RPE, int CM, bool PAIR = false>
+template <int BN, int BK, int STAGES, int RPE, int CM, bool PAIR = false, bool GU = false>
 static cudaError_t launch_cfg(const GemmLaunch& L, cudaStream_t stream) {
   using C = GemmCfg<BN, BK, STAGES, RPE, PAIR>;
-  auto kern = k_gemm_nvfp4<BN, BK, STAGES, RPE, CM, PAIR>;
+  auto kern = k_gemm_nvfp4<BN, BK, STAGES, RPE, CM, PAIR, GU>;
   // per device: shared-memory attribute set, and how many clusters fit at once
   static int max_clusters[64] = {};
   int dev = 0;
@@ -737,28 +883,36 @@ constexpr int ring_stages() {
   return s < 10 ? s : 10;
 }
 
-template <int BN, int RPE, int CM>
+template <int BN, int RPE, int CM, bool GU>
 static cudaError_t launch_one(const GemmLaunch& L, cudaStream_t stream) {
-  return launch_cfg<BN, kStageK, ring_stages<BN, kStageK, RPE>(), RPE, CM>(L, stream);
+  return launch_cfg<BN, kStageK, ring_stages<BN, kStageK, RPE>(), RPE, CM, false, GU>(L, stream);
 }
 
-template <int BN, int RPE>
+template <int BN, int RPE, bool GU>
 static cudaError_t launch_pair(const GemmLaunch& L, cudaStream_t stream) {
-  return launch_cfg<BN, kStageK, ring_stages<BN, kStageK, RPE, true>(), RPE, 2, true>(L, stream);
+  return launch_cfg<BN, kStageK, ring_stages<BN, kStageK, RPE, true>(), RPE, 2, true, GU>(L,
+                                                                                       stream);
+}
+
+template <bool GU>
+static cudaError_t launch_gemm_gu(const GemmLaunch& L, int bn, int rpe, int cm,
+                                  cudaStream_t stream) {
+  if (bn == 256) {
+    if (cm == 2) {
+      if (rpe == 32) return launch_pair<256, 32, GU>(L, stream);
+      return launch_pair<256, 64, GU>(L, stream);
+    }
+    if (rpe == 32) return launch_one<256, 32, 1, GU>(L, stream);
+    return launch_one<256, 64, 1, GU>(L, stream);
+  }
+  if (rpe == 32) return launch_one<128, 32, 1, GU>(L, stream);
+  if (rpe == 64) return launch_one<128, 64, 1, GU>(L, stream);
+  return launch_one<128, 128, 1, GU>(L, stream);
 }
 
 cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, int cm, cudaStream_t stream) {
-  if (bn == 256) {
-    if (cm == 2) {
-      if (rpe == 32) return launch_pair<256, 32>(L, stream);
-      return launch_pair<256, 64>(L, stream);
-    }
-    if (rpe == 32) return launch_one<256, 32, 1>(L, stream);
-    return launch_one<256, 64, 1>(L, stream);
-  }
-  if (rpe == 32) return launch_one<128, 32, 1>(L, stream);
-  if (rpe == 64) return launch_one<128, 64, 1>(L, stream);
-  return launch_one<128, 128, 1>(L, stream);
+  return L.p.gu_half ? launch_gemm_gu<true>(L, bn, rpe, cm, stream)
+                     : launch_gemm_gu<false>(L, bn, rpe, cm, stream);
 }
 
 // Test of the bounded-wait path: one thread waits on an mbarrier that nothing

@@ -37,6 +37,11 @@ struct GemmParams {
   int lora_steps;          // K=16 BF16 MMAs of the LoRA product per tile (0 = none)
   int band_mc;             // tile order: bands of band_mc M-units, each swept over all N
   int addend32;            // addend 32-byte aligned: fetched with 32-byte loads
+  int gu_half;             // > 0: the fused gate|up forward in the interleaved column
+                           // order; tiles are stored back in the logical order
+  unsigned* amax3;         // gu_half > 0 (or null): max |h|, max |gate|, max |up| of the
+                           // BF16 output as FP32 bits, h = silu(gate) * up by the exact
+                           // FP32 recipe
 };
 
 struct GemmLaunch {
@@ -67,19 +72,22 @@ cudaError_t launch_amax_bf16(const uint16_t* x, int64_t M, int64_t K, unsigned* 
 cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
                               const float* amax_opt, uint8_t* codes, uint8_t* sf, float* g,
                               unsigned* ws_amax, int num_sms, cudaStream_t stream);
+// gu_half > 0: forward layout in the interleaved gate|up row order (gu_interleaved).
 cudaError_t launch_pack_weight(const float* W, int64_t N, int64_t K, int backward,
-                               uint8_t* codes, uint8_t* sf, float* g, unsigned* ws_amax,
-                               int num_sms, cudaStream_t stream);
+                               int64_t gu_half, uint8_t* codes, uint8_t* sf, float* g,
+                               unsigned* ws_amax, int num_sms, cudaStream_t stream);
 
 // LoRA down-projections (BF16 tensor cores, FP32 accumulate), written pre-scaled
 // as the left LoRA operand [M, 2 rp] (hi/lo BF16 pair) of the fused GEMM, plus
 // the padded right operand [rows, rp].  The forward also needs at_ws [rp, K] of
 // workspace for the transposed adapter.
+// gu_half > 0: bt_out rows in the interleaved gate|up order (row n = column
+// gu_logical(n) of B).
 cudaError_t launch_lora_down_fwd(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
                                  const float* gw, int64_t M, int64_t K, const uint16_t* A,
                                  const uint16_t* B, int r, int rp, float scale, int64_t N,
-                                 uint16_t* t_out, uint16_t* bt_out, uint16_t* at_ws,
-                                 cudaStream_t stream);
+                                 int64_t gu_half, uint16_t* t_out, uint16_t* bt_out,
+                                 uint16_t* at_ws, cudaStream_t stream);
 cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const float* gw,
                                    int64_t M, int64_t N, const uint16_t* A, const uint16_t* B,
                                    int r, int rp, float scale, int64_t K, uint16_t* u_out,

@@ -132,14 +132,16 @@ template <int RP>
 __global__ void __launch_bounds__(256) k_lora_prep(const uint16_t* __restrict__ A,
                                                    const uint16_t* __restrict__ B, int r,
                                                    int64_t K, int64_t N, int fwd,
+                                                   int64_t gu_half,
                                                    uint16_t* __restrict__ at_out,
                                                    uint16_t* __restrict__ rhs_out) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (fwd) {
-    if (t < N) {  // Bt row n
+    if (t < N) {  // Bt row n (column gu_logical(n) of B in the interleaved order)
+      const int64_t src = gu_half ? gu_logical(t, gu_half) : t;
       uint16_t v[RP];
 #pragma unroll
-      for (int j = 0; j < RP; ++j) v[j] = j < r ? B[(int64_t)j * N + t] : (uint16_t)0;
+      for (int j = 0; j < RP; ++j) v[j] = j < r ? B[(int64_t)j * N + src] : (uint16_t)0;
       store_row<RP>(rhs_out + t * RP, v);
     } else if (t < N + K) {  // At column k: element (j, k) for every j
       const int64_t k = t - N;
@@ -491,12 +493,13 @@ static cudaError_t launch_down_dy(const uint16_t* dy, const float* gdy, const fl
 template <int RP>
 static cudaError_t fwd_rp(const uint8_t* xc, const uint8_t* xsf, const float* gx,
                           const float* gw, int64_t M, int64_t K, const uint16_t* A,
-                          const uint16_t* B, int r, float scale, int64_t N, uint16_t* t_out,
-                          uint16_t* bt_out, uint16_t* at_ws, cudaStream_t stream) {
+                          const uint16_t* B, int r, float scale, int64_t N, int64_t gu_half,
+                          uint16_t* t_out, uint16_t* bt_out, uint16_t* at_ws,
+                          cudaStream_t stream) {
   constexpr int G = RP <= 32 ? 2 : 1;
   note_launch();
-  k_lora_prep<RP><<<(int)((N + K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 1, at_ws,
-                                                                    bt_out);
+  k_lora_prep<RP><<<(int)((N + K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 1, gu_half,
+                                                                    at_ws, bt_out);
   note_launch();
   k_lora_down_fwd<RP, G><<<(int)((M + 16 * G - 1) / (16 * G)), 256, 0, stream>>>(
       xc, xsf, gx, gw, M, K, at_ws, scale, 0, t_out);
@@ -509,7 +512,7 @@ static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* g
                             int64_t K, uint16_t* u_out, uint16_t* ap_out, cudaStream_t stream) {
   if (ap_out) {  // null: A is already [K, RP] (r == RP) and serves as the GEMM operand
     note_launch();
-    k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
+    k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, 0, nullptr, ap_out);
   }
   const cudaError_t e = launch_down_dy<RP, false>(dy, gdy, gw, M, N, B, r, scale, 0, u_out,
                                                   DyQuant{}, stream);
@@ -519,15 +522,16 @@ static cudaError_t dgrad_rp(const uint16_t* dy, const float* gdy, const float* g
 cudaError_t launch_lora_down_fwd(const uint8_t* x_codes, const uint8_t* x_sf, const float* gx,
                                  const float* gw, int64_t M, int64_t K, const uint16_t* A,
                                  const uint16_t* B, int r, int rp, float scale, int64_t N,
-                                 uint16_t* t_out, uint16_t* bt_out, uint16_t* at_ws,
-                                 cudaStream_t stream) {
+                                 int64_t gu_half, uint16_t* t_out, uint16_t* bt_out,
+                                 uint16_t* at_ws, cudaStream_t stream) {
   if (rp == 16)
-    return fwd_rp<16>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, t_out, bt_out, at_ws,
-                      stream);
+    return fwd_rp<16>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, gu_half, t_out, bt_out,
+                      at_ws, stream);
   if (rp == 32)
-    return fwd_rp<32>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, t_out, bt_out, at_ws,
-                      stream);
-  return fwd_rp<64>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, t_out, bt_out, at_ws, stream);
+    return fwd_rp<32>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, gu_half, t_out, bt_out,
+                      at_ws, stream);
+  return fwd_rp<64>(x_codes, x_sf, gx, gw, M, K, A, B, r, scale, N, gu_half, t_out, bt_out,
+                    at_ws, stream);
 }
 
 cudaError_t launch_lora_down_dgrad(const uint16_t* dy, const float* gdy, const float* gw,
@@ -546,7 +550,7 @@ static cudaError_t quant_dgrad_rp(const uint16_t* dy, int64_t M, int64_t N, DyQu
                                   cudaStream_t stream) {
   if (ap_out) {
     note_launch();
-    k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, nullptr, ap_out);
+    k_lora_prep<RP><<<(int)((K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 0, 0, nullptr, ap_out);
   }
   const cudaError_t e =
       launch_down_dy<RP, true>(dy, nullptr, gw, M, N, B, r, scale, 0, u_out, qz, stream);
@@ -831,7 +835,8 @@ static cudaError_t adapter_grad_rp(const uint8_t* xc, const uint8_t* xsf, const 
   constexpr int G = RP <= 32 ? 2 : 1;
   const int mb = (int)((M + 16 * G - 1) / (16 * G));
   note_launch();
-  k_lora_prep<RP><<<(int)((N + K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 1, at_ws, bt_ws);
+  k_lora_prep<RP><<<(int)((N + K + 255) / 256), 256, 0, stream>>>(A, B, r, K, N, 1, 0, at_ws,
+                                                                    bt_ws);
   note_launch();
   k_lora_down_fwd<RP, G><<<mb, 256, 0, stream>>>(xc, xsf, gx, gx, M, K, at_ws, scale, 1, t_ws);
   cudaError_t e =

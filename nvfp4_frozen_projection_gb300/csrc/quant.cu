@@ -128,10 +128,14 @@ __global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__
 // by the forward layout ([N, K], blocks along K) and the backward layout ([K, N],
 // blocks along N), so both hold the same effective weights.
 // Lane l handles tile row l/2, columns 8*(l%2) .. +8.
+// gu_half > 0 (forward layout only): the rows are written in the interleaved
+// gate|up order (gu_interleaved); 16-row tiles stay whole, so the scales are the
+// same bytes, and g is the whole weight's.
 __global__ void __launch_bounds__(256) k_pack_weight(const float* __restrict__ W, int64_t N,
                                                      int64_t K,
                                                      const unsigned* __restrict__ amax_bits,
-                                                     int backward, uint8_t* __restrict__ codes,
+                                                     int backward, int64_t gu_half,
+                                                     uint8_t* __restrict__ codes,
                                                      uint8_t* __restrict__ sf,
                                                      float* __restrict__ g_out) {
   __shared__ uint8_t nib[8][16][17];
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(256) k_pack_weight(const float* __restrict__ W
     const uint32_t s = block_scale(__uint_as_float(m), ts, &st);
     const uint32_t w = encode8(f, st);
     if (!backward) {
-      const int64_t n = tn * 16 + i;
+      const int64_t n = gu_half ? gu_interleaved(tn * 16 + i, gu_half) : tn * 16 + i;
       *reinterpret_cast<uint32_t*>(codes + n * (K >> 1) + tk * 8 + 4 * h) = w;
       if (h == 0) sf[sf_offset(n, tk, K >> 4)] = (uint8_t)s;
     } else {
@@ -209,8 +213,8 @@ cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
 }
 
 cudaError_t launch_pack_weight(const float* W, int64_t N, int64_t K, int backward,
-                               uint8_t* codes, uint8_t* sf, float* g, unsigned* ws_amax,
-                               int num_sms, cudaStream_t stream) {
+                               int64_t gu_half, uint8_t* codes, uint8_t* sf, float* g,
+                               unsigned* ws_amax, int num_sms, cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(ws_amax, 0, sizeof(unsigned), stream);
   if (e != cudaSuccess) return e;
   const int64_t rows = backward ? K : N, cols = backward ? N : K;
@@ -221,7 +225,7 @@ cudaError_t launch_pack_weight(const float* W, int64_t N, int64_t K, int backwar
   const int64_t ntiles = (N / 16) * (K / 16);
   note_launch();
   k_pack_weight<<<grid_for(ntiles * 32, 256, num_sms * 16), 256, 0, stream>>>(
-      W, N, K, ws_amax, backward, codes, sf, g);
+      W, N, K, ws_amax, backward, gu_half, codes, sf, g);
   return cudaGetLastError();
 }
 

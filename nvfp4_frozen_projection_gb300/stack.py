@@ -17,7 +17,7 @@ import numpy as np
 import torch
 
 from . import (NVFP4, pact_lora_linear_dgrad, pact_lora_linear_dgrad_q, pact_lora_linear_fwd,
-               pact_pack_weight_bwd,
+               pact_lora_linear_fwd_gate_up, pact_pack_weight_bwd, pact_pack_weight_fwd_gate_up,
                pact_lora_adapter_grad, pact_pack_weight_fwd, pact_quant_nvfp4, pact_rmsnorm_bwd,
                pact_rmsnorm_quant,
                pact_silu_mul_bwd, pact_silu_mul_quant)
@@ -25,17 +25,28 @@ from . import (NVFP4, pact_lora_linear_dgrad, pact_lora_linear_dgrad_q, pact_lor
 
 class LoraLinear:
     """Frozen weight W [d_out, d_in] packed once into the cached forward and backward
-    NVFP4 layouts, BF16 adapters A [d_in, r] and B [r, d_out], scale = alpha / r."""
+    NVFP4 layouts, BF16 adapters A [d_in, r] and B [r, d_out], scale = alpha / r.
+    gate_up: W is a fused [gate; up] weight whose forward also yields the SiLU
+    statistics of its output (forward_gate_up)."""
 
-    def __init__(self, W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, scale: float):
+    def __init__(self, W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, scale: float,
+                 gate_up: bool = False):
         self.d_out, self.d_in = W.shape
-        self.w_fwd = pact_pack_weight_fwd(W)
+        self.gate_up = gate_up
+        self.w_fwd = pact_pack_weight_fwd_gate_up(W) if gate_up else pact_pack_weight_fwd(W)
         self.w_bwd = pact_pack_weight_bwd(W)
         self.A, self.B, self.scale = A, B, float(scale)
 
     def forward(self, xq: NVFP4, y: torch.Tensor, residual=None, out_amax=None):
+        if self.gate_up:
+            raise ValueError("a gate|up projection runs forward_gate_up")
         return pact_lora_linear_fwd(xq, self.w_fwd, self.A, self.B, self.scale,
                                     residual=residual, y=y, out_amax=out_amax)
+
+    def forward_gate_up(self, xq: NVFP4, y: torch.Tensor, amax3: torch.Tensor):
+        """y = [gate | up], amax3 = (max |silu(gate) up|, max |gate|, max |up|)."""
+        return pact_lora_linear_fwd_gate_up(xq, self.w_fwd, self.A, self.B, self.scale, y=y,
+                                            amax3=amax3)
 
     def dgrad(self, dyq: NVFP4, dy: torch.Tensor, dx: torch.Tensor, accumulate=False):
         return pact_lora_linear_dgrad(dyq, dy, self.w_bwd, self.A, self.B, self.scale, dx=dx,
@@ -84,6 +95,7 @@ class DecoderProjectionStack:
         self.xq2 = NVFP4.empty(m, hidden, dev)
         self.rstd2 = torch.empty(m, dtype=torch.float32, device=dev)
         self.gu = torch.empty(m, 2 * inter, **bf)
+        self.gu_amax3 = torch.empty(3, dtype=torch.float32, device=dev)
         self.hq = NVFP4.empty(m, inter, dev)
         self.gq = NVFP4.empty(m, inter, dev)
         self.uq = NVFP4.empty(m, inter, dev)
@@ -143,8 +155,9 @@ class DecoderProjectionStack:
         else:
             main.wait_stream(side)
         pact_rmsnorm_quant(self.h1, self.gamma2, self.eps, out=self.xq2, rstd=self.rstd2)
-        p["gate_up"].forward(self.xq2, self.gu)
-        pact_silu_mul_quant(self.gu, outs=(self.hq, self.gq, self.uq))
+        # the gate|up GEMM's epilogue yields the three amaxes: one pass of SiLU-multiply
+        p["gate_up"].forward_gate_up(self.xq2, self.gu, self.gu_amax3)
+        pact_silu_mul_quant(self.gu, amax3=self.gu_amax3, outs=(self.hq, self.gq, self.uq))
         p["down"].forward(self.hq, self.out, residual=self.h1)
         return self.out
 
@@ -204,7 +217,7 @@ class DecoderProjectionStack:
         for k in ("q", "k", "v", "o", "gate_up", "down"):
             p = d[k]
             proj[k] = LoraLinear(t32(p.W), t32(p.A).bfloat16(), t32(p.B).bfloat16(),
-                                 float(p.alpha) / float(p.r))
+                                 float(p.alpha) / float(p.r), gate_up=(k == "gate_up"))
         return cls(d["x"].shape[0], proj, t32(d["gamma1"]).bfloat16(),
                    t32(d["gamma2"]).bfloat16(), float(d["eps"]))
 

@@ -68,6 +68,12 @@ def test_layer_forward_stages(layer):
               residual=ins["x"])
     check_rmsnorm_quant("xq2", st.xq2, st.rstd2, st.h1, gamma2, eps)
     check_fwd("gate|up", st.gu, st.xq2, d["gate_up"], packs["gate_up"][0], rows)
+    # the gate|up GEMM's epilogue amaxes, which the one-pass SiLU-multiply used
+    gu = host(st.gu)
+    inter = gu.shape[1] // 2
+    want = np.float32([np.abs(orc.silu_mul_fp32(gu)).max(), np.abs(gu[:, :inter]).max(),
+                       np.abs(gu[:, inter:]).max()])
+    assert st.gu_amax3.cpu().numpy().view(np.uint32).tolist() == want.view(np.uint32).tolist()
     check_silu_quant("SiLU-multiply", st.hq, st.gq, st.uq, st.gu)
     check_fwd("down (+ residual h1)", st.out, st.hq, d["down"], packs["down"][0], rows,
               residual=st.h1)
