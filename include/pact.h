@@ -351,6 +351,18 @@ int pact_profile_next_gemm(void* begin_event, void* end_event);
  */
 int pact_test_wait_timeout(uint32_t limit_us, pact_stream_t stream);
 
+/*
+ * Test of the debug build's bounds checks (no counterpart in the method).  The
+ * library built with -DPACT_DEBUG (libpact_debug.so) checks the index of every
+ * store whose address it computes by hand against the buffer's extent; a failed
+ * check skips the store and records PACT_DEV_BOUNDS in the device status word
+ * instead of trapping.  This launches one thread that evaluates one failing check
+ * and accesses no memory: afterwards pact_check_status() reports
+ * PACT_ERR_DEVICE_STATUS in the debug build and PACT_OK in the release build, whose
+ * checks compile away.
+ */
+int pact_test_bounds_check(pact_stream_t stream);
+
 /* Synchronises the stream, then returns and clears the device status word:
  * PACT_OK, PACT_ERR_TIMEOUT or PACT_ERR_DEVICE_STATUS.  For tests and debugging. */
 int pact_check_status(pact_stream_t stream);

@@ -22,13 +22,19 @@ __all__ = [
     "pact_lora_linear_fwd", "pact_lora_linear_fwd_noalloc", "pact_lora_linear_dgrad",
     "pact_lora_linear_dgrad_q", "pact_lora_adapter_grad", "pact_rmsnorm_quant",
     "pact_silu_mul_quant", "pact_silu_mul_bwd", "pact_rmsnorm_bwd", "pact_test_pexp",
-    "pact_test_wait_timeout", "pact_check_status", "pact_device_supported", "pact_launch_count", "pact_profile_next_gemm",
+    "pact_pack_weight_fwd_gate_up", "pact_lora_linear_fwd_gate_up",
+    "pact_test_wait_timeout", "pact_test_bounds_check", "pact_check_status",
+    "pact_device_supported", "pact_launch_count", "pact_profile_next_gemm", "pact_version",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def library_path() -> str:
+    """libpact.so, or with PACT_DEBUG=1 in the environment the bounds-checked debug
+    build libpact_debug.so (built by build.build_debug())."""
+    if os.environ.get("PACT_DEBUG") == "1":
+        return os.path.join(_HERE, "libpact_debug.so")
     return os.path.join(_HERE, "libpact.so")
 
 
@@ -78,6 +84,7 @@ _SIGNATURES = {
     "pact_rmsnorm_bwd": (_int, [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "pact_test_pexp": (_int, [_vp, _vp, _i64, _vp]),
     "pact_test_wait_timeout": (_int, [ctypes.c_uint32, _vp]),
+    "pact_test_bounds_check": (_int, [_vp]),
     "pact_check_status": (_int, [_vp]),
     "pact_launch_count": (ctypes.c_uint64, []),
     "pact_profile_next_gemm": (_int, [_vp, _vp]),
@@ -442,6 +449,17 @@ def pact_test_wait_timeout(limit_us: int = 1000) -> None:
     """Launch a kernel whose bounded wait runs out after limit_us microseconds; the
     next pact_check_status() raises PactError with code PACT_ERR_TIMEOUT (6)."""
     _check(load_library().pact_test_wait_timeout(int(limit_us), _stream()))
+
+
+def pact_test_bounds_check() -> None:
+    """Evaluate one failing bounds check on the GPU (no memory access): with the debug
+    library the next pact_check_status() raises PactError (PACT_ERR_DEVICE_STATUS);
+    with the release library it passes."""
+    _check(load_library().pact_test_bounds_check(_stream()))
+
+
+def pact_version() -> str:
+    return load_library().pact_version().decode()
 
 
 def pact_check_status() -> None:

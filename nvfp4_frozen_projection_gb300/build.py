@@ -17,6 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpact.so")
+# the debug build: every source as one unit (debug_all.cu), stores bounds-checked
+DEBUG_LIB = os.path.join(HERE, "libpact_debug.so")
 SOURCES = ["api.cu", "quant.cu", "gemm.cu", "lora.cu", "norm_act.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -48,6 +50,28 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
+def build_debug(force: bool = False) -> str:
+    """Compile libpact_debug.so (-DPACT_DEBUG, one translation unit) if it is missing or
+    older than its sources.  The library's bounds checks then record a failed check
+    in the status word (pact_check_status) instead of writing out of bounds."""
+    if not force and os.path.exists(DEBUG_LIB) and os.path.getmtime(DEBUG_LIB) >= _deps_mtime():
+        return DEBUG_LIB
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    obj = os.path.join(OBJ_DIR, "debug_all.o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-DPACT_DEBUG", "-c", os.path.join(CSRC, "debug_all.cu"),
+           "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for the debug build:\n{r.stdout}\n{r.stderr}")
+    tmp = DEBUG_LIB + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, obj, "-Xcompiler", "-fPIC"],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, DEBUG_LIB)
+    return DEBUG_LIB
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link libpact.so if it is missing or older than its sources."""
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
@@ -65,4 +89,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--debug" in sys.argv:
+        print(build_debug(force="--force" in sys.argv))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

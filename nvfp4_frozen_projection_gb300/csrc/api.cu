@@ -140,7 +140,11 @@ extern "C" {
 
 const char* pact_last_error(void) { return g_err; }
 
-const char* pact_version(void) { return "libpact 0.1 (sm_103a)"; }
+#ifdef PACT_DEBUG
+const char* pact_version(void) { return "libpact 0.2 (sm_103a, debug: bounds-checked stores)"; }
+#else
+const char* pact_version(void) { return "libpact 0.2 (sm_103a)"; }
+#endif
 
 uint64_t pact_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -177,6 +181,9 @@ int pact_check_status(pact_stream_t stream) {
     cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (v & PACT_DEV_TIMEOUT)
       return fail(PACT_ERR_TIMEOUT, "a kernel wait timed out (status 0x%x)", v);
+    if (v & PACT_DEV_BOUNDS)
+      return fail(PACT_ERR_DEVICE_STATUS, "a bounds check of the debug build failed (status 0x%x)",
+                  v);
     return fail(PACT_ERR_DEVICE_STATUS, "device status 0x%x", v);
   }
   return PACT_OK;
@@ -626,6 +633,14 @@ int pact_test_wait_timeout(uint32_t limit_us, pact_stream_t stream) {
     return fail(PACT_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");
   cudaError_t e = launch_wait_timeout((uint64_t)limit_us * 1000ull, (cudaStream_t)stream);
   return e == cudaSuccess ? PACT_OK : cuda_fail(e, "wait-timeout launch");
+}
+
+int pact_test_bounds_check(pact_stream_t stream) {
+  DeviceInfo* d;
+  int rc = device_info(&d);
+  if (rc) return rc;
+  cudaError_t e = launch_bounds_check((cudaStream_t)stream);
+  return e == cudaSuccess ? PACT_OK : cuda_fail(e, "bounds-check launch");
 }
 
 int pact_test_pexp(const float* x, float* y, int64_t n, pact_stream_t stream) {

@@ -46,7 +46,9 @@
 
 namespace pact {
 
+#ifndef PACT_DEBUG
 __device__ unsigned g_pact_status;
+#endif
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 // FP4 elements of K per ring stage: 128-byte tile rows, so each stage moves one
@@ -936,6 +938,21 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   note_launch();
   k_wait_timeout<<<1, 32, 0, stream>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+// Evaluates one bounds check that fails (index n of an n-element range) without
+// touching memory: the debug build records PACT_DEV_BOUNDS, the release build
+// compiles the check to true and records nothing.
+__global__ void k_bounds_check(int n, int* sink) {
+  const int i = n;
+  if (!PACT_IN(i < n)) return;
+  if (sink) sink[0] = i;  // never reached with sink null (the launch passes null)
+}
+
+cudaError_t launch_bounds_check(cudaStream_t stream) {
+  note_launch();
+  k_bounds_check<<<1, 1, 0, stream>>>(1, nullptr);
   return cudaGetLastError();
 }
 

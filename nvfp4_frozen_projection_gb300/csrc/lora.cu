@@ -410,10 +410,11 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
         bf16x8_to_f32(xc[h][1], f8);
         const uint32_t w1 = encode8(f8, st);
         const int64_t row = row0 + 8 * h;
-        if (h ? ok1 : ok0)
+        if ((h ? ok1 : ok0) && PACT_IN(row < M && cc < nch))
           *reinterpret_cast<uint2*>(qz.codes + row * (N >> 1) + (int64_t)cc * 32 + 8 * c) =
               make_uint2(w0, w1);
-        qz.sf[(h ? sfo1 : sfo0) + (int64_t)cc * 512] = (uint8_t)sc;
+        if (PACT_IN((h ? sfo1 : sfo0) + (int64_t)cc * 512 < pad_to(M, 128) * (N >> 4)))
+          qz.sf[(h ? sfo1 : sfo0) + (int64_t)cc * 512] = (uint8_t)sc;
       }
     }
   }
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
     float sum = 0.0f;
     for (int j = 0; j < ns; ++j) sum += ld_shared_cluster_f32(local, (uint32_t)j);
     const int64_t m = mb0 + rl;
-    if (m < M) {
+    if (m < M && PACT_IN(col < RP)) {
       const float v = sum * f;
       const __nv_bfloat16 hi = __float2bfloat16_rn(v);
       const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));

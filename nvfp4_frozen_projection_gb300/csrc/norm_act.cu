@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_stat(const uint16_t* __restrict
     for (int off = 16; off >= 1; off >>= 1)
       acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, off));
     const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, (float)H), eps)));
-    if (lane == 0) rstd[row] = rs;
+    if (lane == 0 && PACT_IN(row < M)) rstd[row] = rs;
 #pragma unroll
     for (int j = 0; j < BPL; ++j) {
       const int b = lane + 32 * j;
@@ -232,13 +232,15 @@ __global__ void __launch_bounds__(256) k_rmsnorm_encode(
       }
       BlockStep st;
       sb = block_scale_fast(__uint_as_float(am), ts, &st);
-      *reinterpret_cast<uint2*>(codes + (int64_t)r * (H >> 1) + cb * 8) =
-          make_uint2(encode8(f, st), encode8(f + 8, st));
+      const uint2 cw = make_uint2(encode8(f, st), encode8(f + 8, st));
+      if (PACT_IN(r < (uint64_t)M && cb < bpr))
+        *reinterpret_cast<uint2*>(codes + (int64_t)r * (H >> 1) + cb * 8) = cw;
     }
     // scale bytes of blocks cb .. cb+3 (same row) into one word
     uint32_t w = sb | (__shfl_down_sync(0xFFFFFFFFu, sb, 1) << 8);
     w |= __shfl_down_sync(0xFFFFFFFFu, w, 2) << 16;
-    if (live && (cb & 3u) == 0u) *reinterpret_cast<uint32_t*>(sf + sf_offset(r, cb, bpr)) = w;
+    if (live && (cb & 3u) == 0u && PACT_IN(sf_offset(r, cb, bpr) + 4 <= Mpad * (int64_t)bpr))
+      *reinterpret_cast<uint32_t*>(sf + sf_offset(r, cb, bpr)) = w;
   }
 }
 
@@ -440,6 +442,7 @@ __global__ void __launch_bounds__(256, 2) k_silu_encode(const uint16_t* __restri
     fetch(it + stride);
     const int64_t row = bpr_div.div(it), b = it - (uint32_t)row * bpr;
     const int64_t so = sf_offset(row, b, bpr);
+    if (!PACT_IN(so < Mpad * (int64_t)bpr)) continue;
     if (row >= M) {
 #pragma unroll
       for (int k = 0; k < 3; ++k) out.sf[k][so] = 0;
@@ -563,6 +566,7 @@ __global__ void __launch_bounds__(256) k_silu_bwd(
       amax = max(amax, max(max((og[i / 2] & 0x7FFFu) << 16, (og[i / 2] >> 16 & 0x7FFFu) << 16),
                            max((ou[i / 2] & 0x7FFFu) << 16, (ou[i / 2] >> 16 & 0x7FFFu) << 16)));
     }
+    if (!PACT_IN(row < M && b < bpr)) continue;
     uint4* pg = reinterpret_cast<uint4*>(dgu + row * 2 * I + b * 16);
     uint4* pu = reinterpret_cast<uint4*>(dgu + row * 2 * I + I + b * 16);
     pg[0] = make_uint4(og[0], og[1], og[2], og[3]);
@@ -651,6 +655,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
           amax = max(amax, max((o[i / 2] & 0x7FFFu) << 16, (o[i / 2] >> 16 & 0x7FFFu) << 16));
         }
         uint4* op = reinterpret_cast<uint4*>(dx + row * H + b * 16);
+        if (!PACT_IN(row < M && b < nb)) continue;
         op[0] = make_uint4(o[0], o[1], o[2], o[3]);
         op[1] = make_uint4(o[4], o[5], o[6], o[7]);
       }

@@ -113,12 +113,13 @@ __global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__
       sb = block_scale_fast(__uint_as_float(max(absmax_bf16x8_bits(v0), absmax_bf16x8_bits(v1))),
                             ts, &st);
       const uint2 cw = make_uint2(encode8(f, st), encode8(f + 8, st));
-      *reinterpret_cast<uint2*>(codes + (int64_t)r * (K >> 1) + cb * 8) = cw;
+      if (PACT_IN(r < (uint64_t)M && cb < bpr))
+        *reinterpret_cast<uint2*>(codes + (int64_t)r * (K >> 1) + cb * 8) = cw;
     }
     // scale bytes of blocks cb .. cb+3 (same row) into one word
     uint32_t w = sb | (__shfl_down_sync(0xFFFFFFFFu, sb, 1) << 8);
     w |= __shfl_down_sync(0xFFFFFFFFu, w, 2) << 16;
-    if (live && (cb & 3u) == 0u)
+    if (live && (cb & 3u) == 0u && PACT_IN(sf_offset(r, cb, bpr) + 4 <= Mpad * (int64_t)bpr))
       *reinterpret_cast<uint32_t*>(sf + sf_offset(r, cb, bpr)) = w;
   }
 }
@@ -160,8 +161,10 @@ __global__ void __launch_bounds__(256) k_pack_weight(const float* __restrict__ W
     const uint32_t w = encode8(f, st);
     if (!backward) {
       const int64_t n = gu_half ? gu_interleaved(tn * 16 + i, gu_half) : tn * 16 + i;
-      *reinterpret_cast<uint32_t*>(codes + n * (K >> 1) + tk * 8 + 4 * h) = w;
-      if (h == 0) sf[sf_offset(n, tk, K >> 4)] = (uint8_t)s;
+      if (PACT_IN(n < N && tk < (K >> 4))) {
+        *reinterpret_cast<uint32_t*>(codes + n * (K >> 1) + tk * 8 + 4 * h) = w;
+        if (h == 0) sf[sf_offset(n, tk, K >> 4)] = (uint8_t)s;
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) nib[warp][i][8 * h + j] = (uint8_t)((w >> (4 * j)) & 0xFu);
@@ -171,8 +174,10 @@ __global__ void __launch_bounds__(256) k_pack_weight(const float* __restrict__ W
 #pragma unroll
       for (int j = 0; j < 8; ++j) o |= (uint32_t)nib[warp][8 * h + j][i] << (4 * j);
       const int64_t k = tk * 16 + i;
-      *reinterpret_cast<uint32_t*>(codes + k * (N >> 1) + tn * 8 + 4 * h) = o;
-      if (h == 0) sf[sf_offset(k, tn, N >> 4)] = (uint8_t)s;
+      if (PACT_IN(k < K && tn < (N >> 4))) {
+        *reinterpret_cast<uint32_t*>(codes + k * (N >> 1) + tn * 8 + 4 * h) = o;
+        if (h == 0) sf[sf_offset(k, tn, N >> 4)] = (uint8_t)s;
+      }
       __syncwarp();
     }
   }
