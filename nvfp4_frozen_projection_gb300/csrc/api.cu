@@ -94,14 +94,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D tiled map over a row-major [rows, inner] matrix of elem-byte elements.
+// 2-D tiled map over a row-major [rows, inner] matrix of elem-byte elements whose
+// rows are ld elements apart (ld = inner when 0).
 int make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
              uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
-             CUtensorMapSwizzle swz) {
+             CUtensorMapSwizzle swz, uint64_t ld = 0) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(PACT_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+  cuuint64_t strides[1] = {(ld ? ld : inner) * (uint64_t)elem_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -206,8 +207,12 @@ int pact_quant_nvfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const
   if ((rc = check_nvfp4(out, "out", M, K, 16))) return rc;
   if (!ws || ws_bytes < pact_quant_nvfp4_workspace_size(M, K) || !aligned(ws, 256))
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
-  cudaError_t e = launch_quant_bf16(x, M, K, ldx, amax_opt, (uint8_t*)out->codes,
-                                    (uint8_t*)out->sf, out->g, (unsigned*)ws, d->sms,
+  CUtensorMap tmx;
+  if ((rc = make_map(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 64, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B, ldx)))
+    return rc;
+  cudaError_t e = launch_quant_bf16(tmx, x, M, K, ldx, amax_opt, (uint8_t*)out->codes,
+                                    (uint8_t*)out->sf, out->g, (unsigned*)ws, d->status, d->sms,
                                     (cudaStream_t)stream);
   return e == cudaSuccess ? PACT_OK : cuda_fail(e, "quant launch");
 }

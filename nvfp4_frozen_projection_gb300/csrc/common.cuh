@@ -350,6 +350,111 @@ __device__ __forceinline__ uint32_t block_scale_fast(float amax_blk, const Tenso
   return s;
 }
 
+// ------------------------------------------------------------------ block encode by table
+// The streaming encoders take a block's bracket from a per-CTA table indexed by the
+// scale byte (256 entries per tensor scale g, built once per CTA), leave the rare
+// elements where the bracket straddles a threshold to a per-lane fix-up after the
+// whole iteration, and keep the common path free of branches.
+//
+// The bracket (rlo, rhi) of 1/t for the decode step t of one scale byte:
+//   t == 0       -> (0, 0): every product is a signed zero, which is the code of a
+//                   block with t == 0;
+//   certifiable  -> the verified bracket of block_step;
+//   otherwise    -> (0, +inf): the two codes of every nonzero element differ (zero
+//                   and a saturated or NaN product), so each goes to e2m1_fix.
+__device__ __forceinline__ float2 step_bracket(float t) {
+  if (!(t > 0.0f)) return make_float2(0.0f, 0.0f);
+  const BlockStep b = block_step(t);
+  return step_certifiable(b) ? make_float2(b.rlo, b.rhi)
+                             : make_float2(0.0f, __int_as_float(0x7F800000));
+}
+
+// Entry s of the bracket table of a tensor scale g.
+__device__ __forceinline__ float2 bracket_entry(uint32_t s, float g) {
+  return step_bracket(__fmul_rn(e4m3_to_f32(s), g));
+}
+
+// The block scale byte e4m3(RN(amax_blk / d)): from the product with RN(1/d) when
+// both ends of its error interval (as in block_scale_fast) round to the same byte,
+// which one conversion of the pair decides; otherwise from the division.
+__device__ __forceinline__ uint32_t scale_byte(float amax_blk, const TensorScale& ts) {
+  const float q = __fmul_rn(amax_blk, ts.rcp_d);
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+      : "=h"(r)
+      : "f"(__fmul_rn(q, 1.0f + 0x1p-21f)), "f"(__fmul_rn(q, 1.0f - 0x1p-21f)));
+  const uint32_t lo = r & 0xFFu;
+  if (lo == (uint32_t)(r >> 8) && ts.rcp_d > 0.0f) return lo;
+  return ts.g == 0.0f ? 0u : e4m3_from_f32(__fdiv_rn(amax_blk, ts.d));
+}
+
+// The 16 codes of one block (w0: elements 0..7, w1: 8..15, element i in bits 4i..4i+3)
+// from the products with rlo, and the nibbles where the products with rhi disagree.
+__device__ __forceinline__ void codes16(const float* f, float2 br, uint32_t& w0, uint32_t& w1,
+                                        uint32_t& d0, uint32_t& d1) {
+  w0 = e2m1x8_of_products(f, br.x);
+  w1 = e2m1x8_of_products(f + 8, br.x);
+  d0 = w0 ^ e2m1x8_of_products(f, br.y);
+  d1 = w1 ^ e2m1x8_of_products(f + 8, br.y);
+}
+
+// The exact code of x under step t where the bracket's codes lo (from rlo) and hi
+// (from rhi) differ.  Adjacent magnitudes of one sign leave one threshold m between
+// them, decided as in fix_straddles; anything else comes from a block whose products
+// are not certified and takes the full exact decision.
+__device__ __forceinline__ uint32_t e2m1_fix(float x, float t, uint32_t lo, uint32_t hi) {
+  const uint32_t c = lo & 7u;
+  if (((lo ^ hi) & 8u) == 0u && (hi & 7u) == c + 1u) {
+    const float2 dv = e2m1x2_to_f32x2(c | ((c + 1u) << 4));
+    const float m = __fmul_rn(__fadd_rn(dv.x, dv.y), 0.5f);
+    const float hh = __int_as_float((__float_as_int(m) & 0x7F800000) - (24 << 23));
+    const float hl = c == 0u ? __fmul_rn(hh, 0.5f) : hh;
+    const float D = __fmaf_rn(-m, t, fabsf(x));
+    const uint32_t mag =
+        D > __fmul_rn(hh, t) ? c + 1u : (D >= -__fmul_rn(hl, t) ? c + (c & 1u) : c);
+    return (sign_bit(x) << 3) | mag;
+  }
+  return e2m1_code_exact(x, t);
+}
+
+// Codes w with the nibbles flagged in d replaced by e2m1_fix; elem(i) gives the value
+// of element i (0..7) of the word.  Visits only the flagged elements.
+template <class Elem>
+__device__ __forceinline__ uint32_t fix_word(uint32_t w, uint32_t d, float t, Elem elem) {
+#pragma unroll 1
+  while (d) {
+    const uint32_t sh = ((uint32_t)__ffs(d) - 1u) & ~3u;  // 4 i
+    const uint32_t dn = (d >> sh) & 0xFu;
+    d ^= dn << sh;
+    const uint32_t lo = (w >> sh) & 0xFu;
+    const uint32_t c = e2m1_fix(elem(sh >> 2), t, lo, lo ^ dn);
+    w ^= (lo ^ c) << sh;
+  }
+  return w;
+}
+
+// Element i (runtime, 0..7) of eight packed BF16 values, as FP32.
+__device__ __forceinline__ float bf16x8_at(const uint4& v, uint32_t i) {
+  const uint32_t h = i >> 1;
+  const uint32_t w = h == 0 ? v.x : (h == 1 ? v.y : (h == 2 ? v.z : v.w));
+  return __uint_as_float((i & 1u) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// max |x| over 16 BF16 values (two 16-byte vectors) as FP32 bits.
+__device__ __forceinline__ uint32_t absmax_bf16x16_bits(const uint4& a, const uint4& b) {
+  const uint32_t k = 0x7FFF7FFFu;
+  const uint32_t m = __vmaxu2(__vmaxu2(__vmaxu2(a.x & k, a.y & k), __vmaxu2(a.z & k, a.w & k)),
+                              __vmaxu2(__vmaxu2(b.x & k, b.y & k), __vmaxu2(b.z & k, b.w & k)));
+  return max(m >> 16, m & 0xFFFFu) << 16;
+}
+
+// Offset of the scale word of blocks 4 cg .. 4 cg + 3 of row r (the 128x4 atom layout
+// of sf_offset; upr = blocks per row / 4).  32-bit: callers keep pad128(M) * K / 16
+// below 2^31.
+__device__ __forceinline__ uint32_t sf_word_offset(uint32_t r, uint32_t cg, uint32_t upr) {
+  return ((r >> 7) * upr + cg) * 512u + (r & 31u) * 16u + ((r & 127u) >> 5) * 4u;
+}
+
 // ------------------------------------------------------------------ bf16
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -398,6 +503,16 @@ __device__ __forceinline__ uint32_t absmax_bf16x8_bits(const uint4& v) {
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// A read-only 16-byte load that allocates in L1: for a lane that reads a contiguous
+// run in several loads, the later loads of a 32-byte sector hit L1.
+__device__ __forceinline__ uint4 ldg_nc(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;

@@ -90,9 +90,11 @@ cudaError_t launch_bounds_check(cudaStream_t stream);
 // amax pass alone (contiguous rows): max |x| as FP32 bits into *ws_amax.
 cudaError_t launch_amax_bf16(const uint16_t* x, int64_t M, int64_t K, unsigned* ws_amax,
                              int num_sms, cudaStream_t stream);
-cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
-                              const float* amax_opt, uint8_t* codes, uint8_t* sf, float* g,
-                              unsigned* ws_amax, int num_sms, cudaStream_t stream);
+// tmx: BF16 map over x [M, K] (row stride ldx), box 64 x 32, 128-byte swizzle.
+cudaError_t launch_quant_bf16(const CUtensorMap& tmx, const uint16_t* x, int64_t M, int64_t K,
+                              int64_t ldx, const float* amax_opt, uint8_t* codes, uint8_t* sf,
+                              float* g, unsigned* ws_amax, unsigned* status, int num_sms,
+                              cudaStream_t stream);
 // gu_half > 0: forward layout in the interleaved gate|up row order (gu_interleaved).
 cudaError_t launch_pack_weight(const float* W, int64_t N, int64_t K, int backward,
                                int64_t gu_half, uint8_t* codes, uint8_t* sf, float* g,

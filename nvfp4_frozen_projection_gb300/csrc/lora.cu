@@ -326,10 +326,13 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
   const int nch = (int)(N >> 6);
   const int ch0 = (int)((int64_t)nch * split / ns), ch1 = (int)((int64_t)nch * (split + 1) / ns);
   TensorScale tsq = {0.0f, 0.0f, 0.0f};
+  __shared__ float2 brk[QUANT ? 256 : 1];  // bracket table of the dY scale (bracket_entry)
   if constexpr (QUANT) {
     const float amax = qz.amax_opt ? *qz.amax_opt : __uint_as_float(*qz.amax_bits);
     tsq = tensor_scale(amax);
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *qz.g_out = tsq.g;
+    brk[threadIdx.x] = bracket_entry(threadIdx.x, tsq.g);  // blockDim.x == 256; read after
+                                                           // the ring loop's first barrier
   }
   // rows r .. RP - 1 of every B slot stay zero (the copies never touch them)
   for (int i = threadIdx.x; i < kDyRing * (RP - r) * (kDyBRow / 4); i += blockDim.x) {
@@ -399,22 +402,35 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
       }
     }
     if constexpr (QUANT) {
+      // the lane's two blocks (rows row0 and row0 + 8), brackets from the table; the
+      // rare straddling elements are fixed from the registers afterwards
+      uint32_t w[4], d[4], sc[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t am = max(absmax_bf16x8_bits(xc[h][0]), absmax_bf16x8_bits(xc[h][1]));
-        float f8[8];
-        BlockStep st;
-        const uint32_t sc = block_scale_fast(__uint_as_float(am), tsq, &st);
-        bf16x8_to_f32(xc[h][0], f8);
-        const uint32_t w0 = encode8(f8, st);
-        bf16x8_to_f32(xc[h][1], f8);
-        const uint32_t w1 = encode8(f8, st);
+        sc[h] = scale_byte(__uint_as_float(absmax_bf16x16_bits(xc[h][0], xc[h][1])), tsq);
+        float f[16];
+        bf16x8_to_f32(xc[h][0], f);
+        bf16x8_to_f32(xc[h][1], f + 8);
+        codes16(f, brk[sc[h]], w[2 * h], w[2 * h + 1], d[2 * h], d[2 * h + 1]);
+      }
+      if (d[0] | d[1] | d[2] | d[3]) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (d[q]) {
+            const float tq = __fmul_rn(e4m3_to_f32(sc[q >> 1]), tsq.g);
+            w[q] = fix_word(w[q], d[q], tq,
+                            [&](uint32_t i) { return bf16x8_at(xc[q >> 1][q & 1], i); });
+          }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t w0 = w[2 * h], w1 = w[2 * h + 1];
         const int64_t row = row0 + 8 * h;
         if ((h ? ok1 : ok0) && PACT_IN(row < M && cc < nch))
           *reinterpret_cast<uint2*>(qz.codes + row * (N >> 1) + (int64_t)cc * 32 + 8 * c) =
               make_uint2(w0, w1);
         if (PACT_IN((h ? sfo1 : sfo0) + (int64_t)cc * 512 < pad_to(M, 128) * (N >> 4)))
-          qz.sf[(h ? sfo1 : sfo0) + (int64_t)cc * 512] = (uint8_t)sc;
+          qz.sf[(h ? sfo1 : sfo0) + (int64_t)cc * 512] = (uint8_t)sc[h];
       }
     }
   }

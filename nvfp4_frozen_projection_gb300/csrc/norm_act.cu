@@ -191,8 +191,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm_encode(
     const float* __restrict__ rstd, int64_t M, int64_t Mpad, int64_t H, FastDiv bpr_div,
     const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ sf, float* __restrict__ g_out) {
+  __shared__ float2 brk[256];
   const TensorScale ts = tensor_scale(__uint_as_float(*amax_bits));
+  brk[threadIdx.x] = bracket_entry(threadIdx.x, ts.g);  // blockDim.x == 256
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
+  __syncthreads();
   const uint32_t bpr = (uint32_t)(H >> 4);
   const uint32_t total = (uint32_t)Mpad * bpr;  // < 2^31 (checked by the caller)
   const uint32_t lane = threadIdx.x & 31u;
@@ -219,20 +222,31 @@ __global__ void __launch_bounds__(256) k_rmsnorm_encode(
     if (live && r < M) {
       const float rs = __ldg(rstd + r);
       const uint4* gp = reinterpret_cast<const uint4*>(gamma + cb * 16);
+      const uint4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
       float f[16], gm[16];
       bf16x8_to_f32(v0, f);
       bf16x8_to_f32(v1, f + 8);
-      bf16x8_to_f32(__ldg(gp), gm);
-      bf16x8_to_f32(__ldg(gp + 1), gm + 8);
-      uint32_t am = 0;
+      bf16x8_to_f32(g0, gm);
+      bf16x8_to_f32(g1, gm + 8);
+      float am = 0.0f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         f[i] = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
-        am = max(am, __float_as_uint(f[i]) & 0x7FFFFFFFu);
+        am = fmaxf(am, fabsf(f[i]));
       }
-      BlockStep st;
-      sb = block_scale_fast(__uint_as_float(am), ts, &st);
-      const uint2 cw = make_uint2(encode8(f, st), encode8(f + 8, st));
+      sb = scale_byte(am, ts);
+      uint2 cw;
+      uint32_t d0, d1;
+      codes16(f, brk[sb], cw.x, cw.y, d0, d1);
+      if (d0 | d1) {
+        const float t = __fmul_rn(e4m3_to_f32(sb), ts.g);
+        cw.x = fix_word(cw.x, d0, t, [&](uint32_t i) {
+          return __fmul_rn(__fmul_rn(bf16x8_at(v0, i), rs), bf16x8_at(g0, i));
+        });
+        cw.y = fix_word(cw.y, d1, t, [&](uint32_t i) {
+          return __fmul_rn(__fmul_rn(bf16x8_at(v1, i), rs), bf16x8_at(g1, i));
+        });
+      }
       if (PACT_IN(r < (uint64_t)M && cb < bpr))
         *reinterpret_cast<uint2*>(codes + (int64_t)r * (H >> 1) + cb * 8) = cw;
     }
@@ -411,11 +425,15 @@ __global__ void __launch_bounds__(256, 2) k_silu_encode(const uint16_t* __restri
                                                         const unsigned* __restrict__ amax3,
                                                         SiluOut out) {
   TensorScale ts[3];
+  __shared__ float2 brk[2][256];  // bracket tables of the gate and up scales
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
     ts[k] = tensor_scale(amax3_opt ? amax3_opt[k] : __uint_as_float(amax3[k]));
     if (blockIdx.x == 0 && threadIdx.x == 0) *out.g[k] = ts[k].g;
   }
+  brk[0][threadIdx.x] = bracket_entry(threadIdx.x, ts[1].g);  // blockDim.x == 256
+  brk[1][threadIdx.x] = bracket_entry(threadIdx.x, ts[2].g);
+  __syncthreads();
   const float lo_f = 1.0f - 2.0f * kSiluRel, hi_f = 1.0f + 2.0f * kSiluRel;
   const float rcp_d = ts[0].rcp_d;
   const uint32_t bpr = (uint32_t)(I >> 4);
@@ -510,15 +528,22 @@ __global__ void __launch_bounds__(256, 2) k_silu_encode(const uint16_t* __restri
     // ---- gate and up: their BF16 values are exact
 #pragma unroll
     for (int k = 1; k < 3; ++k) {
-      const uint32_t am = max(absmax_bf16x8_bits(k == 1 ? g0 : u0), absmax_bf16x8_bits(k == 1 ? g1 : u1));
-      BlockStep sk;
-      const uint32_t s = block_scale_fast(__uint_as_float(am), ts[k], &sk);
+      const uint4& a0 = k == 1 ? g0 : u0;
+      const uint4& a1 = k == 1 ? g1 : u1;
+      const uint32_t s = scale_byte(__uint_as_float(absmax_bf16x16_bits(a0, a1)), ts[k]);
       uint2 ck;
-      float v[8];  // one half of the block at a time keeps fewer values live
-      bf16x8_to_f32(k == 1 ? g0 : u0, v);
-      ck.x = encode8(v, sk);
-      bf16x8_to_f32(k == 1 ? g1 : u1, v);
-      ck.y = encode8(v, sk);
+      uint32_t d0, d1;
+      {
+        float v[16];
+        bf16x8_to_f32(a0, v);
+        bf16x8_to_f32(a1, v + 8);
+        codes16(v, brk[k - 1][s], ck.x, ck.y, d0, d1);
+      }
+      if (d0 | d1) {
+        const float t = __fmul_rn(e4m3_to_f32(s), ts[k].g);
+        ck.x = fix_word(ck.x, d0, t, [&](uint32_t i) { return bf16x8_at(a0, i); });
+        ck.y = fix_word(ck.y, d1, t, [&](uint32_t i) { return bf16x8_at(a1, i); });
+      }
       *reinterpret_cast<uint2*>(out.codes[k] + row * (I >> 1) + b * 8) = ck;
       out.sf[k][so] = (uint8_t)s;
     }

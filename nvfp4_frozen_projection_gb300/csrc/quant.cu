@@ -8,6 +8,7 @@
 // device word and pass 2 re-reads the tensor (mostly from L2) and encodes it.
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace pact {
 
@@ -59,68 +60,117 @@ __global__ void __launch_bounds__(256) k_amax_f32(const float* __restrict__ w, i
 }
 
 // ---------------------------------------------------------------- pass 2: encode
-// Lane = one block of 16 elements, warp = 32 consecutive blocks (a contiguous 1 KB
-// of a contiguous tensor), blocks numbered row-major over [pad128(M), K/16].  Each
-// lane holds the next block's 32 bytes in flight while it encodes the current one.
-// A block's 8 code bytes leave as one 8-byte store (256 contiguous bytes per warp);
-// the scale bytes of four consecutive blocks (one 4-byte word of the 128x4 atom
-// layout, never split across rows since K/16 is a multiple of 4) are gathered by
-// two shuffles and stored by the first lane of the four.  Blocks of rows past M (up
-// to pad128(M)) get zero scale bytes so the padded scale array is fully defined.
-__device__ __forceinline__ void quant_fetch(const uint16_t* x, int64_t ldx, uint32_t blk,
-                                            uint32_t total, uint32_t M, const FastDiv& bpr_div,
-                                            uint32_t bpr, uint4& v0, uint4& v1) {
-  if (blk < total) {
-    const uint32_t r = bpr_div.div(blk);
-    if (r < M) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * ldx + (blk - r * bpr) * 16);
-      v0 = ldg_stream(src);
-      v1 = ldg_stream(src + 1);
-    }
-  }
-}
+// Tile = 32 rows x 64 columns (4 KB), lane = one row of it: a unit of four
+// consecutive blocks (128 bytes).  Each warp runs its own two-stage ring: its lane 0
+// fetches the warp's next tiles by TMA (128-byte swizzle, so that each lane's reads
+// of its own row are free of bank conflicts), and the warp encodes one tile while
+// the next is in flight.  Warps take tiles in turn over the tensor, tile t covering
+// row group t / (K/64) and column group t % (K/64), so the warps of the grid sweep
+// the tensor front to back.  A unit's four scale bytes are one 4-byte word of the
+// 128x4 atom layout (K/16 is a multiple of 4), stored whole; its 32 code bytes leave
+// as two 16-byte stores.  The brackets come from the CTA's table (bracket_entry);
+// elements where a bracket straddles a threshold (about one in 10^3) are fixed after
+// the unit's four blocks are encoded, from the values still held in registers.
+// Rows past M read as zeros (the tensor map's bounds) and store zero scale words up
+// to pad128(M), so the padded scale array is fully defined.
+constexpr int kQuantThreads = 256;
+constexpr int kQuantWarps = kQuantThreads / 32;
+constexpr int kQuantStages = 2;
+constexpr uint32_t kQuantTileBytes = 32 * 128;
+constexpr uint64_t kQuantWaitNs = 2000000000ull;
 
-__global__ void __launch_bounds__(256) k_quant_bf16(const uint16_t* __restrict__ x, int64_t M,
-                                                    int64_t K, int64_t ldx, int64_t Mpad,
-                                                    FastDiv bpr_div,
-                                                    const float* __restrict__ amax_opt,
-                                                    const unsigned* __restrict__ amax_bits,
-                                                    uint8_t* __restrict__ codes,
-                                                    uint8_t* __restrict__ sf,
-                                                    float* __restrict__ g_out) {
+size_t quant_smem_bytes() { return 1024 + (size_t)kQuantWarps * kQuantStages * kQuantTileBytes; }
+
+__global__ void __launch_bounds__(kQuantThreads, 3) k_quant_bf16(
+    const __grid_constant__ CUtensorMap tmx, const uint16_t* __restrict__ x, int64_t M, int64_t K,
+    int64_t ldx, int64_t Mpad, FastDiv upr_div, const float* __restrict__ amax_opt,
+    const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+    float* __restrict__ g_out, unsigned* __restrict__ status) {
+  extern __shared__ uint8_t qsm[];
+  __shared__ float2 brk[256];
+  __shared__ __align__(8) uint64_t full[kQuantWarps][kQuantStages];
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
   const float amax = amax_opt ? *amax_opt : __uint_as_float(*amax_bits);
   const TensorScale ts = tensor_scale(amax);
+  brk[threadIdx.x] = bracket_entry(threadIdx.x, ts.g);  // blockDim.x == 256
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
-  const uint32_t bpr = (uint32_t)(K >> 4);           // blocks per row
-  const uint32_t total = (uint32_t)Mpad * bpr;        // < 2^31 (checked by the caller)
-  const uint32_t lane = threadIdx.x & 31u;
-  // warps take 32-block strips in turn, so each warp iteration covers 1 KB
-  const uint32_t stride = gridDim.x * blockDim.x;
-  uint32_t blk = blockIdx.x * blockDim.x + threadIdx.x;
-  uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
-  quant_fetch(x, ldx, blk, total, (uint32_t)M, bpr_div, bpr, n0, n1);
-  for (; blk - lane < total; blk += stride) {  // warp-uniform trip count
-    const uint4 v0 = n0, v1 = n1;
-    quant_fetch(x, ldx, blk + stride, total, (uint32_t)M, bpr_div, bpr, n0, n1);
-    const bool live = blk < total;
-    const uint32_t r = bpr_div.div(blk), cb = blk - r * bpr;
-    uint32_t sb = 0;
-    if (live && r < M) {
-      float f[16];
-      bf16x8_to_f32(v0, f);
-      bf16x8_to_f32(v1, f + 8);
-      BlockStep st;
-      sb = block_scale_fast(__uint_as_float(max(absmax_bf16x8_bits(v0), absmax_bf16x8_bits(v1))),
-                            ts, &st);
-      const uint2 cw = make_uint2(encode8(f, st), encode8(f + 8, st));
-      if (PACT_IN(r < (uint64_t)M && cb < bpr))
-        *reinterpret_cast<uint2*>(codes + (int64_t)r * (K >> 1) + cb * 8) = cw;
+  if (lane == 0) {
+    for (int i = 0; i < kQuantStages; ++i) mbar_init(smem_addr(&full[warp][i]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint32_t ring = ((smem_addr(qsm) + 1023u) & ~1023u) + warp * kQuantStages * kQuantTileBytes;
+  const uint32_t upr = (uint32_t)(K >> 6);  // column groups (units per row)
+  const uint32_t ntiles = (uint32_t)(Mpad >> 5) * upr;
+  const uint32_t first = blockIdx.x * kQuantWarps + warp, step = gridDim.x * kQuantWarps;
+  auto issue = [&](uint32_t t, int slot) {
+    const uint32_t rg = upr_div.div(t), cg = t - rg * upr;
+    const uint32_t bar = smem_addr(&full[warp][slot]);
+    mbar_expect_tx(bar, kQuantTileBytes);
+    tma_load_2d(ring + slot * kQuantTileBytes, &tmx, (int32_t)(cg * 64u), (int32_t)(rg * 32u), bar);
+  };
+  if (lane == 0) {
+    prefetch_tensormap(&tmx);
+    for (int i = 0; i < kQuantStages; ++i)
+      if (first + i * step < ntiles) issue(first + i * step, i);
+  }
+  uint32_t k = 0;
+  for (uint32_t t = first; t < ntiles; t += step, ++k) {
+    const int slot = (int)(k % kQuantStages);
+    if (!mbar_wait(smem_addr(&full[warp][slot]), (k / kQuantStages) & 1u, kQuantWaitNs, nullptr)) {
+      // give the warp's other copy in flight a bounded chance to land before leaving
+      if (lane == 0) {
+        atomicOr(status, PACT_DEV_TIMEOUT);
+        const uint32_t k2 = k + 1;
+        if (t + step < ntiles)
+          mbar_wait(smem_addr(&full[warp][k2 % kQuantStages]), (k2 / kQuantStages) & 1u,
+                    kQuantWaitNs, nullptr);
+      }
+      __syncwarp();
+      break;
     }
-    // scale bytes of blocks cb .. cb+3 (same row) into one word
-    uint32_t w = sb | (__shfl_down_sync(0xFFFFFFFFu, sb, 1) << 8);
-    w |= __shfl_down_sync(0xFFFFFFFFu, w, 2) << 16;
-    if (live && (cb & 3u) == 0u && PACT_IN(sf_offset(r, cb, bpr) + 4 <= Mpad * (int64_t)bpr))
-      *reinterpret_cast<uint32_t*>(sf + sf_offset(r, cb, bpr)) = w;
+    const uint32_t row_smem = ring + slot * kQuantTileBytes + lane * 128u;
+    uint4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = ld_shared_v4(row_smem + ((c ^ (lane & 7u)) << 4));
+    __syncwarp();  // every lane's reads of the slot are done
+    if (lane == 0 && t + kQuantStages * step < ntiles) {
+      fence_proxy_async_smem();
+      issue(t + kQuantStages * step, slot);
+    }
+    const uint32_t rg = upr_div.div(t), cg = t - rg * upr;
+    const uint32_t r = rg * 32u + lane;
+    const uint32_t so = sf_word_offset(r, cg, upr);
+    if (r >= (uint32_t)M) {
+      if (PACT_IN(so + 4u <= (uint32_t)Mpad * upr * 4u)) *reinterpret_cast<uint32_t*>(sf + so) = 0u;
+      continue;
+    }
+    uint32_t w[8], d[8], sw = 0u, any = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t sb =
+          scale_byte(__uint_as_float(absmax_bf16x16_bits(v[2 * j], v[2 * j + 1])), ts);
+      sw |= sb << (8 * j);
+      float f[16];
+      bf16x8_to_f32(v[2 * j], f);
+      bf16x8_to_f32(v[2 * j + 1], f + 8);
+      codes16(f, brk[sb], w[2 * j], w[2 * j + 1], d[2 * j], d[2 * j + 1]);
+      any |= d[2 * j] | d[2 * j + 1];
+    }
+    if (any) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (d[q]) {
+          const float tq = __fmul_rn(e4m3_to_f32((sw >> (8 * (q >> 1))) & 0xFFu), ts.g);
+          w[q] = fix_word(w[q], d[q], tq, [&](uint32_t i) { return bf16x8_at(v[q], i); });
+        }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(codes + (int64_t)r * (K >> 1) + cg * 32u);
+    if (PACT_IN(cg < upr)) {
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    if (PACT_IN(so + 4u <= (uint32_t)Mpad * upr * 4u)) *reinterpret_cast<uint32_t*>(sf + so) = sw;
   }
 }
 
@@ -200,9 +250,10 @@ cudaError_t launch_amax_bf16(const uint16_t* x, int64_t M, int64_t K, unsigned* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
-                              const float* amax_opt, uint8_t* codes, uint8_t* sf, float* g,
-                              unsigned* ws_amax, int num_sms, cudaStream_t stream) {
+cudaError_t launch_quant_bf16(const CUtensorMap& tmx, const uint16_t* x, int64_t M, int64_t K,
+                              int64_t ldx, const float* amax_opt, uint8_t* codes, uint8_t* sf,
+                              float* g, unsigned* ws_amax, unsigned* status, int num_sms,
+                              cudaStream_t stream) {
   if (!amax_opt) {
     cudaError_t e = cudaMemsetAsync(ws_amax, 0, sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
@@ -210,10 +261,21 @@ cudaError_t launch_quant_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
     k_amax_bf16<<<grid_for(M * K / 8, 256, num_sms * 4), 256, 0, stream>>>(x, M, K, ldx,
                                                                             ws_amax);
   }
+  static bool attr_set[64] = {};  // per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        k_quant_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)quant_smem_bytes());
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
   const int64_t Mpad = pad_to(M, 128);
+  const int64_t ntiles = (Mpad / 32) * (K / 64);
   note_launch();
-  k_quant_bf16<<<grid_for(Mpad * (K / 16), 256, num_sms * 8), 256, 0, stream>>>(
-      x, M, K, ldx, Mpad, FastDiv::make((uint32_t)(K / 16)), amax_opt, ws_amax, codes, sf, g);
+  k_quant_bf16<<<grid_for(ntiles, kQuantWarps, num_sms * 3), kQuantThreads, quant_smem_bytes(),
+                 stream>>>(tmx, x, M, K, ldx, Mpad, FastDiv::make((uint32_t)(K / 64)), amax_opt,
+                           ws_amax, codes, sf, g, status);
   return cudaGetLastError();
 }
 

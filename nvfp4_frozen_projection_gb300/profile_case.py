@@ -7,6 +7,8 @@ Cases (M = tokens; the other sizes are the Llama-3B layer's):
   gemm-gate-up-fwd    Y = X W^T (NVFP4, 3072 -> 2 x 8192) + LoRA term
   quant               NVFP4 quantisation of a BF16 [M, 3072] tensor
   silu                SiLU-multiply -> NVFP4 of a BF16 [M, 2 x 8192] tensor
+  silu-amax3          the same in one pass, with the three amaxes the gate|up forward
+                      GEMM emits (the GEMM runs once, before the repetitions)
   lora-down-fwd       the q projection's forward (down-projection + GEMM)
   gemm-o-fwd          the o projection's forward: the same GEMM plus the residual add
   dgrad-q-gate-up     the fused gate|up input gradient (dY quantised inside the LoRA
@@ -18,8 +20,10 @@ Cases (M = tokens; the other sizes are the Llama-3B layer's):
   silu-bwd            SiLU-multiply backward from [M, 8192] NVFP4 gate/up copies
   pack-weight         forward and backward NVFP4 packs of the gate|up weight [2 x 8192, 3072]
 
-The default M (4096) keeps every case's inputs above the 129 MB L2 and its device
-memory under 1 GB, which is the size a full ncu capture wants.  Each run exits 0
+The default M (4096) keeps the inputs of the SiLU, GEMM and weight-pack cases above
+the 129 MB L2 and every case's device memory under 1 GB, the size a full ncu capture
+wants; the [M, 3072] cases (quant, rmsnorm, rmsnorm-bwd) need --m 32768 (16384 for
+rmsnorm-bwd) for their inputs to exceed the L2.  Each run exits 0
 only if the library's status word is clear.
 """
 from __future__ import annotations
@@ -29,7 +33,8 @@ import argparse
 import torch
 
 from . import (pact_check_status, pact_lora_adapter_grad, pact_lora_linear_dgrad,
-               pact_lora_linear_dgrad_q,
+               pact_lora_linear_dgrad_q, pact_lora_linear_fwd_gate_up,
+               pact_pack_weight_fwd_gate_up,
                pact_lora_linear_fwd, pact_pack_weight_bwd, pact_pack_weight_fwd,
                pact_quant_nvfp4, pact_rmsnorm_bwd, pact_rmsnorm_quant, pact_silu_mul_bwd,
                pact_silu_mul_quant)
@@ -96,6 +101,14 @@ def run(case: str, m: int, reps: int) -> None:
         outs = pact_silu_mul_quant(gu)
         for _ in range(reps):
             pact_silu_mul_quant(gu, outs=outs)
+    elif case == "silu-amax3":
+        W, A, B = _lora(HIDDEN, 2 * INTER, 32, dev, gen)
+        x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
+        gu, amax3 = pact_lora_linear_fwd_gate_up(pact_quant_nvfp4(x),
+                                                 pact_pack_weight_fwd_gate_up(W), A, B, 2.0)
+        outs = pact_silu_mul_quant(gu, amax3=amax3)
+        for _ in range(reps):
+            pact_silu_mul_quant(gu, amax3=amax3, outs=outs)
     elif case == "rmsnorm":
         x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
         gamma = (1.0 + 0.1 * torch.randn(HIDDEN, device=dev, generator=gen)).bfloat16()
