@@ -250,7 +250,7 @@ int pact_lora_linear_dgrad_q(const uint16_t* dy, const float* dy_amax_opt,
  * once the per-tensor scale is factored out) and dY accumulate in FP32 over row
  * splits whose partial sums are added in a fixed order, so results are
  * deterministic run to run.
- * Rules: M >= 1, N and K multiples of 64; dy 16-byte, B 8-byte, dA and dB 4-byte
+ * Rules: M >= 1, N and K multiples of 64; dy and B 16-byte, dA and dB 4-byte
  * aligned; xq codes/sf 16-byte aligned.  ws: pact_lora_adapter_grad_workspace_size()
  * bytes, 256-byte aligned, owned by the caller and free again when the stream
  * reaches the end of the call.  Errors are reported before any launch.

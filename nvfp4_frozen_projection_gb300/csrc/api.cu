@@ -94,11 +94,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // 2-D tiled map over a row-major [rows, inner] matrix of elem-byte elements whose
 // rows are ld elements apart (ld = inner when 0).
-int make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
+int pact::make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
              uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
-             CUtensorMapSwizzle swz, uint64_t ld = 0) {
+             CUtensorMapSwizzle swz, uint64_t ld) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(PACT_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t dims[2] = {inner, rows};
@@ -111,6 +113,8 @@ int make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void*
   if (r != CUDA_SUCCESS) return fail(PACT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return PACT_OK;
 }
+
+namespace {
 
 // ---------------------------------------------------------------- validation helpers
 int64_t pad_to(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
@@ -432,8 +436,8 @@ int pact_lora_linear_dgrad(const pact_nvfp4* dyq, const uint16_t* dy, const pact
   if ((rc = check_nvfp4(dyq, "dyq", M, N, 128)) || (rc = check_nvfp4(w_bwd, "w_bwd", K, N, 128)))
     return rc;
   if (!dy || !A || !B || !dx) return fail(PACT_ERR_INVALID_ARG, "dy, A, B and dx are required");
-  if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(B, 8) || !aligned(A, 2))
-    return fail(PACT_ERR_ALIGN, "dx and dy must be 16-byte aligned, B 8-byte aligned");
+  if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(B, 16) || !aligned(A, 2))
+    return fail(PACT_ERR_ALIGN, "dx, dy and B must be 16-byte aligned");
   if (!ws || ws_bytes < pact_lora_linear_dgrad_workspace_size(M, N, K, r) || !aligned(ws, 256))
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
   const int rp = rp_for(r);
@@ -471,9 +475,9 @@ int pact_lora_linear_dgrad_q(const uint16_t* dy, const float* dy_amax_opt,
       (rc = check_nvfp4(w_bwd, "w_bwd", K, N, 128)))
     return rc;
   if (!dy || !A || !B || !dx) return fail(PACT_ERR_INVALID_ARG, "dy, A, B and dx are required");
-  if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(B, 8) || !aligned(A, 2) ||
+  if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(B, 16) || !aligned(A, 2) ||
       (dy_amax_opt && !aligned(dy_amax_opt, 4)))
-    return fail(PACT_ERR_ALIGN, "dx and dy must be 16-byte aligned, B 8-byte aligned");
+    return fail(PACT_ERR_ALIGN, "dx, dy and B must be 16-byte aligned");
   if (!ws || ws_bytes < pact_lora_linear_dgrad_q_workspace_size(M, N, K, r) || !aligned(ws, 256))
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
   const int rp = rp_for(r);
@@ -515,8 +519,8 @@ int pact_lora_adapter_grad(const pact_nvfp4* xq, const uint16_t* dy, const uint1
   if ((rc = check_nvfp4(xq, "xq", M, K, 16))) return rc;
   if (!dy || !A || !B || !dA || !dB)
     return fail(PACT_ERR_INVALID_ARG, "dy, A, B, dA and dB are required");
-  if (!aligned(dy, 16) || !aligned(B, 8) || !aligned(A, 2) || !aligned(dA, 4) || !aligned(dB, 4))
-    return fail(PACT_ERR_ALIGN, "dy must be 16-byte aligned, B 8-byte aligned");
+  if (!aligned(dy, 16) || !aligned(B, 16) || !aligned(A, 2) || !aligned(dA, 4) || !aligned(dB, 4))
+    return fail(PACT_ERR_ALIGN, "dy and B must be 16-byte aligned");
   if (!ws || ws_bytes < pact_lora_adapter_grad_workspace_size(M, N, K, r) || !aligned(ws, 256))
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
   const int rp = rp_for(r);

@@ -84,6 +84,12 @@ int gemm_stage_row_bytes();
 bool gemm_uses_pair(int64_t M, int64_t N, int rpe);
 cudaError_t launch_gemm_nvfp4(const GemmLaunch& L, int bn, int rpe, int cm, cudaStream_t stream);
 cudaError_t status_word_ptr(unsigned** ptr);
+// 2-D tiled tensor map over a row-major [rows, inner] matrix of elem_bytes elements
+// whose rows are ld elements apart (ld = inner when 0); PACT_OK or an error code (the
+// message in pact_last_error).
+int make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
+             uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+             CUtensorMapSwizzle swz, uint64_t ld = 0);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_bounds_check(cudaStream_t stream);
 

@@ -284,81 +284,100 @@ struct DyQuant {
 // U' = f * (dY B^T), dy [M, N] BF16, B [r, N] row-major, for 128-row blocks of dY
 // whose column range is split over a cluster of NS CTAs (NS a power of two <= 8,
 // along grid x).  Warp w multiplies rows 16w .. 16w + 15 of the block; the eight
-// warps step through the same 64-column chunks, so each chunk of B (RP rows, zero
-// past r) is copied into shared memory once per CTA (a 4-slot cp.async ring) and
-// read by all of them.  Lane (g, c) holds 16 consecutive elements of rows g and
-// g + 8, [16c, 16c + 16) of the chunk: in K step s of the m16n8k16 MMA its k slots
-// 2c, 2c + 1 / 2c + 8, 2c + 9 carry columns 16c + 4s + 0, 1 / 2, 3, and the B
-// fragment is read at the same columns (a k permutation both operands share).
-// The CTAs' partial sums meet in distributed shared memory at the end: CTA j of
-// the cluster adds the NS partials of rows [128 j / NS, 128 (j + 1) / NS) in rank
-// order, so the result does not depend on scheduling.
+// warps step through the same 64-column chunks, which one thread fetches by TMA into
+// a 4-slot ring: per slot the block's 128 dY rows and the chunk of B (r rows), both
+// 128-byte rows in the 128-byte swizzle (rows r .. RP - 1 of the B part are zeroed
+// once and never copied into).  A slot is refilled when all eight warps have
+// released it (an mbarrier with eight arrivals), so warps run ahead of one another
+// by up to the ring's depth instead of meeting at a CTA barrier every chunk.  Lane
+// (g, c) holds 16
+// consecutive elements of rows g and g + 8, [16c, 16c + 16) of the chunk: in K step
+// s of the m16n8k16 MMA its k slots 2c, 2c + 1 / 2c + 8, 2c + 9 carry columns
+// 16c + 4s + 0, 1 / 2, 3, and the B fragment is read at the same columns (a k
+// permutation both operands share).  The CTAs' partial sums meet in distributed
+// shared memory at the end: CTA j of the cluster adds the NS partials of rows
+// [128 j / NS, 128 (j + 1) / NS) in rank order, so the result does not depend on
+// scheduling.
 // With QUANT the same pass quantises dY to NVFP4, byte for byte as the quantiser
-// does (the same block-scale table and element encode): a lane's 16 elements of a
-// row are exactly one NVFP4 block.  The grid covers the rows up to the 128-row
-// padding of the scale atoms, whose scales encode zero.
-constexpr int kDyRing = 4;      // chunk slots (3 chunks in flight)
-constexpr int kDyBRow = 136;    // bytes per B row in shared memory: 128 + 8 makes the
-                                // fragment reads of a half-warp hit 32 distinct banks
-constexpr int kDyXRow = 144;    // bytes per dY row: 128 + 16, conflict-free 16-byte reads
-constexpr int kDyXSlot = 128 * kDyXRow;
+// does (the same bracket table and element encode): a lane's 16 elements of a row
+// are exactly one NVFP4 block.  The grid covers the rows up to the 128-row padding
+// of the scale atoms, whose scales encode zero (the rows past M read as zeros).
+constexpr int kDyRing = 4;  // chunk slots
+constexpr uint64_t kDyWaitNs = 2000000000ull;
 
 template <int RP>
+constexpr uint32_t dy_slot_bytes() {
+  return 128 * 128 + RP * 128;  // dY rows, then B rows; a multiple of 1024
+}
+template <int RP>
 constexpr int dy_smem_bytes() {
-  return kDyRing * (RP * kDyBRow + kDyXSlot);  // >= 128 RP 4 bytes of partial sums
+  return 1024 + kDyRing * (int)dy_slot_bytes<RP>();  // >= 128 RP 4 bytes of partial sums
+}
+
+// Byte offset of 16-byte chunk q of row `row` in a tile of 128-byte rows written by
+// a TMA copy with the 128-byte swizzle (tile base 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t q) {
+  return row * 128u + ((q ^ (row & 7u)) << 4);
 }
 
 template <int RP, bool QUANT>
-__global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restrict__ dy,
+__global__ void __launch_bounds__(256, 2) k_lora_down_dy(const __grid_constant__ CUtensorMap tm_dy,
+                                                         const __grid_constant__ CUtensorMap tm_b,
                                                          const float* __restrict__ gdy,
                                                          const float* __restrict__ gw, int64_t M,
-                                                         int64_t N, const uint16_t* __restrict__ B,
-                                                         int r, float scale, int plain,
-                                                         uint16_t* __restrict__ u_out, DyQuant qz) {
+                                                         int64_t N, int r, float scale, int plain,
+                                                         uint16_t* __restrict__ u_out, DyQuant qz,
+                                                         unsigned* __restrict__ status) {
   constexpr int NT = RP / 8;
-  constexpr int SLOT = RP * kDyBRow;
-  constexpr int XOFF = kDyRing * SLOT;  // the dY ring follows the B ring
-  extern __shared__ __align__(16) uint8_t dsm[];
+  constexpr uint32_t SLOT = dy_slot_bytes<RP>();
+  constexpr uint32_t BOFF = 128 * 128;  // B rows follow the dY rows in a slot
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[kDyRing], empty[kDyRing];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int ns = (int)gridDim.x, split = (int)blockIdx.x;  // split == rank in the cluster
   const int64_t mb0 = (int64_t)blockIdx.y * 128;
   const int nch = (int)(N >> 6);
   const int ch0 = (int)((int64_t)nch * split / ns), ch1 = (int)((int64_t)nch * (split + 1) / ns);
+  const uint32_t ring = (smem_addr(dsm) + 1023u) & ~1023u;
+  uint8_t* const ring_ptr = dsm + (ring - smem_addr(dsm));
   TensorScale tsq = {0.0f, 0.0f, 0.0f};
   __shared__ float2 brk[QUANT ? 256 : 1];  // bracket table of the dY scale (bracket_entry)
   if constexpr (QUANT) {
     const float amax = qz.amax_opt ? *qz.amax_opt : __uint_as_float(*qz.amax_bits);
     tsq = tensor_scale(amax);
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *qz.g_out = tsq.g;
-    brk[threadIdx.x] = bracket_entry(threadIdx.x, tsq.g);  // blockDim.x == 256; read after
-                                                           // the ring loop's first barrier
+    brk[threadIdx.x] = bracket_entry(threadIdx.x, tsq.g);  // blockDim.x == 256
   }
-  // rows r .. RP - 1 of every B slot stay zero (the copies never touch them)
-  for (int i = threadIdx.x; i < kDyRing * (RP - r) * (kDyBRow / 4); i += blockDim.x) {
-    const int slot = i / ((RP - r) * (kDyBRow / 4)), rem = i - slot * ((RP - r) * (kDyBRow / 4));
-    reinterpret_cast<uint32_t*>(dsm + slot * SLOT + r * kDyBRow)[rem] = 0u;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDyRing; ++i) {
+      mbar_init(smem_addr(&full[i]), 1);
+      mbar_init(smem_addr(&empty[i]), 8);
+    }
+    fence_mbar_init();
   }
-  const uint32_t sbase = smem_addr(dsm);
-  // one chunk: the B columns (RP rows, 8-byte pieces) and the block's 128 dY rows
-  // (16-byte pieces, zeros past M), one cp.async group
-  auto load_chunk = [&](int ch, int slot) {
-    for (int pc = threadIdx.x; pc < r * 16; pc += blockDim.x) {
-      const int row = pc >> 4, q8 = pc & 15;
-      cp_async8(sbase + slot * SLOT + row * kDyBRow + q8 * 8,
-                B + (int64_t)row * N + (int64_t)ch * 64 + q8 * 4);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int pc = (int)threadIdx.x + 256 * i, row = pc >> 3, q16 = pc & 7;
-      const int64_t m = mb0 + row;
-      const bool ok = m < M;
-      cp_async16(sbase + XOFF + slot * kDyXSlot + row * kDyXRow + q16 * 16,
-                 ok ? dy + m * N + (int64_t)ch * 64 + q16 * 8 : dy, ok ? 16u : 0u);
-    }
+  // rows r .. RP - 1 of every slot's B part stay zero (the copies bring r rows)
+  for (int i = threadIdx.x; i < kDyRing * (RP - r) * 32; i += blockDim.x) {
+    const int slot = i / ((RP - r) * 32), rem = i - slot * ((RP - r) * 32);
+    reinterpret_cast<uint32_t*>(ring_ptr + slot * SLOT + BOFF + r * 128)[rem] = 0u;
+  }
+  __syncthreads();
+  const uint32_t chunk_bytes = BOFF + (uint32_t)r * 128u;
+  auto issue = [&](int ch, int slot) {
+    const uint32_t bar = smem_addr(&full[slot]);
+    mbar_expect_tx(bar, chunk_bytes);
+    tma_load_2d(ring + slot * SLOT, &tm_dy, ch * 64, (int32_t)mb0, bar);
+    tma_load_2d(ring + slot * SLOT + BOFF, &tm_b, ch * 64, 0, bar);
   };
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tm_dy);
+    prefetch_tensormap(&tm_b);
+    for (int i = 0; i < kDyRing; ++i)
+      if (ch0 + i < ch1) issue(ch0 + i, i);
+  }
   const int64_t row0 = mb0 + warp * 16 + g;
   const bool ok0 = row0 < M, ok1 = row0 + 8 < M;
+  const uint32_t xr = (uint32_t)(warp * 16 + g);  // tile row of the lane's first row
   float acc[NT][4];
 #pragma unroll
   for (int jn = 0; jn < NT; ++jn) acc[jn][0] = acc[jn][1] = acc[jn][2] = acc[jn][3] = 0.0f;
@@ -370,24 +389,20 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
   };
   const int64_t sfo0 = sf_row(row0), sfo1 = sf_row(row0 + 8);
 
-#pragma unroll
-  for (int i = 0; i < kDyRing - 1; ++i) {
-    if (ch0 + i < ch1) load_chunk(ch0 + i, i);
-    cp_async_commit();
-  }
   for (int cc = ch0; cc < ch1; ++cc) {
     const int k = cc - ch0, slot = k % kDyRing;
-    cp_async_wait<kDyRing - 2>();  // this thread's copies of chunk cc have landed
-    __syncthreads();                 // everyone's have; chunk cc - 1 is done with
-    if (cc + kDyRing - 1 < ch1) load_chunk(cc + kDyRing - 1, (k + kDyRing - 1) % kDyRing);
-    cp_async_commit();
+    const bool landed =
+        mbar_wait(smem_addr(&full[slot]), (uint32_t)(k / kDyRing) & 1u, kDyWaitNs, nullptr);
+    if (!__all_sync(0xFFFFFFFFu, landed)) {  // the whole warp leaves together
+      if (lane == 0) atomicOr(status, PACT_DEV_TIMEOUT);
+      break;
+    }
+    const uint32_t sb = ring + slot * SLOT;
     uint4 xc[2][2];
-    const uint8_t* xs = dsm + XOFF + slot * kDyXSlot + (warp * 16 + g) * kDyXRow + 32 * c;
-    xc[0][0] = *reinterpret_cast<const uint4*>(xs);
-    xc[0][1] = *reinterpret_cast<const uint4*>(xs + 16);
-    xc[1][0] = *reinterpret_cast<const uint4*>(xs + 8 * kDyXRow);
-    xc[1][1] = *reinterpret_cast<const uint4*>(xs + 8 * kDyXRow + 16);
-    const uint8_t* bs = dsm + slot * SLOT + (g * kDyBRow + 32 * c);
+    xc[0][0] = ld_shared_v4(sb + swz128(xr, 2 * c));
+    xc[0][1] = ld_shared_v4(sb + swz128(xr, 2 * c + 1));
+    xc[1][0] = ld_shared_v4(sb + swz128(xr + 8, 2 * c));
+    xc[1][1] = ld_shared_v4(sb + swz128(xr + 8, 2 * c + 1));
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const uint4& lo0 = xc[0][s >> 1];
@@ -396,10 +411,23 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
                              (s & 1) ? lo0.w : lo0.y, (s & 1) ? lo1.w : lo1.y};
 #pragma unroll
       for (int jn = 0; jn < NT; ++jn) {
-        const uint2 bb = *reinterpret_cast<const uint2*>(bs + jn * 8 * kDyBRow + 8 * s);
+        const uint32_t brow = (uint32_t)(jn * 8 + g);
+        const uint2 bb =
+            ld_shared_v2(sb + BOFF + swz128(brow, 2 * c + (s >> 1)) + 8u * (uint32_t)(s & 1));
         const uint32_t bfr[2] = {bb.x, bb.y};
         mma_bf16_16816(acc[jn], a, bfr);
       }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty[slot]));  // the warp is done with the slot
+    // thread 0 refills the slot of the previous chunk once every warp released it
+    if (threadIdx.x == 0 && k >= 1 && cc - 1 + kDyRing < ch1) {
+      const int ps = (k - 1) % kDyRing;
+      if (mbar_wait(smem_addr(&empty[ps]), (uint32_t)((k - 1) / kDyRing) & 1u, kDyWaitNs,
+                    nullptr))
+        issue(cc - 1 + kDyRing, ps);
+      else
+        atomicOr(status, PACT_DEV_TIMEOUT);  // the consumers of that chunk time out too
     }
     if constexpr (QUANT) {
       // the lane's two blocks (rows row0 and row0 + 8), brackets from the table; the
@@ -434,9 +462,8 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const uint16_t* __restr
       }
     }
   }
-  cp_async_wait<0>();  // only empty groups can remain
-  __syncthreads();     // the ring is free: it now holds this CTA's partial sums
-  float* part = reinterpret_cast<float*>(dsm);  // [128 rows][RP]
+  __syncthreads();  // every chunk was consumed: the ring now holds this CTA's partial sums
+  float* part = reinterpret_cast<float*>(ring_ptr);  // [128 rows][RP]
 #pragma unroll
   for (int jn = 0; jn < NT; ++jn) {
     float* p0 = part + (warp * 16 + g) * RP + jn * 8 + 2 * c;
@@ -479,6 +506,15 @@ template <int RP, bool QUANT>
 static cudaError_t launch_down_dy(const uint16_t* dy, const float* gdy, const float* gw,
                                   int64_t M, int64_t N, const uint16_t* B, int r, float scale,
                                   int plain, uint16_t* u_out, DyQuant qz, cudaStream_t stream) {
+  CUtensorMap tm_dy, tm_b;
+  if (make_map(&tm_dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dy, (uint64_t)N, (uint64_t)M, 64, 128,
+               CU_TENSOR_MAP_SWIZZLE_128B) ||
+      make_map(&tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, (uint64_t)N, (uint64_t)r, 64,
+               (uint32_t)r, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  unsigned* status = nullptr;
+  cudaError_t e = status_word_ptr(&status);
+  if (e != cudaSuccess) return e;
   const int ns = dy_splits(N);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -493,9 +529,8 @@ static cudaError_t launch_down_dy(const uint16_t* dy, const float* gdy, const fl
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(k_lora_down_dy<RP, QUANT>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               dy_smem_bytes<RP>());
+    e = cudaFuncSetAttribute(k_lora_down_dy<RP, QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dy_smem_bytes<RP>());
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -503,8 +538,8 @@ static cudaError_t launch_down_dy(const uint16_t* dy, const float* gdy, const fl
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   note_launch();
-  return cudaLaunchKernelEx(&cfg, k_lora_down_dy<RP, QUANT>, dy, gdy, gw, M, N, B, r, scale,
-                            plain, u_out, qz);
+  return cudaLaunchKernelEx(&cfg, k_lora_down_dy<RP, QUANT>, tm_dy, tm_b, gdy, gw, M, N, r,
+                            scale, plain, u_out, qz, status);
 }
 
 template <int RP>

@@ -117,7 +117,9 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant_bf16(
   uint32_t k = 0;
   for (uint32_t t = first; t < ntiles; t += step, ++k) {
     const int slot = (int)(k % kQuantStages);
-    if (!mbar_wait(smem_addr(&full[warp][slot]), (k / kQuantStages) & 1u, kQuantWaitNs, nullptr)) {
+    const bool landed =
+        mbar_wait(smem_addr(&full[warp][slot]), (k / kQuantStages) & 1u, kQuantWaitNs, nullptr);
+    if (!__all_sync(0xFFFFFFFFu, landed)) {  // the whole warp leaves together
       // give the warp's other copy in flight a bounded chance to land before leaving
       if (lane == 0) {
         atomicOr(status, PACT_DEV_TIMEOUT);

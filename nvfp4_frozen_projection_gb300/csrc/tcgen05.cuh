@@ -23,6 +23,13 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return r;
 }
 
+// An 8-byte shared-memory load at a shared-window address (volatile, as above).
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 r;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr) : "memory");
+  return r;
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

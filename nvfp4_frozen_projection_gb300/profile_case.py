@@ -13,6 +13,7 @@ Cases (M = tokens; the other sizes are the Llama-3B layer's):
   gemm-o-fwd          the o projection's forward: the same GEMM plus the residual add
   dgrad-q-gate-up     the fused gate|up input gradient (dY quantised inside the LoRA
                       down-projection, then the GEMM): pact_lora_linear_dgrad_q
+  dgrad-q-q           the same for the q projection (3072 -> 3072, r = 16)
   adapter-grad-q      dA, dB of the q projection (3072 -> 3072, r = 16)
   adapter-grad-gate-up  dA, dB of the fused gate|up projection (3072 -> 2 x 8192, r = 32)
   rmsnorm             RMSNorm -> NVFP4 of a BF16 [M, 3072] tensor (statistic and encode)
@@ -61,10 +62,11 @@ def run(case: str, m: int, reps: int) -> None:
         dx = torch.empty(m, HIDDEN, dtype=torch.bfloat16, device=dev)
         for _ in range(reps):
             pact_lora_linear_dgrad(dyq, dy, wb, A, B, 2.0, dx=dx)
-    elif case == "dgrad-q-gate-up":
-        W, A, B = _lora(HIDDEN, 2 * INTER, 32, dev, gen)
+    elif case in ("dgrad-q-gate-up", "dgrad-q-q"):
+        n_out, r = (2 * INTER, 32) if case == "dgrad-q-gate-up" else (HIDDEN, 16)
+        W, A, B = _lora(HIDDEN, n_out, r, dev, gen)
         wb = pact_pack_weight_bwd(W)
-        dy = (torch.randn(m, 2 * INTER, device=dev, generator=gen) * 0.01).bfloat16()
+        dy = (torch.randn(m, n_out, device=dev, generator=gen) * 0.01).bfloat16()
         amax = dy.float().abs().max().reshape(1)
         dx = torch.empty(m, HIDDEN, dtype=torch.bfloat16, device=dev)
         dyq = None
