@@ -492,14 +492,16 @@ __global__ void __launch_bounds__(256, 2) k_lora_down_dy(const __grid_constant__
   cluster_sync();  // no CTA leaves while a peer may still read its partials
 }
 
-// CTAs per cluster for a dY of N columns: the largest power of two <= 8 that leaves
-// every CTA at least 12 of the 64-column chunks (a CTA's start-up and cluster
-// reduction are worth a few chunks), or 1.
+// CTAs per cluster for a dY of N columns: up to 4 while every CTA keeps at least 4
+// of the 64-column chunks, and 8 for rows of at least 192 chunks.  Measured on
+// GB300 with M = 8192: N = 1024 and 3072 run fastest at 4 (64 row blocks x 4 CTAs
+// fill the 152 SMs; 8 CTAs of 6 chunks lose more to each CTA's start-up and cluster
+// reduction than they gain), N = 16384 at 8.
 static int dy_splits(int64_t N) {
   const int64_t nch = N >> 6;
   int ns = 1;
-  while (ns < 8 && 2 * ns * 12 <= nch) ns *= 2;
-  return ns;
+  while (ns < 4 && 8 * ns <= nch) ns *= 2;
+  return nch >= 8 * 24 ? 8 : ns;
 }
 
 template <int RP, bool QUANT>
