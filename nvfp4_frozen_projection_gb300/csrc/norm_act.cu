@@ -425,14 +425,13 @@ __global__ void __launch_bounds__(256, 2) k_silu_encode(const uint16_t* __restri
                                                         const unsigned* __restrict__ amax3,
                                                         SiluOut out) {
   TensorScale ts[3];
-  __shared__ float2 brk[2][256];  // bracket tables of the gate and up scales
+  __shared__ float2 brk[3][256];  // bracket tables of the h, gate and up scales
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
     ts[k] = tensor_scale(amax3_opt ? amax3_opt[k] : __uint_as_float(amax3[k]));
     if (blockIdx.x == 0 && threadIdx.x == 0) *out.g[k] = ts[k].g;
+    brk[k][threadIdx.x] = bracket_entry(threadIdx.x, ts[k].g);  // blockDim.x == 256
   }
-  brk[0][threadIdx.x] = bracket_entry(threadIdx.x, ts[1].g);  // blockDim.x == 256
-  brk[1][threadIdx.x] = bracket_entry(threadIdx.x, ts[2].g);
   __syncthreads();
   const float lo_f = 1.0f - 2.0f * kSiluRel, hi_f = 1.0f + 2.0f * kSiluRel;
   const float rcp_d = ts[0].rcp_d;
@@ -466,87 +465,86 @@ __global__ void __launch_bounds__(256, 2) k_silu_encode(const uint16_t* __restri
       for (int k = 0; k < 3; ++k) out.sf[k][so] = 0;
       continue;
     }
-    uint32_t w[2] = {0u, 0u};
-    uint32_t sh = 0;
+    const uint32_t gb = absmax_bf16x16_bits(g0, g1), ub = absmax_bf16x16_bits(u0, u1);
+    // gate and up (their BF16 values are exact) and the fast h, from one unpack
+    uint32_t wg[2], wu[2], dg[2], du[2], wh[2], dh[2];
+    const uint32_t sg = scale_byte(__uint_as_float(gb), ts[1]);
+    const uint32_t su = scale_byte(__uint_as_float(ub), ts[2]);
+    float hf[16], am_blk;
     {
-      // ---- h
-      float gf[16], uf[16], hf[16];
+      float gf[16], uf[16];
       bf16x8_to_f32(g0, gf);
       bf16x8_to_f32(g1, gf + 8);
       bf16x8_to_f32(u0, uf);
       bf16x8_to_f32(u1, uf + 8);
-      const float am_blk = silu_block_fast(gf, uf, hf);
-      bool fast = silu_block_fast_ok(max(absmax_bf16x8_bits(g0), absmax_bf16x8_bits(g1)),
-                                     max(absmax_bf16x8_bits(u0), absmax_bf16x8_bits(u1)),
-                                     bf16x8_has_tiny(g0) || bf16x8_has_tiny(g1), am_blk) &&
-                  ts[0].g > 0.0f;
-      BlockStep st = {0.0f, 0.0f, 0.0f};
-      float fl = 0.0f, fh = 0.0f;
-      fast = fast && rcp_d > 0.0f;
-      if (fast) {
-        const float q = __fmul_rn(am_blk, rcp_d);
-        sh = e4m3_from_f32(__fmul_rn(q, lo_f));
-        fast = sh == e4m3_from_f32(__fmul_rn(q, hi_f));
-        st = scale_step(sh, ts[0]);
-        fl = __fmul_rn(st.rlo, lo_f);
-        fh = __fmul_rn(st.rhi, hi_f);
-        fast = fast && step_certifiable(st) && fh <= 3.4028234663852886e38f;
-      }
-      uint32_t redo = 0xFFFFu;
-      if (fast) {
-        redo = 0;
-#pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          // packed pairs: each lane rounds as the scalar multiply does
-          const float2 xl = __fmul2_rn(make_float2(hf[i], hf[i + 1]), make_float2(fl, fl));
-          const float2 xh = __fmul2_rn(make_float2(hf[i], hf[i + 1]), make_float2(fh, fh));
-          const uint32_t cl = e2m1x2_mag(xl.x, xl.y);
-          const uint32_t ch = e2m1x2_mag(xh.x, xh.y);
-          const uint32_t d = cl ^ ch;
-          redo |= ((d & 0x0Fu) ? 1u : 0u) << i;
-          redo |= ((d & 0xF0u) ? 1u : 0u) << (i + 1);
-          w[i >> 3] |= cl << (4 * (i & 7));
-        }
-      } else {
-        // the exact block maximum and scale; every code from its exact value below
-        uint32_t em = 0;
+      am_blk = silu_block_fast(gf, uf, hf);
+      codes16(gf, brk[1][sg], wg[0], wg[1], dg[0], dg[1]);
+      codes16(uf, brk[2][su], wu[0], wu[1], du[0], du[1]);
+    }
+    // ---- h: scale and codes from the fast values where both roundings are certain
+    bool fast = silu_block_fast_ok(gb, ub, bf16x8_has_tiny(g0) || bf16x8_has_tiny(g1), am_blk) &&
+                ts[0].g > 0.0f && rcp_d > 0.0f;
+    uint32_t sh = 0;
+    if (fast) {
+      const float q = __fmul_rn(am_blk, rcp_d);
+      uint16_t pr;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+          : "=h"(pr)
+          : "f"(__fmul_rn(q, hi_f)), "f"(__fmul_rn(q, lo_f)));
+      sh = pr & 0xFFu;
+      fast = sh == (uint32_t)(pr >> 8);
+    }
+    float2 br = brk[0][sh];
+    const float fl = __fmul_rn(br.x, lo_f), fh = __fmul_rn(br.y, hi_f);
+    fast = fast && br.x > 0.0f && fh <= 3.4028234663852886e38f;
+    float th;  // the decode step of h's block
+    if (fast) {
+      wh[0] = e2m1x8_of_products(hf, fl);
+      wh[1] = e2m1x8_of_products(hf + 8, fl);
+      dh[0] = wh[0] ^ e2m1x8_of_products(hf, fh);
+      dh[1] = wh[1] ^ e2m1x8_of_products(hf + 8, fh);
+      th = __fmul_rn(e4m3_to_f32(sh), ts[0].g);
+    } else {
+      // the exact block maximum and scale; every code from its exact value below
+      uint32_t em = 0;
 #pragma unroll 1
-        for (int i = 0; i < 16; ++i)
-          em = max(em, __float_as_uint(silu_exact_at(g0, g1, u0, u1, i)) & 0x7FFFFFFFu);
-        sh = block_scale_fast(__uint_as_float(em), ts[0], &st);
-      }
-      while (redo) {
-        const int i = __ffs(redo) - 1;
-        redo &= redo - 1;
-        const uint32_t c = e2m1_code_exact(silu_exact_at(g0, g1, u0, u1, i), st.t);
-        const int sh4 = 4 * (i & 7);
-        w[i >> 3] = (w[i >> 3] & ~(0xFu << sh4)) | (c << sh4);
-      }
+      for (int i = 0; i < 16; ++i)
+        em = max(em, __float_as_uint(silu_exact_at(g0, g1, u0, u1, i)) & 0x7FFFFFFFu);
+      BlockStep st;
+      sh = block_scale_fast(__uint_as_float(em), ts[0], &st);
+      th = st.t;
+      wh[0] = wh[1] = 0u;
+      dh[0] = dh[1] = 0xFFFFFFFFu;  // every element
     }
-    *reinterpret_cast<uint2*>(out.codes[0] + row * (I >> 1) + b * 8) = make_uint2(w[0], w[1]);
-    out.sf[0][so] = (uint8_t)sh;
-    // ---- gate and up: their BF16 values are exact
+    // the rare elements whose code the fast values leave open: exact h
+    if (dh[0] | dh[1]) {
 #pragma unroll
-    for (int k = 1; k < 3; ++k) {
-      const uint4& a0 = k == 1 ? g0 : u0;
-      const uint4& a1 = k == 1 ? g1 : u1;
-      const uint32_t s = scale_byte(__uint_as_float(absmax_bf16x16_bits(a0, a1)), ts[k]);
-      uint2 ck;
-      uint32_t d0, d1;
-      {
-        float v[16];
-        bf16x8_to_f32(a0, v);
-        bf16x8_to_f32(a1, v + 8);
-        codes16(v, brk[k - 1][s], ck.x, ck.y, d0, d1);
+      for (int q = 0; q < 2; ++q) {
+#pragma unroll 1
+        while (dh[q]) {
+          const uint32_t sh4 = ((uint32_t)__ffs(dh[q]) - 1u) & ~3u;
+          dh[q] &= ~(0xFu << sh4);
+          const uint32_t c =
+              e2m1_code_exact(silu_exact_at(g0, g1, u0, u1, 8 * q + (int)(sh4 >> 2)), th);
+          wh[q] = (wh[q] & ~(0xFu << sh4)) | (c << sh4);
+        }
       }
-      if (d0 | d1) {
-        const float t = __fmul_rn(e4m3_to_f32(s), ts[k].g);
-        ck.x = fix_word(ck.x, d0, t, [&](uint32_t i) { return bf16x8_at(a0, i); });
-        ck.y = fix_word(ck.y, d1, t, [&](uint32_t i) { return bf16x8_at(a1, i); });
-      }
-      *reinterpret_cast<uint2*>(out.codes[k] + row * (I >> 1) + b * 8) = ck;
-      out.sf[k][so] = (uint8_t)s;
     }
+    if (dg[0] | dg[1] | du[0] | du[1]) {
+      const float tg = __fmul_rn(e4m3_to_f32(sg), ts[1].g);
+      const float tu = __fmul_rn(e4m3_to_f32(su), ts[2].g);
+      wg[0] = fix_word(wg[0], dg[0], tg, [&](uint32_t i) { return bf16x8_at(g0, i); });
+      wg[1] = fix_word(wg[1], dg[1], tg, [&](uint32_t i) { return bf16x8_at(g1, i); });
+      wu[0] = fix_word(wu[0], du[0], tu, [&](uint32_t i) { return bf16x8_at(u0, i); });
+      wu[1] = fix_word(wu[1], du[1], tu, [&](uint32_t i) { return bf16x8_at(u1, i); });
+    }
+    const int64_t co = row * (I >> 1) + b * 8;
+    *reinterpret_cast<uint2*>(out.codes[0] + co) = make_uint2(wh[0], wh[1]);
+    *reinterpret_cast<uint2*>(out.codes[1] + co) = make_uint2(wg[0], wg[1]);
+    *reinterpret_cast<uint2*>(out.codes[2] + co) = make_uint2(wu[0], wu[1]);
+    out.sf[0][so] = (uint8_t)sh;
+    out.sf[1][so] = (uint8_t)sg;
+    out.sf[2][so] = (uint8_t)su;
   }
 }
 

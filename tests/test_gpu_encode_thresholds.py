@@ -14,7 +14,8 @@ import oracle as orc
 from exact_round import code_of_quotient
 from nvfp4_frozen_projection_gb300 import workloads as wl
 from nvfp4_frozen_projection_gb300 import (NVFP4, pact_check_status, pact_lora_linear_dgrad_q,
-                                           pact_pack_weight_bwd, pact_quant_nvfp4)
+                                           pact_pack_weight_bwd, pact_pack_weight_fwd,
+                                           pact_quant_nvfp4, pact_silu_mul_quant)
 
 from gpu_helpers import assert_nvfp4_equal, bf16, dev, f32, host
 
@@ -114,3 +115,43 @@ def test_fused_dy_quant_near_threshold_quotients():
         pact_check_status()
         assert_nvfp4_equal(dyq, orc.quantize(x, g=orc.global_scale(amax)),
                            f"fused dY quant, trial {trial}")
+
+
+def test_silu_gate_up_copies_near_threshold_quotients():
+    """SiLU-multiply -> NVFP4 encodes its gate and up copies with the same element
+    encode: threshold-straddling gate and up tensors (their amaxes passed in, h's
+    exact amax from the oracle) must give the oracle's bytes for h, gate and up."""
+    rng = np.random.default_rng(99)
+    for trial in range(12):
+        xg, ag = _case(rng, rows=64, cols=128)
+        xu, au = _case(rng, rows=64, cols=128)
+        gu = np.concatenate([xg, xu], axis=1)
+        h = orc.silu_mul_fp32(gu)
+        ah = np.float32(np.abs(h).max())
+        a3 = torch.tensor([float(ah), float(ag), float(au)], dtype=torch.float32, device=dev())
+        hq, gq, uq = pact_silu_mul_quant(bf16(gu), amax3=a3)
+        pact_check_status()
+        assert_nvfp4_equal(hq, orc.quantize(h, g=orc.global_scale(ah)), f"h, trial {trial}")
+        assert_nvfp4_equal(gq, orc.quantize(xg, g=orc.global_scale(ag)), f"gate, trial {trial}")
+        assert_nvfp4_equal(uq, orc.quantize(xu, g=orc.global_scale(au)), f"up, trial {trial}")
+
+
+def test_weight_pack_near_threshold_quotients():
+    """The frozen-weight packs encode with the same element rule: a weight whose 16x16
+    tiles each hold a scale-448 element and threshold-straddling values, and whose
+    amax (one element set to it) puts the per-tensor scale where the straddles are,
+    must give the oracle's bytes in both layouts."""
+    rng = np.random.default_rng(5)
+    for trial in range(8):
+        x, amax = _case(rng, rows=64, cols=128)
+        W = x.copy()
+        t = np.float32(448.0) * orc.global_scale(amax)
+        for r0 in range(0, 64, 16):          # one scale-448 element per 16x16 tile
+            for c0 in range(0, 128, 16):
+                W[r0 + 1, c0 + 1] = _bf16(5.85 * float(t))
+        W[0, 0] = amax                        # the tensor's amax, so g is the crafted one
+        assert orc.global_scale(orc.amax(W)) == orc.global_scale(amax)
+        rf, rb = orc.pack_weight(W)
+        assert_nvfp4_equal(pact_pack_weight_fwd(f32(W)), rf, f"pack fwd, trial {trial}")
+        assert_nvfp4_equal(pact_pack_weight_bwd(f32(W)), rb, f"pack bwd, trial {trial}")
+        pact_check_status()
