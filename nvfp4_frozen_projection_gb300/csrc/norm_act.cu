@@ -418,7 +418,7 @@ struct SiluOut {
   float* g[3];
 };
 
-__global__ void __launch_bounds__(256, 2) k_silu_encode(const uint16_t* __restrict__ gu,
+__global__ void __launch_bounds__(256, 3) k_silu_encode(const uint16_t* __restrict__ gu,
                                                         int64_t M, int64_t Mpad, int64_t I,
                                                         FastDiv bpr_div,
                                                         const float* __restrict__ amax3_opt,

@@ -5,6 +5,8 @@
 Cases (M = tokens; the other sizes are the Llama-3B layer's):
   gemm-gate-up-dgrad  dX = dY W (NVFP4, K = 2 x 8192) + LoRA term, out 3072 wide
   gemm-gate-up-fwd    Y = X W^T (NVFP4, 3072 -> 2 x 8192) + LoRA term
+  gemm-gate-up-stats  the same GEMM on the interleaved gate|up weight, its epilogue
+                      also forming the SiLU-multiply amaxes (pact_lora_linear_fwd_gate_up)
   quant               NVFP4 quantisation of a BF16 [M, 3072] tensor
   silu                SiLU-multiply -> NVFP4 of a BF16 [M, 2 x 8192] tensor
   silu-amax3          the same in one pass, with the three amaxes the gate|up forward
@@ -103,6 +105,14 @@ def run(case: str, m: int, reps: int) -> None:
         outs = pact_silu_mul_quant(gu)
         for _ in range(reps):
             pact_silu_mul_quant(gu, outs=outs)
+    elif case == "gemm-gate-up-stats":
+        W, A, B = _lora(HIDDEN, 2 * INTER, 32, dev, gen)
+        wg = pact_pack_weight_fwd_gate_up(W)
+        xq = pact_quant_nvfp4(torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16())
+        y = torch.empty(m, 2 * INTER, dtype=torch.bfloat16, device=dev)
+        a3 = torch.empty(3, dtype=torch.float32, device=dev)
+        for _ in range(reps):
+            pact_lora_linear_fwd_gate_up(xq, wg, A, B, 2.0, y=y, amax3=a3)
     elif case == "silu-amax3":
         W, A, B = _lora(HIDDEN, 2 * INTER, 32, dev, gen)
         x = torch.randn(m, HIDDEN, device=dev, generator=gen).bfloat16()
