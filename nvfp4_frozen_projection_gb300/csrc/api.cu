@@ -559,7 +559,11 @@ int pact_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M, int6
   if ((rc = check_nvfp4(yq, "yq", M, H, 16))) return rc;
   if (!ws || ws_bytes < 256 || !aligned(ws, 256))
     return fail(PACT_ERR_INVALID_ARG, "workspace missing, too small or not 256-byte aligned");
-  cudaError_t e = launch_rmsnorm_quant(x, gamma, M, H, eps, (uint8_t*)yq->codes, (uint8_t*)yq->sf,
+  CUtensorMap tmx;
+  if ((rc = make_map(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, M, 64, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B)))
+    return rc;
+  cudaError_t e = launch_rmsnorm_quant(tmx, x, gamma, M, H, eps, (uint8_t*)yq->codes, (uint8_t*)yq->sf,
                                        yq->g, rstd, (unsigned*)ws, d->status, d->sms,
                                        (cudaStream_t)stream);
   return e == cudaSuccess ? PACT_OK : cuda_fail(e, "rmsnorm launch");

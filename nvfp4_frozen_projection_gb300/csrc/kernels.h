@@ -143,7 +143,9 @@ cudaError_t launch_lora_adapter_grad(const uint8_t* x_codes, const uint8_t* x_sf
                                      uint16_t* bt_ws, uint16_t* t_ws, uint16_t* u_ws, float* part,
                                      int num_sms, cudaStream_t stream);
 
-cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M,
+// tmx: BF16 map over x [M, H], box 64 x 32, 128-byte swizzle.
+cudaError_t launch_rmsnorm_quant(const CUtensorMap& tmx, const uint16_t* x,
+                                 const uint16_t* gamma, int64_t M,
                                  int64_t H, float eps, uint8_t* codes, uint8_t* sf, float* g,
                                  float* rstd, unsigned* ws_amax, unsigned* status, int num_sms,
                                  cudaStream_t stream);

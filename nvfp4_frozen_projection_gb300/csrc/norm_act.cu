@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "encode_tiles.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -182,80 +183,46 @@ __global__ void __launch_bounds__(256) k_rmsnorm_stat(const uint16_t* __restrict
 }
 
 // Pass 2: y recomputed from x (read again, mostly from L2) and the stored rstd, then
-// encoded.  Streaming layout of the activation quantiser: lane = one block of 16
-// elements, warp = 32 consecutive blocks of the row-major [pad128(M), H/16] block
-// grid, the next block's loads in flight while the current one is encoded; gamma
-// and rstd come through L1.  Rows past M up to pad128(M) get zero scale bytes.
-__global__ void __launch_bounds__(256) k_rmsnorm_encode(
-    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
-    const float* __restrict__ rstd, int64_t M, int64_t Mpad, int64_t H, FastDiv bpr_div,
-    const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ sf, float* __restrict__ g_out) {
-  __shared__ float2 brk[256];
-  const TensorScale ts = tensor_scale(__uint_as_float(*amax_bits));
-  brk[threadIdx.x] = bracket_entry(threadIdx.x, ts.g);  // blockDim.x == 256
-  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
-  __syncthreads();
-  const uint32_t bpr = (uint32_t)(H >> 4);
-  const uint32_t total = (uint32_t)Mpad * bpr;  // < 2^31 (checked by the caller)
-  const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t stride = gridDim.x * blockDim.x;
-  uint32_t blk = blockIdx.x * blockDim.x + threadIdx.x;
-  uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
-  auto fetch = [&](uint32_t b) {
-    if (b < total) {
-      const uint32_t r = bpr_div.div(b);
-      if (r < M) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * H + (b - r * bpr) * 16);
-        n0 = __ldg(src);
-        n1 = __ldg(src + 1);
-      }
-    }
-  };
-  fetch(blk);
-  for (; blk - lane < total; blk += stride) {  // warp-uniform trip count
-    const uint4 v0 = n0, v1 = n1;
-    fetch(blk + stride);
-    const bool live = blk < total;
-    const uint32_t r = bpr_div.div(blk), cb = blk - r * bpr;
-    uint32_t sb = 0;
-    if (live && r < M) {
-      const float rs = __ldg(rstd + r);
-      const uint4* gp = reinterpret_cast<const uint4*>(gamma + cb * 16);
-      const uint4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
-      float f[16], gm[16];
-      bf16x8_to_f32(v0, f);
-      bf16x8_to_f32(v1, f + 8);
-      bf16x8_to_f32(g0, gm);
-      bf16x8_to_f32(g1, gm + 8);
-      float am = 0.0f;
+// encoded, through the shared tile encoder (encode_tiles.cuh): x arrives in 32-row x
+// 64-column TMA tiles, a lane takes four blocks of one row, gamma comes through L1
+// (every lane of a warp reads the same 64 values of a tile) and rstd once per tile.
+struct RmsNormValues {
+  const uint16_t* gamma;
+  const float* rstd;
+  float rs;
+  __device__ __forceinline__ void row(uint32_t r) { rs = __ldg(rstd + r); }
+  __device__ __forceinline__ uint32_t block(const uint4& a, const uint4& b, uint32_t col,
+                                            float* f) {
+    const uint4* gp = reinterpret_cast<const uint4*>(gamma + col);
+    float gm[16];
+    bf16x8_to_f32(a, f);
+    bf16x8_to_f32(b, f + 8);
+    bf16x8_to_f32(__ldg(gp), gm);
+    bf16x8_to_f32(__ldg(gp + 1), gm + 8);
+    float am = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        f[i] = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
-        am = fmaxf(am, fabsf(f[i]));
-      }
-      sb = scale_byte(am, ts);
-      uint2 cw;
-      uint32_t d0, d1;
-      codes16(f, brk[sb], cw.x, cw.y, d0, d1);
-      if (d0 | d1) {
-        const float t = __fmul_rn(e4m3_to_f32(sb), ts.g);
-        cw.x = fix_word(cw.x, d0, t, [&](uint32_t i) {
-          return __fmul_rn(__fmul_rn(bf16x8_at(v0, i), rs), bf16x8_at(g0, i));
-        });
-        cw.y = fix_word(cw.y, d1, t, [&](uint32_t i) {
-          return __fmul_rn(__fmul_rn(bf16x8_at(v1, i), rs), bf16x8_at(g1, i));
-        });
-      }
-      if (PACT_IN(r < (uint64_t)M && cb < bpr))
-        *reinterpret_cast<uint2*>(codes + (int64_t)r * (H >> 1) + cb * 8) = cw;
+    for (int i = 0; i < 16; ++i) {
+      f[i] = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
+      am = fmaxf(am, fabsf(f[i]));
     }
-    // scale bytes of blocks cb .. cb+3 (same row) into one word
-    uint32_t w = sb | (__shfl_down_sync(0xFFFFFFFFu, sb, 1) << 8);
-    w |= __shfl_down_sync(0xFFFFFFFFu, w, 2) << 16;
-    if (live && (cb & 3u) == 0u && PACT_IN(sf_offset(r, cb, bpr) + 4 <= Mpad * (int64_t)bpr))
-      *reinterpret_cast<uint32_t*>(sf + sf_offset(r, cb, bpr)) = w;
+    return __float_as_uint(am);
   }
+  __device__ __forceinline__ float elem(const uint4& a, uint32_t i, uint32_t col) {
+    const float gi = __uint_as_float((uint32_t)__ldg(gamma + col + i) << 16);
+    return __fmul_rn(__fmul_rn(bf16x8_at(a, i), rs), gi);
+  }
+};
+
+__global__ void __launch_bounds__(kTileThreads, 2) k_rmsnorm_encode(
+    const __grid_constant__ CUtensorMap tmx, const uint16_t* __restrict__ gamma,
+    const float* __restrict__ rstd, int64_t M, int64_t H, int64_t Mpad, FastDiv upr_div,
+    const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+    float* __restrict__ g_out, unsigned* __restrict__ status) {
+  extern __shared__ uint8_t esm[];
+  const TensorScale ts = tensor_scale(__uint_as_float(*amax_bits));
+  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
+  RmsNormValues op{gamma, rstd, 0.0f};
+  encode_tiles(&tmx, M, H, Mpad, upr_div, ts, codes, sf, status, esm, op);
 }
 
 // ============================================================== SiLU-multiply
@@ -717,7 +684,7 @@ static cudaError_t dispatch_bpl(int64_t H, F&& f) {
   }
 }
 
-cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M,
+cudaError_t launch_rmsnorm_quant(const CUtensorMap& tmx, const uint16_t* x, const uint16_t* gamma, int64_t M,
                                  int64_t H, float eps, uint8_t* codes, uint8_t* sf, float* g,
                                  float* rstd, unsigned* ws_amax, unsigned* status, int num_sms,
                                  cudaStream_t stream) {
@@ -737,9 +704,21 @@ cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {};  // per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(k_rmsnorm_encode, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tile_encode_smem_bytes());
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int64_t ntiles = (Mpad / 32) * (H / 64);
   note_launch();
-  k_rmsnorm_encode<<<blocks_for(Mpad * (H / 16), 256, num_sms * 8), 256, 0, stream>>>(
-      x, gamma, rstd, M, Mpad, H, FastDiv::make((uint32_t)(H / 16)), ws_amax, codes, sf, g);
+  k_rmsnorm_encode<<<blocks_for(ntiles, kTileWarps, num_sms * 2), kTileThreads,
+                     tile_encode_smem_bytes(), stream>>>(
+      tmx, gamma, rstd, M, H, Mpad, FastDiv::make((uint32_t)(H / 64)), ws_amax, codes, sf, g,
+      status);
   return cudaGetLastError();
 }
 

@@ -7,6 +7,7 @@
 // must be known before the first code is written, so pass 1 reduces amax into a
 // device word and pass 2 re-reads the tensor (mostly from L2) and encodes it.
 #include "common.cuh"
+#include "encode_tiles.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -60,120 +61,29 @@ __global__ void __launch_bounds__(256) k_amax_f32(const float* __restrict__ w, i
 }
 
 // ---------------------------------------------------------------- pass 2: encode
-// Tile = 32 rows x 64 columns (4 KB), lane = one row of it: a unit of four
-// consecutive blocks (128 bytes).  Each warp runs its own two-stage ring: its lane 0
-// fetches the warp's next tiles by TMA (128-byte swizzle, so that each lane's reads
-// of its own row are free of bank conflicts), and the warp encodes one tile while
-// the next is in flight.  Warps take tiles in turn over the tensor, tile t covering
-// row group t / (K/64) and column group t % (K/64), so the warps of the grid sweep
-// the tensor front to back.  A unit's four scale bytes are one 4-byte word of the
-// 128x4 atom layout (K/16 is a multiple of 4), stored whole; its 32 code bytes leave
-// as two 16-byte stores.  The brackets come from the CTA's table (bracket_entry);
-// elements where a bracket straddles a threshold (about one in 10^3) are fixed after
-// the unit's four blocks are encoded, from the values still held in registers.
-// Rows past M read as zeros (the tensor map's bounds) and store zero scale words up
-// to pad128(M), so the padded scale array is fully defined.
-constexpr int kQuantThreads = 256;
-constexpr int kQuantWarps = kQuantThreads / 32;
-constexpr int kQuantStages = 2;
-constexpr uint32_t kQuantTileBytes = 32 * 128;
-constexpr uint64_t kQuantWaitNs = 2000000000ull;
+// The BF16 values themselves, through the shared tile encoder (encode_tiles.cuh).
+struct QuantValues {
+  __device__ __forceinline__ void row(uint32_t) {}
+  __device__ __forceinline__ uint32_t block(const uint4& a, const uint4& b, uint32_t, float* f) {
+    bf16x8_to_f32(a, f);
+    bf16x8_to_f32(b, f + 8);
+    return absmax_bf16x16_bits(a, b);
+  }
+  __device__ __forceinline__ float elem(const uint4& a, uint32_t i, uint32_t) {
+    return bf16x8_at(a, i);
+  }
+};
 
-size_t quant_smem_bytes() { return 1024 + (size_t)kQuantWarps * kQuantStages * kQuantTileBytes; }
-
-__global__ void __launch_bounds__(kQuantThreads, 3) k_quant_bf16(
-    const __grid_constant__ CUtensorMap tmx, const uint16_t* __restrict__ x, int64_t M, int64_t K,
-    int64_t ldx, int64_t Mpad, FastDiv upr_div, const float* __restrict__ amax_opt,
-    const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-    float* __restrict__ g_out, unsigned* __restrict__ status) {
+__global__ void __launch_bounds__(kTileThreads, 2) k_quant_bf16(
+    const __grid_constant__ CUtensorMap tmx, int64_t M, int64_t K, int64_t Mpad, FastDiv upr_div,
+    const float* __restrict__ amax_opt, const unsigned* __restrict__ amax_bits,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ g_out,
+    unsigned* __restrict__ status) {
   extern __shared__ uint8_t qsm[];
-  __shared__ float2 brk[256];
-  __shared__ __align__(8) uint64_t full[kQuantWarps][kQuantStages];
-  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-  const float amax = amax_opt ? *amax_opt : __uint_as_float(*amax_bits);
-  const TensorScale ts = tensor_scale(amax);
-  brk[threadIdx.x] = bracket_entry(threadIdx.x, ts.g);  // blockDim.x == 256
+  const TensorScale ts = tensor_scale(amax_opt ? *amax_opt : __uint_as_float(*amax_bits));
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = ts.g;
-  if (lane == 0) {
-    for (int i = 0; i < kQuantStages; ++i) mbar_init(smem_addr(&full[warp][i]), 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  const uint32_t ring = ((smem_addr(qsm) + 1023u) & ~1023u) + warp * kQuantStages * kQuantTileBytes;
-  const uint32_t upr = (uint32_t)(K >> 6);  // column groups (units per row)
-  const uint32_t ntiles = (uint32_t)(Mpad >> 5) * upr;
-  const uint32_t first = blockIdx.x * kQuantWarps + warp, step = gridDim.x * kQuantWarps;
-  auto issue = [&](uint32_t t, int slot) {
-    const uint32_t rg = upr_div.div(t), cg = t - rg * upr;
-    const uint32_t bar = smem_addr(&full[warp][slot]);
-    mbar_expect_tx(bar, kQuantTileBytes);
-    tma_load_2d(ring + slot * kQuantTileBytes, &tmx, (int32_t)(cg * 64u), (int32_t)(rg * 32u), bar);
-  };
-  if (lane == 0) {
-    prefetch_tensormap(&tmx);
-    for (int i = 0; i < kQuantStages; ++i)
-      if (first + i * step < ntiles) issue(first + i * step, i);
-  }
-  uint32_t k = 0;
-  for (uint32_t t = first; t < ntiles; t += step, ++k) {
-    const int slot = (int)(k % kQuantStages);
-    const bool landed =
-        mbar_wait(smem_addr(&full[warp][slot]), (k / kQuantStages) & 1u, kQuantWaitNs, nullptr);
-    if (!__all_sync(0xFFFFFFFFu, landed)) {  // the whole warp leaves together
-      // give the warp's other copy in flight a bounded chance to land before leaving
-      if (lane == 0) {
-        atomicOr(status, PACT_DEV_TIMEOUT);
-        const uint32_t k2 = k + 1;
-        if (t + step < ntiles)
-          mbar_wait(smem_addr(&full[warp][k2 % kQuantStages]), (k2 / kQuantStages) & 1u,
-                    kQuantWaitNs, nullptr);
-      }
-      __syncwarp();
-      break;
-    }
-    const uint32_t row_smem = ring + slot * kQuantTileBytes + lane * 128u;
-    uint4 v[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) v[c] = ld_shared_v4(row_smem + ((c ^ (lane & 7u)) << 4));
-    __syncwarp();  // every lane's reads of the slot are done
-    if (lane == 0 && t + kQuantStages * step < ntiles) {
-      fence_proxy_async_smem();
-      issue(t + kQuantStages * step, slot);
-    }
-    const uint32_t rg = upr_div.div(t), cg = t - rg * upr;
-    const uint32_t r = rg * 32u + lane;
-    const uint32_t so = sf_word_offset(r, cg, upr);
-    if (r >= (uint32_t)M) {
-      if (PACT_IN(so + 4u <= (uint32_t)Mpad * upr * 4u)) *reinterpret_cast<uint32_t*>(sf + so) = 0u;
-      continue;
-    }
-    uint32_t w[8], d[8], sw = 0u, any = 0u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t sb =
-          scale_byte(__uint_as_float(absmax_bf16x16_bits(v[2 * j], v[2 * j + 1])), ts);
-      sw |= sb << (8 * j);
-      float f[16];
-      bf16x8_to_f32(v[2 * j], f);
-      bf16x8_to_f32(v[2 * j + 1], f + 8);
-      codes16(f, brk[sb], w[2 * j], w[2 * j + 1], d[2 * j], d[2 * j + 1]);
-      any |= d[2 * j] | d[2 * j + 1];
-    }
-    if (any) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (d[q]) {
-          const float tq = __fmul_rn(e4m3_to_f32((sw >> (8 * (q >> 1))) & 0xFFu), ts.g);
-          w[q] = fix_word(w[q], d[q], tq, [&](uint32_t i) { return bf16x8_at(v[q], i); });
-        }
-    }
-    uint4* dst = reinterpret_cast<uint4*>(codes + (int64_t)r * (K >> 1) + cg * 32u);
-    if (PACT_IN(cg < upr)) {
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-    if (PACT_IN(so + 4u <= (uint32_t)Mpad * upr * 4u)) *reinterpret_cast<uint32_t*>(sf + so) = sw;
-  }
+  QuantValues op;
+  encode_tiles(&tmx, M, K, Mpad, upr_div, ts, codes, sf, status, qsm, op);
 }
 
 // ---------------------------------------------------------------- weight pack
@@ -268,16 +178,17 @@ cudaError_t launch_quant_bf16(const CUtensorMap& tmx, const uint16_t* x, int64_t
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(
-        k_quant_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)quant_smem_bytes());
+        k_quant_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_encode_smem_bytes());
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int64_t Mpad = pad_to(M, 128);
   const int64_t ntiles = (Mpad / 32) * (K / 64);
   note_launch();
-  k_quant_bf16<<<grid_for(ntiles, kQuantWarps, num_sms * 3), kQuantThreads, quant_smem_bytes(),
-                 stream>>>(tmx, x, M, K, ldx, Mpad, FastDiv::make((uint32_t)(K / 64)), amax_opt,
-                           ws_amax, codes, sf, g, status);
+  k_quant_bf16<<<grid_for(ntiles, kTileWarps, num_sms * 2), kTileThreads,
+                 tile_encode_smem_bytes(), stream>>>(tmx, M, K, Mpad,
+                                                     FastDiv::make((uint32_t)(K / 64)), amax_opt,
+                                                     ws_amax, codes, sf, g, status);
   return cudaGetLastError();
 }
 
