@@ -45,17 +45,21 @@ __device__ __forceinline__ void ring_issue(const RowRing& rr, int k, const void*
 }
 
 // Dynamic shared memory of a row-ring kernel: [gamma (padded to 128)] [warps x ns
-// slots] [warps x ns barriers].  Warps per CTA and ring depth are chosen so the
-// whole fits in 200 KB.
+// slots] [warps x ns barriers].  Three CTAs share an SM when at least four warps
+// with two slots each fit in 66 KB: the statistic's per-lane sums are serial
+// chains, so more warps beat deeper rings (on GB300 at H = 3072, 3 CTAs of 4 warps
+// with 2 slots ran 10-15 % faster than 1 CTA of 8 warps with 4 slots).  Wider rows
+// take one CTA per SM within 200 KB.
 struct RingShape {
-  int warps, ns;
+  int warps, ns, ctas_per_sm;
   size_t smem;
 };
 static RingShape ring_shape(int64_t H, int copies_per_row, bool with_gamma) {
   const size_t row = (size_t)H * 2 * copies_per_row;
   const size_t fixed = with_gamma ? (size_t)((H * 2 + 127) / 128 * 128) : 0;
-  const size_t avail = 200 * 1024 - fixed;
   RingShape r;
+  r.ctas_per_sm = fixed + 8 * row <= 66 * 1024 ? 3 : 1;
+  const size_t avail = (r.ctas_per_sm == 3 ? 66 : 200) * 1024 - fixed;
   r.warps = (int)std::min<size_t>(8, std::max<size_t>(1, avail / (2 * row)));
   r.ns = (int)std::min<size_t>(4, std::max<size_t>(2, avail / (r.warps * row)));
   r.smem = fixed + (size_t)r.warps * r.ns * row + (size_t)r.warps * r.ns * 8 + 128;
@@ -699,7 +703,7 @@ cudaError_t launch_rmsnorm_quant(const CUtensorMap& tmx, const uint16_t* x, cons
                                            (int)rs.smem);
     if (err != cudaSuccess) return err;
     note_launch();
-    ks<<<blocks_for(M, rs.warps, num_sms), 32 * rs.warps, rs.smem, stream>>>(
+    ks<<<blocks_for(M, rs.warps, num_sms * rs.ctas_per_sm), 32 * rs.warps, rs.smem, stream>>>(
         x, gamma, M, H, eps, rs.ns, rstd, ws_amax, status);
     return cudaGetLastError();
   });
