@@ -613,6 +613,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
   const int nb = (int)(H >> 4);
   const float g = *yg;
   uint32_t amax = 0;  // max |dx| over this thread's outputs, as FP32 bits of the BF16 values
+  uint32_t am2 = 0;   // the same, packed (max.xorsign.abs on BF16 pairs, signs masked at the end)
   for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < M;
        row += (int64_t)gridDim.x * 8) {
     uint2 cw[BPL];
@@ -672,7 +673,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
             if (dres) v[k] += r[i + k];
           }
           o[i / 2] = pack_bf16x2(v[0], v[1]);
-          amax = max(amax, max((o[i / 2] & 0x7FFFu) << 16, (o[i / 2] >> 16 & 0x7FFFu) << 16));
+          asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(am2) : "r"(am2), "r"(o[i / 2]));
         }
         uint4* op = reinterpret_cast<uint4*>(dx + row * H + b * 16);
         if (!PACT_IN(row < M && b < nb)) continue;
@@ -681,6 +682,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
       }
     }
   }
+  am2 &= 0x7FFF7FFFu;
+  amax = max(amax, max(am2 << 16, am2 & 0xFFFF0000u));
   if (out_amax) block_max_atomic(amax, out_amax);
 }
 
