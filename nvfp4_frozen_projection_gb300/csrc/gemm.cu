@@ -669,7 +669,8 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t stg = base + C::STG_OFF + (uint32_t)(ew * C::NSTG * C::STG_BUF);
     const float ga = *p.ga, gb = *p.gb;
     const float s_main = (ga > 0.0f && gb > 0.0f) ? __fmul_rn(ga, gb) : 1.0f;
-    uint32_t amax = 0;
+    uint32_t amax = 0;  // packed BF16 pairs while the tiles are drained, FP32 bits after
+    const bool want_amax = p.out_amax != nullptr;
     uint32_t aphase = 0;
     uint32_t nstore = 0;
     float gu_xh = 0.0f, gu_xw = 0.0f;  // gate|up statistics (amax3): lane's and warp's
@@ -749,10 +750,10 @@ __global__ void __launch_bounds__(448, 1)
       for (int ch = 0; ch < NCH; ++ch) {
         const int n = n0 + c0 + 32 * ch;
         if (n >= p.N || !blk_live) continue;  // uniform across the warp (N % 32 == 0)
-        if (row_ok) {
+        if (want_amax && row_ok) {  // packed max |.| of BF16 pairs (signs masked at the end)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            amax = max(amax, max((out[ch][i] & 0x7FFFu) << 16, (out[ch][i] >> 16 & 0x7FFFu) << 16));
+            asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(amax) : "r"(amax), "r"(out[ch][i]));
         }
         // staging buffer nstore % NSTG: wait until its previous store has read it
         const uint32_t buf = stg + (nstore % C::NSTG) * C::STG_BUF;
@@ -780,8 +781,9 @@ __global__ void __launch_bounds__(448, 1)
       aphase ^= 1u;
     }
     if (lane == 0) bulk_wait_all();
-    if (p.out_amax) {
-      amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+    if (want_amax) {
+      amax &= 0x7FFF7FFFu;
+      amax = __reduce_max_sync(0xFFFFFFFFu, max(amax << 16, amax & 0xFFFF0000u));
       if (lane == 0 && amax) atomicMax(p.out_amax, amax);
     }
     if constexpr (GU) {  // order: h, gate, up
