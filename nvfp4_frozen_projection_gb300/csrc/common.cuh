@@ -440,12 +440,22 @@ __device__ __forceinline__ float bf16x8_at(const uint4& v, uint32_t i) {
   return __uint_as_float((i & 1u) ? (w & 0xFFFF0000u) : (w << 16));
 }
 
-// max |x| over 16 BF16 values (two 16-byte vectors) as FP32 bits.
+// max(|a|, |b|) of two BF16 pairs, lane by lane; the sign bits are garbage (the xor of
+// the inputs') and masked by the caller.  Finite inputs: a NaN would lose.
+__device__ __forceinline__ uint32_t maxabs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// max |x| over 16 BF16 values (two 16-byte vectors) as FP32 bits: seven packed
+// max-abs operations, then the larger of the two halves.
 __device__ __forceinline__ uint32_t absmax_bf16x16_bits(const uint4& a, const uint4& b) {
-  const uint32_t k = 0x7FFF7FFFu;
-  const uint32_t m = __vmaxu2(__vmaxu2(__vmaxu2(a.x & k, a.y & k), __vmaxu2(a.z & k, a.w & k)),
-                              __vmaxu2(__vmaxu2(b.x & k, b.y & k), __vmaxu2(b.z & k, b.w & k)));
-  return max(m >> 16, m & 0xFFFFu) << 16;
+  const uint32_t m =
+      maxabs_bf16x2(maxabs_bf16x2(maxabs_bf16x2(a.x, a.y), maxabs_bf16x2(a.z, a.w)),
+                    maxabs_bf16x2(maxabs_bf16x2(b.x, b.y), maxabs_bf16x2(b.z, b.w))) &
+      0x7FFF7FFFu;
+  return max(m << 16, m & 0xFFFF0000u);
 }
 
 // Offset of the scale word of blocks 4 cg .. 4 cg + 3 of row r (the 128x4 atom layout
