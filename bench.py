@@ -5,7 +5,7 @@ One step = one forward + input-gradient pass of the Llama-3B-shaped decoder-laye
 projection stack (workload "layer-3b": M = 8 x 1024 tokens, hidden 3072,
 q/k/v/o 3072 -> 3072/1024/1024/3072, gate|up 3072 -> 2 x 8192, down 8192 -> 3072,
 r = 16 LoRA on every projection): both fused RMSNorm -> NVFP4 quantisers, every
-activation/gradient quantisation, the fused SiLU-multiply -> NVFP4, the 14 NVFP4
+activation/gradient quantisation, the fused SiLU-multiply -> NVFP4, the 12 NVFP4
 GEMMs with fused LoRA branches, and the RMSNorm and SiLU-multiply backward
 kernels.  The attention core and its backward are replaced by seeded tensors.
 
@@ -25,6 +25,7 @@ exchange step, so the ranks are independent replicas (weak scaling).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -55,6 +56,21 @@ GEMM_SHAPES = {"q.fwd": (3072, 3072), "k.fwd": (1024, 3072), "v.fwd": (1024, 307
                "o.dgrad": (3072, 3072), "q.dgrad": (3072, 3072), "k.dgrad": (3072, 1024),
                "v.dgrad": (3072, 1024)}
 PROJS = ("q", "k", "v", "o", "gate_up", "down")
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# gate|up forward GEMM with the SiLU statistics at 8192 tokens, from a one-pass ncu
+# capture of that launch (profile_case gemm-gate-up-stats --m 8192), and the SHA-256
+# of the sources and build script that kernel was compiled from when it was taken.
+# The roofline reports it only while those files are unchanged, else null.
+GU_FWD_TRAFFIC = {
+    "bytes": 45258240 + 217333760,
+    "tokens": 8192,
+    "sources": ("nvfp4_frozen_projection_gb300/csrc/gemm.cu",
+                "nvfp4_frozen_projection_gb300/csrc/tcgen05.cuh",
+                "nvfp4_frozen_projection_gb300/csrc/common.cuh",
+                "nvfp4_frozen_projection_gb300/csrc/kernels.h",
+                "nvfp4_frozen_projection_gb300/build.py"),
+    "sha256": "39907dbafefbeb382edd3c61018a60e49f235c9d5edd672a685802a52031ede9",
+}
 INPUTS = ("x", "attn", "dy", "dq", "dk", "dv")
 
 
@@ -501,6 +517,24 @@ def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
     return units_per_rank * world / (ms * 1e-3)
 
 
+def sources_sha256(paths) -> str:
+    """SHA-256 over the given repository files, in order."""
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def dominant_traffic(dominant: str, tokens: int):
+    """Per-launch DRAM bytes of the dominant GEMM from the stored capture, or None
+    when the capture does not cover this kernel, size or build."""
+    t = GU_FWD_TRAFFIC
+    if dominant != "gate_up.fwd" or tokens != t["tokens"]:
+        return None
+    return t["bytes"] if sources_sha256(t["sources"]) == t["sha256"] else None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -751,7 +785,7 @@ def main():
         "roofline": {"bound": "tensor", "kernel": f"k_gemm_nvfp4 ({dominant})",
                      "achieved": dk_["tflops"], "peak": fp4_peak, "unit": "TFLOP/s",
                      "frac": dk_["tflops"] / fp4_peak,
-                     "traffic": None,
+                     "traffic": dominant_traffic(dominant, m),
                      "peak_source": f"{src} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
         "gemm_kernels": {k: {"ms": round(v["ms"], 5), "tflops": round(v["tflops"], 1)}
                          for k, v in kern.items()},

@@ -222,5 +222,6 @@ class DecoderProjectionStack:
                    t32(d["gamma2"]).bfloat16(), float(d["eps"]))
 
     def gemm_flops(self) -> float:
-        """2*M*N*K over the 14 frozen-projection GEMMs of one forward + dgrad pass."""
+        """2*M*N*K over the 12 frozen-projection GEMMs of one forward + dgrad pass (six
+        projections, q, k, v, o, gate|up and down, each forward and input gradient)."""
         return 2.0 * sum(l.gemm_flops(self.m) for l in self.p.values())
