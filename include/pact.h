@@ -26,9 +26,12 @@
  *   - Errors raised inside a kernel (a bounded wait that ran out) are recorded in
  *     a device status word that pact_check_status() reads.
  *   - Outputs must not alias inputs unless a call says so.
- *   - Floating-point inputs are finite.  A NaN or an infinity in an input gives
- *     unspecified output values (codes, scales and per-tensor scales included), but
- *     every call still stays within its buffers and ends; no value steers an
+ *   - Floating-point inputs are finite.  The debug build (libpact_debug.so) rejects
+ *     a NaN: the kernels that quantise, normalise or take an output amax record it
+ *     in the status word, and pact_check_status returns PACT_ERR_DEVICE_STATUS.
+ *     The release build does not look; a NaN or an infinity there gives
+ *     unspecified output values (codes, scales and per-tensor scales included),
+ *     but every call still stays within its buffers and ends: no value steers an
  *     address or a loop bound.
  */
 #ifndef PACT_H

@@ -146,7 +146,7 @@ extern "C" {
 const char* pact_last_error(void) { return g_err; }
 
 #ifdef PACT_DEBUG
-const char* pact_version(void) { return "libpact 0.2 (sm_103a, debug: bounds-checked stores)"; }
+const char* pact_version(void) { return "libpact 0.2 (sm_103a, debug: bounds-checked stores, NaN checks)"; }
 #else
 const char* pact_version(void) { return "libpact 0.2 (sm_103a)"; }
 #endif
@@ -189,6 +189,9 @@ int pact_check_status(pact_stream_t stream) {
     if (v & PACT_DEV_BOUNDS)
       return fail(PACT_ERR_DEVICE_STATUS, "a bounds check of the debug build failed (status 0x%x)",
                   v);
+    if (v & PACT_DEV_NAN)
+      return fail(PACT_ERR_DEVICE_STATUS,
+                  "the debug build found a NaN among the input values (status 0x%x)", v);
     return fail(PACT_ERR_DEVICE_STATUS, "device status 0x%x", v);
   }
   return PACT_OK;

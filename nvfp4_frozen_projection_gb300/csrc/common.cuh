@@ -12,6 +12,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "status.h"
+
 #if defined(__CUDA_ARCH__) && !defined(__CUDA_ARCH_FEAT_SM103_ALL)
 #error "libpact kernels are written for sm_103a only"
 #endif
@@ -451,6 +453,8 @@ __device__ __forceinline__ uint32_t maxabs_bf16x2(uint32_t a, uint32_t b) {
 // max |x| over 16 BF16 values (two 16-byte vectors) as FP32 bits: seven packed
 // max-abs operations, then the larger of the two halves.
 __device__ __forceinline__ uint32_t absmax_bf16x16_bits(const uint4& a, const uint4& b) {
+  PACT_NAN_BF16X2(a.x), PACT_NAN_BF16X2(a.y), PACT_NAN_BF16X2(a.z), PACT_NAN_BF16X2(a.w);
+  PACT_NAN_BF16X2(b.x), PACT_NAN_BF16X2(b.y), PACT_NAN_BF16X2(b.z), PACT_NAN_BF16X2(b.w);
   const uint32_t m =
       maxabs_bf16x2(maxabs_bf16x2(maxabs_bf16x2(a.x, a.y), maxabs_bf16x2(a.z, a.w)),
                     maxabs_bf16x2(maxabs_bf16x2(b.x, b.y), maxabs_bf16x2(b.z, b.w))) &
@@ -504,6 +508,7 @@ __device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, __half2 
 
 // max |bf16| over 8 packed values, as FP32 bits (non-negative, so unsigned order).
 __device__ __forceinline__ uint32_t absmax_bf16x8_bits(const uint4& v) {
+  PACT_NAN_BF16X2(v.x), PACT_NAN_BF16X2(v.y), PACT_NAN_BF16X2(v.z), PACT_NAN_BF16X2(v.w);
   uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
                         __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
   uint32_t hi = m >> 16, lo = m & 0xFFFFu;

@@ -750,6 +750,10 @@ __global__ void __launch_bounds__(448, 1)
       for (int ch = 0; ch < NCH; ++ch) {
         const int n = n0 + c0 + 32 * ch;
         if (n >= p.N || !blk_live) continue;  // uniform across the warp (N % 32 == 0)
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) PACT_NAN_BF16X2(out[ch][i]);
+        }
         if (want_amax && row_ok) {  // packed max |.| of BF16 pairs (signs masked at the end)
 #pragma unroll
           for (int i = 0; i < 16; ++i)

@@ -5,36 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "status.h"
+
 namespace pact {
-
-// Device status word bits (read and cleared by pact_check_status).
-enum : unsigned {
-  PACT_DEV_TIMEOUT = 1u,
-  PACT_DEV_BOUNDS = 1u << 1,  // a bounds check of the debug build failed
-  PACT_DEV_ROLE_TMA = 1u << 8,
-  PACT_DEV_ROLE_MMA = 1u << 9,
-  PACT_DEV_ROLE_EPI = 1u << 10,
-  PACT_DEV_ROLE_SF = 1u << 11,
-};
-
-// Debug builds (PACT_DEBUG; the whole library as the one translation unit
-// debug_all.cu) check the index arithmetic of the kernels' hand-computed stores
-// against the buffer extents: a check that fails records PACT_DEV_BOUNDS in the
-// status word and the store is skipped, so an out-of-bounds index shows up in
-// pact_check_status instead of corrupting memory.  Release builds compile the
-// checks away.
-#ifdef PACT_DEBUG
-// the status word itself (the debug build is a single unit; release builds define
-// it in gemm.cu)
-__device__ unsigned g_pact_status;
-__device__ __forceinline__ bool in_bounds(bool ok) {
-  if (!ok) atomicOr(&g_pact_status, PACT_DEV_BOUNDS);
-  return ok;
-}
-#define PACT_IN(cond) ::pact::in_bounds(cond)
-#else
-#define PACT_IN(cond) true
-#endif
 
 // Counts one kernel launch (pact_launch_count); called before every <<<>>>.
 void note_launch();

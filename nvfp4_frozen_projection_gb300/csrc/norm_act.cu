@@ -163,8 +163,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm_stat(const uint16_t* __restrict
         bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + 32 * b), gm);
         bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + 32 * b + 16), gm + 8);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          amax = max(amax, __float_as_uint(__fmul_rn(__fmul_rn(f[i], rs), gm[i])) & 0x7FFFFFFFu);
+        for (int i = 0; i < 16; ++i) {
+          const float y = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
+          PACT_NAN_F32(y);
+          amax = max(amax, __float_as_uint(y) & 0x7FFFFFFFu);
+        }
       }
     }
     __syncwarp();
@@ -585,6 +588,8 @@ __global__ void __launch_bounds__(256) k_silu_bwd(
       asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(am2) : "r"(am2), "r"(t));
     }
     if (!PACT_IN(row < M && b < bpr)) continue;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) PACT_NAN_BF16X2(og[i]), PACT_NAN_BF16X2(ou[i]);
     uint4* pg = reinterpret_cast<uint4*>(dgu + row * 2 * I + b * 16);
     uint4* pu = reinterpret_cast<uint4*>(dgu + row * 2 * I + I + b * 16);
     pg[0] = make_uint4(og[0], og[1], og[2], og[3]);
@@ -677,6 +682,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(
         }
         uint4* op = reinterpret_cast<uint4*>(dx + row * H + b * 16);
         if (!PACT_IN(row < M && b < nb)) continue;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) PACT_NAN_BF16X2(o[i]);
         op[0] = make_uint4(o[0], o[1], o[2], o[3]);
         op[1] = make_uint4(o[4], o[5], o[6], o[7]);
       }

@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(256) k_amax_f32(const float* __restrict__ w, i
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nv;
        v += (int64_t)gridDim.x * blockDim.x) {
     uint4 a = ldg_stream(p + v);
+    PACT_NAN_F32(__uint_as_float(a.x)), PACT_NAN_F32(__uint_as_float(a.y));
+    PACT_NAN_F32(__uint_as_float(a.z)), PACT_NAN_F32(__uint_as_float(a.w));
     m = max(m, max(max(a.x & 0x7FFFFFFFu, a.y & 0x7FFFFFFFu),
                    max(a.z & 0x7FFFFFFFu, a.w & 0x7FFFFFFFu)));
   }
