@@ -62,14 +62,14 @@ PROJS = ("q", "k", "v", "o", "gate_up", "down")
 # of the sources and build script that kernel was compiled from when it was taken.
 # The roofline reports it only while those files are unchanged, else null.
 GU_FWD_TRAFFIC = {
-    "bytes": 45384704 + 217257216,
+    "bytes": 45270528 + 217363968,
     "tokens": 8192,
     "sources": ("nvfp4_frozen_projection_gb300/csrc/gemm.cu",
                 "nvfp4_frozen_projection_gb300/csrc/tcgen05.cuh",
                 "nvfp4_frozen_projection_gb300/csrc/common.cuh",
                 "nvfp4_frozen_projection_gb300/csrc/kernels.h",
                 "nvfp4_frozen_projection_gb300/build.py"),
-    "sha256": "b1e89ff517765334599c2cd2a6788ad06ffa44c7d477254db1171af99c21a5ea",
+    "sha256": "b0eba341ef1ab925e59f704fd668f431de0ef14d6080b8111c11ceddf71483ac",
 }
 INPUTS = ("x", "attn", "dy", "dq", "dk", "dv")
 
