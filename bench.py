@@ -191,7 +191,9 @@ def run_reference(args):
     value = flops / dt / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
-        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        # the launch's GPU count (the oracle itself runs on the host cores, rank 0 only)
+        "n_gpus": int(os.environ.get("WORLD_SIZE", str(args.gpus))), "steps": args.steps,
+        "warmup": args.warmup, "device": "host cores",
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "layer-3b", "tokens_per_step": rows, "hidden": 3072,
