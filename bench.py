@@ -196,11 +196,12 @@ def run_reference(args):
         "warmup": args.warmup, "device": "host cores",
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "layer-3b", "tokens_per_step": rows, "hidden": 3072,
-                   "intermediate": 8192, "r": 16},
+        "config": step_config(int(os.environ.get("WORLD_SIZE", str(args.gpus)))),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
                          "kind": "oracle",
-                         "sample": f"each step: first {rows} tokens of the layer-3b step"},
+                         "sample": f"each step: the first {rows} tokens of the layer-3b step "
+                                   "(fwd+dgrad chain, FP64 GEMMs on exactly dequantised "
+                                   "operands); TFLOP/s of that sample"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -519,6 +520,18 @@ def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
     return units_per_rank * world / (ms * 1e-3)
 
 
+def step_config(world: int) -> dict:
+    """The workload's configuration, the same on both arms: the layer-3b step at 8192
+    tokens, whatever sample of it an arm times."""
+    return {"workload": "layer-3b", "tokens_per_step": 8192, "hidden": 3072,
+            "intermediate": 8192, "q_kv_o": [3072, 1024, 1024, 3072], "r": 16,
+            "gemms_per_step": 12, "fused": "gate|up runs as one GEMM",
+            "gemm_flops_per_step": wl.gemm_flops_per_step(5, m=8192),
+            "l2": "no flush between timed steps: one step moves several GB through HBM "
+                  "(L2 is 129 MB); ms_per_step_l2_flushed flushes before every step",
+            "parallelism": f"replicas x{world}"}
+
+
 def sources_sha256(paths) -> str:
     """SHA-256 over the given repository files, in order."""
     h = hashlib.sha256()
@@ -727,6 +740,9 @@ def main():
     dominant = max(step_share, key=step_share.get)
     dk_ = kern[dominant]
     m, hid = stack.m, stack.hidden
+    cfg = step_config(world)
+    assert cfg["tokens_per_step"] == m and cfg["gemm_flops_per_step"] == flops, \
+        "the stack and the reported configuration disagree"
     # memory-bound calls alone: algorithmic bytes (inputs read once, outputs written
     # once) over the median call time, warm and with L2 flushed before each call
     mem_calls = {
@@ -769,13 +785,8 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4", "data": "synthetic",
-        "config": {"workload": "layer-3b", "tokens_per_step": m, "hidden": hid,
-                   "intermediate": stack.inter, "q_kv_o": [3072, 1024, 1024, 3072], "r": 16,
-                   "gemms_per_step": 12, "fused": "gate|up runs as one GEMM",
-                   "gemm_flops_per_step": flops,
-                   "l2": "no flush between timed steps: one step moves several GB through HBM "
-                         "(L2 is 129 MB); ms_per_step_l2_flushed flushes before every step",
-                   "graph": graph is not None, "parallelism": f"replicas x{world}"},
+        "config": cfg,
+        "graph": graph is not None,
         "ms_per_step_median": ms_median,
         "ms_per_step_l2_flushed": ms_flushed,
         "clocks": clocks,

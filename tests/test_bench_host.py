@@ -44,3 +44,14 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
 
     monkeypatch.setattr(bench.wl, "layer3b", boom)
     assert bench.run_reference(Args()) == 0
+
+
+def test_both_arms_report_one_configuration():
+    # the GPU arm asserts its stack matches this dictionary; it must describe the
+    # layer-3b workload the stack is built from
+    cfg = bench.step_config(1)
+    d = bench.wl.layer3b()
+    m = d["x"].shape[0]
+    flops = 2.0 * sum(2.0 * m * d[k].W.shape[0] * d[k].W.shape[1] for k in bench.PROJS)
+    assert cfg["tokens_per_step"] == m and cfg["gemm_flops_per_step"] == flops
+    assert cfg["workload"] == "layer-3b" and bench.step_config(4)["parallelism"] == "replicas x4"
