@@ -695,11 +695,13 @@ __global__ void __launch_bounds__(448, 1)
           if (p.addend32) {
             // a lane reads its own row: 32-byte loads fill whole sectors, so each
             // load instruction costs half the L1 transactions of 16-byte ones (the
-            // MIO queue these share with the scale-staging warps' shared loads)
+            // MIO queue these share with the scale-staging warps' shared loads), and
+            // they do not allocate in L1, which the ring leaves small and which
+            // nothing reads twice (the o and down forwards 6-7 % faster on GB300)
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               uint32_t* o8 = &out[ch][8 * k];
-              asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+              asm volatile("ld.global.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                            : "=r"(o8[0]), "=r"(o8[1]), "=r"(o8[2]), "=r"(o8[3]), "=r"(o8[4]),
                              "=r"(o8[5]), "=r"(o8[6]), "=r"(o8[7])
                            : "l"(ap + 16 * k));
