@@ -62,14 +62,14 @@ PROJS = ("q", "k", "v", "o", "gate_up", "down")
 # of the sources and build script that kernel was compiled from when it was taken.
 # The roofline reports it only while those files are unchanged, else null.
 GU_FWD_TRAFFIC = {
-    "bytes": 45270528 + 217363968,
+    "bytes": 45287168 + 217468160,
     "tokens": 8192,
     "sources": ("nvfp4_frozen_projection_gb300/csrc/gemm.cu",
                 "nvfp4_frozen_projection_gb300/csrc/tcgen05.cuh",
                 "nvfp4_frozen_projection_gb300/csrc/common.cuh",
                 "nvfp4_frozen_projection_gb300/csrc/kernels.h",
                 "nvfp4_frozen_projection_gb300/build.py"),
-    "sha256": "b0eba341ef1ab925e59f704fd668f431de0ef14d6080b8111c11ceddf71483ac",
+    "sha256": "992159fdd64dbaf786ba81e33f97074b780bf2470ec31dc4174ccbd7270cbad8",
 }
 INPUTS = ("x", "attn", "dy", "dq", "dk", "dv")
 
