@@ -428,7 +428,9 @@ def test_rmsnorm_statistic_error_bound_and_output():
         assert np.all(np.abs(y - yref) <= np.abs(yref) * 2.0 ** -22 + 1e-45)
 
 
-def test_rmsnorm_bwd_finite_differences():
+def _rmsnorm_bwd_fd_ok(bwd) -> bool:
+    """Whether bwd(y, gamma, rstd, dy) equals central finite differences of an FP64
+    RMSNorm forward."""
     rng = np.random.default_rng(11)
     R, H = 3, 32
     x = rng.standard_normal((R, H))
@@ -441,7 +443,7 @@ def test_rmsnorm_bwd_finite_differences():
         return xx * rs[:, None] * gamma, rs
 
     y, rs = fwd(x)
-    dx = orc.rmsnorm_bwd_from_y(y, gamma, rs, dy)
+    dx = bwd(y, gamma, rs, dy)
     h = 1e-6
     num = np.zeros_like(x)
     for i in range(R):
@@ -450,7 +452,38 @@ def test_rmsnorm_bwd_finite_differences():
             xp[i, j] += h
             xm[i, j] -= h
             num[i, j] = (np.sum(fwd(xp)[0] * dy) - np.sum(fwd(xm)[0] * dy)) / (2 * h)
-    np.testing.assert_allclose(dx, num, rtol=1e-6, atol=1e-8)
+    return bool(np.allclose(dx, num, rtol=1e-6, atol=1e-8))
+
+
+def test_rmsnorm_bwd_finite_differences():
+    assert _rmsnorm_bwd_fd_ok(orc.rmsnorm_bwd_from_y)
+
+
+def _rms_bwd_planted(kind):
+    """The oracle's RMSNorm backward with one plausible mistake planted (CPU only)."""
+    def bwd(y, gamma, rstd, dy):
+        g = np.asarray(gamma, np.float64)[None, :]
+        n = np.asarray(y, np.float64) / g
+        dn = np.asarray(dy, np.float64) * g
+        H = n.shape[1]
+        c = (dn * n).sum(axis=1, keepdims=True) / H
+        rs = np.asarray(rstd, np.float64)[:, None]
+        if kind == "projection term dropped":
+            return rs * dn
+        if kind == "mean over H - 1":
+            return rs * (dn - n * (dn * n).sum(axis=1, keepdims=True) / (H - 1))
+        if kind == "gamma not applied to dy":
+            return rs * (np.asarray(dy, np.float64) - n * c)
+        if kind == "rstd squared":
+            return rs * rs * (dn - n * c)
+        raise ValueError(kind)
+    return bwd
+
+
+@pytest.mark.parametrize("kind", ["projection term dropped", "mean over H - 1",
+                                  "gamma not applied to dy", "rstd squared"])
+def test_rmsnorm_bwd_pin_catches_planted_mistakes(kind):
+    assert not _rmsnorm_bwd_fd_ok(_rms_bwd_planted(kind))
 
 
 # -------------------------------------------------------------- exp, SiLU
@@ -483,7 +516,9 @@ def test_silu_mul_special_values():
     assert h[5] == 200.0
 
 
-def test_silu_mul_bwd_finite_differences():
+def _silu_mul_bwd_fd_ok(bwd) -> bool:
+    """Whether bwd(g, u, dh) -> [dgate | dup] equals central finite differences of
+    h = g sigmoid(g) u in FP64."""
     rng = np.random.default_rng(12)
     g = rng.standard_normal((2, 16)) * 3
     u = rng.standard_normal((2, 16))
@@ -492,7 +527,7 @@ def test_silu_mul_bwd_finite_differences():
     def f(gg, uu):
         return np.sum(dh * gg / (1 + np.exp(-gg)) * uu)
 
-    grads = orc.silu_mul_bwd_from(g, u, dh)
+    grads = bwd(g, u, dh)
     h = 1e-6
     ng = np.zeros_like(g)
     nu = np.zeros_like(u)
@@ -502,8 +537,40 @@ def test_silu_mul_bwd_finite_differences():
             e[i, j] = h
             ng[i, j] = (f(g + e, u) - f(g - e, u)) / (2 * h)
             nu[i, j] = (f(g, u + e) - f(g, u - e)) / (2 * h)
-    np.testing.assert_allclose(grads[:, :16], ng, rtol=1e-6, atol=1e-8)
-    np.testing.assert_allclose(grads[:, 16:], nu, rtol=1e-6, atol=1e-8)
+    return bool(np.allclose(grads[:, :16], ng, rtol=1e-6, atol=1e-8) and
+                np.allclose(grads[:, 16:], nu, rtol=1e-6, atol=1e-8))
+
+
+def test_silu_mul_bwd_finite_differences():
+    assert _silu_mul_bwd_fd_ok(orc.silu_mul_bwd_from)
+
+
+def _silu_bwd_planted(kind):
+    """The oracle's SiLU-multiply backward with one plausible mistake (CPU only)."""
+    def bwd(g, u, dh):
+        s = 1.0 / (1.0 + np.exp(-g))
+        dgate = dh * u * s * (1.0 + g * (1.0 - s))
+        dup = dh * g * s
+        if kind == "sigmoid derivative dropped":
+            dgate = dh * u * s
+        elif kind == "outputs swapped":
+            dgate, dup = dup, dgate
+        elif kind == "sign of the sigmoid argument":
+            sm = 1.0 / (1.0 + np.exp(g))
+            dgate = dh * u * sm * (1.0 + g * (1.0 - sm))
+            dup = dh * g * sm
+        elif kind == "up gradient without gate":
+            dup = dh * s
+        else:
+            raise ValueError(kind)
+        return np.concatenate([dgate, dup], axis=1)
+    return bwd
+
+
+@pytest.mark.parametrize("kind", ["sigmoid derivative dropped", "outputs swapped",
+                                  "sign of the sigmoid argument", "up gradient without gate"])
+def test_silu_mul_bwd_pin_catches_planted_mistakes(kind):
+    assert not _silu_mul_bwd_fd_ok(_silu_bwd_planted(kind))
 
 
 def test_silu_mul_quant_separate_copies():
