@@ -342,7 +342,7 @@ def test_fwd_dgrad_adjoint():
     assert lhs == pytest.approx(rhs, rel=1e-12)
 
 
-def test_adapter_grad_is_the_derivative_of_the_forward():
+def _adapter_grad_is_derivative(grad_fn) -> bool:
     """The forward is linear in A and in B, so for any directions E_A, E_B
     <fwd(A + E_A, B) - fwd(A, B), dY> == <dA, E_A> and likewise for B, exactly up to
     FP64 rounding: the gradients are checked against the forward, not restated."""
@@ -354,15 +354,51 @@ def test_adapter_grad_is_the_derivative_of_the_forward():
     A = rng.standard_normal((K, r))
     B = rng.standard_normal((r, N))
     dy = rng.standard_normal((M, N))
-    dA, dB = orc.lora_adapter_grad(xq, dy, A, B, alpha)
-    assert dA.shape == (K, r) and dB.shape == (r, N)
+    dA, dB = grad_fn(xq, dy, A, B, alpha)
+    if dA.shape != (K, r) or dB.shape != (r, N):
+        return False
     loss = lambda A_, B_: float(np.sum(orc.lora_linear_fwd(xq, wf, A_, B_, alpha) * dy))
     base = loss(A, B)
     for _ in range(4):
         EA = rng.standard_normal((K, r))
         EB = rng.standard_normal((r, N))
-        assert loss(A + EA, B) - base == pytest.approx(float(np.sum(dA * EA)), rel=1e-9, abs=1e-9)
-        assert loss(A, B + EB) - base == pytest.approx(float(np.sum(dB * EB)), rel=1e-9, abs=1e-9)
+        if loss(A + EA, B) - base != pytest.approx(float(np.sum(dA * EA)), rel=1e-9, abs=1e-9):
+            return False
+        if loss(A, B + EB) - base != pytest.approx(float(np.sum(dB * EB)), rel=1e-9, abs=1e-9):
+            return False
+    return True
+
+
+def test_adapter_grad_is_the_derivative_of_the_forward():
+    assert _adapter_grad_is_derivative(orc.lora_adapter_grad)
+
+
+def _adapter_grad_planted(kind):
+    """The oracle's adapter gradients with one plausible mistake (CPU only)."""
+    def grad(xq, dy, A, B, alpha):
+        xh = orc.dequant(xq)
+        A = np.asarray(A, np.float64)
+        B = np.asarray(B, np.float64)
+        dy64 = np.asarray(dy, np.float64)
+        s = alpha / A.shape[1]
+        dA = s * (xh.T @ (dy64 @ B.T))
+        dB = s * ((xh @ A).T @ dy64)
+        if kind == "scale alpha instead of alpha/r":
+            return dA * A.shape[1], dB * A.shape[1]
+        if kind == "dA without the input":
+            return s * (np.ones_like(xh).T @ (dy64 @ B.T)), dB
+        if kind == "dB without the down-projection":
+            return dA, s * (np.ones((xh.shape[0], A.shape[1])).T @ dy64)
+        if kind == "dB sign":
+            return dA, -dB
+        raise ValueError(kind)
+    return grad
+
+
+@pytest.mark.parametrize("kind", ["scale alpha instead of alpha/r", "dA without the input",
+                                  "dB without the down-projection", "dB sign"])
+def test_adapter_grad_pin_catches_planted_mistakes(kind):
+    assert not _adapter_grad_is_derivative(_adapter_grad_planted(kind))
 
 
 def test_adapter_grad_brute_force_and_zero_cases():
